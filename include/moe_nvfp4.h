@@ -1,0 +1,216 @@
+/*
+ * moe_nvfp4.h — C ABI of libmoe_nvfp4.so: a single-GPU NVFP4 Mixture-of-
+ * Experts layer forward for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (sources cited by page title and section):
+ *   router softmax + top-K            ["MegaMoE" blog, "The problem"]
+ *   token permutation by expert       [FlashInfer PR #4366: the "contiguous
+ *                                      gather" grouped GEMM; "Tests": cluster
+ *                                      padding and partial tiles]
+ *   activation quantization to NVFP4  ["MegaMoE", "Our approach": W4A4 with
+ *   (E2M1 + E4M3 block-16 scales +     block-16 scaling; newruntime post on
+ *   FP32 per-tensor or per-token       PR #5319, "Retrieval answer": W4A4
+ *   global scale)                      per-tensor or per-token, W4A16]
+ *   grouped GEMM FC1 (gate|up) + SwiGLU or ReLU2, router weight on the FC2
+ *   input or at the output reduction, requantization to NVFP4
+ *                                     [PR #4366, "Motivation"]
+ *   grouped GEMM FC2
+ *   finalize: unpermute + weighted top-K reduction, fused into the FC2
+ *   epilogue or a separate deterministic kernel
+ *                                     [PR #5319 post, "Retrieval answer":
+ *                                      fused vs --no-fused-finalize]
+ *   W4A16 variant: NVFP4 weights, BF16 activations.
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates device memory and keeps no pointer after returning.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every
+ *     entry point except moe_nvfp4_last_device_status only enqueues work on
+ *     `stream` and returns without synchronizing.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns an error code and enqueues nothing.  Device-side
+ *     faults are never used to report errors.
+ *   - Numeric contract: see the per-function comments; results do not depend
+ *     on the stream, the launch order of other work, or the SM count, except
+ *     the fused finalize (floating-point atomics; not bit-reproducible).
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad shape, flag, null or misaligned pointer */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid request this build/device cannot run  */
+    MOE_ERR_WORKSPACE = 3,     /* buffer smaller than the *_bytes() query     */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed                  */
+    MOE_ERR_TIMEOUT = 5        /* a device-side wait gave up (see status word)*/
+} moe_status;
+
+/* ---- flags (one uint32_t) ------------------------------------------------ */
+/* bits 0-1: activation of FC1 */
+#define MOE_ACT_SWIGLU 0u            /* h = silu(gate) * up, W1 = [gate; up] */
+#define MOE_ACT_RELU2 1u             /* h = max(z, 0)^2, non-gated          */
+#define MOE_ACT_MASK 3u
+/* bits 2-3: precision mode */
+#define MOE_W4A4_PER_TENSOR (0u << 2) /* caller-supplied FP32 global scales   */
+#define MOE_W4A4_PER_TOKEN (1u << 2)  /* per-row amax/2688 global scales      */
+#define MOE_W4A16 (2u << 2)           /* BF16 activations, NVFP4 weights      */
+#define MOE_MODE_MASK (3u << 2)
+/* bit 4: router weight applied to the FC2 input (after the activation,
+ * before the FC2-input quantization or BF16 store) instead of at the output
+ * reduction (default) [PR #4366, "Motivation"]. */
+#define MOE_ROUTER_W_ON_INPUT (1u << 4)
+/* bit 5: deterministic two-stage finalize (FC2 stores per-route rows, a
+ * fixed-order reduction kernel sums them) instead of the fused FC2-epilogue
+ * scatter (default). */
+#define MOE_FINALIZE_DETERMINISTIC (1u << 5)
+/* bit 6: router weights are the full softmax over all E experts evaluated
+ * at the selected ones, instead of the softmax over the K selected. */
+#define MOE_ROUTE_NO_RENORM (1u << 6)
+#define MOE_FLAGS_KNOWN 0x7Fu
+
+/* ---- shapes ---------------------------------------------------------------- */
+typedef struct {
+    int T;  /* tokens, >= 1                                                  */
+    int H;  /* hidden size, multiple of 128                                  */
+    int I;  /* per-expert intermediate size, multiple of 128                 */
+    int E;  /* experts, 1..1024                                              */
+    int K;  /* experts per token (top-K), 1..min(E, 32)                      */
+} moe_shape;
+
+/* ---- weight preparation ------------------------------------------------------ */
+/* Size in bytes of the prepared-weight buffer for this shape and activation
+ * (only the activation bits of `flags` matter).  0 if the shape is invalid. */
+MOE_API size_t moe_nvfp4_prepared_bytes(moe_shape s, uint32_t flags);
+
+/* Quantize BF16 checkpoint weights to NVFP4 and reorder them into the
+ * prepared layout consumed by moe_nvfp4_forward in every precision mode
+ * ["MegaMoE", "Usage": weights accepted in checkpoint layout, quantized and
+ * reordered by the layer; PR #5319 post: W4A4 and W4A16 share the layout].
+ *   w1_bf16  [E][N1][H] row-major, N1 = 2I for SwiGLU (rows 0..I-1 gate,
+ *            I..2I-1 up), N1 = I for ReLU2.  16-byte aligned.
+ *   w2_bf16  [E][H][I] row-major.  16-byte aligned.
+ *   prepared output, `prepared_bytes` >= moe_nvfp4_prepared_bytes(); 256-byte
+ *            aligned.  Per expert and matrix: global scale amax/2688 (1 if the
+ *            matrix is zero), E4M3 scale per 16 elements along the reduction
+ *            dimension, E2M1 codes.  Layout (versioned, MOE_PREPARED_VERSION):
+ *              Gw1[E] f32 | Gw2[E] f32 | W1 codes [E][N1][H/2] |
+ *              W1 scales [E][N1/128][H/64][512] | W2 codes [E][H][I/2] |
+ *              W2 scales [E][H/128][I/64][512]
+ *            each region 256-byte aligned.  W1 rows are reordered for SwiGLU
+ *            so that every 128-row tile holds 64 gate rows then the 64
+ *            matching up rows.  A 512-byte scale atom holds 128 rows x 4
+ *            scales: byte (r%32)*16 + (r/32)*4 + j for row r, scale j.
+ * Errors: MOE_ERR_INVALID_ARG (shape, flags, null/misaligned pointer),
+ * MOE_ERR_WORKSPACE (prepared_bytes too small), MOE_ERR_CUDA.  Enqueues two
+ * kernels on `stream`; the input buffers must stay valid until they finish. */
+MOE_API moe_status moe_nvfp4_prepare_weights(moe_shape s, uint32_t flags,
+                                     const void* w1_bf16, const void* w2_bf16,
+                                     void* prepared, size_t prepared_bytes,
+                                     void* stream);
+
+#define MOE_PREPARED_VERSION 1
+
+/* ---- forward ------------------------------------------------------------------- */
+/* Size in bytes of the workspace moe_nvfp4_forward needs.  0 if invalid. */
+MOE_API size_t moe_nvfp4_workspace_bytes(moe_shape s, uint32_t flags);
+
+/* The layer forward, y = MoE(x).
+ *   x_bf16        [T][H] BF16, 16-byte aligned.
+ *   router_logits [T][E] FP32 (finite), 16-byte aligned.
+ *   router_bias   [E] FP32 added to the logits before selection, or NULL.
+ *   act_scale_fc1 per-tensor W4A4: device FP32[1], the FC1-input global scale
+ *                 G1 (> 0, decode direction: x ~ q * s * G1); else NULL.
+ *   act_scale_fc2 per-tensor W4A4: device FP32[1], FC2-input scale G2 (> 0);
+ *                 else NULL.
+ *   prepared      output of moe_nvfp4_prepare_weights for the same shape
+ *                 and activation.
+ *   workspace     >= moe_nvfp4_workspace_bytes(), 256-byte aligned; holds
+ *                 the intermediates (layout: moe_nvfp4_workspace_layout).
+ *   y_bf16        [T][H] BF16 output, overwritten; 16-byte aligned; must not
+ *                 alias any input.
+ * Selection: the K largest logit+bias, ties to the lower expert index.
+ * Bit-exact, on every device and at every size: expert ids, counts, offsets,
+ * the permutation and the NVFP4 codes/scales of x.  Floating-point: router
+ * weights (expf), FC outputs and y (tensor-core FP32 accumulation).
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE, MOE_ERR_UNSUPPORTED (no
+ * sm_103a/sm_100-family device), MOE_ERR_CUDA.  Nothing is synchronized. */
+MOE_API moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags,
+                             const void* x_bf16, const float* router_logits,
+                             const float* router_bias,
+                             const float* act_scale_fc1, const float* act_scale_fc2,
+                             const void* prepared,
+                             void* workspace, size_t workspace_bytes,
+                             void* y_bf16, void* stream);
+
+/* Byte offsets of the intermediates inside the workspace (for tests and
+ * debugging; MOE_WORKSPACE_VERSION).  Each entry is 256-byte aligned.
+ * rows_cap = the padded-row capacity (a multiple of 128).               */
+typedef struct {
+    uint64_t rows_cap;       /* padded-row capacity                          */
+    uint64_t status;         /* uint32[4]: [0] error bits of the last run    */
+    uint64_t topk_ids;       /* int32 [T][K]                                 */
+    uint64_t topk_w;         /* f32   [T][K]                                 */
+    uint64_t count;          /* int32 [E]   routes per expert                */
+    uint64_t offsets;        /* int32 [E+1] exclusive prefix of count        */
+    uint64_t padded_offsets; /* int32 [E+1] prefix of count rounded up to 128*/
+    uint64_t meta;           /* int32 [4]: [0] padded rows, [1] M tiles      */
+    uint64_t unit_base;      /* int32 [E][ceil(T/32)] permute scratch        */
+    uint64_t row_of_route;   /* int32 [T*K] padded row of route t*K+k        */
+    uint64_t route_of_row;   /* int32 [rows_cap] route of a row, -1 in pads  */
+    uint64_t tile_expert;    /* int32 [rows_cap/128] expert of each M tile   */
+    uint64_t g1;             /* f32   [T] FC1-input global scale per token   */
+    uint64_t xq_codes;       /* u8    [rows_cap][H/2] permuted x codes       */
+    uint64_t xq_sf;          /* u8    [rows_cap/128][H/64][512] x scales     */
+    uint64_t h_f32;          /* f32   [rows_cap][I] FC2 input before quant   */
+    uint64_t g2;             /* f32   [rows_cap] FC2-input scale per row     */
+    uint64_t hq_codes;       /* u8    [rows_cap][I/2] FC2-input codes        */
+    uint64_t hq_sf;          /* u8    [rows_cap/128][I/64][512]              */
+    uint64_t x_bf16_perm;    /* bf16  [rows_cap][H] permuted x (W4A16)       */
+    uint64_t h_bf16;         /* bf16  [rows_cap][I] FC2 input (W4A16)        */
+    uint64_t o_bf16;         /* bf16  [rows_cap][H] per-route FC2 output     */
+    uint64_t y_acc;          /* f32   [T][H] fused-finalize accumulator      */
+    uint64_t total;          /* workspace bytes                              */
+} moe_workspace_layout;
+
+#define MOE_WORKSPACE_VERSION 1
+
+/* Fill `out` with the workspace layout for this shape and flags.  Regions a
+ * mode does not use have offset UINT64_MAX.  Pure host call, no CUDA. */
+MOE_API moe_status moe_nvfp4_workspace_layout(moe_shape s, uint32_t flags,
+                                      moe_workspace_layout* out);
+
+/* Debug: wait for `stream`, then read and clear the device status word that
+ * the most recent forward on `workspace` left (each forward clears it first).
+ * Returns MOE_OK; MOE_ERR_TIMEOUT if a kernel's bounded wait (1 s) gave up;
+ * MOE_ERR_INVALID_ARG if a kernel met an out-of-range expert id; or
+ * MOE_ERR_CUDA.  Synchronizes `stream`. */
+MOE_API moe_status moe_nvfp4_last_device_status(void* workspace, void* stream);
+
+/* Test hook: convert n FP32 values with the library's device conversions,
+ * E4M3 (round-to-nearest-even, saturating; one byte per value) and E2M1
+ * (same rounding; the 4-bit code in the low nibble of one byte per value).
+ * All pointers are device pointers.  Enqueues one kernel on `stream`. */
+MOE_API moe_status moe_nvfp4_debug_convert(const float* in, int64_t n, uint8_t* e4m3,
+                                   uint8_t* e2m1, void* stream);
+
+/* Library version string, e.g. "moe_nvfp4 1.0 sm_103a". */
+MOE_API const char* moe_nvfp4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_NVFP4_H */

@@ -1,0 +1,224 @@
+"""Python binding of libmoe_nvfp4.so (ctypes).  Argument marshalling only:
+every step of the layer runs in the library's CUDA kernels.  PyTorch
+supplies device memory and streams.
+
+The functions carry the C names (moe_nvfp4_*); ``MoELayer`` bundles the
+buffers of one layer for convenience.  There is no CPU fallback: loading
+fails loudly if the library is missing or the device is not sm_103a.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_nvfp4.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(6)
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+                4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
+
+MOE_ACT_SWIGLU = 0
+MOE_ACT_RELU2 = 1
+MOE_W4A4_PER_TENSOR = 0 << 2
+MOE_W4A4_PER_TOKEN = 1 << 2
+MOE_W4A16 = 2 << 2
+MOE_ROUTER_W_ON_INPUT = 1 << 4
+MOE_FINALIZE_DETERMINISTIC = 1 << 5
+MOE_ROUTE_NO_RENORM = 1 << 6
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int),
+                ("K", ctypes.c_int)]
+
+
+_LAYOUT_FIELDS = ["rows_cap", "status", "topk_ids", "topk_w", "count", "offsets", "padded_offsets", "meta",
+                  "unit_base", "row_of_route", "route_of_row", "tile_expert", "g1", "xq_codes", "xq_sf", "h_f32",
+                  "g2", "hq_codes", "hq_sf", "x_bf16_perm", "h_bf16", "o_bf16", "y_acc", "total"]
+
+
+class moe_workspace_layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in _LAYOUT_FIELDS]
+
+
+_lib = None
+
+
+def lib():
+    """Load libmoe_nvfp4.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m nvfp4_mixture_experts_router_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, S = ctypes.c_void_p, moe_shape
+        u32, i64, sz = ctypes.c_uint32, ctypes.c_int64, ctypes.c_size_t
+        sig = {
+            "moe_nvfp4_version": (ctypes.c_char_p, []),
+            "moe_nvfp4_prepared_bytes": (sz, [S, u32]),
+            "moe_nvfp4_prepare_weights": (ctypes.c_int, [S, u32, P, P, P, sz, P]),
+            "moe_nvfp4_workspace_bytes": (sz, [S, u32]),
+            "moe_nvfp4_workspace_layout": (ctypes.c_int, [S, u32, ctypes.POINTER(moe_workspace_layout)]),
+            "moe_nvfp4_forward": (ctypes.c_int, [S, u32, P, P, P, P, P, P, P, sz, P, P]),
+            "moe_nvfp4_last_device_status": (ctypes.c_int, [P, P]),
+            "moe_nvfp4_debug_convert": (ctypes.c_int, [P, i64, P, P, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+EXPORTED = ["moe_nvfp4_version", "moe_nvfp4_prepared_bytes", "moe_nvfp4_prepare_weights",
+            "moe_nvfp4_workspace_bytes", "moe_nvfp4_workspace_layout", "moe_nvfp4_forward",
+            "moe_nvfp4_last_device_status", "moe_nvfp4_debug_convert"]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, code: int):
+    if code != MOE_OK:
+        raise MoEError(fn, code)
+
+
+def shape(T: int, H: int, I: int, E: int, K: int) -> moe_shape:
+    return moe_shape(T, H, I, E, K)
+
+
+# ---- C entry points ---------------------------------------------------------
+
+def moe_nvfp4_version() -> str:
+    return lib().moe_nvfp4_version().decode()
+
+
+def moe_nvfp4_prepared_bytes(s: moe_shape, flags: int) -> int:
+    return int(lib().moe_nvfp4_prepared_bytes(s, flags))
+
+
+def moe_nvfp4_workspace_bytes(s: moe_shape, flags: int) -> int:
+    return int(lib().moe_nvfp4_workspace_bytes(s, flags))
+
+
+def moe_nvfp4_workspace_layout(s: moe_shape, flags: int) -> dict:
+    out = moe_workspace_layout()
+    _check("moe_nvfp4_workspace_layout", lib().moe_nvfp4_workspace_layout(s, flags, ctypes.byref(out)))
+    return {n: int(getattr(out, n)) for n in _LAYOUT_FIELDS}
+
+
+def moe_nvfp4_prepare_weights(s: moe_shape, flags: int, w1_bf16: torch.Tensor, w2_bf16: torch.Tensor,
+                              prepared: torch.Tensor, stream=None) -> None:
+    code = lib().moe_nvfp4_prepare_weights(s, flags, _ptr(w1_bf16), _ptr(w2_bf16), _ptr(prepared),
+                                           prepared.numel() * prepared.element_size(), _stream(stream))
+    _check("moe_nvfp4_prepare_weights", code)
+
+
+def moe_nvfp4_forward(s: moe_shape, flags: int, x_bf16: torch.Tensor, router_logits: torch.Tensor,
+                      router_bias: Optional[torch.Tensor], act_scale_fc1: Optional[torch.Tensor],
+                      act_scale_fc2: Optional[torch.Tensor], prepared: torch.Tensor, workspace: torch.Tensor,
+                      y_bf16: torch.Tensor, stream=None) -> None:
+    code = lib().moe_nvfp4_forward(s, flags, _ptr(x_bf16), _ptr(router_logits), _ptr(router_bias),
+                                   _ptr(act_scale_fc1), _ptr(act_scale_fc2), _ptr(prepared), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _ptr(y_bf16), _stream(stream))
+    _check("moe_nvfp4_forward", code)
+
+
+def moe_nvfp4_last_device_status(workspace: torch.Tensor, stream=None) -> int:
+    return int(lib().moe_nvfp4_last_device_status(_ptr(workspace), _stream(stream)))
+
+
+def moe_nvfp4_debug_convert(x: torch.Tensor, stream=None):
+    """Device E4M3 and E2M1 codes of the float32 CUDA tensor x."""
+    x = x.contiguous()
+    e4 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    e2 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check("moe_nvfp4_debug_convert",
+           lib().moe_nvfp4_debug_convert(_ptr(x), x.numel(), _ptr(e4), _ptr(e2), _stream(stream)))
+    return e4, e2
+
+
+# ---- convenience ---------------------------------------------------------------
+
+@dataclass
+class MoELayer:
+    """Buffers of one MoE layer on one device: prepared weights + workspace."""
+    T: int
+    H: int
+    I: int
+    E: int
+    K: int
+    flags: int
+    prepared: torch.Tensor
+    workspace: torch.Tensor
+
+    @property
+    def shape(self) -> moe_shape:
+        return moe_shape(self.T, self.H, self.I, self.E, self.K)
+
+    @classmethod
+    def create(cls, T, H, I, E, K, flags, device="cuda") -> "MoELayer":
+        s = moe_shape(T, H, I, E, K)
+        pb = moe_nvfp4_prepared_bytes(s, flags)
+        wb = moe_nvfp4_workspace_bytes(s, flags)
+        if pb == 0 or wb == 0:
+            raise MoEError("moe_nvfp4_*_bytes", MOE_ERR_INVALID_ARG)
+        prepared = torch.empty(pb, dtype=torch.uint8, device=device)
+        workspace = torch.empty(wb, dtype=torch.uint8, device=device)
+        return cls(T, H, I, E, K, flags, prepared, workspace)
+
+    def prepare(self, w1_bf16: torch.Tensor, w2_bf16: torch.Tensor, stream=None):
+        moe_nvfp4_prepare_weights(self.shape, self.flags, w1_bf16, w2_bf16, self.prepared, stream)
+
+    def forward(self, x_bf16, logits, bias=None, g1=None, g2=None, y=None, stream=None) -> torch.Tensor:
+        if y is None:
+            y = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=x_bf16.device)
+        moe_nvfp4_forward(self.shape, self.flags, x_bf16, logits, bias, g1, g2, self.prepared, self.workspace,
+                          y, stream)
+        return y
+
+    # -- views of the intermediates (tests / debugging) --
+    def layout(self) -> dict:
+        return moe_nvfp4_workspace_layout(self.shape, self.flags)
+
+    def view(self, name: str, dtype: torch.dtype, numel: int) -> torch.Tensor:
+        off = self.layout()[name]
+        if off == 2 ** 64 - 1:
+            raise KeyError(f"workspace region {name} is not used in this mode")
+        nbytes = numel * torch.empty((), dtype=dtype).element_size()
+        return self.workspace[off:off + nbytes].view(dtype)
+
+    def prepared_regions(self) -> dict:
+        """Byte offsets of the prepared-weight regions (same rule as the library)."""
+        def up(v):
+            return (v + 255) // 256 * 256
+        N1 = 2 * self.I if (self.flags & 3) == MOE_ACT_SWIGLU else self.I
+        E, H, I = self.E, self.H, self.I
+        o = 0
+        r = {}
+        for name, nbytes in [("gw1", 4 * E), ("gw2", 4 * E), ("w1_codes", E * N1 * H // 2),
+                             ("w1_sf", E * N1 * H // 16), ("w2_codes", E * H * I // 2), ("w2_sf", E * H * I // 16)]:
+            r[name] = (o, nbytes)
+            o = up(o + nbytes)
+        r["total"] = (o, 0)
+        return r

@@ -1,0 +1,96 @@
+// Kernel launchers (host side) used by the orchestrator in moe_api.cu.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Launch helper: every launch goes through cudaLaunchKernelEx so that the
+// programmatic-dependent-launch attribute can be set uniformly.
+struct LaunchCtx {
+    cudaStream_t stream = nullptr;
+    bool pdl = false;
+
+    template <typename... KArgs, typename... Args>
+    cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, Args... args) const {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    }
+};
+
+// routing.cu
+cudaError_t setup_routing_kernels();
+cudaError_t launch_router(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
+                          int renorm, int* ids, float* w, unsigned int* status_reset);
+cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base, int* count,
+                           int* offsets, int* padded_offsets, int* meta, int* tile_expert, int* row_of_route,
+                           int* route_of_row, unsigned int* status);
+
+// rowops.cu
+cudaError_t launch_quantize_x(const LaunchCtx& c, int T, int H, int K, const void* x, const float* g1_in,
+                              int per_token, float* g1_out, const int* row_of_route, uint8_t* codes, uint8_t* sf,
+                              float* y_acc_zero);
+cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const void* x, const int* row_of_route,
+                                 void* x_perm, float* y_acc_zero);
+cudaError_t launch_quantize_h(const LaunchCtx& c, uint64_t rows_cap, int I, const int* meta,
+                              const int* route_of_row, const float* h, float* g2, uint8_t* codes, uint8_t* sf);
+cudaError_t launch_finalize_deterministic(const LaunchCtx& c, int T, int H, int K, const int* row_of_route,
+                                          const float* topk_w, int weight_on_output, const void* o, void* y);
+cudaError_t launch_finalize_fused(const LaunchCtx& c, int T, int H, const float* y_acc, void* y);
+cudaError_t launch_prepare(cudaStream_t s, int E, int N1, int H, int I, int act, const void* w1, const void* w2,
+                           uint8_t* prepared, uint64_t gw1, uint64_t gw2, uint64_t w1c, uint64_t w1s, uint64_t w2c,
+                           uint64_t w2s);
+cudaError_t launch_debug_convert(cudaStream_t s, const float* in, int64_t n, uint8_t* e4m3, uint8_t* e2m1);
+
+// gemm_nvf4.cu — grouped block-scaled GEMMs on tcgen05
+enum GemmEpilogue : int {
+    kEpiFc1Quant = 0,   // FC1: activation, route weight, NVFP4 requant with per-tensor G2
+    kEpiFc1F32 = 1,     // FC1: activation, route weight, FP32 store (per-token G2 later)
+    kEpiFc2Store = 2,   // FC2: BF16 per-route rows (deterministic finalize)
+    kEpiFc2Scatter = 3  // FC2: weighted FP32 atomic add into the token row (fused finalize)
+};
+
+struct GemmParams {
+    // operands
+    const uint8_t* sfa;          // A scales [rows_cap/128][kdim/64][512]
+    const uint8_t* sfb;          // B scales [E][N/128][kdim/64][512]
+    int kdim;                    // reduction length (elements)
+    int n;                       // output columns per expert (B rows per expert)
+    const int* meta;             // meta[1] = number of M tiles
+    const int* tile_expert;      // expert of each M tile
+    const int* route_of_row;     // route of each padded row, -1 in pad rows
+    int num_experts;             // E (bounds check of tile_expert)
+    unsigned int* status;
+    // epilogue
+    int act;                     // MOE_ACT_*
+    int topk;                    // K
+    const float* gw;             // per-expert weight global scale [E]
+    const float* g_act;          // activation global scale: per-tensor [1] or per-token/row array
+    int g_act_per_token;         // 0: g_act[0]; 1 (FC1): g_act[token]; 2 (FC2): g_act[row]
+    const float* topk_w;         // [T*K] router weights
+    int weight_on_input;         // FC1: multiply h by the route weight
+    int weight_on_output;        // FC2 scatter: multiply o by the route weight
+    const float* g2;             // FC1 quant: per-tensor FC2-input scale [1]
+    int out_cols;                // width of the output row (I for FC1, H for FC2)
+    uint8_t* out_codes;          // FC1 quant: [rows_cap][I/2]
+    uint8_t* out_sf;             // FC1 quant: [rows_cap/128][I/64][512]
+    float* out_f32;              // FC1 F32: [rows_cap][I]; FC2 scatter: y_acc [T][H]
+    __nv_bfloat16* out_bf16;     // FC2 store: [rows_cap][H]
+};
+
+cudaError_t setup_gemm_kernels();
+cudaError_t launch_gemm_nvf4(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             const GemmParams& p, int num_sms);
+
+}  // namespace moe

@@ -1,0 +1,321 @@
+// Host side of libmoe_nvfp4.so: argument validation, workspace carving,
+// tensor-map encoding and the launch sequence of the layer forward.  No
+// host synchronization and no allocation on the forward path: the expert
+// counts never leave the device (the GEMM tile schedulers read them).
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe_nvfp4.h"
+#include "common.cuh"
+#include "kernels.h"
+#include "layout.h"
+
+using namespace moe;
+
+namespace {
+
+struct DeviceState {
+    bool ready = false;
+    moe_status status = MOE_ERR_UNSUPPORTED;
+    int sms = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+moe_status device_state(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        d.ready = true;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            d.status = MOE_ERR_CUDA;
+        } else if (major != 10 || minor != 3) {
+            d.status = MOE_ERR_UNSUPPORTED;  // the binary carries sm_103a code only
+        } else if (setup_routing_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess) {
+            d.status = MOE_ERR_CUDA;
+        } else {
+            d.status = MOE_OK;
+        }
+        if (d.status == MOE_OK && g_encode == nullptr) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr) {
+                d.status = MOE_ERR_CUDA;
+            } else {
+                g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            }
+        }
+    }
+    *sms = d.sms;
+    return d.status;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+moe_status validate_shape(moe_shape s, uint32_t flags) {
+    if (flags & ~MOE_FLAGS_KNOWN) return MOE_ERR_INVALID_ARG;
+    if (act_of(flags) > 1 || mode_of(flags) > 2) return MOE_ERR_INVALID_ARG;
+    if (s.T < 1 || s.T > (1 << 22)) return MOE_ERR_INVALID_ARG;
+    if (s.H < 128 || s.H % 128 != 0 || s.H > 65536) return MOE_ERR_INVALID_ARG;
+    if (s.I < 128 || s.I % 128 != 0 || s.I > 65536) return MOE_ERR_INVALID_ARG;
+    if (s.E < 1 || s.E > 1024) return MOE_ERR_INVALID_ARG;
+    if (s.K < 1 || s.K > 32 || s.K > s.E) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)s.T * s.K > (1 << 26)) return MOE_ERR_INVALID_ARG;
+    // every row count that reaches a TMA coordinate must stay below 2^31
+    const uint64_t N1 = (uint64_t)n1_of(s.I, flags);
+    if ((uint64_t)s.E * N1 >= (1ull << 31) || (uint64_t)s.E * (uint64_t)s.H >= (1ull << 31)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+// 2-D uint8 tensor map over a row-major [rows][row_bytes] array, 128x128
+// boxes, 128-byte swizzle (the canonical K-major UMMA operand layout).
+bool encode_operand_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes) {
+    const cuuint64_t dims[2] = {row_bytes, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {128, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.0 sm_103a (prepared v1, workspace v1)"; }
+
+size_t moe_nvfp4_prepared_bytes(moe_shape s, uint32_t flags) {
+    if (validate_shape(s, flags) != MOE_OK) return 0;
+    return (size_t)prepared_layout(s, flags).total;
+}
+
+size_t moe_nvfp4_workspace_bytes(moe_shape s, uint32_t flags) {
+    if (validate_shape(s, flags) != MOE_OK) return 0;
+    return (size_t)workspace_layout(s, flags).total;
+}
+
+moe_status moe_nvfp4_workspace_layout(moe_shape s, uint32_t flags, moe_workspace_layout* out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    const moe_status st = validate_shape(s, flags);
+    if (st != MOE_OK) return st;
+    *out = workspace_layout(s, flags);
+    return MOE_OK;
+}
+
+moe_status moe_nvfp4_prepare_weights(moe_shape s, uint32_t flags, const void* w1_bf16, const void* w2_bf16,
+                                     void* prepared, size_t prepared_bytes, void* stream) {
+    moe_status st = validate_shape(s, flags);
+    if (st != MOE_OK) return st;
+    if (!w1_bf16 || !w2_bf16 || !prepared) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w1_bf16, 16) || !aligned(w2_bf16, 16) || !aligned(prepared, 256)) return MOE_ERR_INVALID_ARG;
+    const PreparedLayout L = prepared_layout(s, flags);
+    if (prepared_bytes < L.total) return MOE_ERR_WORKSPACE;
+    int sms = 0;
+    st = device_state(&sms);
+    if (st != MOE_OK) return st;
+    const int N1 = n1_of(s.I, flags);
+    return cuda_status(launch_prepare(static_cast<cudaStream_t>(stream), s.E, N1, s.H, s.I, act_of(flags), w1_bf16,
+                                      w2_bf16, static_cast<uint8_t*>(prepared), L.gw1, L.gw2, L.w1_codes, L.w1_sf,
+                                      L.w2_codes, L.w2_sf));
+}
+
+moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags, const void* x_bf16, const float* router_logits,
+                             const float* router_bias, const float* act_scale_fc1, const float* act_scale_fc2,
+                             const void* prepared, void* workspace, size_t workspace_bytes, void* y_bf16,
+                             void* stream) {
+    moe_status st = validate_shape(s, flags);
+    if (st != MOE_OK) return st;
+    const int mode = mode_of(flags);
+    if (!x_bf16 || !router_logits || !prepared || !workspace || !y_bf16) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(router_logits, 16) || !aligned(y_bf16, 16) || !aligned(prepared, 256) ||
+        !aligned(workspace, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (router_bias && !aligned(router_bias, 4)) return MOE_ERR_INVALID_ARG;
+    if (mode == kModePerTensor) {
+        if (!act_scale_fc1 || !act_scale_fc2 || !aligned(act_scale_fc1, 4) || !aligned(act_scale_fc2, 4))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const moe_workspace_layout W = workspace_layout(s, flags);
+    if (workspace_bytes < W.total) return MOE_ERR_WORKSPACE;
+    const size_t y_bytes = (size_t)s.T * s.H * 2;
+    if (overlaps(y_bf16, y_bytes, workspace, W.total) || overlaps(y_bf16, y_bytes, x_bf16, y_bytes) ||
+        overlaps(y_bf16, y_bytes, router_logits, (size_t)s.T * s.E * 4))
+        return MOE_ERR_INVALID_ARG;
+    if (mode == kModeW4A16) return MOE_ERR_UNSUPPORTED;
+
+    int sms = 0;
+    st = device_state(&sms);
+    if (st != MOE_OK) return st;
+
+    const PreparedLayout P = prepared_layout(s, flags);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const uint8_t* pw = static_cast<const uint8_t*>(prepared);
+    auto wsp = [&](uint64_t off) { return ws + off; };
+    unsigned int* status = reinterpret_cast<unsigned int*>(wsp(W.status));
+    int* ids = reinterpret_cast<int*>(wsp(W.topk_ids));
+    float* topk_w = reinterpret_cast<float*>(wsp(W.topk_w));
+    int* meta = reinterpret_cast<int*>(wsp(W.meta));
+    int* row_of_route = reinterpret_cast<int*>(wsp(W.row_of_route));
+    int* route_of_row = reinterpret_cast<int*>(wsp(W.route_of_row));
+    int* tile_expert = reinterpret_cast<int*>(wsp(W.tile_expert));
+    const bool det = (flags & MOE_FINALIZE_DETERMINISTIC) != 0;
+    const bool on_input = (flags & MOE_ROUTER_W_ON_INPUT) != 0;
+    const int act = act_of(flags);
+    const int N1 = n1_of(s.I, flags);
+    float* y_acc = det ? nullptr : reinterpret_cast<float*>(wsp(W.y_acc));
+
+    LaunchCtx c;
+    c.stream = static_cast<cudaStream_t>(stream);
+    c.pdl = true;
+    cudaError_t e;
+
+    e = launch_router(c, s.T, s.E, s.K, router_logits, router_bias, (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1, ids,
+                      topk_w, status);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_permute(c, s.T, s.E, s.K, ids, reinterpret_cast<int*>(wsp(W.unit_base)),
+                       reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
+                       reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert, row_of_route, route_of_row,
+                       status);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // ---- W4A4 ----
+    const bool per_token = mode == kModePerToken;
+    float* g1 = reinterpret_cast<float*>(wsp(W.g1));
+    uint8_t* xq_codes = wsp(W.xq_codes);
+    uint8_t* xq_sf = wsp(W.xq_sf);
+    uint8_t* hq_codes = wsp(W.hq_codes);
+    uint8_t* hq_sf = wsp(W.hq_sf);
+    e = launch_quantize_x(c, s.T, s.H, s.K, x_bf16, act_scale_fc1, per_token ? 1 : 0, g1, row_of_route, xq_codes,
+                          xq_sf, y_acc);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    CUtensorMap tmA1, tmB1, tmA2, tmB2;
+    if (!encode_operand_map(&tmA1, xq_codes, W.rows_cap, (uint64_t)s.H / 2) ||
+        !encode_operand_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2) ||
+        !encode_operand_map(&tmA2, hq_codes, W.rows_cap, (uint64_t)s.I / 2) ||
+        !encode_operand_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2))
+        return MOE_ERR_CUDA;
+
+    GemmParams g1p{};
+    g1p.sfa = xq_sf;
+    g1p.sfb = pw + P.w1_sf;
+    g1p.kdim = s.H;
+    g1p.n = N1;
+    g1p.meta = meta;
+    g1p.tile_expert = tile_expert;
+    g1p.route_of_row = route_of_row;
+    g1p.num_experts = s.E;
+    g1p.status = status;
+    g1p.act = act;
+    g1p.topk = s.K;
+    g1p.gw = reinterpret_cast<const float*>(pw + P.gw1);
+    g1p.topk_w = topk_w;
+    g1p.weight_on_input = on_input ? 1 : 0;
+    g1p.out_cols = s.I;
+    int epi1;
+    if (per_token) {
+        g1p.g_act = g1;
+        g1p.g_act_per_token = 1;
+        g1p.out_f32 = reinterpret_cast<float*>(wsp(W.h_f32));
+        epi1 = kEpiFc1F32;
+    } else {
+        g1p.g_act = act_scale_fc1;
+        g1p.g_act_per_token = 0;
+        g1p.g2 = act_scale_fc2;
+        g1p.out_codes = hq_codes;
+        g1p.out_sf = hq_sf;
+        epi1 = kEpiFc1Quant;
+    }
+    e = launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (per_token) {
+        e = launch_quantize_h(c, W.rows_cap, s.I, meta, route_of_row, reinterpret_cast<const float*>(wsp(W.h_f32)),
+                              reinterpret_cast<float*>(wsp(W.g2)), hq_codes, hq_sf);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+
+    GemmParams g2p{};
+    g2p.sfa = hq_sf;
+    g2p.sfb = pw + P.w2_sf;
+    g2p.kdim = s.I;
+    g2p.n = s.H;
+    g2p.meta = meta;
+    g2p.tile_expert = tile_expert;
+    g2p.route_of_row = route_of_row;
+    g2p.num_experts = s.E;
+    g2p.status = status;
+    g2p.act = act;
+    g2p.topk = s.K;
+    g2p.gw = reinterpret_cast<const float*>(pw + P.gw2);
+    g2p.topk_w = topk_w;
+    g2p.weight_on_output = on_input ? 0 : 1;
+    g2p.out_cols = s.H;
+    if (per_token) {
+        g2p.g_act = reinterpret_cast<const float*>(wsp(W.g2));
+        g2p.g_act_per_token = 2;
+    } else {
+        g2p.g_act = act_scale_fc2;
+        g2p.g_act_per_token = 0;
+    }
+    int epi2;
+    if (det) {
+        g2p.out_bf16 = reinterpret_cast<__nv_bfloat16*>(wsp(W.o_bf16));
+        epi2 = kEpiFc2Store;
+    } else {
+        g2p.out_f32 = y_acc;
+        epi2 = kEpiFc2Scatter;
+    }
+    e = launch_gemm_nvf4(c, epi2, tmA2, tmB2, g2p, sms);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    if (det)
+        e = launch_finalize_deterministic(c, s.T, s.H, s.K, row_of_route, topk_w, on_input ? 0 : 1, wsp(W.o_bf16),
+                                          y_bf16);
+    else
+        e = launch_finalize_fused(c, s.T, s.H, y_acc, y_bf16);
+    return cuda_status(e);
+}
+
+moe_status moe_nvfp4_last_device_status(void* workspace, void* stream) {
+    if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word & (kStatusTimeoutProducer | kStatusTimeoutMma | kStatusTimeoutEpilogue)) return MOE_ERR_TIMEOUT;
+    if (word & (kStatusBadExpert | kStatusBadRow)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status moe_nvfp4_debug_convert(const float* in, int64_t n, uint8_t* e4m3, uint8_t* e2m1, void* stream) {
+    if (n < 0 || (n > 0 && (!in || !e4m3 || !e2m1))) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    int sms = 0;
+    const moe_status st = device_state(&sms);
+    if (st != MOE_OK) return st;
+    return cuda_status(launch_debug_convert(static_cast<cudaStream_t>(stream), in, n, e4m3, e2m1));
+}
+
+}  // extern "C"

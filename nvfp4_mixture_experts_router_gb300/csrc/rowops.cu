@@ -1,0 +1,367 @@
+// Row-parallel kernels around the grouped GEMMs: NVFP4 quantization of x
+// (scattered straight into the permuted rows), per-row quantization of the
+// FC2 input (per-token mode), the W4A16 gather, both finalize variants and
+// weight preparation.  All of them are HBM-bound: one warp per row, 16-byte
+// vector loads and stores, lanes on consecutive 16-element blocks.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ void load16_bf16(const __nv_bfloat16* p, float (&v)[16]) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
+    const uint4 b = *reinterpret_cast<const uint4*>(p + 8);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ void load16_f32(const float* p, float (&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 q = reinterpret_cast<const float4*>(p)[i];
+        v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+    }
+}
+
+// Four consecutive lanes hold the scales of four consecutive blocks; the
+// first of them gets the packed 32-bit word (byte j%4 = scale of block j).
+__device__ __forceinline__ uint32_t pack_sf4(uint32_t s) {
+    const uint32_t s1 = __shfl_down_sync(0xffffffffu, s, 1);
+    const uint32_t s2 = __shfl_down_sync(0xffffffffu, s, 2);
+    const uint32_t s3 = __shfl_down_sync(0xffffffffu, s, 3);
+    return s | (s1 << 8) | (s2 << 16) | (s3 << 24);
+}
+
+__device__ __forceinline__ void zero_row_f32(float* p, int n, int lane) {
+    for (int c = lane * 4; c < n; c += 128) *reinterpret_cast<float4*>(p + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+}  // namespace
+
+// x [T][H] BF16 -> NVFP4 codes/scales written to each of the token's K
+// permuted rows.  Per-token mode derives G1 = amax/2688 from the row.
+__global__ void __launch_bounds__(256) quantize_x_kernel(int T, int H, int K, const __nv_bfloat16* __restrict__ x,
+                                                         const float* __restrict__ g1_in, int per_token,
+                                                         float* __restrict__ g1_out,
+                                                         const int* __restrict__ row_of_route,
+                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                         float* __restrict__ y_acc_zero) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const __nv_bfloat16* xr = x + (size_t)t * H;
+    float G;
+    if (per_token) {
+        float amax = 0.0f;
+        for (int c = lane * 16; c < H; c += 512) {
+            float v[16];
+            load16_bf16(xr + c, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        }
+        G = global_scale_from_amax(warp_max(amax));
+        if (lane == 0) g1_out[t] = G;
+    } else {
+        G = __ldg(g1_in);
+    }
+    const int my_row = lane < K ? row_of_route[(size_t)t * K + lane] : 0;
+    for (int base = 0; base < H; base += 512) {
+        const int c = base + lane * 16;
+        const bool active = c < H;
+        float v[16];
+        uint32_t q[2] = {0u, 0u};
+        uint32_t s = 0;
+        if (active) {
+            load16_bf16(xr + c, v);
+            s = quant_block16(v, G, q);
+        }
+        const uint32_t word = pack_sf4(s);
+        for (int k = 0; k < K; ++k) {
+            const int row = __shfl_sync(0xffffffffu, my_row, k);
+            if (active) {
+                *reinterpret_cast<uint2*>(codes + (size_t)row * (H / 2) + c / 2) = make_uint2(q[0], q[1]);
+                if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(row, c / 16, H)) = word;
+            }
+        }
+    }
+    if (y_acc_zero) zero_row_f32(y_acc_zero + (size_t)t * H, H, lane);
+    pdl_launch_dependents();
+}
+
+// W4A16: copy each token's BF16 row to its K permuted rows.
+__global__ void __launch_bounds__(256) gather_x_bf16_kernel(int T, int H, int K, const __nv_bfloat16* __restrict__ x,
+                                                            const int* __restrict__ row_of_route,
+                                                            __nv_bfloat16* __restrict__ x_perm,
+                                                            float* __restrict__ y_acc_zero) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    const int my_row = lane < K ? row_of_route[(size_t)t * K + lane] : 0;
+    for (int base = 0; base < H / 8; base += 32) {
+        const int c = base + lane;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (c < H / 8) v = src[c];
+        for (int k = 0; k < K; ++k) {
+            const int row = __shfl_sync(0xffffffffu, my_row, k);
+            if (c < H / 8) reinterpret_cast<uint4*>(x_perm + (size_t)row * H)[c] = v;
+        }
+    }
+    if (y_acc_zero) zero_row_f32(y_acc_zero + (size_t)t * H, H, lane);
+    pdl_launch_dependents();
+}
+
+// Per-token W4A4: FC2 input row (FP32) -> G2 = amax/2688, NVFP4 codes/scales.
+__global__ void __launch_bounds__(256) quantize_h_kernel(int I, const int* __restrict__ meta,
+                                                         const int* __restrict__ route_of_row,
+                                                         const float* __restrict__ h, float* __restrict__ g2,
+                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= meta[0] || route_of_row[row] < 0) return;
+    const float* hr = h + (size_t)row * I;
+    float amax = 0.0f;
+    for (int c = lane * 16; c < I; c += 512) {
+        float v[16];
+        load16_f32(hr + c, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const float G = global_scale_from_amax(warp_max(amax));
+    if (lane == 0) g2[row] = G;
+    for (int base = 0; base < I; base += 512) {
+        const int c = base + lane * 16;
+        const bool active = c < I;
+        float v[16];
+        uint32_t q[2] = {0u, 0u};
+        uint32_t s = 0;
+        if (active) {
+            load16_f32(hr + c, v);
+            s = quant_block16(v, G, q);
+        }
+        const uint32_t word = pack_sf4(s);
+        if (active) {
+            *reinterpret_cast<uint2*>(codes + (size_t)row * (I / 2) + c / 2) = make_uint2(q[0], q[1]);
+            if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(row, c / 16, I)) = word;
+        }
+    }
+    pdl_launch_dependents();
+}
+
+// Deterministic finalize: y[t] = BF16( sum_k w'_k * o[row(t,k)] ), k in
+// ascending order, FP32 accumulation; w' = router weight (output side) or 1.
+__global__ void __launch_bounds__(128) finalize_det_kernel(int T, int H, int K, const int* __restrict__ row_of_route,
+                                                           const float* __restrict__ topk_w, int weight_on_output,
+                                                           const __nv_bfloat16* __restrict__ o,
+                                                           __nv_bfloat16* __restrict__ y) {
+    pdl_wait();
+    const int t = blockIdx.x;
+    for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < K; ++k) {
+            const int row = row_of_route[(size_t)t * K + k];
+            const float w = weight_on_output ? topk_w[(size_t)t * K + k] : 1.0f;
+            const uint4 v = reinterpret_cast<const uint4*>(o + (size_t)row * H)[c];
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(w, __uint_as_float(u[i] << 16), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(w, __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
+            }
+        }
+        uint32_t out[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+            out[i] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        reinterpret_cast<uint4*>(y + (size_t)t * H)[c] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+    pdl_launch_dependents();
+}
+
+// Fused finalize tail: the FC2 epilogue accumulated y in FP32; round to BF16.
+__global__ void __launch_bounds__(256) finalize_fused_kernel(int64_t n8, const float* __restrict__ y_acc,
+                                                             __nv_bfloat16* __restrict__ y) {
+    pdl_wait();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 a = reinterpret_cast<const float4*>(y_acc)[2 * i];
+        const float4 b = reinterpret_cast<const float4*>(y_acc)[2 * i + 1];
+        const __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
+        const __nv_bfloat162 p2 = __floats2bfloat162_rn(b.x, b.y), p3 = __floats2bfloat162_rn(b.z, b.w);
+        reinterpret_cast<uint4*>(y)[i] =
+            make_uint4(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1),
+                       *reinterpret_cast<const uint32_t*>(&p2), *reinterpret_cast<const uint32_t*>(&p3));
+    }
+    pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// weight preparation
+// ---------------------------------------------------------------------------
+__global__ void prep_zero_kernel(uint32_t* amax_bits, int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) amax_bits[i] = 0u;
+}
+
+// blockIdx.y = expert, blockIdx.z = matrix (0: W1, 1: W2); grid-stride chunks.
+__global__ void __launch_bounds__(256) prep_amax_kernel(int E, int64_t n1, int64_t n2,
+                                                        const __nv_bfloat16* __restrict__ w1,
+                                                        const __nv_bfloat16* __restrict__ w2,
+                                                        uint32_t* __restrict__ amax_bits) {
+    const int e = blockIdx.y, which = blockIdx.z;
+    const int64_t n = which ? n2 : n1;
+    const __nv_bfloat16* w = which ? w2 + (size_t)e * n2 : w1 + (size_t)e * n1;
+    float m = 0.0f;
+    for (int64_t i = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) * 8; i < n; i += (int64_t)gridDim.x * blockDim.x * 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(w + i);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[k] << 16)), fabsf(__uint_as_float(u[k] & 0xFFFF0000u))));
+    }
+    m = warp_max(m);
+    __shared__ float s_m[8];
+    if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = 0.0f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) b = fmaxf(b, s_m[i]);
+        atomicMax(amax_bits + which * E + e, __float_as_uint(b));   // non-negative: uint order = float order
+    }
+}
+
+__global__ void prep_scales_kernel(int E, const uint32_t* __restrict__ amax_bits, float* __restrict__ gw1,
+                                   float* __restrict__ gw2) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < 2 * E) {
+        const float G = global_scale_from_amax(__uint_as_float(amax_bits[i]));
+        if (i < E) gw1[i] = G;
+        else gw2[i - E] = G;
+    }
+}
+
+// One warp per weight row (W1 rows first, then W2 rows).
+__global__ void __launch_bounds__(256) prep_quant_kernel(int E, int N1, int H, int I, int act,
+                                                         const __nv_bfloat16* __restrict__ w1,
+                                                         const __nv_bfloat16* __restrict__ w2,
+                                                         const float* __restrict__ gw1, const float* __restrict__ gw2,
+                                                         uint8_t* __restrict__ w1c, uint8_t* __restrict__ w1s,
+                                                         uint8_t* __restrict__ w2c, uint8_t* __restrict__ w2s) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gr = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t rows1 = (int64_t)E * N1, rows2 = (int64_t)E * H;
+    if (gr >= rows1 + rows2) return;
+    const bool first = gr < rows1;
+    const int64_t r = first ? gr : gr - rows1;
+    const int Nrows = first ? N1 : H;
+    const int Kd = first ? H : I;
+    const int e = (int)(r / Nrows), rr = (int)(r % Nrows);
+    const __nv_bfloat16* src = first ? w1 + (size_t)r * H : w2 + (size_t)r * I;
+    const float G = first ? gw1[e] : gw2[e];
+    const int prow = first ? prepared_w1_row(rr, I, act) : rr;
+    uint8_t* codes = first ? w1c + (size_t)e * N1 * (H / 2) : w2c + (size_t)e * H * (I / 2);
+    uint8_t* sf = first ? w1s + (size_t)e * N1 * (H / 16) : w2s + (size_t)e * H * (I / 16);
+    for (int base = 0; base < Kd; base += 512) {
+        const int c = base + lane * 16;
+        const bool active = c < Kd;
+        float v[16];
+        uint32_t q[2] = {0u, 0u};
+        uint32_t s = 0;
+        if (active) {
+            load16_bf16(src + c, v);
+            s = quant_block16(v, G, q);
+        }
+        const uint32_t word = pack_sf4(s);
+        if (active) {
+            *reinterpret_cast<uint2*>(codes + (size_t)prow * (Kd / 2) + c / 2) = make_uint2(q[0], q[1]);
+            if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(prow, c / 16, Kd)) = word;
+        }
+    }
+}
+
+__global__ void debug_convert_kernel(const float* __restrict__ in, int64_t n, uint8_t* __restrict__ e4m3,
+                                     uint8_t* __restrict__ e2m1) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = in[i];
+        uint16_t r;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+        e4m3[i] = (uint8_t)(r & 0xFF);
+        e2m1[i] = (uint8_t)(f32x2_to_e2m1x2(v, 0.0f) & 0xF);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_quantize_x(const LaunchCtx& c, int T, int H, int K, const void* x, const float* g1_in,
+                              int per_token, float* g1_out, const int* row_of_route, uint8_t* codes, uint8_t* sf,
+                              float* y_acc_zero) {
+    return c.launch(quantize_x_kernel, dim3((T + 7) / 8), dim3(256), 0, T, H, K,
+                    (const __nv_bfloat16*)x, g1_in, per_token, g1_out, row_of_route, codes, sf, y_acc_zero);
+}
+
+cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const void* x, const int* row_of_route,
+                                 void* x_perm, float* y_acc_zero) {
+    return c.launch(gather_x_bf16_kernel, dim3((T + 7) / 8), dim3(256), 0, T, H, K, (const __nv_bfloat16*)x,
+                    row_of_route, (__nv_bfloat16*)x_perm, y_acc_zero);
+}
+
+cudaError_t launch_quantize_h(const LaunchCtx& c, uint64_t rows_cap, int I, const int* meta,
+                              const int* route_of_row, const float* h, float* g2, uint8_t* codes, uint8_t* sf) {
+    return c.launch(quantize_h_kernel, dim3((unsigned)((rows_cap + 7) / 8)), dim3(256), 0, I, meta, route_of_row, h,
+                    g2, codes, sf);
+}
+
+cudaError_t launch_finalize_deterministic(const LaunchCtx& c, int T, int H, int K, const int* row_of_route,
+                                          const float* topk_w, int weight_on_output, const void* o, void* y) {
+    return c.launch(finalize_det_kernel, dim3(T), dim3(128), 0, T, H, K, row_of_route, topk_w, weight_on_output,
+                    (const __nv_bfloat16*)o, (__nv_bfloat16*)y);
+}
+
+cudaError_t launch_finalize_fused(const LaunchCtx& c, int T, int H, const float* y_acc, void* y) {
+    const int64_t n8 = (int64_t)T * H / 8;
+    int64_t blocks = (n8 + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    return c.launch(finalize_fused_kernel, dim3((unsigned)blocks), dim3(256), 0, n8, y_acc, (__nv_bfloat16*)y);
+}
+
+cudaError_t launch_prepare(cudaStream_t s, int E, int N1, int H, int I, int act, const void* w1, const void* w2,
+                           uint8_t* prepared, uint64_t gw1, uint64_t gw2, uint64_t w1c, uint64_t w1s, uint64_t w2c,
+                           uint64_t w2s) {
+    // per-matrix amax words (2E uint32) are kept at the start of the W1 code
+    // region, which the final quantization kernel overwrites afterwards
+    uint32_t* scratch = reinterpret_cast<uint32_t*>(prepared + w1c);
+    prep_zero_kernel<<<(2 * E + 255) / 256, 256, 0, s>>>(scratch, 2 * E);
+    const int64_t n1 = (int64_t)N1 * H, n2 = (int64_t)H * I;
+    int64_t chunks = (n1 / 8 + 255) / 256;
+    if (chunks > 64) chunks = 64;
+    prep_amax_kernel<<<dim3((unsigned)chunks, E, 2), 256, 0, s>>>(E, n1, n2, (const __nv_bfloat16*)w1,
+                                                                  (const __nv_bfloat16*)w2, scratch);
+    prep_scales_kernel<<<(2 * E + 255) / 256, 256, 0, s>>>(E, scratch, reinterpret_cast<float*>(prepared + gw1),
+                                                          reinterpret_cast<float*>(prepared + gw2));
+    const int64_t rows = (int64_t)E * (N1 + H);
+    prep_quant_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+        E, N1, H, I, act, (const __nv_bfloat16*)w1, (const __nv_bfloat16*)w2,
+        reinterpret_cast<const float*>(prepared + gw1), reinterpret_cast<const float*>(prepared + gw2),
+        prepared + w1c, prepared + w1s, prepared + w2c, prepared + w2s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_convert(cudaStream_t s, const float* in, int64_t n, uint8_t* e4m3, uint8_t* e2m1) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 8192) blocks = 8192;
+    if (blocks < 1) blocks = 1;
+    debug_convert_kernel<<<(unsigned)blocks, 256, 0, s>>>(in, n, e4m3, e2m1);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

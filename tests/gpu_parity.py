@@ -1,0 +1,184 @@
+"""Shared driver for the GPU parity tests: run one layer configuration
+through the CUDA library (C ABI) and through the CPU oracle on the same
+seeded inputs, and compare every stage.
+
+Acceptance (stated once, used everywhere):
+  * bit-exact: expert ids, counts, offsets, padded offsets, the permutation
+    (row_of_route, route_of_row, M-tile -> expert map), the NVFP4 codes and
+    scales of x (and the per-token G1), the prepared weight codes/scales/G.
+  * router weights: |w - w_ref| <= 2e-6 * w_ref + 1e-7 (float32 expf vs FP64).
+  * FC2-input codes: >= 99.9 % of E2M1 codes identical (accumulation order
+    may move a value across a rounding boundary).
+  * y: max |y - y_ref| <= 2e-2 * rms(y_ref).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+import oracle
+from nvfp4_mixture_experts_router_gb300 import api, synth
+
+Y_TOL = 2e-2
+CODE_MATCH = 0.999
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def sf_rowmajor(buf: np.ndarray, rows: Sequence[int], cols: int) -> np.ndarray:
+    """Scales of the given rows, row-major [len(rows), cols/16], read from a
+    buffer in the 512-byte atom layout [rows/128][cols/64][512]."""
+    r = np.asarray(rows, dtype=np.int64)[:, None]
+    j = np.arange(cols // 16, dtype=np.int64)[None, :]
+    off = ((r >> 7) * (cols >> 6) + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3)
+    return buf[off]
+
+
+def nibbles(codes: np.ndarray) -> np.ndarray:
+    return np.stack([codes & 15, codes >> 4], axis=-1).reshape(codes.shape[0], -1)
+
+
+def canonical_w1_rows(N1: int, I: int, swiglu: bool) -> np.ndarray:
+    """prepared row -> checkpoint row of FC1 (inverse of the gate/up interleave)."""
+    p = np.arange(N1)
+    if not swiglu:
+        return p
+    tile, within = p // 128, p % 128
+    up = within >= 64
+    j = tile * 64 + (within % 64)
+    return np.where(up, I + j, j)
+
+
+@dataclass
+class Inputs:
+    c: synth.MoEConfig
+    x: torch.Tensor            # device BF16 [T, H]
+    logits: torch.Tensor       # device FP32 [T, E]
+    bias: Optional[torch.Tensor]
+    w1: torch.Tensor           # device BF16 [E, N1, H]
+    w2: torch.Tensor           # device BF16 [E, H, I]
+    x_np: np.ndarray
+    logits_np: np.ndarray
+    bias_np: Optional[np.ndarray]
+    w1_np: np.ndarray
+    w2_np: np.ndarray
+
+
+def make_inputs(c: synth.MoEConfig, device="cuda") -> Inputs:
+    x = synth.gen_x(c, device)
+    logits = synth.gen_logits(c, device, x)
+    bias = synth.gen_bias(c, device)
+    w1 = synth.gen_w1(c, device)
+    w2 = synth.gen_w2(c, device)
+    return Inputs(c, x, logits, bias, w1, w2, bits(x), logits.cpu().numpy(),
+                  None if bias is None else bias.cpu().numpy(), bits(w1), bits(w2))
+
+
+def oracle_layer(c: synth.MoEConfig) -> oracle.Layer:
+    return oracle.Layer(c.H, c.I, c.E, c.K, act=c.act, mode=c.mode, router_on_input=c.router_on_input,
+                        renorm=c.renorm)
+
+
+def scales_for(inp: Inputs, tokens=None):
+    """Per-tensor calibration (oracle): G1 over all of x, G2 over the FC2
+    inputs of the given tokens."""
+    c = inp.c
+    if c.mode != synth.MODE_PER_TENSOR:
+        return None, None
+    G1 = oracle.tensor_global_scale(oracle.bf16_bits_to_f64(inp.x_np).astype(np.float32))
+    G2 = oracle.fc2_input_scale(oracle_layer(c), inp.x_np, inp.logits_np, inp.bias_np,
+                                lambda e: (inp.w1_np[e], inp.w2_np[e]), G1, tokens=tokens)
+    return np.float32(G1), np.float32(G2)
+
+
+def run_gpu(inp: Inputs, G1, G2):
+    c = inp.c
+    layer = api.MoELayer.create(c.T, c.H, c.I, c.E, c.K, c.flags())
+    layer.prepare(inp.w1, inp.w2)
+    g1 = None if G1 is None else torch.tensor([G1], dtype=torch.float32, device="cuda")
+    g2 = None if G2 is None else torch.tensor([G2], dtype=torch.float32, device="cuda")
+    y = layer.forward(inp.x, inp.logits, inp.bias, g1, g2)
+    torch.cuda.synchronize()
+    assert api.moe_nvfp4_last_device_status(layer.workspace) == api.MOE_OK
+    return layer, y
+
+
+def check_routing(layer: api.MoELayer, ref: oracle.Result):
+    T, K, E = layer.T, layer.K, layer.E
+    ids = layer.view("topk_ids", torch.int32, T * K).cpu().numpy().reshape(T, K)
+    w = layer.view("topk_w", torch.float32, T * K).cpu().numpy().reshape(T, K)
+    assert np.array_equal(ids, ref.ids), "expert ids differ"
+    assert np.all(np.abs(w - ref.w) <= 2e-6 * ref.w + 1e-7), f"router weights: max err {np.abs(w - ref.w).max()}"
+    g = ref.grouping
+    assert np.array_equal(layer.view("count", torch.int32, E).cpu().numpy(), g.count)
+    assert np.array_equal(layer.view("offsets", torch.int32, E + 1).cpu().numpy(), g.offsets)
+    assert np.array_equal(layer.view("padded_offsets", torch.int32, E + 1).cpu().numpy(), g.padded_offsets)
+    meta = layer.view("meta", torch.int32, 4).cpu().numpy()
+    assert meta[0] == g.rows and meta[1] == g.rows // 128
+    ror = layer.view("row_of_route", torch.int32, T * K).cpu().numpy()
+    assert np.array_equal(ror, g.row_of_route), "row_of_route differs"
+    rrow = layer.view("route_of_row", torch.int32, g.rows).cpu().numpy()
+    assert np.array_equal(rrow, g.route_of_row[:g.rows]), "route_of_row differs"
+    tiles = layer.view("tile_expert", torch.int32, g.rows // 128).cpu().numpy()
+    want = np.repeat(np.arange(E), (g.padded_offsets[1:] - g.padded_offsets[:-1]) // 128)
+    assert np.array_equal(tiles, want), "tile -> expert map differs"
+    return ror
+
+
+def check_x_quant(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray):
+    T, K, H = layer.T, layer.K, layer.H
+    lay = layer.layout()
+    cap = lay["rows_cap"]
+    codes = layer.view("xq_codes", torch.uint8, cap * H // 2).cpu().numpy().reshape(cap, H // 2)
+    sfbuf = layer.view("xq_sf", torch.uint8, cap * H // 16).cpu().numpy()
+    toks = ref.tokens
+    for k in range(K):
+        rows = ror.reshape(T, K)[toks, k]
+        assert np.array_equal(codes[rows], ref.x_codes), f"x codes differ (slot {k})"
+        assert np.array_equal(sf_rowmajor(sfbuf, rows, H), ref.x_sf), f"x scales differ (slot {k})"
+    if layer.flags & api.MOE_W4A4_PER_TOKEN:
+        g1 = layer.view("g1", torch.float32, T).cpu().numpy()[toks]
+        assert np.array_equal(g1, ref.G1), "per-token G1 differs"
+
+
+def check_fc2_input(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray) -> float:
+    if (layer.flags & (3 << 2)) == api.MOE_W4A16:
+        return 1.0
+    I = layer.I
+    cap = layer.layout()["rows_cap"]
+    codes = layer.view("hq_codes", torch.uint8, cap * I // 2).cpu().numpy().reshape(cap, I // 2)
+    routes = sorted(ref.h_codes)
+    rows = ror[routes]
+    got = nibbles(codes[rows])
+    want = nibbles(np.stack([ref.h_codes[r] for r in routes]))
+    frac = float(np.mean(got == want))
+    assert frac >= CODE_MATCH, f"FC2-input codes: only {frac:.5f} identical"
+    return frac
+
+
+def check_y(y: torch.Tensor, ref: oracle.Result) -> float:
+    yg = y.float().cpu().numpy()[ref.tokens].astype(np.float64)
+    rms = float(np.sqrt(np.mean(ref.y64 ** 2)))
+    err = float(np.max(np.abs(yg - ref.y64)))
+    assert np.isfinite(yg).all(), "non-finite output"
+    assert err <= Y_TOL * rms, f"max|y - y_ref| = {err:.4g} > {Y_TOL} * rms {rms:.4g}"
+    return err / rms
+
+
+def full_parity(c: synth.MoEConfig, tokens=None):
+    inp = make_inputs(c)
+    G1, G2 = scales_for(inp, tokens)
+    layer, y = run_gpu(inp, G1, G2)
+    ref = oracle.forward(oracle_layer(c), inp.x_np, inp.logits_np, inp.bias_np,
+                         lambda e: (inp.w1_np[e], inp.w2_np[e]), G1=G1, G2=G2, tokens=tokens)
+    ror = check_routing(layer, ref)
+    if c.mode != synth.MODE_W4A16:
+        check_x_quant(layer, ref, ror)
+    frac = check_fc2_input(layer, ref, ror)
+    rel = check_y(y, ref)
+    return dict(code_match=frac, y_rel_err=rel, layer=layer, y=y, ref=ref, inp=inp)

@@ -1,0 +1,129 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle,
+stage by stage, on seeded inputs; acceptance rules in tests/gpu_parity.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from nvfp4_mixture_experts_router_gb300 import api, build, synth
+
+from gpu_parity import (bits, canonical_w1_rows, full_parity, make_inputs, nibbles, run_gpu, scales_for,
+                        sf_rowmajor)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    api.lib()
+
+
+def test_device_conversions_match_oracle():
+    """cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32 vs the oracle's converters over
+    a float32 sweep (all exponents, midpoints and their neighbours)."""
+    hi = np.arange(1 << 24, dtype=np.uint32)[::7] << 8
+    pats = np.concatenate([hi, hi | 1, hi | 0xFF])
+    f = pats.view(np.float32)
+    f = f[np.isfinite(f)]
+    e4, e2 = api.moe_nvfp4_debug_convert(torch.from_numpy(f).cuda())
+    torch.cuda.synchronize()
+    want4 = oracle.f32_to_e4m3(f)
+    want2 = oracle.f32_to_e2m1(f)
+    got4, got2 = e4.cpu().numpy(), e2.cpu().numpy()
+    bad4 = np.nonzero(got4 != want4)[0]
+    bad2 = np.nonzero(got2 != want2)[0]
+    assert bad4.size == 0, (f[bad4[:8]], got4[bad4[:8]], want4[bad4[:8]])
+    assert bad2.size == 0, (f[bad2[:8]], got2[bad2[:8]], want2[bad2[:8]])
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_prepare_weights_matches_oracle(act):
+    c = synth.MoEConfig("prep", 4, 384, 256, 3, 2, act=act, seed=9)
+    inp = make_inputs(c)
+    layer = api.MoELayer.create(c.T, c.H, c.I, c.E, c.K, c.flags())
+    layer.prepare(inp.w1, inp.w2)
+    torch.cuda.synchronize()
+    buf = layer.prepared.cpu().numpy()
+    reg = layer.prepared_regions()
+    N1, H, I, E = c.N1, c.H, c.I, c.E
+    gw1 = buf[reg["gw1"][0]:reg["gw1"][0] + 4 * E].view(np.float32)
+    gw2 = buf[reg["gw2"][0]:reg["gw2"][0] + 4 * E].view(np.float32)
+    canon = canonical_w1_rows(N1, I, act == 0)
+    for e in range(E):
+        p1 = oracle.prepare_matrix(inp.w1_np[e])
+        p2 = oracle.prepare_matrix(inp.w2_np[e])
+        assert gw1[e] == p1.G and gw2[e] == p2.G
+        o = reg["w1_codes"][0] + e * N1 * H // 2
+        c1 = buf[o:o + N1 * H // 2].reshape(N1, H // 2)
+        assert np.array_equal(c1, p1.codes[canon])
+        o = reg["w1_sf"][0] + e * N1 * H // 16
+        assert np.array_equal(sf_rowmajor(buf[o:o + N1 * H // 16], np.arange(N1), H), p1.sf[canon])
+        o = reg["w2_codes"][0] + e * H * I // 2
+        assert np.array_equal(buf[o:o + H * I // 2].reshape(H, I // 2), p2.codes)
+        o = reg["w2_sf"][0] + e * H * I // 16
+        assert np.array_equal(sf_rowmajor(buf[o:o + H * I // 16], np.arange(H), I), p2.sf)
+
+
+def test_tiny_config_parity():
+    """configs: tiny W4A4 (T=16, H=256, I=128, E=8, top-2, SwiGLU, per-tensor,
+    output-side weight, fused finalize)."""
+    r = full_parity(synth.config(0))
+    assert r["code_match"] >= 0.999
+
+
+MATRIX = []
+for T, H, I, E, K in [(1, 256, 128, 8, 2), (7, 384, 256, 8, 2), (129, 256, 128, 8, 1), (40, 256, 256, 1, 1),
+                      (200, 384, 128, 16, 4)]:
+    for mode in (synth.MODE_PER_TENSOR, synth.MODE_PER_TOKEN):
+        for act in (0, 1):
+            for on_input in (False, True):
+                for det in (False, True):
+                    MATRIX.append((T, H, I, E, K, mode, act, on_input, det))
+
+
+@pytest.mark.parametrize("T,H,I,E,K,mode,act,on_input,det", MATRIX)
+def test_matrix_parity(T, H, I, E, K, mode, act, on_input, det):
+    """Token count x activation x placement x finalize x scaling mode x top-K
+    x experts (the axes of the wrapper accuracy matrix, FlashInfer PR #4366,
+    "Tests"), small shapes with partial tiles, H=384 and empty experts."""
+    seed = (T * 31 + H + I + E * 7 + K * 3 + mode * 11 + act * 5 + on_input * 2 + det) % 1000
+    c = synth.MoEConfig("m", T, H, I, E, K, act=act, mode=mode, router_on_input=on_input, deterministic=det,
+                        seed=seed, logits="normal")
+    full_parity(c)
+
+
+def test_mid_config_parity():
+    """configs: mid W4A4 (T=512, H=2048, I=768, E=64, top-6, per-token,
+    router weight on input, logit bias skew)."""
+    full_parity(synth.config(1))
+
+
+def test_deterministic_finalize_is_bitwise_reproducible():
+    c = synth.MoEConfig("det", 300, 256, 128, 16, 4, deterministic=True, seed=5, logits="normal")
+    inp = make_inputs(c)
+    G1, G2 = scales_for(inp)
+    layer, y0 = run_gpu(inp, G1, G2)
+    g1 = torch.tensor([G1], device="cuda")
+    g2 = torch.tensor([G2], device="cuda")
+    for _ in range(5):
+        y = layer.forward(inp.x, inp.logits, inp.bias, g1, g2)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+
+
+def test_all_tokens_to_one_expert():
+    """Degenerate routing: a huge bias sends every token to experts 3 and 5."""
+    c = synth.MoEConfig("skew", 300, 256, 128, 8, 2, mode=synth.MODE_PER_TOKEN, seed=3, logits="normal")
+    inp = make_inputs(c)
+    inp.bias = torch.zeros(8, device="cuda")
+    inp.bias[3] = 100.0
+    inp.bias[5] = 90.0
+    inp.bias_np = inp.bias.cpu().numpy()
+    layer, y = run_gpu(inp, None, None)
+    ref = oracle.forward(oracle.Layer(c.H, c.I, c.E, c.K, mode=c.mode), inp.x_np, inp.logits_np, inp.bias_np,
+                         lambda e: (inp.w1_np[e], inp.w2_np[e]))
+    from gpu_parity import check_routing, check_y
+    check_routing(layer, ref)
+    check_y(y, ref)
+    assert (ref.grouping.count[[3, 5]] == 300).all()
