@@ -9,7 +9,15 @@ Acceptance (stated once, used everywhere):
   * router weights: |w - w_ref| <= 2e-6 * w_ref + 1e-7 (float32 expf vs FP64).
   * FC2-input codes: >= 99.9 % of E2M1 codes identical (accumulation order
     may move a value across a rounding boundary).
-  * y: max |y - y_ref| <= 2e-2 * rms(y_ref).
+  * y: |y - y_ref| <= 2e-2 * rms(y_ref) + ulp_bf16(y_ref)/2 + slack_t per
+    element, y_ref the oracle's FP64 output.  The half ulp is the rounding
+    of the BF16 output itself (for outliers beyond ~8x the RMS it alone
+    exceeds 2e-2 * rms).  slack_t is zero unless a route of token t has an
+    FC2 input that differs from the oracle's (a code moved across a
+    rounding boundary, which the 99.9 % rule admits); then it is the exact
+    worst-case effect of that difference on the output:
+        sum_k w'_k * Gw2 * sum_j |a_gpu_j*G2_gpu - a_ref_j*G2_ref| * max_n |W2q[n,j]|
+    with W2q the oracle's dequantized FC2 weight of the route's expert.
 """
 from __future__ import annotations
 
@@ -146,39 +154,86 @@ def check_x_quant(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray):
         assert np.array_equal(g1, ref.G1), "per-token G1 differs"
 
 
-def check_fc2_input(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray) -> float:
+def ulp_bf16(v: np.ndarray) -> np.ndarray:
+    a = np.maximum(np.abs(v), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def _e2m1_values(n: np.ndarray) -> np.ndarray:
+    mag = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    return mag[n & 7] * np.where(n & 8, -1.0, 1.0)
+
+
+def _e4m3_values(b: np.ndarray) -> np.ndarray:
+    e, m = (b >> 3) & 15, b & 7
+    return np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * 2.0 ** (e.astype(np.float64) - 7))
+
+
+def check_fc2_input(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray, G2, prepared: dict):
+    """FC2-input code identity and the per-token output slack of the routes
+    whose FC2 input differs (see module docstring)."""
+    n_tok = len(ref.tokens)
+    slack = np.zeros(n_tok)
     if (layer.flags & (3 << 2)) == api.MOE_W4A16:
-        return 1.0
-    I = layer.I
+        return 1.0, slack
+    I, K = layer.I, layer.K
     cap = layer.layout()["rows_cap"]
     codes = layer.view("hq_codes", torch.uint8, cap * I // 2).cpu().numpy().reshape(cap, I // 2)
+    sfbuf = layer.view("hq_sf", torch.uint8, cap * I // 16).cpu().numpy()
+    per_token = bool(layer.flags & api.MOE_W4A4_PER_TOKEN)
+    g2_gpu = layer.view("g2", torch.float32, cap).cpu().numpy() if per_token else None
     routes = sorted(ref.h_codes)
     rows = ror[routes]
     got = nibbles(codes[rows])
     want = nibbles(np.stack([ref.h_codes[r] for r in routes]))
     frac = float(np.mean(got == want))
     assert frac >= CODE_MATCH, f"FC2-input codes: only {frac:.5f} identical"
-    return frac
+    got_sf = sf_rowmajor(sfbuf, rows, I)
+    pos = {int(t): i for i, t in enumerate(ref.tokens)}
+    colmax = {}
+    for i, r in enumerate(routes):
+        g2g = float(g2_gpu[rows[i]]) if per_token else float(G2)
+        g2r = float(ref.G2[r])
+        same = np.array_equal(got[i], want[i]) and np.array_equal(got_sf[i], ref.h_sf[r]) and g2g == g2r
+        if same:
+            continue
+        t, k = divmod(r, K)
+        e = int(ref.ids[t, k])
+        if e not in colmax:
+            colmax[e] = np.abs(prepared[e][2]).max(axis=0)
+        sg = np.repeat(_e4m3_values(got_sf[i]), 16)
+        sr = np.repeat(_e4m3_values(ref.h_sf[r]), 16)
+        d = np.abs(_e2m1_values(got[i]) * sg * g2g - _e2m1_values(want[i]) * sr * g2r)
+        wk = 1.0 if layer.flags & api.MOE_ROUTER_W_ON_INPUT else float(ref.w[t, k])
+        slack[pos[t]] += wk * prepared[e][3] * float(np.dot(d, colmax[e]))
+    return frac, slack
 
 
-def check_y(y: torch.Tensor, ref: oracle.Result) -> float:
+def check_y(y: torch.Tensor, ref: oracle.Result, slack=None) -> float:
     yg = y.float().cpu().numpy()[ref.tokens].astype(np.float64)
-    rms = float(np.sqrt(np.mean(ref.y64 ** 2)))
-    err = float(np.max(np.abs(yg - ref.y64)))
     assert np.isfinite(yg).all(), "non-finite output"
-    assert err <= Y_TOL * rms, f"max|y - y_ref| = {err:.4g} > {Y_TOL} * rms {rms:.4g}"
-    return err / rms
+    rms = float(np.sqrt(np.mean(ref.y64 ** 2)))
+    tol = Y_TOL * rms + 0.5 * ulp_bf16(ref.y64)
+    if slack is not None:
+        tol = tol + slack[:, None] * (1 + 1e-6)
+    err = np.abs(yg - ref.y64)
+    bad = np.argwhere(err > tol)
+    assert bad.size == 0, (f"{len(bad)} outputs out of tolerance; worst err/rms "
+                           f"{float(np.max(err / rms)):.4g} at token {ref.tokens[bad[0][0]]}")
+    return float(np.max(err) / rms)
 
 
 def full_parity(c: synth.MoEConfig, tokens=None):
     inp = make_inputs(c)
     G1, G2 = scales_for(inp, tokens)
     layer, y = run_gpu(inp, G1, G2)
+    prepared = {}
     ref = oracle.forward(oracle_layer(c), inp.x_np, inp.logits_np, inp.bias_np,
-                         lambda e: (inp.w1_np[e], inp.w2_np[e]), G1=G1, G2=G2, tokens=tokens)
+                         lambda e: (inp.w1_np[e], inp.w2_np[e]), G1=G1, G2=G2, tokens=tokens, prepared=prepared)
     ror = check_routing(layer, ref)
     if c.mode != synth.MODE_W4A16:
         check_x_quant(layer, ref, ror)
-    frac = check_fc2_input(layer, ref, ror)
-    rel = check_y(y, ref)
-    return dict(code_match=frac, y_rel_err=rel, layer=layer, y=y, ref=ref, inp=inp)
+    frac, slack = check_fc2_input(layer, ref, ror, G2, prepared)
+    rel = check_y(y, ref, slack)
+    return dict(code_match=frac, y_rel_err=rel, layer=layer, y=y, ref=ref, inp=inp,
+                flipped_tokens=int(np.sum(slack > 0)))

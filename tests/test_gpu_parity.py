@@ -125,5 +125,5 @@ def test_all_tokens_to_one_expert():
                          lambda e: (inp.w1_np[e], inp.w2_np[e]))
     from gpu_parity import check_routing, check_y
     check_routing(layer, ref)
-    check_y(y, ref)
+    check_y(y, ref, None)
     assert (ref.grouping.count[[3, 5]] == 300).all()
