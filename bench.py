@@ -1,0 +1,523 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 MoE layer forward (libmoe_nvfp4.so, C ABI).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mid|tiny|dsv3|w4a16|prefill] [--tokens T]
+
+A step is one full layer forward (router, permutation, activation
+quantization, FC1 + activation + requantization, FC2, finalize) over one
+batch of T synthetic tokens.  Default workload: the mid configuration
+(T=512, H=2048, I=768, E=64, top-6, SwiGLU, W4A4 per-token scales, router
+weight on the FC2 input, fused finalize).
+
+Prints one JSON line (rank 0).  `value` is whole-job tokens/s with inputs
+resident in HBM; L2 is defeated by rotating several copies of the prepared
+weights (together larger than the 129 MB L2) across steps.  `e2e` is the same
+metric through the C ABI with each step's x and logits copied from pinned
+host memory and y copied back inside the timed region.  `roofline` is the
+dominant kernel's algorithmic bytes (or FLOPs) per launch over its mean
+CUDA-event duration.  Multi-GPU: independent replicas (one per rank, no
+collective on the data path), weak scaling.
+
+--impl reference times the CPU oracle (oracle/, plain C++ FP64) on the host
+cores on a bounded token sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s and NVFP4 TFLOPS (% of GB300 dense FP4 peak) vs tokens"
+L2_BYTES = 129 * 1024 * 1024
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense-rate ratio used to scale the measured bf16 peak
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="mid", choices=["tiny", "mid", "dsv3", "w4a16", "prefill"])
+    p.add_argument("--tokens", type=int, default=None, help="token count (sweeps of dsv3 / w4a16)")
+    p.add_argument("--stage-steps", type=int, default=200)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def workload_config(name, tokens):
+    from nvfp4_mixture_experts_router_gb300 import synth
+    idx = {"tiny": 0, "mid": 1, "dsv3": 2, "w4a16": 3, "prefill": 4}[name]
+    return synth.config(idx, tokens)
+
+
+def describe(c):
+    from nvfp4_mixture_experts_router_gb300 import synth
+    act = "SwiGLU" if c.act == synth.ACT_SWIGLU else "ReLU2"
+    mode = {0: "W4A4 per-tensor", 1: "W4A4 per-token", 2: "W4A16"}[c.mode]
+    place = "router weight on FC2 input" if c.router_on_input else "router weight at output"
+    fin = "deterministic finalize" if c.deterministic else "fused finalize"
+    return f"{c.name}: T={c.T}, H={c.H}, I={c.I}, E={c.E}, top-{c.K}, {act}, {mode}, {place}, {fin}"
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def flops_per_step(c):
+    R = c.T * c.K
+    return 2.0 * R * (c.N1 * c.H + c.I * c.H)
+
+
+def stage_bytes(c, active):
+    """Algorithmic bytes per launch of each stage (minimum HBM traffic)."""
+    from nvfp4_mixture_experts_router_gb300 import synth
+    T, H, I, E, K, N1 = c.T, c.H, c.I, c.E, c.K, c.N1
+    R = T * K
+    nv = 0.5625                                  # NVFP4: 0.5 B code + 1/16 B scale per element
+    w4a16 = c.mode == synth.MODE_W4A16
+    per_token = c.mode == synth.MODE_PER_TOKEN
+    a_elem = 2.0 if w4a16 else nv
+    h_out = 2.0 if w4a16 else (4.0 if per_token else nv)
+    fused = not c.deterministic
+    return {
+        "router": T * E * 4 + T * K * 8 + (E * 4 if c.bias != "none" else 0),
+        "permute": T * K * 4 * 4,
+        "quantize_x": T * H * 2 + R * H * a_elem + (T * H * 4 if fused else 0),
+        "fc1": active * N1 * H * nv + R * H * a_elem + R * I * h_out,
+        "quantize_h": (R * I * 4 + R * I * nv) if per_token else 0,
+        "fc2": active * H * I * nv + R * I * (2.0 if w4a16 else nv) + (T * H * 4 if fused else R * H * 2),
+        "finalize": (T * H * 4 + T * H * 2) if fused else (R * H * 2 + T * H * 2),
+    }
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    e = d.get(f"{workload}:{kernel}")
+    if not e:
+        return None
+    if e.get("source_sha") != source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_mixture_experts_router_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        def reader():
+            for line in self.proc.stdout:
+                self.samples.append((time.time(), line.strip()))
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        time.sleep(1.0)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = [s for t, s in self.samples if t0 - 0.1 <= t <= t1 + 0.1]
+        if not rows:
+            # nearest samples around a very short region
+            rows = [s for t, s in sorted(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[:2]]
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        mhz.sort()
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def init_dist(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+
+class OracleRunner:
+    """The oracle on host cores, weights prepared once (untimed)."""
+
+    def __init__(self, c, device):
+        import numpy as np
+        import torch
+        import oracle
+        from nvfp4_mixture_experts_router_gb300 import synth
+        self.np, self.oracle, self.c = np, oracle, c
+        self.layer = oracle.Layer(c.H, c.I, c.E, c.K, act=c.act, mode=c.mode, router_on_input=c.router_on_input,
+                                  renorm=c.renorm)
+        x = synth.gen_x(c, device)
+        self.x_np = x.cpu().view(torch.int16).numpy().view(np.uint16)
+        self.logits = synth.gen_logits(c, device, x).cpu().numpy()
+        b = synth.gen_bias(c, device)
+        self.bias = None if b is None else b.cpu().numpy()
+        self.dev = device
+        self.prepared = {}
+        self.G1 = self.G2 = None
+        if c.mode == synth.MODE_PER_TENSOR:
+            self.G1 = oracle.tensor_global_scale(oracle.bf16_bits_to_f64(self.x_np).astype(np.float32))
+            self.G2 = np.float32(self.G1)          # any positive scale: the arithmetic done is the same
+
+    def weights(self, e):
+        import torch
+        from nvfp4_mixture_experts_router_gb300 import synth
+        w1 = synth.gen_w1_expert(self.c, e, self.dev).cpu().view(torch.int16).numpy().view(self.np.uint16)
+        w2 = synth.gen_w2_expert(self.c, e, self.dev).cpu().view(torch.int16).numpy().view(self.np.uint16)
+        return w1, w2
+
+    def prepare_for(self, tokens):
+        ids, _ = self.oracle.router(self.logits, self.bias, self.c.K, self.c.renorm)
+        need = sorted(set(int(e) for t in tokens for e in ids[t]))
+        for e in need:
+            if e not in self.prepared:
+                self.prepared[e] = self.oracle.prepare_expert(self.layer, self.weights, e)
+
+    def run(self, tokens):
+        return self.oracle.forward(self.layer, self.x_np, self.logits, self.bias, self.weights, G1=self.G1,
+                                   G2=self.G2, tokens=tokens, prepared=self.prepared)
+
+
+def cpu_cores():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except Exception:
+        n = os.cpu_count() or 1
+    return int(os.environ.get("OMP_NUM_THREADS", n))
+
+
+def cpu_baseline(c, device, budget_s=15.0):
+    from nvfp4_mixture_experts_router_gb300 import synth
+    r = OracleRunner(c, device)
+    probe = synth.sample_tokens(c, min(4, c.T))
+    r.prepare_for(probe)
+    t0 = time.perf_counter()
+    r.run(probe)
+    per_tok = (time.perf_counter() - t0) / len(probe)
+    n = max(1, min(c.T, int(budget_s / max(per_tok, 1e-6))))
+    toks = synth.sample_tokens(c, n)
+    r.prepare_for(toks)
+    t0 = time.perf_counter()
+    r.run(toks)
+    dt = time.perf_counter() - t0
+    return {"value": round(len(toks) / dt, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{len(toks)} of the workload's {c.T} tokens (seeded subset), all their routes; "
+                      f"expert weights prepared by the oracle beforehand (untimed)"}
+
+
+def run_reference(args, c, world, rank):
+    if rank != 0:
+        return
+    import torch
+    from nvfp4_mixture_experts_router_gb300 import synth
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    r = OracleRunner(c, device)
+    # per-step sample sized so that warmup + steps fit in about two minutes
+    probe = synth.sample_tokens(c, 1)
+    r.prepare_for(probe)
+    t0 = time.perf_counter()
+    r.run(probe)
+    per_tok = max(time.perf_counter() - t0, 1e-4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = max(1, min(c.T, int(budget / per_tok)))
+    samples = [synth.sample_tokens(c.with_(seed=c.seed), n)]
+    toks = samples[0]
+    r.prepare_for(toks)
+    for _ in range(args.warmup):
+        r.run(toks)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r.run(toks)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1000 * dt / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64 (oracle, NVFP4 emulated)", "data": "synthetic",
+           "config": {"workload": describe(c), "tokens_per_step": n},
+           "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                            "sample": f"{n} token(s) of the workload per step, weights prepared untimed"},
+           "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, c, world, rank, local):
+    import torch
+    import torch.distributed as dist
+    from nvfp4_mixture_experts_router_gb300 import api, build, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+    api.lib()
+
+    flags = c.flags()
+    s = api.shape(c.T, c.H, c.I, c.E, c.K)
+    x = synth.gen_x(c, dev)
+    logits = synth.gen_logits(c, dev, x)
+    bias = synth.gen_bias(c, dev)
+    g1 = g2 = None
+    if c.mode == synth.MODE_PER_TENSOR:
+        g1 = (x.float().abs().max() / 2688.0).reshape(1).contiguous()          # calibration of the FC1 input
+
+    # prepared weights: enough copies that consecutive steps miss in L2
+    pb = api.moe_nvfp4_prepared_bytes(s, flags)
+    n_sets = max(1, min(8, math.ceil(3 * L2_BYTES / pb) if pb < 3 * L2_BYTES else 1))
+    layer = api.MoELayer.create(c.T, c.H, c.I, c.E, c.K, flags, device=dev)
+    w1 = synth.gen_w1(c, dev)
+    w2 = synth.gen_w2(c, dev)
+    preps = []
+    for i in range(n_sets):
+        buf = torch.empty(pb, dtype=torch.uint8, device=dev)
+        api.moe_nvfp4_prepare_weights(s, flags, w1, w2, buf)
+        preps.append(buf)
+    torch.cuda.synchronize()
+    del w1, w2
+    if c.mode == synth.MODE_PER_TENSOR:
+        # FC2-input calibration from a per-token pass of the library itself
+        tok = api.MoELayer.create(c.T, c.H, c.I, c.E, c.K, (flags & ~(3 << 2)) | api.MOE_W4A4_PER_TOKEN, dev)
+        tok.prepared = preps[0]
+        tok.forward(x, logits, bias)
+        cap = tok.layout()["rows_cap"]
+        g2 = (tok.view("g2", torch.float32, cap)[:int(tok.view("meta", torch.int32, 4)[0])].max()).reshape(1)
+        g2 = g2.contiguous()
+        del tok
+    y = torch.empty(c.T, c.H, dtype=torch.bfloat16, device=dev)
+    ws = layer.workspace
+
+    def step(i, yy=y, xx=x, ll=logits):
+        api.moe_nvfp4_forward(s, flags, xx, ll, bias, g1, g2, preps[i % n_sets], ws, yy)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    status = api.moe_nvfp4_last_device_status(ws)
+    if status != api.MOE_OK:
+        raise RuntimeError(f"device status {api.STATUS_NAMES.get(status)} after warm-up")
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record()
+    for i in range(args.steps):
+        step(i)
+    ev1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if rank == 0:
+        clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * c.T * args.steps / (ms / 1000.0)
+
+    # per-stage durations (stage events; programmatic dependent launch off)
+    nst = min(args.stage_steps, max(args.steps, 1))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(api.NUM_STAGE_EVENTS)] for _ in range(nst)]
+    for i in range(nst):
+        api.moe_nvfp4_forward_staged(s, flags, x, logits, bias, g1, g2, preps[i % n_sets], ws, y, evs[i])
+    torch.cuda.synchronize()
+    stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(nst)) / nst
+                for j, name in enumerate(api.STAGES)}
+    count = layer.view("count", torch.int32, c.E).cpu()
+    active = int((count > 0).sum())
+    sbytes = stage_bytes(c, active)
+
+    # end to end: host x/logits -> device, forward, y -> host, every step
+    n_host = 2
+    hx = [x.cpu().pin_memory() for _ in range(n_host)]
+    hl = [logits.cpu().pin_memory() for _ in range(n_host)]
+    hy = [torch.empty(c.T, c.H, dtype=torch.bfloat16).pin_memory() for _ in range(n_host)]
+    dx = torch.empty_like(x)
+    dl = torch.empty_like(logits)
+    e2e_steps = args.steps
+    for i in range(min(args.warmup, 5)):
+        dx.copy_(hx[i % n_host], non_blocking=True)
+        dl.copy_(hl[i % n_host], non_blocking=True)
+        step(i, y, dx, dl)
+        hy[i % n_host].copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e2e_steps):
+        dx.copy_(hx[i % n_host], non_blocking=True)
+        dl.copy_(hl[i % n_host], non_blocking=True)
+        step(i, y, dx, dl)
+        hy[i % n_host].copy_(y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * c.T * e2e_steps / (e2e_ms / 1000.0)
+    h2d = c.T * c.H * 2 + c.T * c.E * 4
+    d2h = c.T * c.H * 2
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    hbm, bf16, bf16s, peak_src = measured_peaks()
+    fp4_peak = bf16 * FP4_OVER_BF16
+    flops = flops_per_step(c)
+    dom = max(stage_ms, key=lambda k: stage_ms[k])
+    dom_ms = stage_ms[dom]
+    if dom in ("fc1", "fc2"):
+        # GEMM: report the bound that limits it at this shape
+        gemm_flops = 2.0 * c.T * c.K * c.H * (c.N1 if dom == "fc1" else c.I)
+        t_flop = gemm_flops / (fp4_peak * 1e12)
+        t_byte = sbytes[dom] / (hbm * 1e9)
+        bound = "tensor" if t_flop > t_byte else "hbm"
+    else:
+        bound = "hbm"
+        gemm_flops = 0.0
+    if bound == "hbm":
+        achieved = sbytes[dom] / (dom_ms / 1000.0) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": traffic_for(dom, args.workload),
+                "kernel": dom, "algorithmic_bytes_per_launch": int(sbytes[dom]),
+                "mean_launch_us": round(dom_ms * 1000, 2), "peak_source": f"{peak_src} hbm_gbs"}
+    else:
+        achieved = gemm_flops / (dom_ms / 1000.0) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / fp4_peak, 4), "traffic": traffic_for(dom, args.workload),
+                "kernel": dom, "algorithmic_flops_per_launch": gemm_flops,
+                "mean_launch_us": round(dom_ms * 1000, 2),
+                "peak_source": f"{peak_src} bf16_tflops x {FP4_OVER_BF16:g} (nominal fp4/bf16 ratio)"}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        try:
+            cpu = cpu_baseline(c, dev)
+        except Exception as ex:   # the baseline must not sink the GPU line
+            cpu = {"value": None, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                   "sample": f"failed: {type(ex).__name__}: {ex}"}
+
+    tflops = flops / (ms_per_step / 1000.0) / 1e12
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3/16) -> f32",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": describe(c), "T": c.T, "H": c.H, "I": c.I, "E": c.E, "K": c.K,
+                   "l2": f"inputs larger than L2: {n_sets} prepared-weight copies "
+                         f"({n_sets * pb / 1e6:.0f} MB) rotated across steps",
+                   "parallelism": f"replicas x{world}"},
+        "tflops": round(tflops, 2), "pct_fp4_peak": round(100 * tflops / fp4_peak, 3),
+        "fp4_peak_tflops": round(fp4_peak, 1),
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": api.moe_nvfp4_forward_launches(s, flags) * args.steps,
+        "roofline": roof,
+        "stages_us": {k: round(v * 1000, 2) for k, v in stage_ms.items()},
+        "stage_gbs": {k: round(sbytes[k] / (stage_ms[k] / 1000) / 1e9, 1) for k in stage_ms if stage_ms[k] > 0},
+        "active_experts": active,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    world, rank, local = init_dist(args)
+    c = workload_config(args.workload, args.tokens)
+    if args.impl == "reference":
+        run_reference(args, c, world, rank)
+    else:
+        run_ours(args, c, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

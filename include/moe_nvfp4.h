@@ -156,6 +156,29 @@ MOE_API moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags,
                              void* workspace, size_t workspace_bytes,
                              void* y_bf16, void* stream);
 
+/* Same as moe_nvfp4_forward, and records caller-created CUDA events
+ * (cudaEvent_t, created with timing enabled) on `stream` at the stage
+ * boundaries, for per-stage timing:
+ *   events[0] before the router, [1] after the router, [2] after the
+ *   permutation, [3] after the activation quantization (W4A4) or gather
+ *   (W4A16), [4] after FC1, [5] after the FC2-input quantization (recorded
+ *   right after [4] when the mode has none), [6] after FC2, [7] after the
+ *   finalize.  MOE_NUM_STAGE_EVENTS events, none NULL.
+ * The recordings serialize the stages (no programmatic dependent launch),
+ * so the sum of the stages can exceed the plain forward's time. */
+#define MOE_NUM_STAGE_EVENTS 8
+MOE_API moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags,
+                                            const void* x_bf16, const float* router_logits,
+                                            const float* router_bias,
+                                            const float* act_scale_fc1, const float* act_scale_fc2,
+                                            const void* prepared,
+                                            void* workspace, size_t workspace_bytes,
+                                            void* y_bf16, void* stream, void* const* events);
+
+/* Number of kernel launches one moe_nvfp4_forward enqueues for this shape
+ * and flags (-1 if invalid).  Pure host call. */
+MOE_API int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags);
+
 /* Byte offsets of the intermediates inside the workspace (for tests and
  * debugging; MOE_WORKSPACE_VERSION).  Each entry is 256-byte aligned.
  * rows_cap = the padded-row capacity (a multiple of 128).               */

@@ -72,6 +72,9 @@ def lib():
             "moe_nvfp4_workspace_bytes": (sz, [S, u32]),
             "moe_nvfp4_workspace_layout": (ctypes.c_int, [S, u32, ctypes.POINTER(moe_workspace_layout)]),
             "moe_nvfp4_forward": (ctypes.c_int, [S, u32, P, P, P, P, P, P, P, sz, P, P]),
+            "moe_nvfp4_forward_staged": (ctypes.c_int, [S, u32, P, P, P, P, P, P, P, sz, P, P,
+                                                        ctypes.POINTER(ctypes.c_void_p)]),
+            "moe_nvfp4_forward_launches": (ctypes.c_int, [S, u32]),
             "moe_nvfp4_last_device_status": (ctypes.c_int, [P, P]),
             "moe_nvfp4_debug_convert": (ctypes.c_int, [P, i64, P, P, P]),
         }
@@ -85,7 +88,11 @@ def lib():
 
 EXPORTED = ["moe_nvfp4_version", "moe_nvfp4_prepared_bytes", "moe_nvfp4_prepare_weights",
             "moe_nvfp4_workspace_bytes", "moe_nvfp4_workspace_layout", "moe_nvfp4_forward",
+            "moe_nvfp4_forward_staged", "moe_nvfp4_forward_launches",
             "moe_nvfp4_last_device_status", "moe_nvfp4_debug_convert"]
+EXPORTED.sort()
+NUM_STAGE_EVENTS = 8
+STAGES = ["router", "permute", "quantize_x", "fc1", "quantize_h", "fc2", "finalize"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -142,6 +149,22 @@ def moe_nvfp4_forward(s: moe_shape, flags: int, x_bf16: torch.Tensor, router_log
                                    _ptr(act_scale_fc1), _ptr(act_scale_fc2), _ptr(prepared), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _ptr(y_bf16), _stream(stream))
     _check("moe_nvfp4_forward", code)
+
+
+def moe_nvfp4_forward_staged(s: moe_shape, flags: int, x_bf16, router_logits, router_bias, act_scale_fc1,
+                             act_scale_fc2, prepared, workspace, y_bf16, events, stream=None) -> None:
+    """Forward that records the torch.cuda.Event objects ``events``
+    (NUM_STAGE_EVENTS, timing enabled) at the stage boundaries."""
+    arr = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
+    code = lib().moe_nvfp4_forward_staged(s, flags, _ptr(x_bf16), _ptr(router_logits), _ptr(router_bias),
+                                          _ptr(act_scale_fc1), _ptr(act_scale_fc2), _ptr(prepared),
+                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _ptr(y_bf16), _stream(stream), arr)
+    _check("moe_nvfp4_forward_staged", code)
+
+
+def moe_nvfp4_forward_launches(s: moe_shape, flags: int) -> int:
+    return int(lib().moe_nvfp4_forward_launches(s, flags))
 
 
 def moe_nvfp4_last_device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -140,10 +140,10 @@ moe_status moe_nvfp4_prepare_weights(moe_shape s, uint32_t flags, const void* w1
                                       L.w2_codes, L.w2_sf));
 }
 
-moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags, const void* x_bf16, const float* router_logits,
-                             const float* router_bias, const float* act_scale_fc1, const float* act_scale_fc2,
-                             const void* prepared, void* workspace, size_t workspace_bytes, void* y_bf16,
-                             void* stream) {
+static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, const float* router_logits,
+                               const float* router_bias, const float* act_scale_fc1, const float* act_scale_fc2,
+                               const void* prepared, void* workspace, size_t workspace_bytes, void* y_bf16,
+                               void* stream, void* const* events) {
     moe_status st = validate_shape(s, flags);
     if (st != MOE_OK) return st;
     const int mode = mode_of(flags);
@@ -187,17 +187,22 @@ moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags, const void* x_bf16, co
 
     LaunchCtx c;
     c.stream = static_cast<cudaStream_t>(stream);
-    c.pdl = true;
+    c.pdl = events == nullptr;   // stage events between kernels would serialize them anyway
     cudaError_t e;
+    auto mark = [&](int i) -> bool {
+        return events == nullptr ||
+               cudaEventRecord(static_cast<cudaEvent_t>(events[i]), c.stream) == cudaSuccess;
+    };
+    if (!mark(0)) return MOE_ERR_CUDA;
 
     e = launch_router(c, s.T, s.E, s.K, router_logits, router_bias, (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1, ids,
                       topk_w, status);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (e != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
     e = launch_permute(c, s.T, s.E, s.K, ids, reinterpret_cast<int*>(wsp(W.unit_base)),
                        reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
                        reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert, row_of_route, route_of_row,
                        status);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (e != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
 
     // ---- W4A4 ----
     const bool per_token = mode == kModePerToken;
@@ -208,7 +213,7 @@ moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags, const void* x_bf16, co
     uint8_t* hq_sf = wsp(W.hq_sf);
     e = launch_quantize_x(c, s.T, s.H, s.K, x_bf16, act_scale_fc1, per_token ? 1 : 0, g1, row_of_route, xq_codes,
                           xq_sf, y_acc);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (e != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
     if (!encode_operand_map(&tmA1, xq_codes, W.rows_cap, (uint64_t)s.H / 2) ||
@@ -248,12 +253,13 @@ moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags, const void* x_bf16, co
         epi1 = kEpiFc1Quant;
     }
     e = launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (e != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
     if (per_token) {
         e = launch_quantize_h(c, W.rows_cap, s.I, meta, route_of_row, reinterpret_cast<const float*>(wsp(W.h_f32)),
                               reinterpret_cast<float*>(wsp(W.g2)), hq_codes, hq_sf);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
+    if (!mark(5)) return MOE_ERR_CUDA;
 
     GemmParams g2p{};
     g2p.sfa = hq_sf;
@@ -287,14 +293,40 @@ moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags, const void* x_bf16, co
         epi2 = kEpiFc2Scatter;
     }
     e = launch_gemm_nvf4(c, epi2, tmA2, tmB2, g2p, sms);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (e != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
 
     if (det)
         e = launch_finalize_deterministic(c, s.T, s.H, s.K, row_of_route, topk_w, on_input ? 0 : 1, wsp(W.o_bf16),
                                           y_bf16);
     else
         e = launch_finalize_fused(c, s.T, s.H, y_acc, y_bf16);
-    return cuda_status(e);
+    if (e != cudaSuccess || !mark(7)) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags, const void* x_bf16, const float* router_logits,
+                             const float* router_bias, const float* act_scale_fc1, const float* act_scale_fc2,
+                             const void* prepared, void* workspace, size_t workspace_bytes, void* y_bf16,
+                             void* stream) {
+    return forward_impl(s, flags, x_bf16, router_logits, router_bias, act_scale_fc1, act_scale_fc2, prepared,
+                        workspace, workspace_bytes, y_bf16, stream, nullptr);
+}
+
+moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags, const void* x_bf16, const float* router_logits,
+                                    const float* router_bias, const float* act_scale_fc1,
+                                    const float* act_scale_fc2, const void* prepared, void* workspace,
+                                    size_t workspace_bytes, void* y_bf16, void* stream, void* const* events) {
+    if (!events) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < MOE_NUM_STAGE_EVENTS; ++i)
+        if (!events[i]) return MOE_ERR_INVALID_ARG;
+    return forward_impl(s, flags, x_bf16, router_logits, router_bias, act_scale_fc1, act_scale_fc2, prepared,
+                        workspace, workspace_bytes, y_bf16, stream, events);
+}
+
+int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags) {
+    if (validate_shape(s, flags) != MOE_OK) return -1;
+    // router, 3 permutation kernels, quantize/gather, FC1, [FC2-input quant], FC2, finalize
+    return 8 + (mode_of(flags) == kModePerToken ? 1 : 0);
 }
 
 moe_status moe_nvfp4_last_device_status(void* workspace, void* stream) {
