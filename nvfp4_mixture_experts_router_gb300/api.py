@@ -155,6 +155,9 @@ def moe_nvfp4_forward_staged(s: moe_shape, flags: int, x_bf16, router_logits, ro
                              act_scale_fc2, prepared, workspace, y_bf16, events, stream=None) -> None:
     """Forward that records the torch.cuda.Event objects ``events``
     (NUM_STAGE_EVENTS, timing enabled) at the stage boundaries."""
+    for ev in events:
+        if not ev.cuda_event:       # torch creates the CUDA event lazily, on its first record
+            ev.record(stream)
     arr = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
     code = lib().moe_nvfp4_forward_staged(s, flags, _ptr(x_bf16), _ptr(router_logits), _ptr(router_bias),
                                           _ptr(act_scale_fc1), _ptr(act_scale_fc2), _ptr(prepared),

@@ -9,15 +9,20 @@
 // [FlashInfer PR #4366, "Tests": padding and partial tiles], so every M tile
 // belongs to exactly one expert (tile_expert).
 //
-// Kernel design (one persistent CTA per SM, 192 threads):
+// Kernel design (one persistent CTA per SM, 224 threads):
 //   warp 0      TMA producer: per pipeline stage one 128x128-byte A tile and
 //               one 128x128-byte B tile (cp.async.bulk.tensor, 128-byte
 //               swizzle) plus the matching 2 KB of scale atoms of each
 //               operand (cp.async.bulk), all completing on one mbarrier.
+//   warp 6      scale mover: once a stage has landed, tcgen05.cp of its 8
+//               scale atoms into the stage's tensor-memory slot, then
+//               tcgen05.commit to the stage's sf_ready barrier.
 //   warp 1      allocates 512 tensor-memory columns; lane 0 issues, per
-//               stage, tcgen05.cp of the scale atoms into tensor memory and
-//               four 128x128x64 block-scaled MMAs into an FP32 accumulator
-//               in tensor memory, then tcgen05.commit frees the stage.
+//               stage, four 128x128x64 block-scaled MMAs into an FP32
+//               accumulator in tensor memory, then tcgen05.commit frees the
+//               stage.  (The tcgen05 issue slot of a single thread is the
+//               scarce resource at these tile sizes, so the scale copies are
+//               issued from another warp.)
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp w reads lanes
 //               32*(w%4)..+31, one output row per thread), fused activation /
 //               scaling / requantization / scatter, then release the buffer.
@@ -40,7 +45,7 @@ constexpr int kStages = 6;
 constexpr int kTileBytesA = kBM * kBKBytes;   // 16 KB
 constexpr int kTileBytesB = kBN * kBKBytes;   // 16 KB
 constexpr int kSfBytes = 4 * 512;             // 4 scale atoms (128 rows x 64 elems each)
-constexpr int kNumThreads = 192;
+constexpr int kNumThreads = 224;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 128;
 constexpr uint32_t kSfColBase = 256;          // columns 256.. hold the per-stage scales
@@ -60,6 +65,7 @@ struct Smem {
     uint64_t* acc_full;
     uint64_t* acc_empty;
     uint64_t* drain;
+    uint64_t* sf_ready;
     uint32_t* tmem_holder;
     volatile int* abort;
 };
@@ -77,7 +83,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     s.acc_full = bars + 2 * kStages;
     s.acc_empty = s.acc_full + 2;
     s.drain = s.acc_empty + 2;
-    s.tmem_holder = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.sf_ready = s.drain + 1;
+    s.tmem_holder = reinterpret_cast<uint32_t*>(s.sf_ready + kStages);
     s.abort = reinterpret_cast<volatile int*>(s.tmem_holder + 1);
     return s;
 }
@@ -109,8 +116,12 @@ __device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
+                // silu(z) = z / (1 + e^-z).  The ex2-based exponential and a
+                // correctly rounded reciprocal keep the relative error near
+                // 1e-6; the IEEE division + full-range expf path costs ~6x
+                // the epilogue time and made FC1 epilogue-bound.
                 const float zg = h[i] * alpha, zu = u[i] * alpha;
-                h[i] = zg / (1.0f + expf(-zg)) * zu * pw;
+                h[i] = zg * __frcp_rn(1.0f + __expf(-zg)) * zu * pw;
             }
             col0 = n_tile * 64 + ch * 32;
         } else {
@@ -205,7 +216,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(&s.acc_full[i], 1);
             mbar_init(&s.acc_empty[i], 4 * 32);
         }
-        mbar_init(s.drain, 1);
+        mbar_init(s.drain, 2);   // the MMA thread and the scale mover both retire their ops into it
+        for (int i = 0; i < kStages; ++i) mbar_init(&s.sf_ready[i], 1);
         *s.abort = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
@@ -275,10 +287,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const int nkb = min(4, kblocks - 4 * ks);
                     const uint32_t sfa_t = tmem_base + kSfColBase + (uint32_t)stage * kSfColsPerStage;
                     const uint32_t sfb_t = sfa_t + 16;
-                    for (int j = 0; j < nkb; ++j) {
-                        tc_cp_sf_atom(sfa_t + 4 * j, sdesc_sf_atom(smem_u32(s.sfa + stage * kSfBytes + j * 512)));
-                        tc_cp_sf_atom(sfb_t + 4 * j, sdesc_sf_atom(smem_u32(s.sfb + stage * kSfBytes + j * 512)));
-                    }
+                    // the scale mover's copies for this stage have completed
+                    if (!mbar_wait(&s.sf_ready[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                    tc_fence_after();
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(s.a + stage * kTileBytesA));
                     const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(s.b + stage * kTileBytesB));
                     for (int j = 0; j < nkb; ++j) {
@@ -292,6 +303,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 tc_commit(&s.acc_full[acc]);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
+            }
+        }
+    } else if (warp == 6) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+                for (int ks = 0; ks < kstages; ++ks) {
+                    if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                    tc_fence_after();
+                    const int nkb = min(4, kblocks - 4 * ks);
+                    const uint32_t sfa_t = tmem_base + kSfColBase + (uint32_t)stage * kSfColsPerStage;
+                    const uint32_t sfb_t = sfa_t + 16;
+                    for (int j = 0; j < nkb; ++j) {
+                        tc_cp_sf_atom(sfa_t + 4 * j, sdesc_sf_atom(smem_u32(s.sfa + stage * kSfBytes + j * 512)));
+                        tc_cp_sf_atom(sfb_t + 4 * j, sdesc_sf_atom(smem_u32(s.sfb + stage * kSfBytes + j * 512)));
+                    }
+                    tc_commit(&s.sf_ready[stage]);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
             }
         }
     } else {
@@ -319,7 +350,7 @@ done:
     if (*s.abort) {
         // Something timed out: let in-flight copies land and retire every
         // issued MMA before the tensor memory and shared memory go away.
-        if (warp == 1 && lane == 0) {
+        if ((warp == 1 || warp == 6) && lane == 0) {
             tc_commit(s.drain);
             mbar_wait(s.drain, 0, &no_abort, p.status, kStatusTimeoutMma);
         }
