@@ -230,6 +230,48 @@ MOE_API moe_status moe_nvfp4_last_device_status(void* workspace, void* stream);
 MOE_API moe_status moe_nvfp4_debug_convert(const float* in, int64_t n, uint8_t* e4m3,
                                    uint8_t* e2m1, void* stream);
 
+/* ---- routing without any caller-allocated scratch ------------------------- */
+/* No counterpart on the pages: this entry point exists for callers that
+ * cannot allocate device memory (for example code running inside another
+ * engine's fixed memory budget, or a latency-critical loop that must not
+ * call cudaMalloc), yet need the routing stage on its own.
+ *
+ * Runs the router (softmax + top-K, selection and weights as in
+ * moe_nvfp4_forward) and the stable permutation by expert, writing only
+ * into the caller's output buffers (device pointers, 4-byte aligned):
+ *   topk_ids [T*K] int32, topk_w [T*K] f32, count [E], offsets [E+1],
+ *   padded_offsets [E+1] (prefix of the counts rounded up to 128),
+ *   row_of_route [T*K] (padded row of route t*K+k),
+ *   route_of_row [rows_cap] with rows_cap = round_up(T*K + min(E, T*K)*127,
+ *   128) (the workspace layout's rows_cap); entries [0, padded_offsets[E])
+ *   are written (-1 in pad rows), the rest are left untouched.
+ * flags: 0 or MOE_ROUTE_NO_RENORM.  Results are bit-identical to the routing
+ * intermediates moe_nvfp4_forward leaves in its workspace.
+ *
+ * Scratch: a fixed MOE_NOALLOC_SCRATCH_BYTES array in device memory, part of
+ * the library image, which every GPU that loads the library holds until the
+ * process exits.  It allocates nothing (no cudaMalloc/cudaFree, no
+ * allocating library call).  Shapes whose scratch need (8 + rows_cap/128 +
+ * E*ceil(T/32) int32, plus alignment) exceeds the array return
+ * MOE_ERR_WORKSPACE before anything is launched; E = 256 fits up to about
+ * 32 000 tokens.  All calls share the one array (it keeps the last call's
+ * contents; every entry a call reads is written by that call first), so calls
+ * whose work may overlap on the GPU (different streams, or other host
+ * threads) race and must be serialized by the caller.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) and
+ * prepares the kernels; make that first call before any stream capture.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE, MOE_ERR_UNSUPPORTED,
+ * MOE_ERR_CUDA.  Enqueues four kernels on `stream`; does not synchronize. */
+#define MOE_NOALLOC_SCRATCH_BYTES (1 << 20)
+MOE_API moe_status moe_nvfp4_route_noalloc(int T, int E, int K, uint32_t flags,
+                                           const float* router_logits,
+                                           const float* router_bias,
+                                           int32_t* topk_ids, float* topk_w,
+                                           int32_t* count, int32_t* offsets,
+                                           int32_t* padded_offsets,
+                                           int32_t* row_of_route,
+                                           int32_t* route_of_row, void* stream);
+
 /* Library version string, e.g. "moe_nvfp4 1.0 sm_103a". */
 MOE_API const char* moe_nvfp4_version(void);
 

@@ -77,6 +77,8 @@ def lib():
             "moe_nvfp4_forward_launches": (ctypes.c_int, [S, u32]),
             "moe_nvfp4_last_device_status": (ctypes.c_int, [P, P]),
             "moe_nvfp4_debug_convert": (ctypes.c_int, [P, i64, P, P, P]),
+            "moe_nvfp4_route_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, u32, P, P,
+                                                       P, P, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -89,7 +91,7 @@ def lib():
 EXPORTED = ["moe_nvfp4_version", "moe_nvfp4_prepared_bytes", "moe_nvfp4_prepare_weights",
             "moe_nvfp4_workspace_bytes", "moe_nvfp4_workspace_layout", "moe_nvfp4_forward",
             "moe_nvfp4_forward_staged", "moe_nvfp4_forward_launches",
-            "moe_nvfp4_last_device_status", "moe_nvfp4_debug_convert"]
+            "moe_nvfp4_last_device_status", "moe_nvfp4_debug_convert", "moe_nvfp4_route_noalloc"]
 EXPORTED.sort()
 NUM_STAGE_EVENTS = 8
 STAGES = ["router", "permute", "quantize_x", "fc1", "quantize_h", "fc2", "finalize"]
@@ -182,6 +184,20 @@ def moe_nvfp4_debug_convert(x: torch.Tensor, stream=None):
     _check("moe_nvfp4_debug_convert",
            lib().moe_nvfp4_debug_convert(_ptr(x), x.numel(), _ptr(e4), _ptr(e2), _stream(stream)))
     return e4, e2
+
+
+def moe_nvfp4_route_noalloc(T: int, E: int, K: int, flags: int, router_logits: torch.Tensor,
+                            router_bias: Optional[torch.Tensor], out: dict, stream=None) -> None:
+    """Routing + permutation into the caller's buffers, with the library's
+    fixed device scratch instead of a workspace (for callers that cannot
+    allocate device memory).  ``out`` holds int32/float32 CUDA tensors
+    topk_ids, topk_w, count, offsets, padded_offsets, row_of_route,
+    route_of_row (sizes as in include/moe_nvfp4.h)."""
+    code = lib().moe_nvfp4_route_noalloc(T, E, K, flags, _ptr(router_logits), _ptr(router_bias),
+                                         _ptr(out["topk_ids"]), _ptr(out["topk_w"]), _ptr(out["count"]),
+                                         _ptr(out["offsets"]), _ptr(out["padded_offsets"]),
+                                         _ptr(out["row_of_route"]), _ptr(out["route_of_row"]), _stream(stream))
+    _check("moe_nvfp4_route_noalloc", code)
 
 
 # ---- convenience ---------------------------------------------------------------
