@@ -1,0 +1,123 @@
+// Fused GEMM epilogues shared by the NVFP4 (gemm_nvf4.cu) and W4A16
+// (gemm_w4a16.cu) grouped GEMMs.  One thread owns one output row (one
+// tensor-memory lane) and reads 128 FP32 accumulator columns of its tile.
+#pragma once
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// SwiGLU tile: columns 0..63 gate, 64..127 up (prepared-weight interleave);
+// yields 64 FC2-input values.  ReLU2 tile: 128 values.
+template <int EPI>
+__device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr, int row, int route, int e,
+                                             int n_tile) {
+    const int token = route >= 0 ? route / p.topk : 0;
+    const float g_act = p.g_act == nullptr ? 1.0f : (p.g_act_per_token ? p.g_act[token] : p.g_act[0]);
+    const float alpha = __fmul_rn(g_act, p.gw[e]);
+    const float pw = (p.weight_on_input && route >= 0) ? p.topk_w[route] : 1.0f;
+    const bool swiglu = p.act == MOE_ACT_SWIGLU;
+    const int chunks = swiglu ? 2 : 4;
+    const float g2 = (EPI == kEpiFc1Quant) ? p.g2[0] : 1.0f;
+    uint32_t sf_pair[4];
+    for (int ch = 0; ch < chunks; ++ch) {
+        float h[32];
+        int col0;
+        if (swiglu) {
+            float u[32];
+            tmem_ld32(taddr + ch * 32, h);
+            tmem_ld32(taddr + 64 + ch * 32, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                // silu(z) = z / (1 + e^-z).  The ex2-based exponential and a
+                // correctly rounded reciprocal keep the relative error near
+                // 1e-6; the IEEE division + full-range expf path costs ~6x
+                // the epilogue time and made FC1 epilogue-bound.
+                const float zg = h[i] * alpha, zu = u[i] * alpha;
+                h[i] = zg * __frcp_rn(1.0f + __expf(-zg)) * zu * pw;
+            }
+            col0 = n_tile * 64 + ch * 32;
+        } else {
+            tmem_ld32(taddr + ch * 32, h);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float z = fmaxf(h[i] * alpha, 0.0f);
+                h[i] = z * z * pw;
+            }
+            col0 = n_tile * 128 + ch * 32;
+        }
+        if (route < 0) continue;
+        if (EPI == kEpiFc1Quant) {
+            uint32_t q[4];
+            float blk[16];
+            uint32_t c2[2];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) blk[i] = h[i];
+            const uint32_t s0 = quant_block16(blk, g2, c2);
+            q[0] = c2[0]; q[1] = c2[1];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) blk[i] = h[16 + i];
+            const uint32_t s1 = quant_block16(blk, g2, c2);
+            q[2] = c2[0]; q[3] = c2[1];
+            *reinterpret_cast<uint4*>(p.out_codes + (size_t)row * (p.out_cols / 2) + col0 / 2) =
+                make_uint4(q[0], q[1], q[2], q[3]);
+            sf_pair[ch] = s0 | (s1 << 8);
+            // two scales per 32 columns: a 16-bit store at an even scale index
+            *reinterpret_cast<uint16_t*>(p.out_sf + sf_offset(row, col0 / 16, p.out_cols)) = (uint16_t)sf_pair[ch];
+        } else if (EPI == kEpiFc1Bf16) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 b = __floats2bfloat162_rn(h[2 * i], h[2 * i + 1]);
+                w[i] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + (size_t)row * p.out_cols + col0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        } else {
+            float4* dst = reinterpret_cast<float4*>(p.out_f32 + (size_t)row * p.out_cols + col0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+        }
+    }
+}
+
+template <int EPI>
+__device__ __forceinline__ void epilogue_fc2(const GemmParams& p, uint32_t taddr, int row, int route, int e,
+                                             int n_tile) {
+    const float g_act = p.g_act_per_token == 2 ? p.g_act[row] : (p.g_act ? p.g_act[0] : 1.0f);
+    float alpha = __fmul_rn(g_act, p.gw[e]);
+    int token = 0;
+    if (EPI == kEpiFc2Scatter && route >= 0) {
+        token = route / p.topk;
+        if (p.weight_on_output) alpha = alpha * p.topk_w[route];
+    }
+    for (int ch = 0; ch < 4; ++ch) {
+        float o[32];
+        tmem_ld32(taddr + ch * 32, o);
+        tmem_ld_wait();
+        if (route < 0) continue;
+        const int col0 = n_tile * 128 + ch * 32;
+        if (EPI == kEpiFc2Store) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * i] * alpha, o[2 * i + 1] * alpha);
+                w[i] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + (size_t)row * p.out_cols + col0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        } else {
+            float4* dst = reinterpret_cast<float4*>(p.out_f32 + (size_t)token * p.out_cols + col0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                atomicAdd(dst + i, make_float4(o[4 * i] * alpha, o[4 * i + 1] * alpha, o[4 * i + 2] * alpha,
+                                               o[4 * i + 3] * alpha));
+        }
+    }
+}
+
+}  // namespace moe

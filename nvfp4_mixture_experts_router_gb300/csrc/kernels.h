@@ -58,7 +58,8 @@ enum GemmEpilogue : int {
     kEpiFc1Quant = 0,   // FC1: activation, route weight, NVFP4 requant with per-tensor G2
     kEpiFc1F32 = 1,     // FC1: activation, route weight, FP32 store (per-token G2 later)
     kEpiFc2Store = 2,   // FC2: BF16 per-route rows (deterministic finalize)
-    kEpiFc2Scatter = 3  // FC2: weighted FP32 atomic add into the token row (fused finalize)
+    kEpiFc2Scatter = 3, // FC2: weighted FP32 atomic add into the token row (fused finalize)
+    kEpiFc1Bf16 = 4     // FC1 (W4A16): activation, route weight, BF16 store
 };
 
 struct GemmParams {
@@ -86,10 +87,14 @@ struct GemmParams {
     uint8_t* out_codes;          // FC1 quant: [rows_cap][I/2]
     uint8_t* out_sf;             // FC1 quant: [rows_cap/128][I/64][512]
     float* out_f32;              // FC1 F32: [rows_cap][I]; FC2 scatter: y_acc [T][H]
-    __nv_bfloat16* out_bf16;     // FC2 store: [rows_cap][H]
+                                 // (g_act == nullptr: no activation global scale, W4A16)
+    __nv_bfloat16* out_bf16;     // FC2 store: [rows_cap][H]; FC1 BF16: [rows_cap][I]
 };
 
 cudaError_t setup_gemm_kernels();
+cudaError_t setup_gemm_w4a16_kernels();
+cudaError_t launch_gemm_w4a16(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmBq,
+                              const GemmParams& p, int num_sms);
 cudaError_t launch_gemm_nvf4(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              const GemmParams& p, int num_sms);
 

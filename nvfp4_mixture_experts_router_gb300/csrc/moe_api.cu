@@ -41,7 +41,8 @@ moe_status device_state(int* sms) {
             d.status = MOE_ERR_CUDA;
         } else if (major != 10 || minor != 3) {
             d.status = MOE_ERR_UNSUPPORTED;  // the binary carries sm_103a code only
-        } else if (setup_routing_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess) {
+        } else if (setup_routing_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess ||
+                   setup_gemm_w4a16_kernels() != cudaSuccess) {
             d.status = MOE_ERR_CUDA;
         } else {
             d.status = MOE_OK;
@@ -84,15 +85,18 @@ moe_status validate_shape(moe_shape s, uint32_t flags) {
     return MOE_OK;
 }
 
-// 2-D uint8 tensor map over a row-major [rows][row_bytes] array, 128x128
-// boxes, 128-byte swizzle (the canonical K-major UMMA operand layout).
-bool encode_operand_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes) {
+// 2-D uint8 tensor map over a row-major [rows][row_bytes] array with
+// box_bytes x 128-row boxes.  128-byte boxes use the 128-byte swizzle (the
+// canonical K-major UMMA operand layout); narrower boxes are unswizzled.
+bool encode_operand_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes,
+                        uint32_t box_bytes = 128) {
     const cuuint64_t dims[2] = {row_bytes, rows};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {128, 128};
+    const cuuint32_t box[2] = {box_bytes, 128};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -162,7 +166,6 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     if (overlaps(y_bf16, y_bytes, workspace, W.total) || overlaps(y_bf16, y_bytes, x_bf16, y_bytes) ||
         overlaps(y_bf16, y_bytes, router_logits, (size_t)s.T * s.E * 4))
         return MOE_ERR_INVALID_ARG;
-    if (mode == kModeW4A16) return MOE_ERR_UNSUPPORTED;
 
     int sms = 0;
     st = device_state(&sms);
@@ -203,6 +206,70 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
                        reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert, row_of_route, route_of_row,
                        status);
     if (e != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
+
+    if (mode == kModeW4A16) {
+        // ---- W4A16: BF16 activations, weights widened on chip ----
+        __nv_bfloat16* x_perm = reinterpret_cast<__nv_bfloat16*>(wsp(W.x_bf16_perm));
+        __nv_bfloat16* h_bf16 = reinterpret_cast<__nv_bfloat16*>(wsp(W.h_bf16));
+        e = launch_gather_x_bf16(c, s.T, s.H, s.K, x_bf16, row_of_route, x_perm, y_acc);
+        if (e != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
+        CUtensorMap tA1, tB1, tA2, tB2;
+        if (!encode_operand_map(&tA1, x_perm, W.rows_cap, (uint64_t)s.H * 2) ||
+            !encode_operand_map(&tB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 32) ||
+            !encode_operand_map(&tA2, h_bf16, W.rows_cap, (uint64_t)s.I * 2) ||
+            !encode_operand_map(&tB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 32))
+            return MOE_ERR_CUDA;
+        GemmParams a{};
+        a.sfb = pw + P.w1_sf;
+        a.kdim = s.H;
+        a.n = N1;
+        a.meta = meta;
+        a.tile_expert = tile_expert;
+        a.route_of_row = route_of_row;
+        a.num_experts = s.E;
+        a.status = status;
+        a.act = act;
+        a.topk = s.K;
+        a.gw = reinterpret_cast<const float*>(pw + P.gw1);
+        a.topk_w = topk_w;
+        a.weight_on_input = on_input ? 1 : 0;
+        a.out_cols = s.I;
+        a.out_bf16 = h_bf16;
+        e = launch_gemm_w4a16(c, kEpiFc1Bf16, tA1, tB1, a, sms);
+        if (e != cudaSuccess || !mark(4) || !mark(5)) return MOE_ERR_CUDA;
+        GemmParams b{};
+        b.sfb = pw + P.w2_sf;
+        b.kdim = s.I;
+        b.n = s.H;
+        b.meta = meta;
+        b.tile_expert = tile_expert;
+        b.route_of_row = route_of_row;
+        b.num_experts = s.E;
+        b.status = status;
+        b.act = act;
+        b.topk = s.K;
+        b.gw = reinterpret_cast<const float*>(pw + P.gw2);
+        b.topk_w = topk_w;
+        b.weight_on_output = on_input ? 0 : 1;
+        b.out_cols = s.H;
+        int epi2;
+        if (det) {
+            b.out_bf16 = reinterpret_cast<__nv_bfloat16*>(wsp(W.o_bf16));
+            epi2 = kEpiFc2Store;
+        } else {
+            b.out_f32 = y_acc;
+            epi2 = kEpiFc2Scatter;
+        }
+        e = launch_gemm_w4a16(c, epi2, tA2, tB2, b, sms);
+        if (e != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
+        if (det)
+            e = launch_finalize_deterministic(c, s.T, s.H, s.K, row_of_route, topk_w, on_input ? 0 : 1,
+                                              wsp(W.o_bf16), y_bf16);
+        else
+            e = launch_finalize_fused(c, s.T, s.H, y_acc, y_bf16);
+        if (e != cudaSuccess || !mark(7)) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
 
     // ---- W4A4 ----
     const bool per_token = mode == kModePerToken;
@@ -325,7 +392,7 @@ moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags, const void* x_b
 
 int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return -1;
-    // router, 3 permutation kernels, quantize/gather, FC1, [FC2-input quant], FC2, finalize
+    // router, 3 permutation kernels, quantize or gather, FC1, [FC2-input quant], FC2, finalize
     return 8 + (mode_of(flags) == kModePerToken ? 1 : 0);
 }
 

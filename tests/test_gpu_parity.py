@@ -75,7 +75,7 @@ def test_tiny_config_parity():
 MATRIX = []
 for T, H, I, E, K in [(1, 256, 128, 8, 2), (7, 384, 256, 8, 2), (129, 256, 128, 8, 1), (40, 256, 256, 1, 1),
                       (200, 384, 128, 16, 4)]:
-    for mode in (synth.MODE_PER_TENSOR, synth.MODE_PER_TOKEN):
+    for mode in (synth.MODE_PER_TENSOR, synth.MODE_PER_TOKEN, synth.MODE_W4A16):
         for act in (0, 1):
             for on_input in (False, True):
                 for det in (False, True):
@@ -97,6 +97,13 @@ def test_mid_config_parity():
     """configs: mid W4A4 (T=512, H=2048, I=768, E=64, top-6, per-token,
     router weight on input, logit bias skew)."""
     full_parity(synth.config(1))
+
+
+@pytest.mark.parametrize("T", [16, 200])
+def test_w4a16_config_parity(T):
+    """configs: W4A16 (H=4096, I=1536, E=128, top-8, ReLU2, non-gated FC1,
+    fused finalize), at small token counts."""
+    full_parity(synth.config(3, T))
 
 
 def test_deterministic_finalize_is_bitwise_reproducible():
