@@ -191,7 +191,8 @@ typedef struct {
     uint64_t offsets;        /* int32 [E+1] exclusive prefix of count        */
     uint64_t padded_offsets; /* int32 [E+1] prefix of count rounded up to 128*/
     uint64_t meta;           /* int32 [4]: [0] padded rows, [1] M tiles      */
-    uint64_t unit_base;      /* int32 [E][ceil(T/32)] permute scratch        */
+    uint64_t unit_base;      /* int32 [E][ceil(T/32)] per-unit starting rows */
+    uint64_t unit_mask;      /* uint32 [E][ceil(T/32)] per-unit token masks  */
     uint64_t row_of_route;   /* int32 [T*K] padded row of route t*K+k        */
     uint64_t route_of_row;   /* int32 [rows_cap] route of a row, -1 in pads  */
     uint64_t tile_expert;    /* int32 [rows_cap/128] expert of each M tile   */
@@ -209,7 +210,7 @@ typedef struct {
     uint64_t total;          /* workspace bytes                              */
 } moe_workspace_layout;
 
-#define MOE_WORKSPACE_VERSION 1
+#define MOE_WORKSPACE_VERSION 2
 
 /* Fill `out` with the workspace layout for this shape and flags.  Regions a
  * mode does not use have offset UINT64_MAX.  Pure host call, no CUDA. */
@@ -252,9 +253,9 @@ MOE_API moe_status moe_nvfp4_debug_convert(const float* in, int64_t n, uint8_t* 
  * the library image, which every GPU that loads the library holds until the
  * process exits.  It allocates nothing (no cudaMalloc/cudaFree, no
  * allocating library call).  Shapes whose scratch need (8 + rows_cap/128 +
- * E*ceil(T/32) int32, plus alignment) exceeds the array return
+ * 2*E*ceil(T/32) int32, plus alignment) exceeds the array return
  * MOE_ERR_WORKSPACE before anything is launched; E = 256 fits up to about
- * 32 000 tokens.  All calls share the one array (it keeps the last call's
+ * 16 000 tokens.  All calls share the one array (it keeps the last call's
  * contents; every entry a call reads is written by that call first), so calls
  * whose work may overlap on the GPU (different streams, or other host
  * threads) race and must be serialized by the caller.  The first call on each

@@ -98,6 +98,16 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
     return (c & 8u) ? -m : m;
 }
 
+// Padded row of token t's route to expert e: the (expert, unit) starting row
+// plus the number of the unit's earlier tokens that chose e (bit j of the
+// unit's mask of e is token u*32+j).
+__device__ __forceinline__ int route_row(int t, int e, int U, const int* __restrict__ unit_base,
+                                         const uint32_t* __restrict__ unit_mask) {
+    const int u = t / kUnitTokens, j = t % kUnitTokens;
+    const size_t idx = (size_t)e * U + u;
+    return unit_base[idx] + __popc(unit_mask[idx] & ((1u << j) - 1u));
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

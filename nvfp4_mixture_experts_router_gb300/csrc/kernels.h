@@ -33,15 +33,31 @@ struct LaunchCtx {
 cudaError_t setup_routing_kernels();
 cudaError_t launch_router(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
                           int renorm, int* ids, float* w, unsigned int* status_reset);
-cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base, int* count,
-                           int* offsets, int* padded_offsets, int* meta, int* tile_expert, int* row_of_route,
-                           int* route_of_row, unsigned int* status);
+cudaError_t launch_route_count(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
+                               int renorm, int* ids, float* w, int* unit_cnt, uint32_t* unit_mask,
+                               unsigned int* status_reset);
+cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
+                                int* padded_offsets, int* meta, int* tile_expert, int* route_of_row);
+cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base,
+                           uint32_t* unit_mask, int* count, int* offsets, int* padded_offsets, int* meta,
+                           int* tile_expert, int* row_of_route, int* route_of_row, unsigned int* status);
+
+// Where a row-parallel kernel hands out the permuted rows itself (step 3 of
+// the permutation fused in): the routing intermediates it reads and writes.
+struct RouteScatter {
+    const int* topk_ids;        // [T*K]
+    const int* unit_base;       // [E][U] starting rows
+    const uint32_t* unit_mask;  // [E][U] token masks
+    int E;
+    int* row_of_route;          // [T*K] out
+    int* route_of_row;          // [rows_cap] out (valid rows)
+};
 
 // rowops.cu
 cudaError_t launch_quantize_x(const LaunchCtx& c, int T, int H, int K, const void* x, const float* g1_in,
-                              int per_token, float* g1_out, const int* row_of_route, uint8_t* codes, uint8_t* sf,
+                              int per_token, float* g1_out, const RouteScatter& rs, uint8_t* codes, uint8_t* sf,
                               float* y_acc_zero);
-cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const void* x, const int* row_of_route,
+cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const void* x, const RouteScatter& rs,
                                  void* x_perm, float* y_acc_zero);
 cudaError_t launch_quantize_h(const LaunchCtx& c, uint64_t rows_cap, int I, const int* meta,
                               const int* route_of_row, const float* h, float* g2, uint8_t* codes, uint8_t* sf);

@@ -99,6 +99,7 @@ inline moe_workspace_layout workspace_layout(moe_shape s, uint32_t flags) {
     L.padded_offsets = take(4 * (E + 1));
     L.meta = take(16);
     L.unit_base = take(4 * E * units);
+    L.unit_mask = take(4 * E * units);
     L.row_of_route = take(4 * T * K);
     L.route_of_row = take(4 * cap);
     L.tile_expert = take(4 * (cap / kTileM));

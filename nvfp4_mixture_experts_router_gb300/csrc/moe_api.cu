@@ -107,7 +107,7 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 
 extern "C" {
 
-const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.0 sm_103a (prepared v1, workspace v1)"; }
+const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.1 sm_103a (prepared v1, workspace v2)"; }
 
 size_t moe_nvfp4_prepared_bytes(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return 0;
@@ -198,20 +198,28 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     };
     if (!mark(0)) return MOE_ERR_CUDA;
 
-    e = launch_router(c, s.T, s.E, s.K, router_logits, router_bias, (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1, ids,
-                      topk_w, status);
+    e = launch_route_count(c, s.T, s.E, s.K, router_logits, router_bias, (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1,
+                           ids, topk_w, reinterpret_cast<int*>(wsp(W.unit_base)),
+                           reinterpret_cast<uint32_t*>(wsp(W.unit_mask)), status);
     if (e != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
-    e = launch_permute(c, s.T, s.E, s.K, ids, reinterpret_cast<int*>(wsp(W.unit_base)),
-                       reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
-                       reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert, row_of_route, route_of_row,
-                       status);
+    e = launch_permute_scan(c, s.T, s.E, reinterpret_cast<int*>(wsp(W.unit_base)),
+                            reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
+                            reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert, route_of_row);
     if (e != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
+    // the quantize / gather kernel hands out the permuted rows itself
+    RouteScatter rs;
+    rs.topk_ids = ids;
+    rs.unit_base = reinterpret_cast<const int*>(wsp(W.unit_base));
+    rs.unit_mask = reinterpret_cast<const uint32_t*>(wsp(W.unit_mask));
+    rs.E = s.E;
+    rs.row_of_route = row_of_route;
+    rs.route_of_row = route_of_row;
 
     if (mode == kModeW4A16) {
         // ---- W4A16: BF16 activations, weights widened on chip ----
         __nv_bfloat16* x_perm = reinterpret_cast<__nv_bfloat16*>(wsp(W.x_bf16_perm));
         __nv_bfloat16* h_bf16 = reinterpret_cast<__nv_bfloat16*>(wsp(W.h_bf16));
-        e = launch_gather_x_bf16(c, s.T, s.H, s.K, x_bf16, row_of_route, x_perm, y_acc);
+        e = launch_gather_x_bf16(c, s.T, s.H, s.K, x_bf16, rs, x_perm, y_acc);
         if (e != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
         CUtensorMap tA1, tB1, tA2, tB2;
         if (!encode_operand_map(&tA1, x_perm, W.rows_cap, (uint64_t)s.H * 2) ||
@@ -278,8 +286,8 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     uint8_t* xq_sf = wsp(W.xq_sf);
     uint8_t* hq_codes = wsp(W.hq_codes);
     uint8_t* hq_sf = wsp(W.hq_sf);
-    e = launch_quantize_x(c, s.T, s.H, s.K, x_bf16, act_scale_fc1, per_token ? 1 : 0, g1, row_of_route, xq_codes,
-                          xq_sf, y_acc);
+    e = launch_quantize_x(c, s.T, s.H, s.K, x_bf16, act_scale_fc1, per_token ? 1 : 0, g1, rs, xq_codes, xq_sf,
+                          y_acc);
     if (e != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
@@ -392,8 +400,8 @@ moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags, const void* x_b
 
 int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return -1;
-    // router, 3 permutation kernels, quantize or gather, FC1, [FC2-input quant], FC2, finalize
-    return 8 + (mode_of(flags) == kModePerToken ? 1 : 0);
+    // router + unit counts, scan, quantize or gather (+ row scatter), FC1, [FC2-input quant], FC2, finalize
+    return 6 + (mode_of(flags) == kModePerToken ? 1 : 0);
 }
 
 moe_status moe_nvfp4_last_device_status(void* workspace, void* stream) {

@@ -6,10 +6,11 @@
 // outputs), or a latency-critical loop where a cudaMalloc and the device
 // synchronization it can imply are not acceptable.  For them this file
 // offers the routing stage (softmax + top-K, then the stable permutation by
-// expert) with its only scratch -- per-unit expert counts, the M-tile map
-// and a status word -- in a fixed array in device memory that every GPU
-// loading the library holds until the process exits.  It launches the same
-// kernels as the routing stage of moe_nvfp4_forward.
+// expert) with its only scratch -- per-unit expert counts and token masks,
+// the M-tile map and a status word -- in a fixed array in device memory that
+// every GPU loading the library holds until the process exits.  It computes
+// exactly what the routing stage of moe_nvfp4_forward computes, with the
+// router, the unit masks, the scan and the row scatter as four kernels.
 #include <mutex>
 
 #include "../../include/moe_nvfp4.h"
@@ -83,11 +84,12 @@ moe_status moe_nvfp4_route_noalloc(int T, int E, int K, uint32_t flags, const fl
         return MOE_ERR_INVALID_ARG;
 
     // scratch layout (int32): [0,4) status, [4,8) meta, [8, 8+tiles) M-tile
-    // map, then the per-(expert, unit) counts at the next 64-int boundary
+    // map, then at the next 64-int boundary the per-(expert, unit) starting
+    // rows and the per-(expert, unit) token masks
     const int64_t units = (T + moe::kUnitTokens - 1) / moe::kUnitTokens;
     const int64_t tiles = (int64_t)(moe::rows_capacity(T, K, E) / moe::kTileM);
     const int64_t base_units = (8 + tiles + 63) / 64 * 64;
-    if (base_units + (int64_t)E * units > kScratchInts) return MOE_ERR_WORKSPACE;
+    if (base_units + 2 * (int64_t)E * units > kScratchInts) return MOE_ERR_WORKSPACE;
 
     int* scratch = nullptr;
     const moe_status st = scratch_for_current_device(&scratch);
@@ -96,6 +98,7 @@ moe_status moe_nvfp4_route_noalloc(int T, int E, int K, uint32_t flags, const fl
     int* meta = scratch + 4;
     int* tile_expert = scratch + 8;
     int* unit_base = scratch + base_units;
+    uint32_t* unit_mask = reinterpret_cast<uint32_t*>(unit_base + (int64_t)E * units);
 
     moe::LaunchCtx c;
     c.stream = static_cast<cudaStream_t>(stream);
@@ -105,8 +108,8 @@ moe_status moe_nvfp4_route_noalloc(int T, int E, int K, uint32_t flags, const fl
     cudaError_t e = moe::launch_router(c, T, E, K, router_logits, router_bias,
                                        (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1, topk_ids, topk_w, status);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    e = moe::launch_permute(c, T, E, K, topk_ids, unit_base, count, offsets, padded_offsets, meta, tile_expert,
-                            row_of_route, route_of_row, status);
+    e = moe::launch_permute(c, T, E, K, topk_ids, unit_base, unit_mask, count, offsets, padded_offsets, meta,
+                            tile_expert, row_of_route, route_of_row, status);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

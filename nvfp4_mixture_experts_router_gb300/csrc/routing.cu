@@ -9,28 +9,31 @@
 //
 // Permutation [FlashInfer PR #4366: the grouped GEMM reads each expert's
 // routes as one contiguous, tile-padded segment; "Tests": cluster padding
-// and partial tiles]: a stable counting sort.  Tokens are cut into units of
-// 32; (1) each unit counts its routes per expert, (2) one block scans the
-// counts into per-expert totals, offsets, 128-row padded offsets and a
-// per-(expert, unit) starting row, (3) each unit walks its tokens in order
-// and hands out consecutive rows.  Within an expert the routes therefore sit
-// in ascending token order, which makes the permutation unique.
+// and partial tiles]: a stable counting sort over units of 32 tokens.
+//   (1) per unit and expert, a 32-bit mask of the unit's tokens that chose
+//       the expert (bit j = token u*32+j) and its population count;
+//   (2) one block scans the counts into per-expert totals, offsets, 128-row
+//       padded offsets and a per-(expert, unit) starting row;
+//   (3) a route's row = its (expert, unit) start + popc(mask below its bit):
+//       routes of an expert sit in ascending token order, which makes the
+//       permutation unique.  Step (3) is a few integer operations per route,
+//       so the forward folds it into the kernel that consumes the rows
+//       (quantize_x / gather), see rowops.cu.
+// The forward also folds (1) into the router kernel (route_count_kernel).
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
+namespace {
+
+// Route one token (the calling warp): writes ids / weights (lanes < K) and
+// returns this lane's selected expert (slot = lane) or -1 for lane >= K.
 template <int EPL>
-__global__ void __launch_bounds__(256) router_topk_kernel(int T, int E, int K, const float* __restrict__ logits,
-                                                          const float* __restrict__ bias, int renorm,
-                                                          int* __restrict__ topk_ids, float* __restrict__ topk_w,
-                                                          unsigned int* status_reset) {
-    pdl_wait();
-    // the first kernel of a forward clears the device status word
-    if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0u;
+__device__ __forceinline__ int route_token(int t, int E, int K, const float* __restrict__ logits,
+                                           const float* __restrict__ bias, int renorm, int* __restrict__ topk_ids,
+                                           float* __restrict__ topk_w) {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= T) return;
     float l[EPL];
     uint32_t taken = 0;
 #pragma unroll
@@ -45,8 +48,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(int T, int E, int K, c
             taken |= 1u << i;
         }
     }
-    float sel_v[32];
-    int sel_e[32];
+    float my_v = 0.0f, lmax = 0.0f, den = 0.0f;
+    int my_e = -1;
     for (int k = 0; k < K; ++k) {
         float bv = -INFINITY;
         int be = 0x7fffffff;
@@ -67,61 +70,105 @@ __global__ void __launch_bounds__(256) router_topk_kernel(int T, int E, int K, c
             }
         }
         if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        sel_v[k] = bv;
-        sel_e[k] = be;
+        if (k == 0) lmax = bv;
+        if (renorm) den += expf(bv - lmax);      // same order on every lane
+        if (k == lane) {
+            my_v = bv;
+            my_e = be;
+        }
     }
-    const float lmax = sel_v[0];
-    float den = 0.0f;
-    if (renorm) {
-        for (int k = 0; k < K; ++k) den += expf(sel_v[k] - lmax);
-    } else {
+    if (!renorm) {
         float part = 0.0f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
             if (lane + 32 * i < E) part += expf(l[i] - lmax);
         den = warp_sum(part);
     }
-    for (int k = lane; k < K; k += 32) {
-        // register arrays indexed by a lane-dependent k: select by loop
-        float v = 0.0f;
-        int e = 0;
-        for (int j = 0; j < K; ++j)
-            if (j == k) { v = sel_v[j]; e = sel_e[j]; }
-        topk_ids[(size_t)t * K + k] = e;
-        topk_w[(size_t)t * K + k] = expf(v - lmax) / den;
+    if (lane < K) {
+        topk_ids[(size_t)t * K + lane] = my_e;
+        topk_w[(size_t)t * K + lane] = expf(my_v - lmax) / den;
+    }
+    return lane < K ? my_e : -1;
+}
+
+}  // namespace
+
+// Router only (the allocation-free routing entry point uses it).
+template <int EPL>
+__global__ void __launch_bounds__(256) router_topk_kernel(int T, int E, int K, const float* __restrict__ logits,
+                                                          const float* __restrict__ bias, int renorm,
+                                                          int* __restrict__ topk_ids, float* __restrict__ topk_w,
+                                                          unsigned int* status_reset) {
+    pdl_wait();
+    // the first kernel of a forward clears the device status word
+    if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0u;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t < T) route_token<EPL>(t, E, K, logits, bias, renorm, topk_ids, topk_w);
+    pdl_launch_dependents();
+}
+
+// Router fused with step (1): one block of 32 warps per unit of 32 tokens.
+template <int EPL>
+__global__ void __launch_bounds__(1024) route_count_kernel(int T, int E, int K, const float* __restrict__ logits,
+                                                           const float* __restrict__ bias, int renorm,
+                                                           int* __restrict__ topk_ids, float* __restrict__ topk_w,
+                                                           int* __restrict__ unit_cnt, uint32_t* __restrict__ unit_mask,
+                                                           unsigned int* status_reset) {
+    __shared__ uint32_t s_mask[1024];
+    pdl_wait();
+    if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0u;
+    const int U = (T + kUnitTokens - 1) / kUnitTokens;
+    const int u = blockIdx.x;
+    const int w = threadIdx.x >> 5;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0u;
+    __syncthreads();
+    const int t = u * kUnitTokens + w;
+    if (t < T) {
+        const int e = route_token<EPL>(t, E, K, logits, bias, renorm, topk_ids, topk_w);
+        if (e >= 0) atomicOr(&s_mask[e], 1u << w);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const uint32_t m = s_mask[e];
+        unit_cnt[(size_t)e * U + u] = __popc(m);
+        unit_mask[(size_t)e * U + u] = m;
     }
     pdl_launch_dependents();
 }
 
-// (1) per-unit histogram: warp w of the block handles unit blockIdx.x*8+w.
+// Step (1) from given expert ids: warp w of the block handles unit blockIdx.x*8+w.
 __global__ void __launch_bounds__(256) permute_count_kernel(int T, int E, int K, const int* __restrict__ topk_ids,
-                                                            int* __restrict__ unit_cnt /* [E][U] */,
-                                                            unsigned int* status) {
-    extern __shared__ int s_hist[];  // [8][E]
+                                                            int* __restrict__ unit_cnt,
+                                                            uint32_t* __restrict__ unit_mask, unsigned int* status) {
+    extern __shared__ uint32_t s_masks[];  // [8][E]
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int U = (T + kUnitTokens - 1) / kUnitTokens;
     const int u = blockIdx.x * 8 + warp;
-    int* h = s_hist + warp * E;
-    for (int e = lane; e < E; e += 32) h[e] = 0;
+    uint32_t* m = s_masks + warp * E;
+    for (int e = lane; e < E; e += 32) m[e] = 0u;
     __syncwarp();
     if (u < U) {
         const int t = u * kUnitTokens + lane;
         if (t < T) {
             for (int k = 0; k < K; ++k) {
                 const int e = topk_ids[(size_t)t * K + k];
-                if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+                if (e >= 0 && e < E) atomicOr(&m[e], 1u << lane);
                 else atomicOr(status, kStatusBadExpert);
             }
         }
         __syncwarp();
-        for (int e = lane; e < E; e += 32) unit_cnt[(size_t)e * U + u] = h[e];
+        for (int e = lane; e < E; e += 32) {
+            unit_cnt[(size_t)e * U + u] = __popc(m[e]);
+            unit_mask[(size_t)e * U + u] = m[e];
+        }
     }
     pdl_launch_dependents();
 }
 
 // (2) one block of 1024 threads: totals, offsets, padded offsets, per-unit
-// starting rows, M-tile -> expert map, pad rows of route_of_row set to -1.
+// starting rows (in place of the counts), M-tile -> expert map, pad rows of
+// route_of_row set to -1.
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* __restrict__ unit_base /* [E][U] */,
                                                             int* __restrict__ count, int* __restrict__ offsets,
                                                             int* __restrict__ padded_offsets, int* __restrict__ meta,
@@ -206,69 +253,76 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
     pdl_launch_dependents();
 }
 
-// (3) scatter: one warp per unit walks its 32 tokens in order.
+// (3) standalone: one thread per route.
 __global__ void __launch_bounds__(256) permute_scatter_kernel(int T, int E, int K, const int* __restrict__ topk_ids,
                                                               const int* __restrict__ unit_base,
+                                                              const uint32_t* __restrict__ unit_mask,
                                                               int* __restrict__ row_of_route,
                                                               int* __restrict__ route_of_row) {
-    extern __shared__ int s_next[];  // [8][E]
     pdl_wait();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int U = (T + kUnitTokens - 1) / kUnitTokens;
-    const int u = blockIdx.x * 8 + warp;
-    if (u >= U) return;
-    int* nx = s_next + warp * E;
-    for (int e = lane; e < E; e += 32) nx[e] = unit_base[(size_t)e * U + u];
-    __syncwarp();
-    const int t_end = min(T, (u + 1) * kUnitTokens);
-    for (int t = u * kUnitTokens; t < t_end; ++t) {
-        for (int k = lane; k < K; k += 32) {
-            const int e = topk_ids[(size_t)t * K + k];
-            if (e >= 0 && e < E) {
-                const int row = nx[e];      // experts of one token are distinct
-                nx[e] = row + 1;
-                row_of_route[(size_t)t * K + k] = row;
-                route_of_row[row] = t * K + k;
-            }
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < (int64_t)T * K) {
+        const int e = topk_ids[r];
+        if (e >= 0 && e < E) {
+            const int row = route_row((int)(r / K), e, U, unit_base, unit_mask);
+            row_of_route[r] = row;
+            route_of_row[row] = (int)r;
         }
-        __syncwarp();
     }
     pdl_launch_dependents();
 }
 
+#define MOE_EPL_DISPATCH(E, KERNEL, ...)                                  \
+    do {                                                                  \
+        const int epl_ = ((E) + 31) / 32;                                 \
+        if (epl_ <= 1) return c.launch(KERNEL<1>, __VA_ARGS__);           \
+        if (epl_ <= 2) return c.launch(KERNEL<2>, __VA_ARGS__);           \
+        if (epl_ <= 4) return c.launch(KERNEL<4>, __VA_ARGS__);           \
+        if (epl_ <= 8) return c.launch(KERNEL<8>, __VA_ARGS__);           \
+        if (epl_ <= 16) return c.launch(KERNEL<16>, __VA_ARGS__);         \
+        return c.launch(KERNEL<32>, __VA_ARGS__);                         \
+    } while (0)
+
 cudaError_t launch_router(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
                           int renorm, int* ids, float* w, unsigned int* st) {
-    const int warps = 8;
-    dim3 grid((T + warps - 1) / warps), block(32 * warps);
-    const int epl = (E + 31) / 32;
-    if (epl <= 1) return c.launch(router_topk_kernel<1>, grid, block, 0, T, E, K, logits, bias, renorm, ids, w, st);
-    if (epl <= 2) return c.launch(router_topk_kernel<2>, grid, block, 0, T, E, K, logits, bias, renorm, ids, w, st);
-    if (epl <= 4) return c.launch(router_topk_kernel<4>, grid, block, 0, T, E, K, logits, bias, renorm, ids, w, st);
-    if (epl <= 8) return c.launch(router_topk_kernel<8>, grid, block, 0, T, E, K, logits, bias, renorm, ids, w, st);
-    if (epl <= 16) return c.launch(router_topk_kernel<16>, grid, block, 0, T, E, K, logits, bias, renorm, ids, w, st);
-    return c.launch(router_topk_kernel<32>, grid, block, 0, T, E, K, logits, bias, renorm, ids, w, st);
+    const dim3 grid((T + 7) / 8), block(256);
+    MOE_EPL_DISPATCH(E, router_topk_kernel, grid, block, 0, T, E, K, logits, bias, renorm, ids, w, st);
 }
 
-cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base, int* count,
-                           int* offsets, int* padded_offsets, int* meta, int* tile_expert, int* row_of_route,
-                           int* route_of_row, unsigned int* status) {
+cudaError_t launch_route_count(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
+                               int renorm, int* ids, float* w, int* unit_cnt, uint32_t* unit_mask,
+                               unsigned int* st) {
     const int U = (T + kUnitTokens - 1) / kUnitTokens;
-    const size_t smem = (size_t)8 * E * sizeof(int);
+    MOE_EPL_DISPATCH(E, route_count_kernel, dim3(U), dim3(1024), 0, T, E, K, logits, bias, renorm, ids, w, unit_cnt,
+                     unit_mask, st);
+}
+
+cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
+                                int* padded_offsets, int* meta, int* tile_expert, int* route_of_row) {
+    return c.launch(permute_scan_kernel, dim3(1), dim3(1024), 0, T, E, unit_base, count, offsets, padded_offsets,
+                    meta, tile_expert, route_of_row);
+}
+
+cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base,
+                           uint32_t* unit_mask, int* count, int* offsets, int* padded_offsets, int* meta,
+                           int* tile_expert, int* row_of_route, int* route_of_row, unsigned int* status) {
+    const int U = (T + kUnitTokens - 1) / kUnitTokens;
+    const size_t smem = (size_t)8 * E * sizeof(uint32_t);
     cudaError_t err;
-    err = c.launch(permute_count_kernel, dim3((U + 7) / 8), dim3(256), smem, T, E, K, ids, unit_base, status);
+    err = c.launch(permute_count_kernel, dim3((U + 7) / 8), dim3(256), smem, T, E, K, ids, unit_base, unit_mask,
+                   status);
     if (err != cudaSuccess) return err;
-    err = c.launch(permute_scan_kernel, dim3(1), dim3(1024), 0, T, E, unit_base, count, offsets, padded_offsets,
-                   meta, tile_expert, route_of_row);
+    err = launch_permute_scan(c, T, E, unit_base, count, offsets, padded_offsets, meta, tile_expert, route_of_row);
     if (err != cudaSuccess) return err;
-    return c.launch(permute_scatter_kernel, dim3((U + 7) / 8), dim3(256), smem, T, E, K, ids,
-                    (const int*)unit_base, row_of_route, route_of_row);
+    const int64_t routes = (int64_t)T * K;
+    return c.launch(permute_scatter_kernel, dim3((unsigned)((routes + 255) / 256)), dim3(256), 0, T, E, K, ids,
+                    (const int*)unit_base, (const uint32_t*)unit_mask, row_of_route, route_of_row);
 }
 
 cudaError_t setup_routing_kernels() {
-    const int smem = 8 * 1024 * (int)sizeof(int);
-    cudaError_t e = cudaFuncSetAttribute(permute_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(permute_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = 8 * 1024 * (int)sizeof(uint32_t);
+    return cudaFuncSetAttribute(permute_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 }  // namespace moe

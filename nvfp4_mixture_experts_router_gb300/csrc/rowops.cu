@@ -38,6 +38,21 @@ __device__ __forceinline__ uint32_t pack_sf4(uint32_t s) {
     return s | (s1 << 8) | (s2 << 16) | (s3 << 24);
 }
 
+// Step 3 of the permutation for token t, lane k < K handling route t*K+k:
+// compute the route's padded row, record both directions of the map, and
+// return the row (0 for lanes >= K).
+__device__ __forceinline__ int scatter_token_routes(int t, int T, int K, int lane, const RouteScatter& rs) {
+    if (lane >= K) return 0;
+    const int U = (T + kUnitTokens - 1) / kUnitTokens;
+    const int r = t * K + lane;
+    const int e = rs.topk_ids[r];
+    if (e < 0 || e >= rs.E) return 0;
+    const int row = route_row(t, e, U, rs.unit_base, rs.unit_mask);
+    rs.row_of_route[r] = row;
+    rs.route_of_row[row] = r;
+    return row;
+}
+
 __device__ __forceinline__ void zero_row_f32(float* p, int n, int lane) {
     for (int c = lane * 4; c < n; c += 128) *reinterpret_cast<float4*>(p + c) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
@@ -48,8 +63,7 @@ __device__ __forceinline__ void zero_row_f32(float* p, int n, int lane) {
 // permuted rows.  Per-token mode derives G1 = amax/2688 from the row.
 __global__ void __launch_bounds__(256) quantize_x_kernel(int T, int H, int K, const __nv_bfloat16* __restrict__ x,
                                                          const float* __restrict__ g1_in, int per_token,
-                                                         float* __restrict__ g1_out,
-                                                         const int* __restrict__ row_of_route,
+                                                         float* __restrict__ g1_out, const RouteScatter rs,
                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                          float* __restrict__ y_acc_zero) {
     pdl_wait();
@@ -71,7 +85,7 @@ __global__ void __launch_bounds__(256) quantize_x_kernel(int T, int H, int K, co
     } else {
         G = __ldg(g1_in);
     }
-    const int my_row = lane < K ? row_of_route[(size_t)t * K + lane] : 0;
+    const int my_row = scatter_token_routes(t, T, K, lane, rs);
     for (int base = 0; base < H; base += 512) {
         const int c = base + lane * 16;
         const bool active = c < H;
@@ -97,7 +111,7 @@ __global__ void __launch_bounds__(256) quantize_x_kernel(int T, int H, int K, co
 
 // W4A16: copy each token's BF16 row to its K permuted rows.
 __global__ void __launch_bounds__(256) gather_x_bf16_kernel(int T, int H, int K, const __nv_bfloat16* __restrict__ x,
-                                                            const int* __restrict__ row_of_route,
+                                                            const RouteScatter rs,
                                                             __nv_bfloat16* __restrict__ x_perm,
                                                             float* __restrict__ y_acc_zero) {
     pdl_wait();
@@ -105,7 +119,7 @@ __global__ void __launch_bounds__(256) gather_x_bf16_kernel(int T, int H, int K,
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    const int my_row = lane < K ? row_of_route[(size_t)t * K + lane] : 0;
+    const int my_row = scatter_token_routes(t, T, K, lane, rs);
     for (int base = 0; base < H / 8; base += 32) {
         const int c = base + lane;
         uint4 v = make_uint4(0, 0, 0, 0);
@@ -303,16 +317,16 @@ __global__ void debug_convert_kernel(const float* __restrict__ in, int64_t n, ui
 // launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_quantize_x(const LaunchCtx& c, int T, int H, int K, const void* x, const float* g1_in,
-                              int per_token, float* g1_out, const int* row_of_route, uint8_t* codes, uint8_t* sf,
+                              int per_token, float* g1_out, const RouteScatter& rs, uint8_t* codes, uint8_t* sf,
                               float* y_acc_zero) {
     return c.launch(quantize_x_kernel, dim3((T + 7) / 8), dim3(256), 0, T, H, K,
-                    (const __nv_bfloat16*)x, g1_in, per_token, g1_out, row_of_route, codes, sf, y_acc_zero);
+                    (const __nv_bfloat16*)x, g1_in, per_token, g1_out, rs, codes, sf, y_acc_zero);
 }
 
-cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const void* x, const int* row_of_route,
+cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const void* x, const RouteScatter& rs,
                                  void* x_perm, float* y_acc_zero) {
-    return c.launch(gather_x_bf16_kernel, dim3((T + 7) / 8), dim3(256), 0, T, H, K, (const __nv_bfloat16*)x,
-                    row_of_route, (__nv_bfloat16*)x_perm, y_acc_zero);
+    return c.launch(gather_x_bf16_kernel, dim3((T + 7) / 8), dim3(256), 0, T, H, K, (const __nv_bfloat16*)x, rs,
+                    (__nv_bfloat16*)x_perm, y_acc_zero);
 }
 
 cudaError_t launch_quantize_h(const LaunchCtx& c, uint64_t rows_cap, int I, const int* meta,
