@@ -30,12 +30,14 @@ __device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                // silu(z) = z / (1 + e^-z).  The ex2-based exponential and a
-                // correctly rounded reciprocal keep the relative error near
-                // 1e-6; the IEEE division + full-range expf path costs ~6x
-                // the epilogue time and made FC1 epilogue-bound.
+                // silu(z) = z / (1 + e^-z) with the ex2-based exponential and
+                // the approximate division (relative error ~1e-6; for z below
+                // about -88 the denominator is +inf and the result 0).  The
+                // IEEE division + full-range expf, or a correctly rounded
+                // reciprocal, cost 3-6x this epilogue and made FC1
+                // epilogue-bound.
                 const float zg = h[i] * alpha, zu = u[i] * alpha;
-                h[i] = zg * __frcp_rn(1.0f + __expf(-zg)) * zu * pw;
+                h[i] = __fdividef(zg, 1.0f + __expf(-zg)) * zu * pw;
             }
             col0 = n_tile * 64 + ch * 32;
         } else {

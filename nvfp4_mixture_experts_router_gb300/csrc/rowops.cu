@@ -60,52 +60,77 @@ __device__ __forceinline__ void zero_row_f32(float* p, int n, int lane) {
 }  // namespace
 
 // x [T][H] BF16 -> NVFP4 codes/scales written to each of the token's K
-// permuted rows.  Per-token mode derives G1 = amax/2688 from the row.
-__global__ void __launch_bounds__(256) quantize_x_kernel(int T, int H, int K, const __nv_bfloat16* __restrict__ x,
-                                                         const float* __restrict__ g1_in, int per_token,
-                                                         float* __restrict__ g1_out, const RouteScatter rs,
-                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-                                                         float* __restrict__ y_acc_zero) {
+// permuted rows.  One CTA per token, one thread per 16-element block (a
+// single read of the row; per-token mode reduces the row amax in the CTA and
+// derives G1 = amax/2688).  Also hands out the token's permuted rows (step 3
+// of the permutation) and zeroes its row of the fused-finalize accumulator.
+template <int kMaxPer>   // 16-element blocks per thread (rows up to kMaxPer * 16K elements)
+__global__ void __launch_bounds__(1024) quantize_x_kernel(int T, int H, int K, const __nv_bfloat16* __restrict__ x,
+                                                          const float* __restrict__ g1_in, int per_token,
+                                                          float* __restrict__ g1_out, const RouteScatter rs,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                          float* __restrict__ y_acc_zero) {
+    __shared__ float s_red[32];
+    __shared__ int s_rows[32];
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (t >= T) return;
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nblk = H / 16;
+    if (warp == 0) {
+        const int row = scatter_token_routes(t, T, K, lane, rs);
+        if (lane < K) s_rows[lane] = row;
+    }
     const __nv_bfloat16* xr = x + (size_t)t * H;
+    float v[kMaxPer][16];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+        const int b = tid + i * blockDim.x;
+        if (b < nblk) {
+            load16_bf16(xr + 16 * b, v[i]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+        }
+    }
     float G;
     if (per_token) {
-        float amax = 0.0f;
-        for (int c = lane * 16; c < H; c += 512) {
-            float v[16];
-            load16_bf16(xr + c, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        amax = warp_max(amax);
+        if (lane == 0) s_red[warp] = amax;
+        __syncthreads();
+        if (warp == 0) {
+            float m = lane < (int)(blockDim.x >> 5) ? s_red[lane] : 0.0f;
+            m = warp_max(m);
+            if (lane == 0) s_red[0] = global_scale_from_amax(m);
         }
-        G = global_scale_from_amax(warp_max(amax));
-        if (lane == 0) g1_out[t] = G;
+        __syncthreads();
+        G = s_red[0];
+        if (tid == 0) g1_out[t] = G;
     } else {
         G = __ldg(g1_in);
+        __syncthreads();
     }
-    const int my_row = scatter_token_routes(t, T, K, lane, rs);
-    for (int base = 0; base < H; base += 512) {
-        const int c = base + lane * 16;
-        const bool active = c < H;
-        float v[16];
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+        const int b0 = i * blockDim.x;              // uniform across the warp
+        if (b0 >= nblk) break;
+        const int b = tid + b0;
+        const bool active = b < nblk;
         uint32_t q[2] = {0u, 0u};
         uint32_t s = 0;
-        if (active) {
-            load16_bf16(xr + c, v);
-            s = quant_block16(v, G, q);
-        }
+        if (active) s = quant_block16(v[i], G, q);
         const uint32_t word = pack_sf4(s);
-        for (int k = 0; k < K; ++k) {
-            const int row = __shfl_sync(0xffffffffu, my_row, k);
-            if (active) {
-                *reinterpret_cast<uint2*>(codes + (size_t)row * (H / 2) + c / 2) = make_uint2(q[0], q[1]);
-                if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(row, c / 16, H)) = word;
+        if (active) {
+            for (int k = 0; k < K; ++k) {
+                const int row = s_rows[k];
+                *reinterpret_cast<uint2*>(codes + (size_t)row * (H / 2) + 8 * b) = make_uint2(q[0], q[1]);
+                if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(row, b, H)) = word;
             }
         }
     }
-    if (y_acc_zero) zero_row_f32(y_acc_zero + (size_t)t * H, H, lane);
+    if (y_acc_zero) {
+        float* yr = y_acc_zero + (size_t)t * H;
+        for (int c = tid * 4; c < H; c += blockDim.x * 4) *reinterpret_cast<float4*>(yr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     pdl_launch_dependents();
 }
 
@@ -134,39 +159,59 @@ __global__ void __launch_bounds__(256) gather_x_bf16_kernel(int T, int H, int K,
 }
 
 // Per-token W4A4: FC2 input row (FP32) -> G2 = amax/2688, NVFP4 codes/scales.
-__global__ void __launch_bounds__(256) quantize_h_kernel(int I, const int* __restrict__ meta,
-                                                         const int* __restrict__ route_of_row,
-                                                         const float* __restrict__ h, float* __restrict__ g2,
-                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+// One CTA per row at a time (grid-stride over the padded rows, pad rows
+// skipped), one thread per 16-element block.
+template <int kMaxPer>
+__global__ void __launch_bounds__(1024) quantize_h_kernel(int I, const int* __restrict__ meta,
+                                                          const int* __restrict__ route_of_row,
+                                                          const float* __restrict__ h, float* __restrict__ g2,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+    __shared__ float s_red[32];
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (row >= meta[0] || route_of_row[row] < 0) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rows = meta[0];
+    for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    if (route_of_row[row] < 0) continue;      // pad row (uniform across the CTA)
+    const int nblk = I / 16;
     const float* hr = h + (size_t)row * I;
+    float v[kMaxPer][16];
     float amax = 0.0f;
-    for (int c = lane * 16; c < I; c += 512) {
-        float v[16];
-        load16_f32(hr + c, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < kMaxPer; ++i) {
+        const int b = tid + i * blockDim.x;
+        if (b < nblk) {
+            load16_f32(hr + 16 * b, v[i]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+        }
     }
-    const float G = global_scale_from_amax(warp_max(amax));
-    if (lane == 0) g2[row] = G;
-    for (int base = 0; base < I; base += 512) {
-        const int c = base + lane * 16;
-        const bool active = c < I;
-        float v[16];
+    amax = warp_max(amax);
+    if (lane == 0) s_red[warp] = amax;
+    __syncthreads();
+    if (warp == 0) {
+        float m = lane < (int)(blockDim.x >> 5) ? s_red[lane] : 0.0f;
+        m = warp_max(m);
+        if (lane == 0) s_red[0] = global_scale_from_amax(m);
+    }
+    __syncthreads();
+    const float G = s_red[0];
+    __syncthreads();                         // s_red is reused by the next row
+    if (tid == 0) g2[row] = G;
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+        const int b0 = i * blockDim.x;
+        if (b0 >= nblk) break;
+        const int b = tid + b0;
+        const bool active = b < nblk;
         uint32_t q[2] = {0u, 0u};
         uint32_t s = 0;
-        if (active) {
-            load16_f32(hr + c, v);
-            s = quant_block16(v, G, q);
-        }
+        if (active) s = quant_block16(v[i], G, q);
         const uint32_t word = pack_sf4(s);
         if (active) {
-            *reinterpret_cast<uint2*>(codes + (size_t)row * (I / 2) + c / 2) = make_uint2(q[0], q[1]);
-            if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(row, c / 16, I)) = word;
+            *reinterpret_cast<uint2*>(codes + (size_t)row * (I / 2) + 8 * b) = make_uint2(q[0], q[1]);
+            if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(row, b, I)) = word;
         }
+    }
     }
     pdl_launch_dependents();
 }
@@ -316,11 +361,23 @@ __global__ void debug_convert_kernel(const float* __restrict__ in, int64_t n, ui
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
+// Threads of a one-row-per-CTA kernel: one per 16-element block, a whole
+// number of warps, at most 1024 (rows longer than 16K elements loop).
+static unsigned row_threads(int n) {
+    int t = (n / 16 + 31) / 32 * 32;
+    if (t > 1024) t = 1024;
+    return (unsigned)t;
+}
+
 cudaError_t launch_quantize_x(const LaunchCtx& c, int T, int H, int K, const void* x, const float* g1_in,
                               int per_token, float* g1_out, const RouteScatter& rs, uint8_t* codes, uint8_t* sf,
                               float* y_acc_zero) {
-    return c.launch(quantize_x_kernel, dim3((T + 7) / 8), dim3(256), 0, T, H, K,
-                    (const __nv_bfloat16*)x, g1_in, per_token, g1_out, rs, codes, sf, y_acc_zero);
+    const int per = (H / 16 + 1023) / 1024;
+    const dim3 grid(T), block(row_threads(H));
+    const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
+    if (per <= 1) return c.launch(quantize_x_kernel<1>, grid, block, 0, T, H, K, xb, g1_in, per_token, g1_out, rs, codes, sf, y_acc_zero);
+    if (per <= 2) return c.launch(quantize_x_kernel<2>, grid, block, 0, T, H, K, xb, g1_in, per_token, g1_out, rs, codes, sf, y_acc_zero);
+    return c.launch(quantize_x_kernel<4>, grid, block, 0, T, H, K, xb, g1_in, per_token, g1_out, rs, codes, sf, y_acc_zero);
 }
 
 cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const void* x, const RouteScatter& rs,
@@ -331,8 +388,14 @@ cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const 
 
 cudaError_t launch_quantize_h(const LaunchCtx& c, uint64_t rows_cap, int I, const int* meta,
                               const int* route_of_row, const float* h, float* g2, uint8_t* codes, uint8_t* sf) {
-    return c.launch(quantize_h_kernel, dim3((unsigned)((rows_cap + 7) / 8)), dim3(256), 0, I, meta, route_of_row, h,
-                    g2, codes, sf);
+    const int per = (I / 16 + 1023) / 1024;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const uint64_t want = (uint64_t)sms * (2048 / row_threads(I));   // enough CTAs to fill every SM
+    const dim3 grid((unsigned)(rows_cap < want ? rows_cap : want)), block(row_threads(I));
+    if (per <= 1) return c.launch(quantize_h_kernel<1>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf);
+    if (per <= 2) return c.launch(quantize_h_kernel<2>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf);
+    return c.launch(quantize_h_kernel<4>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf);
 }
 
 cudaError_t launch_finalize_deterministic(const LaunchCtx& c, int T, int H, int K, const int* row_of_route,
