@@ -9,26 +9,36 @@
 // [FlashInfer PR #4366, "Tests": padding and partial tiles], so every M tile
 // belongs to exactly one expert (tile_expert).
 //
-// Kernel design (one persistent CTA per SM, 224 threads):
+// Kernel design (one persistent CTA per SM), tile 128 routes x BN weight
+// rows, BN = 128 or 256:
 //   warp 0      TMA producer: per pipeline stage one 128x128-byte A tile and
-//               one 128x128-byte B tile (cp.async.bulk.tensor, 128-byte
-//               swizzle) plus the matching 2 KB of scale atoms of each
-//               operand (cp.async.bulk), all completing on one mbarrier.
-//   warp 6      scale mover: once a stage has landed, tcgen05.cp of its 8
+//               one BNx128-byte B tile (cp.async.bulk.tensor, 128-byte
+//               swizzle) plus the matching scale atoms of each operand
+//               (cp.async.bulk), all completing on one mbarrier.
+//   warp 2      scale mover: once a stage has landed, tcgen05.cp of its
 //               scale atoms into the stage's tensor-memory slot, then
-//               tcgen05.commit to the stage's sf_ready barrier.
+//               tcgen05.commit to the stage's sf_ready barrier (with BN = 256
+//               the B scales go to a second mover warp, the last warp: 12
+//               copies per stage are too many for one issuing thread).
 //   warp 1      allocates 512 tensor-memory columns; lane 0 issues, per
-//               stage, four 128x128x64 block-scaled MMAs into an FP32
+//               stage, four 128xBNx64 block-scaled MMAs into an FP32
 //               accumulator in tensor memory, then tcgen05.commit frees the
-//               stage.  (The tcgen05 issue slot of a single thread is the
-//               scarce resource at these tile sizes, so the scale copies are
-//               issued from another warp.)
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp w reads lanes
-//               32*(w%4)..+31, one output row per thread), fused activation /
-//               scaling / requantization / scatter, then release the buffer.
-// Two accumulator buffers let the epilogue of tile i overlap the main loop
-// of tile i+1.  Tiles are walked n-fastest so that concurrently running CTAs
-// share the A tile and one expert's weights stay hot in L2.
+//               stage.  The tcgen05 issue slot of this one thread is the
+//               scarce resource (~130 cycles per MMA measured), so scale
+//               copies come from another warp and BN = 256 doubles the
+//               weight bytes each MMA consumes.
+//   warps 3..   epilogue: tcgen05.ld of the accumulator (warp w reads lanes
+//               32*(w%4)..+31, one output row per thread; with BN = 256 a
+//               second group of four warps takes columns 128..255), fused
+//               activation / scaling / requantization / scatter, then
+//               release the accumulator.
+// BN = 128 double-buffers the accumulator (epilogue of tile i overlaps the
+// main loop of tile i+1); BN = 256 needs all 256 spare tensor-memory
+// columns for one accumulator next to the scale slots and drains it with
+// twice the epilogue warps instead.  A weight segment whose length is an odd
+// multiple of 128 ends in a 128-wide tile (N = 128 MMAs).  Tiles are walked
+// n-fastest so that concurrently running CTAs share the A tile and one
+// expert's weights stay hot in L2.
 // Every wait is bounded (1 s); a timeout sets a status bit and all roles
 // drain and exit instead of hanging.
 #include "common.cuh"
@@ -40,21 +50,27 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBN = 128;
 constexpr int kBKBytes = 128;                 // 256 E2M1 elements per stage row
-constexpr int kStages = 6;
 constexpr int kTileBytesA = kBM * kBKBytes;   // 16 KB
-constexpr int kTileBytesB = kBN * kBKBytes;   // 16 KB
-constexpr int kSfBytes = 4 * 512;             // 4 scale atoms (128 rows x 64 elems each)
-constexpr int kNumThreads = 224;
+constexpr int kSfBytesA = 4 * 512;            // 4 scale atoms (128 rows x 64 elements each)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = 128;
-constexpr uint32_t kSfColBase = 256;          // columns 256.. hold the per-stage scales
-constexpr uint32_t kSfColsPerStage = 32;      // 16 (A) + 16 (B)
-constexpr int kSmemBytes = kStages * (kTileBytesA + kTileBytesB + 2 * kSfBytes) + 1024 + 256;
 
-static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
-static_assert(2 * kAccCols <= kSfColBase, "accumulators overlap scales");
+template <int BN>
+struct Cfg {
+    static constexpr int kStages = BN == 128 ? 6 : 4;
+    static constexpr int kAccBufs = BN == 128 ? 2 : 1;
+    static constexpr int kEpiWarps = BN == 128 ? 4 : 8;
+    static constexpr int kMovers = BN == 128 ? 1 : 2;            // scale-copy issuing warps
+    static constexpr int kNumThreads = (2 + kMovers + kEpiWarps) * 32;
+    static constexpr int kRowBlocks = BN / 128;                  // 128-row scale blocks of B
+    static constexpr int kTileBytesB = BN * kBKBytes;
+    static constexpr int kSfBytesB = kRowBlocks * kSfBytesA;
+    static constexpr uint32_t kSfColBase = kAccBufs * BN;        // 256 either way
+    static constexpr uint32_t kSfColsB = 4 * kRowBlocks;         // per 64-element k-block
+    static constexpr uint32_t kSfColsPerStage = 16 + 4 * kSfColsB;
+    static constexpr int kSmemBytes = kStages * (kTileBytesA + kTileBytesB + kSfBytesA + kSfBytesB) + 1024 + 256;
+    static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
+};
 
 struct Smem {
     uint8_t* a;
@@ -63,55 +79,58 @@ struct Smem {
     uint8_t* sfb;
     uint64_t* full;
     uint64_t* empty;
+    uint64_t* sf_ready;
     uint64_t* acc_full;
     uint64_t* acc_empty;
     uint64_t* drain;
-    uint64_t* sf_ready;
     uint32_t* tmem_holder;
     volatile int* abort;
 };
 
+template <int BN>
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
+    using C = Cfg<BN>;
     Smem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.a = base;
-    s.b = s.a + kStages * kTileBytesA;
-    s.sfa = s.b + kStages * kTileBytesB;
-    s.sfb = s.sfa + kStages * kSfBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.sfb + kStages * kSfBytes);
+    s.b = s.a + C::kStages * kTileBytesA;
+    s.sfa = s.b + C::kStages * C::kTileBytesB;
+    s.sfb = s.sfa + C::kStages * kSfBytesA;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.sfb + C::kStages * C::kSfBytesB);
     s.full = bars;
-    s.empty = bars + kStages;
-    s.acc_full = bars + 2 * kStages;
+    s.empty = bars + C::kStages;
+    s.sf_ready = bars + 2 * C::kStages;               // [kMovers][kStages]
+    s.acc_full = bars + (2 + C::kMovers) * C::kStages;
     s.acc_empty = s.acc_full + 2;
     s.drain = s.acc_empty + 2;
-    s.sf_ready = s.drain + 1;
-    s.tmem_holder = reinterpret_cast<uint32_t*>(s.sf_ready + kStages);
+    s.tmem_holder = reinterpret_cast<uint32_t*>(s.drain + 1);
     s.abort = reinterpret_cast<volatile int*>(s.tmem_holder + 1);
     return s;
 }
 
 }  // namespace
 
-template <int EPI>
-__global__ void __launch_bounds__(kNumThreads, 1)
+template <int EPI, int BN>
+__global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmParams p) {
+    using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
-    const Smem s = carve(smem_raw);
+    const Smem s = carve<BN>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int no_abort = 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
+            for (int m = 0; m < C::kMovers; ++m) mbar_init(&s.sf_ready[m * C::kStages + i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.acc_full[i], 1);
-            mbar_init(&s.acc_empty[i], 4 * 32);
+            mbar_init(&s.acc_empty[i], C::kEpiWarps * 32);
         }
-        mbar_init(s.drain, 2);   // the MMA thread and the scale mover both retire their ops into it
-        for (int i = 0; i < kStages; ++i) mbar_init(&s.sf_ready[i], 1);
+        mbar_init(s.drain, 1 + C::kMovers);   // the MMA thread and the scale movers retire their ops into it
         *s.abort = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
@@ -129,10 +148,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     pdl_wait();  // A operand, tile map and tile count come from earlier kernels
 
     const int num_m_tiles = p.meta[1];
-    const int n_tiles = p.n / kBN;
+    const int n_tiles = (p.n + BN - 1) / BN;
     const int total = num_m_tiles * n_tiles;
     const int kblocks = p.kdim / 64;          // 64-element MMA steps
     const int kstages = (kblocks + 3) / 4;    // 4 MMA steps per stage
+    const int rb_per_expert = p.n / 128;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -147,80 +167,101 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     *s.abort = 1;
                     break;
                 }
+                const int nrb = min(C::kRowBlocks, rb_per_expert - n_tile * C::kRowBlocks);
                 const int a_row = m_tile * kBM;
-                const int b_row = e * p.n + n_tile * kBN;
+                const int b_row = e * p.n + n_tile * BN;
                 const uint8_t* sfa_src = p.sfa + (size_t)m_tile * kblocks * 512;
-                const uint8_t* sfb_src = p.sfb + ((size_t)e * n_tiles + n_tile) * kblocks * 512;
+                const uint8_t* sfb_src =
+                    p.sfb + ((size_t)e * rb_per_expert + (size_t)n_tile * C::kRowBlocks) * kblocks * 512;
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
                     const int nkb = min(4, kblocks - 4 * ks);
                     const uint32_t sf_bytes = (uint32_t)nkb * 512u;
-                    mbar_arrive_expect_tx(&s.full[stage], kTileBytesA + kTileBytesB + 2 * sf_bytes);
+                    mbar_arrive_expect_tx(&s.full[stage],
+                                          kTileBytesA + C::kTileBytesB + (uint32_t)(1 + nrb) * sf_bytes);
                     tma_load_2d(s.a + stage * kTileBytesA, &tmA, &s.full[stage], ks * kBKBytes, a_row, pol);
-                    tma_load_2d(s.b + stage * kTileBytesB, &tmB, &s.full[stage], ks * kBKBytes, b_row, pol);
-                    bulk_load(s.sfa + stage * kSfBytes, sfa_src + (size_t)ks * 4 * 512, sf_bytes, &s.full[stage], pol);
-                    bulk_load(s.sfb + stage * kSfBytes, sfb_src + (size_t)ks * 4 * 512, sf_bytes, &s.full[stage], pol);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    tma_load_2d(s.b + stage * C::kTileBytesB, &tmB, &s.full[stage], ks * kBKBytes, b_row, pol);
+                    bulk_load(s.sfa + stage * kSfBytesA, sfa_src + (size_t)ks * 4 * 512, sf_bytes, &s.full[stage],
+                              pol);
+                    for (int rb = 0; rb < nrb; ++rb)
+                        bulk_load(s.sfb + stage * C::kSfBytesB + rb * kSfBytesA,
+                                  sfb_src + ((size_t)rb * kblocks + (size_t)ks * 4) * 512, sf_bytes, &s.full[stage],
+                                  pol);
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_nvf4(kBM, kBN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+                const int n_tile = tile % n_tiles;
+                const int width = min(BN, p.n - n_tile * BN);
+                const uint32_t idesc = idesc_nvf4(kBM, width);
                 if (!mbar_wait(&s.acc_empty[acc], acc_phase ^ 1u, s.abort, p.status, kStatusTimeoutMma)) goto done;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)acc * kAccCols;
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
-                    tc_fence_after();
                     const int nkb = min(4, kblocks - 4 * ks);
-                    const uint32_t sfa_t = tmem_base + kSfColBase + (uint32_t)stage * kSfColsPerStage;
+                    const uint32_t sfa_t = tmem_base + C::kSfColBase + (uint32_t)stage * C::kSfColsPerStage;
                     const uint32_t sfb_t = sfa_t + 16;
-                    // the scale mover's copies for this stage have completed
-                    if (!mbar_wait(&s.sf_ready[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                    // the scale movers' copies for this stage have completed
+                    for (int m = 0; m < C::kMovers; ++m)
+                        if (!mbar_wait(&s.sf_ready[m * C::kStages + stage], phase, s.abort, p.status, kStatusTimeoutMma))
+                            goto done;
                     tc_fence_after();
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(s.a + stage * kTileBytesA));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(s.b + stage * kTileBytesB));
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(s.b + stage * C::kTileBytesB));
                     for (int j = 0; j < nkb; ++j) {
                         // advance 32 bytes (64 E2M1) along K inside the swizzled 128-byte rows
-                        tc_mma_nvf4(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc, sfa_t + 4 * j, sfb_t + 4 * j,
-                                    (ks | j) != 0);
+                        tc_mma_nvf4(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc, sfa_t + 4 * j,
+                                    sfb_t + C::kSfColsB * j, (ks | j) != 0);
                     }
                     tc_commit(&s.empty[stage]);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
                 tc_commit(&s.acc_full[acc]);
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
+                if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
             }
         }
-    } else if (warp == 6) {
+    } else if (warp == 2 || (C::kMovers == 2 && warp == 2 + C::kMovers + C::kEpiWarps - 1)) {
+        // scale mover(s): mover 0 copies A's scales (and B's when it is the
+        // only one), mover 1 copies B's scales
+        const int mover = warp == 2 ? 0 : 1;
+        const bool do_a = mover == 0, do_b = C::kMovers == 1 || mover == 1;
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+                const int n_tile = tile % n_tiles;
+                const int nrb = min(C::kRowBlocks, rb_per_expert - n_tile * C::kRowBlocks);
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
                     tc_fence_after();
                     const int nkb = min(4, kblocks - 4 * ks);
-                    const uint32_t sfa_t = tmem_base + kSfColBase + (uint32_t)stage * kSfColsPerStage;
+                    const uint32_t sfa_t = tmem_base + C::kSfColBase + (uint32_t)stage * C::kSfColsPerStage;
                     const uint32_t sfb_t = sfa_t + 16;
                     for (int j = 0; j < nkb; ++j) {
-                        tc_cp_sf_atom(sfa_t + 4 * j, sdesc_sf_atom(smem_u32(s.sfa + stage * kSfBytes + j * 512)));
-                        tc_cp_sf_atom(sfb_t + 4 * j, sdesc_sf_atom(smem_u32(s.sfb + stage * kSfBytes + j * 512)));
+                        if (do_a)
+                            tc_cp_sf_atom(sfa_t + 4 * j, sdesc_sf_atom(smem_u32(s.sfa + stage * kSfBytesA + j * 512)));
+                        if (do_b)
+                            for (int rb = 0; rb < nrb; ++rb)
+                                tc_cp_sf_atom(sfb_t + C::kSfColsB * j + 4 * rb,
+                                              sdesc_sf_atom(smem_u32(s.sfb + stage * C::kSfBytesB + rb * kSfBytesA +
+                                                                     j * 512)));
                     }
-                    tc_commit(&s.sf_ready[stage]);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    tc_commit(&s.sf_ready[mover * C::kStages + stage]);
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
         }
     } else {
-        const int q = warp & 3;  // tensor-memory lane quadrant of this warp
+        const int q = warp & 3;                    // tensor-memory lane quadrant of this warp
+        const int half = (warp - 3) >> 2;          // which 128 accumulator columns (BN = 256)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -229,22 +270,27 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (e < 0 || e >= p.num_experts) break;
             if (!mbar_wait(&s.acc_full[acc], acc_phase, s.abort, p.status, kStatusTimeoutEpilogue)) break;
             tc_fence_after();
-            const int row = m_tile * kBM + q * 32 + lane;
-            const int route = p.route_of_row[row];
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kAccCols;
-            if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32) epilogue_fc1<EPI>(p, taddr, row, route, e, n_tile);
-            else epilogue_fc2<EPI>(p, taddr, row, route, e, n_tile);
+            const int width = min(BN, p.n - n_tile * BN);
+            if (half * 128 < width) {
+                const int row = m_tile * kBM + q * 32 + lane;
+                const int route = p.route_of_row[row];
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + half * 128);
+                const int vtile = n_tile * C::kRowBlocks + half;   // index of this 128-column slice
+                if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32) epilogue_fc1<EPI>(p, taddr, row, route, e, vtile);
+                else epilogue_fc2<EPI>(p, taddr, row, route, e, vtile);
+            }
             tc_fence_before();
             mbar_arrive(&s.acc_empty[acc]);
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
+            if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
         }
     }
 done:
     if (*s.abort) {
         // Something timed out: let in-flight copies land and retire every
-        // issued MMA before the tensor memory and shared memory go away.
-        if ((warp == 1 || warp == 6) && lane == 0) {
+        // issued MMA and scale copy before the memories go away.
+        const bool issues_tc = warp == 1 || warp == 2 || (C::kMovers == 2 && warp == 2 + C::kMovers + C::kEpiWarps - 1);
+        if (issues_tc && lane == 0) {
             tc_commit(s.drain);
             mbar_wait(s.drain, 0, &no_abort, p.status, kStatusTimeoutMma);
         }
@@ -259,28 +305,51 @@ done:
     }
 }
 
-cudaError_t setup_gemm_kernels() {
+template <int BN>
+static cudaError_t set_smem_all() {
     cudaError_t e;
-    e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc1Quant>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const int b = Cfg<BN>::kSmemBytes;
+    if ((e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc1Quant, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, b)))
+        return e;
+    if ((e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc1F32, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, b)))
+        return e;
+    if ((e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc2Store, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, b)))
+        return e;
+    return cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc2Scatter, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+}
+
+cudaError_t setup_gemm_kernels() {
+    const cudaError_t e = set_smem_all<128>();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc1F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc2Store>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc2Scatter>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmemBytes);
+    return set_smem_all<256>();
+}
+
+template <int BN>
+static cudaError_t launch_bn(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             const GemmParams& p, int num_sms) {
+    const dim3 grid(num_sms), block(Cfg<BN>::kNumThreads);
+    const size_t smem = Cfg<BN>::kSmemBytes;
+    switch (epilogue) {
+        case kEpiFc1Quant: return c.launch(gemm_nvf4_kernel<kEpiFc1Quant, BN>, grid, block, smem, tmA, tmB, p);
+        case kEpiFc1F32: return c.launch(gemm_nvf4_kernel<kEpiFc1F32, BN>, grid, block, smem, tmA, tmB, p);
+        case kEpiFc2Store: return c.launch(gemm_nvf4_kernel<kEpiFc2Store, BN>, grid, block, smem, tmA, tmB, p);
+        case kEpiFc2Scatter: return c.launch(gemm_nvf4_kernel<kEpiFc2Scatter, BN>, grid, block, smem, tmA, tmB, p);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int gemm_nvf4_tile_n(int kdim, int n) {
+    // a 256-wide tile halves the MMA issues per weight byte but leaves room for
+    // only one accumulator, so its epilogue is not overlapped: worth it when the
+    // main loop per tile is long
+    // (measured: 256 wins for K = 7168, loses for K <= 2048)
+    return (kdim >= 4096 && n >= 256) ? 256 : 128;
 }
 
 cudaError_t launch_gemm_nvf4(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const GemmParams& p, int num_sms) {
-    const dim3 grid(num_sms), block(kNumThreads);
-    switch (epilogue) {
-        case kEpiFc1Quant: return c.launch(gemm_nvf4_kernel<kEpiFc1Quant>, grid, block, kSmemBytes, tmA, tmB, p);
-        case kEpiFc1F32: return c.launch(gemm_nvf4_kernel<kEpiFc1F32>, grid, block, kSmemBytes, tmA, tmB, p);
-        case kEpiFc2Store: return c.launch(gemm_nvf4_kernel<kEpiFc2Store>, grid, block, kSmemBytes, tmA, tmB, p);
-        case kEpiFc2Scatter: return c.launch(gemm_nvf4_kernel<kEpiFc2Scatter>, grid, block, kSmemBytes, tmA, tmB, p);
-        default: return cudaErrorInvalidValue;
-    }
+                             const GemmParams& p, int num_sms, int tile_n) {
+    return tile_n == 256 ? launch_bn<256>(c, epilogue, tmA, tmB, p, num_sms)
+                         : launch_bn<128>(c, epilogue, tmA, tmB, p, num_sms);
 }
 
 }  // namespace moe

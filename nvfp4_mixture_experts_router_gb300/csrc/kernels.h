@@ -111,7 +111,9 @@ cudaError_t setup_gemm_kernels();
 cudaError_t setup_gemm_w4a16_kernels();
 cudaError_t launch_gemm_w4a16(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmBq,
                               const GemmParams& p, int num_sms);
+// tile_n = gemm_nvf4_tile_n(kdim, n) (128 or 256); tmB's box must be tile_n rows high
+int gemm_nvf4_tile_n(int kdim, int n);
 cudaError_t launch_gemm_nvf4(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const GemmParams& p, int num_sms);
+                             const GemmParams& p, int num_sms, int tile_n);
 
 }  // namespace moe

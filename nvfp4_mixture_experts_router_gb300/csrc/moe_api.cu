@@ -89,10 +89,10 @@ moe_status validate_shape(moe_shape s, uint32_t flags) {
 // box_bytes x 128-row boxes.  128-byte boxes use the 128-byte swizzle (the
 // canonical K-major UMMA operand layout); narrower boxes are unswizzled.
 bool encode_operand_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes,
-                        uint32_t box_bytes = 128) {
+                        uint32_t box_bytes = 128, uint32_t box_rows = 128) {
     const cuuint64_t dims[2] = {row_bytes, rows};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_bytes, 128};
+    const cuuint32_t box[2] = {box_bytes, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -290,11 +290,12 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
                           y_acc);
     if (e != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
+    const int tn1 = gemm_nvf4_tile_n(s.H, N1), tn2 = gemm_nvf4_tile_n(s.I, s.H);
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
     if (!encode_operand_map(&tmA1, xq_codes, W.rows_cap, (uint64_t)s.H / 2) ||
-        !encode_operand_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2) ||
+        !encode_operand_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 128, tn1) ||
         !encode_operand_map(&tmA2, hq_codes, W.rows_cap, (uint64_t)s.I / 2) ||
-        !encode_operand_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2))
+        !encode_operand_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 128, tn2))
         return MOE_ERR_CUDA;
 
     GemmParams g1p{};
@@ -327,7 +328,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         g1p.out_sf = hq_sf;
         epi1 = kEpiFc1Quant;
     }
-    e = launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms);
+    e = launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms, tn1);
     if (e != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
     if (per_token) {
         e = launch_quantize_h(c, W.rows_cap, s.I, meta, route_of_row, reinterpret_cast<const float*>(wsp(W.h_f32)),
@@ -367,7 +368,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         g2p.out_f32 = y_acc;
         epi2 = kEpiFc2Scatter;
     }
-    e = launch_gemm_nvf4(c, epi2, tmA2, tmB2, g2p, sms);
+    e = launch_gemm_nvf4(c, epi2, tmA2, tmB2, g2p, sms, tn2);
     if (e != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
 
     if (det)

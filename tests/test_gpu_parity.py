@@ -93,6 +93,19 @@ def test_matrix_parity(T, H, I, E, K, mode, act, on_input, det):
     full_parity(c)
 
 
+WIDE = [(384, 4096, 0, 0, False, False), (384, 4096, 1, 1, True, True), (4096, 384, 0, 1, True, False),
+        (4096, 384, 1, 0, False, True), (4096, 384, 2, 1, False, False), (384, 4096, 2, 0, True, True)]
+
+
+@pytest.mark.parametrize("H,I,mode,act,on_input,det", WIDE)
+def test_wide_tile_parity(H, I, mode, act, on_input, det):
+    """Reduction lengths >= 4096 select 256-wide weight tiles (two scale
+    movers); segments of 384 weight rows end in a 128-wide tail tile."""
+    c = synth.MoEConfig("wide", 40, H, I, 3, 2, act=act, mode=mode, router_on_input=on_input,
+                        deterministic=det, seed=77 + mode + act, logits="normal")
+    full_parity(c)
+
+
 def test_mid_config_parity():
     """configs: mid W4A4 (T=512, H=2048, I=768, E=64, top-6, per-token,
     router weight on input, logit bias skew)."""
