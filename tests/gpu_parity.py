@@ -181,11 +181,31 @@ def _e4m3_values(b: np.ndarray) -> np.ndarray:
     return np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * 2.0 ** (e.astype(np.float64) - 7))
 
 
-def check_fc2_input(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray, G2, prepared: dict):
+class W2Colmax:
+    """Per-expert (max_n |W2q[n, j]| over the oracle's dequantized FC2
+    weight, Gw2), from an oracle `prepared` cache or computed on demand."""
+
+    def __init__(self, prepared=None, weights=None):
+        self.prepared, self.weights, self.cache = prepared, weights, {}
+
+    def __getitem__(self, e):
+        if e not in self.cache:
+            if self.prepared is not None and e in self.prepared:
+                w2op, gw2 = self.prepared[e][2], self.prepared[e][3]
+            else:
+                pm = oracle.prepare_matrix(self.weights(e)[1])
+                w2op, gw2 = pm.operand(), float(pm.G)
+            self.cache[e] = (np.abs(w2op).max(axis=0), gw2)
+        return self.cache[e]
+
+
+def check_fc2_input(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray, G2, prepared):
     """FC2-input code identity and the per-token output slack of the routes
     whose FC2 input differs (see module docstring)."""
     n_tok = len(ref.tokens)
     slack = np.zeros(n_tok)
+    if not isinstance(prepared, W2Colmax):
+        prepared = W2Colmax(prepared)
     if (layer.flags & (3 << 2)) == api.MOE_W4A16:
         return _check_fc2_input_bf16(layer, ref, ror, prepared, slack)
     I, K = layer.I, layer.K
@@ -202,7 +222,6 @@ def check_fc2_input(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray, G2
     assert_mostly_identical(got, want, "FC2-input codes")
     got_sf = sf_rowmajor(sfbuf, rows, I)
     pos = {int(t): i for i, t in enumerate(ref.tokens)}
-    colmax = {}
     for i, r in enumerate(routes):
         g2g = float(g2_gpu[rows[i]]) if per_token else float(G2)
         g2r = float(ref.G2[r])
@@ -210,14 +229,12 @@ def check_fc2_input(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray, G2
         if same:
             continue
         t, k = divmod(r, K)
-        e = int(ref.ids[t, k])
-        if e not in colmax:
-            colmax[e] = np.abs(prepared[e][2]).max(axis=0)
+        colmax, gw2 = prepared[int(ref.ids[t, k])]
         sg = np.repeat(_e4m3_values(got_sf[i]), 16)
         sr = np.repeat(_e4m3_values(ref.h_sf[r]), 16)
         d = np.abs(_e2m1_values(got[i]) * sg * g2g - _e2m1_values(want[i]) * sr * g2r)
         wk = 1.0 if layer.flags & api.MOE_ROUTER_W_ON_INPUT else float(ref.w[t, k])
-        slack[pos[t]] += wk * prepared[e][3] * float(np.dot(d, colmax[e]))
+        slack[pos[t]] += wk * gw2 * float(np.dot(d, colmax))
     return frac, slack
 
 
@@ -239,17 +256,14 @@ def _check_fc2_input_bf16(layer, ref, ror, prepared, slack):
     far = np.abs(gv - wv) > ulp + 1e-5 * rowmax
     assert not far.any(), f"FC2-input BF16 values beyond one ulp + 1e-5 * row max: {int(far.sum())}"
     pos = {int(t): i for i, t in enumerate(ref.tokens)}
-    colmax = {}
     for i, r in enumerate(routes):
         if np.array_equal(got[i], want[i]):
             continue
         t, k = divmod(r, K)
-        e = int(ref.ids[t, k])
-        if e not in colmax:
-            colmax[e] = np.abs(prepared[e][2]).max(axis=0)
+        colmax, gw2 = prepared[int(ref.ids[t, k])]
         d = np.abs(oracle.bf16_bits_to_f64(got[i]) - oracle.bf16_bits_to_f64(want[i]))
         wk = 1.0 if layer.flags & api.MOE_ROUTER_W_ON_INPUT else float(ref.w[t, k])
-        slack[pos[t]] += wk * prepared[e][3] * float(np.dot(d, colmax[e]))
+        slack[pos[t]] += wk * gw2 * float(np.dot(d, colmax))
     return frac, slack
 
 
@@ -281,3 +295,63 @@ def full_parity(c: synth.MoEConfig, tokens=None):
     rel = check_y(y, ref, slack)
     return dict(code_match=frac, y_rel_err=rel, layer=layer, y=y, ref=ref, inp=inp,
                 flipped_tokens=int(np.sum(slack > 0)))
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: everything that is cheap for the oracle on all tokens,
+# the expert MLPs on a seeded token sample
+# ---------------------------------------------------------------------------
+
+def check_x_quant_all(layer: api.MoELayer, x_np: np.ndarray, G1, ror: np.ndarray):
+    """NVFP4 codes and scales of x for every token and every one of its K
+    permuted rows, bit for bit."""
+    T, K, H = layer.T, layer.K, layer.H
+    x32 = oracle.bf16_bits_to_f64(x_np).astype(np.float32)
+    G = oracle.row_global_scale(x32) if layer.flags & api.MOE_W4A4_PER_TOKEN else np.float32(G1)
+    codes_ref, sf_ref = oracle.quant_rows(x32, G)
+    cap = layer.layout()["rows_cap"]
+    codes = layer.view("xq_codes", torch.uint8, cap * H // 2).view(cap, H // 2)
+    sfbuf = layer.view("xq_sf", torch.uint8, cap * H // 16).cpu().numpy()
+    rr = ror.reshape(T, K)
+    for k in range(K):
+        rows = rr[:, k]
+        got = codes[torch.as_tensor(rows, device=codes.device, dtype=torch.long)].cpu().numpy()
+        assert np.array_equal(got, codes_ref), f"x codes differ (slot {k})"
+        assert np.array_equal(sf_rowmajor(sfbuf, rows, H), sf_ref), f"x scales differ (slot {k})"
+
+
+def fullsize_parity(c: synth.MoEConfig, n_tokens: int):
+    dev = "cuda"
+    x = synth.gen_x(c, dev)
+    logits = synth.gen_logits(c, dev, x)
+    bias = synth.gen_bias(c, dev)
+    x_np, logits_np = bits(x), logits.cpu().numpy()
+    bias_np = None if bias is None else bias.cpu().numpy()
+    layer = api.MoELayer.create(c.T, c.H, c.I, c.E, c.K, c.flags())
+    w1 = synth.gen_w1(c, dev)
+    w2 = synth.gen_w2(c, dev)
+    layer.prepare(w1, w2)
+    torch.cuda.synchronize()
+    del w1, w2
+
+    def weights(e):
+        return (bits(synth.gen_w1_expert(c, e, dev)), bits(synth.gen_w2_expert(c, e, dev)))
+
+    tokens = synth.sample_tokens(c, n_tokens)
+    L = oracle_layer(c)
+    G1 = G2 = None
+    if c.mode == synth.MODE_PER_TENSOR:
+        G1 = np.float32(oracle.tensor_global_scale(oracle.bf16_bits_to_f64(x_np).astype(np.float32)))
+        G2 = np.float32(oracle.fc2_input_scale(L, x_np, logits_np, bias_np, weights, G1, tokens=tokens))
+    g1 = None if G1 is None else torch.tensor([G1], device=dev)
+    g2 = None if G2 is None else torch.tensor([G2], device=dev)
+    y = layer.forward(x, logits, bias, g1, g2)
+    torch.cuda.synchronize()
+    assert api.moe_nvfp4_last_device_status(layer.workspace) == api.MOE_OK
+    ref = oracle.forward(L, x_np, logits_np, bias_np, weights, G1=G1, G2=G2, tokens=tokens)
+    ror = check_routing(layer, ref)
+    if c.mode != synth.MODE_W4A16:
+        check_x_quant_all(layer, x_np, G1, ror)
+    frac, slack = check_fc2_input(layer, ref, ror, G2, W2Colmax(None, weights))
+    rel = check_y(y, ref, slack)
+    return dict(code_match=frac, y_rel_err=rel, flipped_tokens=int(np.sum(slack > 0)))

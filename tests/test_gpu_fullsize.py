@@ -1,0 +1,48 @@
+"""Parity at the workloads' full sizes, through the same entry point and
+launch configuration the benchmark times: routing, permutation and the x
+quantization checked bit for bit on every token, the expert MLPs (FC2-input
+codes and y) on a seeded sample of tokens the oracle computes one by one."""
+import pytest
+
+from nvfp4_mixture_experts_router_gb300 import api, build, synth
+
+from gpu_parity import fullsize_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    api.lib()
+
+
+def test_dsv3_shape_T4096_deterministic():
+    """DeepSeek-V3-like expert shape: T=4096, H=7168, I=2048, E=256, top-8,
+    per-tensor scales, deterministic finalize."""
+    r = fullsize_parity(synth.config(2, 4096), n_tokens=24)
+    assert r["code_match"] >= 0.999
+
+
+def test_w4a16_T4096():
+    """W4A16: T=4096, H=4096, I=1536, E=128, top-8, ReLU2, fused finalize."""
+    fullsize_parity(synth.config(3, 4096), n_tokens=24)
+
+
+def test_prefill_T16384_zipf():
+    """Prefill scale: T=16384, H=7168, I=2048, E=256, top-8, per-token
+    scales, Zipf-skewed expert popularity (one expert takes most tokens,
+    others none)."""
+    import numpy as np
+    import oracle
+    c = synth.config(4)
+    ids, _ = oracle.router(synth.gen_logits(c).numpy(), synth.gen_bias(c).numpy(), c.K)
+    count = np.bincount(ids.reshape(-1), minlength=c.E)
+    assert count.max() >= 10 * count.mean() and (count == 0).any()
+    r = fullsize_parity(c, n_tokens=16)
+    assert r["code_match"] >= 0.999
+
+
+def test_dsv3_shape_single_token():
+    """T=1 at DSV3 shape: eight experts with one route each."""
+    fullsize_parity(synth.config(2, 1), n_tokens=1)
