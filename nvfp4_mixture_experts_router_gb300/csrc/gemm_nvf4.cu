@@ -15,11 +15,16 @@
 //               one BNx128-byte B tile (cp.async.bulk.tensor, 128-byte
 //               swizzle) plus the matching scale atoms of each operand
 //               (cp.async.bulk), all completing on one mbarrier.
-//   warp 2      scale mover: once a stage has landed, tcgen05.cp of its
-//               scale atoms into the stage's tensor-memory slot, then
-//               tcgen05.commit to the stage's sf_ready barrier (with BN = 256
-//               the B scales go to a second mover warp, the last warp: 12
-//               copies per stage are too many for one issuing thread).
+//   warps 2-5   scale writers, one per tensor-memory lane quadrant: once a
+//               stage's scale atoms have landed (their own barrier, loaded
+//               ahead of the operand tiles), every lane reads its 16-byte
+//               atom row per k-block from shared memory and writes them with
+//               tcgen05.st into the stage's tensor-memory slot; the four
+//               quadrants together form the replicated layout the
+//               block-scaled MMA reads (the same image tcgen05.cp .warpx4
+//               would produce).  tcgen05.cp was measured at ~100 cycles of
+//               copy-engine time per 512-byte atom, which capped a stage of
+//               eight atoms at ~800 cycles whatever the memory traffic.
 //   warp 1      allocates 512 tensor-memory columns; lane 0 issues, per
 //               stage, four 128xBNx64 block-scaled MMAs into an FP32
 //               accumulator in tensor memory, then tcgen05.commit frees the
@@ -27,7 +32,7 @@
 //               scarce resource (~130 cycles per MMA measured), so scale
 //               copies come from another warp and BN = 256 doubles the
 //               weight bytes each MMA consumes.
-//   warps 3..   epilogue: tcgen05.ld of the accumulator (warp w reads lanes
+//   warps 6..   epilogue: tcgen05.ld of the accumulator (warp w reads lanes
 //               32*(w%4)..+31, one output row per thread; with BN = 256 a
 //               second group of four warps takes columns 128..255), fused
 //               activation / scaling / requantization / scatter, then
@@ -60,8 +65,9 @@ struct Cfg {
     static constexpr int kStages = BN == 128 ? 6 : 4;
     static constexpr int kAccBufs = BN == 128 ? 2 : 1;
     static constexpr int kEpiWarps = BN == 128 ? 4 : 8;
-    static constexpr int kMovers = BN == 128 ? 1 : 2;            // scale-copy issuing warps
-    static constexpr int kNumThreads = (2 + kMovers + kEpiWarps) * 32;
+    static constexpr int kSfWarps = 4;                           // scale writers, one per lane quadrant
+    static constexpr int kEpiWarp0 = 2 + kSfWarps;
+    static constexpr int kNumThreads = (kEpiWarp0 + kEpiWarps) * 32;
     static constexpr int kRowBlocks = BN / 128;                  // 128-row scale blocks of B
     static constexpr int kTileBytesB = BN * kBKBytes;
     static constexpr int kSfBytesB = kRowBlocks * kSfBytesA;
@@ -78,6 +84,7 @@ struct Smem {
     uint8_t* sfa;
     uint8_t* sfb;
     uint64_t* full;
+    uint64_t* sf_full;
     uint64_t* empty;
     uint64_t* sf_ready;
     uint64_t* acc_full;
@@ -98,9 +105,10 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     s.sfb = s.sfa + C::kStages * kSfBytesA;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s.sfb + C::kStages * C::kSfBytesB);
     s.full = bars;
-    s.empty = bars + C::kStages;
-    s.sf_ready = bars + 2 * C::kStages;               // [kMovers][kStages]
-    s.acc_full = bars + (2 + C::kMovers) * C::kStages;
+    s.sf_full = bars + C::kStages;
+    s.empty = bars + 2 * C::kStages;
+    s.sf_ready = bars + 3 * C::kStages;
+    s.acc_full = bars + 4 * C::kStages;
     s.acc_empty = s.acc_full + 2;
     s.drain = s.acc_empty + 2;
     s.tmem_holder = reinterpret_cast<uint32_t*>(s.drain + 1);
@@ -123,14 +131,15 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&s.full[i], 1);
+            mbar_init(&s.sf_full[i], 1);
             mbar_init(&s.empty[i], 1);
-            for (int m = 0; m < C::kMovers; ++m) mbar_init(&s.sf_ready[m * C::kStages + i], 1);
+            mbar_init(&s.sf_ready[i], C::kSfWarps * 32);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.acc_full[i], 1);
             mbar_init(&s.acc_empty[i], C::kEpiWarps * 32);
         }
-        mbar_init(s.drain, 1 + C::kMovers);   // the MMA thread and the scale movers retire their ops into it
+        mbar_init(s.drain, 1);   // the MMA thread retires its MMAs into it
         *s.abort = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
@@ -177,16 +186,18 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
                     if (!mbar_wait(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
                     const int nkb = min(4, kblocks - 4 * ks);
                     const uint32_t sf_bytes = (uint32_t)nkb * 512u;
-                    mbar_arrive_expect_tx(&s.full[stage],
-                                          kTileBytesA + C::kTileBytesB + (uint32_t)(1 + nrb) * sf_bytes);
-                    tma_load_2d(s.a + stage * kTileBytesA, &tmA, &s.full[stage], ks * kBKBytes, a_row, pol);
-                    tma_load_2d(s.b + stage * C::kTileBytesB, &tmB, &s.full[stage], ks * kBKBytes, b_row, pol);
-                    bulk_load(s.sfa + stage * kSfBytesA, sfa_src + (size_t)ks * 4 * 512, sf_bytes, &s.full[stage],
-                              pol);
+                    // the small scale atoms first, on their own barrier, so the
+                    // scale movers can start while the operand tiles are in flight
+                    mbar_arrive_expect_tx(&s.sf_full[stage], (uint32_t)(1 + nrb) * sf_bytes);
+                    bulk_load(s.sfa + stage * kSfBytesA, sfa_src + (size_t)ks * 4 * 512, sf_bytes,
+                              &s.sf_full[stage], pol);
                     for (int rb = 0; rb < nrb; ++rb)
                         bulk_load(s.sfb + stage * C::kSfBytesB + rb * kSfBytesA,
-                                  sfb_src + ((size_t)rb * kblocks + (size_t)ks * 4) * 512, sf_bytes, &s.full[stage],
-                                  pol);
+                                  sfb_src + ((size_t)rb * kblocks + (size_t)ks * 4) * 512, sf_bytes,
+                                  &s.sf_full[stage], pol);
+                    mbar_arrive_expect_tx(&s.full[stage], kTileBytesA + C::kTileBytesB);
+                    tma_load_2d(s.a + stage * kTileBytesA, &tmA, &s.full[stage], ks * kBKBytes, a_row, pol);
+                    tma_load_2d(s.b + stage * C::kTileBytesB, &tmB, &s.full[stage], ks * kBKBytes, b_row, pol);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -209,10 +220,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
                     const int nkb = min(4, kblocks - 4 * ks);
                     const uint32_t sfa_t = tmem_base + C::kSfColBase + (uint32_t)stage * C::kSfColsPerStage;
                     const uint32_t sfb_t = sfa_t + 16;
-                    // the scale movers' copies for this stage have completed
-                    for (int m = 0; m < C::kMovers; ++m)
-                        if (!mbar_wait(&s.sf_ready[m * C::kStages + stage], phase, s.abort, p.status, kStatusTimeoutMma))
-                            goto done;
+                    // the scale writers' stores for this stage are done
+                    if (!mbar_wait(&s.sf_ready[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
                     tc_fence_after();
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(s.a + stage * kTileBytesA));
                     const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(s.b + stage * C::kTileBytesB));
@@ -228,47 +237,68 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
                 if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
             }
         }
-    } else if (warp == 2 || (C::kMovers == 2 && warp == 2 + C::kMovers + C::kEpiWarps - 1)) {
-        // scale mover(s): mover 0 copies A's scales (and B's when it is the
-        // only one), mover 1 copies B's scales
-        const int mover = warp == 2 ? 0 : 1;
-        const bool do_a = mover == 0, do_b = C::kMovers == 1 || mover == 1;
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-                const int n_tile = tile % n_tiles;
-                const int nrb = min(C::kRowBlocks, rb_per_expert - n_tile * C::kRowBlocks);
-                for (int ks = 0; ks < kstages; ++ks) {
-                    if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
-                    tc_fence_after();
-                    const int nkb = min(4, kblocks - 4 * ks);
-                    const uint32_t sfa_t = tmem_base + C::kSfColBase + (uint32_t)stage * C::kSfColsPerStage;
-                    const uint32_t sfb_t = sfa_t + 16;
-                    for (int j = 0; j < nkb; ++j) {
-                        if (do_a)
-                            tc_cp_sf_atom(sfa_t + 4 * j, sdesc_sf_atom(smem_u32(s.sfa + stage * kSfBytesA + j * 512)));
-                        if (do_b)
-                            for (int rb = 0; rb < nrb; ++rb)
-                                tc_cp_sf_atom(sfb_t + C::kSfColsB * j + 4 * rb,
-                                              sdesc_sf_atom(smem_u32(s.sfb + stage * C::kSfBytesB + rb * kSfBytesA +
-                                                                     j * 512)));
-                    }
-                    tc_commit(&s.sf_ready[mover * C::kStages + stage]);
-                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+    } else if (warp < C::kEpiWarp0) {
+        // scale writer for lane quadrant warp % 4: lane l holds row l of each
+        // 512-byte atom (4 words = the 4 column slots of rows l, l+32, l+64, l+96)
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            for (int ks = 0; ks < kstages; ++ks) {
+                // warp-uniform outcome: tcgen05.st below is a warp-collective instruction
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&s.sf_full[stage], phase, s.abort, p.status, kStatusTimeoutMma)))
+                    goto done;
+                const uint32_t sfa_t = tmem_base + C::kSfColBase + (uint32_t)stage * C::kSfColsPerStage;
+                const uint32_t sfb_t = sfa_t + 16;
+                uint32_t ra[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(s.sfa + stage * kSfBytesA + j * 512 + lane * 16);
+                    ra[4 * j] = v.x; ra[4 * j + 1] = v.y; ra[4 * j + 2] = v.z; ra[4 * j + 3] = v.w;
                 }
+                tmem_st16(sfa_t + lane_off, ra);
+                if (C::kRowBlocks == 1) {
+                    uint32_t rb_[16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(s.sfb + stage * C::kSfBytesB + j * 512 + lane * 16);
+                        rb_[4 * j] = v.x; rb_[4 * j + 1] = v.y; rb_[4 * j + 2] = v.z; rb_[4 * j + 3] = v.w;
+                    }
+                    tmem_st16(sfb_t + lane_off, rb_);
+                } else {
+                    // k-block j: 8 columns, row block 0 then row block 1
+                    uint32_t rb_[32];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int rb = 0; rb < 2; ++rb) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(s.sfb + stage * C::kSfBytesB +
+                                                                            rb * kSfBytesA + j * 512 + lane * 16);
+                            rb_[8 * j + 4 * rb] = v.x; rb_[8 * j + 4 * rb + 1] = v.y;
+                            rb_[8 * j + 4 * rb + 2] = v.z; rb_[8 * j + 4 * rb + 3] = v.w;
+                        }
+                    tmem_st32(sfb_t + lane_off, rb_);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&s.sf_ready[stage]);
+                if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
             }
         }
     } else {
         const int q = warp & 3;                    // tensor-memory lane quadrant of this warp
-        const int half = (warp - 3) >> 2;          // which 128 accumulator columns (BN = 256)
+        const int half = (warp - C::kEpiWarp0) >> 2;   // which 128 accumulator columns (BN = 256)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const int m_tile = tile / n_tiles, n_tile = tile % n_tiles;
             const int e = p.tile_expert[m_tile];
             if (e < 0 || e >= p.num_experts) break;
-            if (!mbar_wait(&s.acc_full[acc], acc_phase, s.abort, p.status, kStatusTimeoutEpilogue)) break;
+            // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.acc_full[acc], acc_phase, s.abort, p.status,
+                                                   kStatusTimeoutEpilogue)))
+                break;
             tc_fence_after();
             const int width = min(BN, p.n - n_tile * BN);
             if (half * 128 < width) {
@@ -289,11 +319,11 @@ done:
     if (*s.abort) {
         // Something timed out: let in-flight copies land and retire every
         // issued MMA and scale copy before the memories go away.
-        const bool issues_tc = warp == 1 || warp == 2 || (C::kMovers == 2 && warp == 2 + C::kMovers + C::kEpiWarps - 1);
-        if (issues_tc && lane == 0) {
+        if (warp == 1 && lane == 0) {
             tc_commit(s.drain);
             mbar_wait(s.drain, 0, &no_abort, p.status, kStatusTimeoutMma);
         }
+        if (warp >= 2 && warp < C::kEpiWarp0) tmem_st_wait();   // scale writers' stores in flight
         for (int i = 0; i < 100; ++i) __nanosleep(10000);
     }
     tc_fence_before();

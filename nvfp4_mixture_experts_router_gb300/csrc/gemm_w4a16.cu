@@ -204,7 +204,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         uint32_t phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             for (int kb = 0; kb < kblocks; ++kb) {
-                if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutProducer)) goto done;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutProducer)))
+                    goto done;
                 const uint4 c0 = *reinterpret_cast<const uint4*>(s.q + stage * kTileBytesQ + r * 32);
                 const uint4 c1 = *reinterpret_cast<const uint4*>(s.q + stage * kTileBytesQ + r * 32 + 16);
                 const uint32_t sfw = *reinterpret_cast<const uint32_t*>(s.sf + stage * kSfBytes + sf_off);
@@ -229,7 +231,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int m_tile = tile / n_tiles, n_tile = tile % n_tiles;
             const int e = p.tile_expert[m_tile];
             if (e < 0 || e >= p.num_experts) break;
-            if (!mbar_wait(&s.acc_full[acc], acc_phase, s.abort, p.status, kStatusTimeoutEpilogue)) break;
+            // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.acc_full[acc], acc_phase, s.abort, p.status,
+                                                   kStatusTimeoutEpilogue)))
+                break;
             tc_fence_after();
             const int row = m_tile * kBM + q * 32 + lane;
             const int route = p.route_of_row[row];
