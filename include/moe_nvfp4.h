@@ -80,7 +80,15 @@ typedef enum {
 /* bit 6: router weights are the full softmax over all E experts evaluated
  * at the selected ones, instead of the softmax over the K selected. */
 #define MOE_ROUTE_NO_RENORM (1u << 6)
-#define MOE_FLAGS_KNOWN 0x7Fu
+/* bits 7-8: GEMM tile scheduling (W4A4 only; results are the same either
+ * way up to FP32 accumulation order).  MOE_GEMM_PAIRS_ALWAYS runs each GEMM
+ * whose weight height is a multiple of 256 on CTA pairs (cta_group::2
+ * MMAs, 256 x 256 tiles over two 128-row M tiles of one expert); the default
+ * and MOE_GEMM_PAIRS_NEVER run them on single CTAs, which measured faster
+ * on every configuration so far.  Setting both is invalid. */
+#define MOE_GEMM_PAIRS_NEVER (1u << 7)
+#define MOE_GEMM_PAIRS_ALWAYS (1u << 8)
+#define MOE_FLAGS_KNOWN 0x1FFu
 
 /* ---- shapes ---------------------------------------------------------------- */
 typedef struct {
@@ -190,12 +198,15 @@ typedef struct {
     uint64_t count;          /* int32 [E]   routes per expert                */
     uint64_t offsets;        /* int32 [E+1] exclusive prefix of count        */
     uint64_t padded_offsets; /* int32 [E+1] prefix of count rounded up to 128*/
-    uint64_t meta;           /* int32 [4]: [0] padded rows, [1] M tiles      */
+    uint64_t meta;           /* int32 [4]: [0] padded rows, [1] M tiles,     */
+                             /*   [2] M-tile pairs (tile_pair entries)       */
     uint64_t unit_base;      /* int32 [E][ceil(T/32)] per-unit starting rows */
     uint64_t unit_mask;      /* uint32 [E][ceil(T/32)] per-unit token masks  */
     uint64_t row_of_route;   /* int32 [T*K] padded row of route t*K+k        */
     uint64_t route_of_row;   /* int32 [rows_cap] route of a row, -1 in pads  */
     uint64_t tile_expert;    /* int32 [rows_cap/128] expert of each M tile   */
+    uint64_t tile_pair;      /* int32 [rows_cap/128] M-tile pairs of one     */
+                             /*   expert: (first tile << 1) | has_second     */
     uint64_t g1;             /* f32   [T] FC1-input global scale per token   */
     uint64_t xq_codes;       /* u8    [rows_cap][H/2] permuted x codes       */
     uint64_t xq_sf;          /* u8    [rows_cap/128][H/64][512] x scales     */
@@ -210,7 +221,7 @@ typedef struct {
     uint64_t total;          /* workspace bytes                              */
 } moe_workspace_layout;
 
-#define MOE_WORKSPACE_VERSION 2
+#define MOE_WORKSPACE_VERSION 3
 
 /* Fill `out` with the workspace layout for this shape and flags.  Regions a
  * mode does not use have offset UINT64_MAX.  Pure host call, no CUDA. */

@@ -30,6 +30,8 @@ MOE_W4A16 = 2 << 2
 MOE_ROUTER_W_ON_INPUT = 1 << 4
 MOE_FINALIZE_DETERMINISTIC = 1 << 5
 MOE_ROUTE_NO_RENORM = 1 << 6
+MOE_GEMM_PAIRS_NEVER = 1 << 7
+MOE_GEMM_PAIRS_ALWAYS = 1 << 8
 
 
 class MoEError(RuntimeError):
@@ -44,7 +46,7 @@ class moe_shape(ctypes.Structure):
 
 
 _LAYOUT_FIELDS = ["rows_cap", "status", "topk_ids", "topk_w", "count", "offsets", "padded_offsets", "meta",
-                  "unit_base", "unit_mask", "row_of_route", "route_of_row", "tile_expert", "g1", "xq_codes", "xq_sf", "h_f32",
+                  "unit_base", "unit_mask", "row_of_route", "route_of_row", "tile_expert", "tile_pair", "g1", "xq_codes", "xq_sf", "h_f32",
                   "g2", "hq_codes", "hq_sf", "x_bf16_perm", "h_bf16", "o_bf16", "y_acc", "total"]
 
 

@@ -124,26 +124,38 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// CLUSTER = true: acquire at cluster scope, for phases completed by arrivals
+// from the other CTA of a pair.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
+    if (CLUSTER)
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
 // Bounded wait for the phase with `parity`.  Gives up (returns false) when
 // *abort is set by another role or after kWaitLimitNs; in the latter case it
 // sets *abort and ORs `err_bit` into the global status word.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned int* status, uint32_t err_bit) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -241,8 +253,6 @@ constexpr uint32_t kSwizzleNone = 0, kSwizzle128B = 2;
 __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     return sdesc(saddr, 16, 1024, kSwizzle128B);
 }
-// Scale-factor source of tcgen05.cp.32x128b: 32 rows x 16 B, contiguous.
-__device__ __forceinline__ uint64_t sdesc_sf_atom(uint32_t saddr) { return sdesc(saddr, 0, 128, kSwizzleNone); }
 
 // Instruction descriptor, block-scaled MMA kind::mxf4nvf4 with E2M1 A and B
 // (format code 1 at bits 7-9 / 10-12), K-major both, UE4M3 scales (bit 23 =
@@ -275,10 +285,76 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
         : "memory");
 }
 
-// Copy one 512-byte scale atom (32 rows x 16 B) from shared memory into 4
-// tensor-memory columns, replicated into all four 32-lane sub-partitions.
-__device__ __forceinline__ void tc_cp_sf_atom(uint32_t taddr, uint64_t sdesc_src) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc_src) : "memory");
+// ---------------------------------------------------------------------------
+// CTA pairs (thread-block clusters of 2) and the pair-wide tcgen05 forms
+// ---------------------------------------------------------------------------
+// In a kernel that uses cta_group::2 every tcgen05 instruction carrying a
+// cta_group qualifier (alloc, dealloc, relinquish, mma, commit) uses ::2.
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of both CTAs (warp-uniform call sites only).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared::cluster address of this CTA's shared-memory object `p` in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+// Arrive on an mbarrier of any CTA of the cluster, without release
+// semantics.  Used only where what the arrival announces is already complete
+// and visible (landed TMA copies, waited-for tensor-memory loads and stores):
+// a release at cluster scope made each such arrival wait for the SM's
+// outstanding memory traffic (0.5-3 us measured).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// Both CTAs of the pair each run this in one warp; the two allocations are
+// made together and sit at the same tensor-memory address in both.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_result, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_result)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// M = 256 block-scaled MMA over the CTA pair, issued by the even CTA: rows
+// 0..127 of A, D and the A scales live in the even CTA, rows 128..255 in the
+// odd one (same shared-memory / tensor-memory addresses); B is split by rows
+// (first half in the even CTA) and every CTA's tensor memory holds the B
+// scales of all N rows.
+__device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the mbarrier at `bar`'s offset in every CTA of `cta_mask` once all
+// previously issued pair MMAs of this thread have completed.
+__device__ __forceinline__ void tc_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
 }
 
 // Load 32 consecutive FP32 columns of this warp's 32 lanes.

@@ -8,10 +8,11 @@
 namespace moe {
 
 // Launch helper: every launch goes through cudaLaunchKernelEx so that the
-// programmatic-dependent-launch attribute can be set uniformly.
+// programmatic-dependent-launch and cluster attributes can be set uniformly.
 struct LaunchCtx {
     cudaStream_t stream = nullptr;
     bool pdl = false;
+    int cluster = 1;   // CTAs per thread-block cluster (x)
 
     template <typename... KArgs, typename... Args>
     cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, Args... args) const {
@@ -20,11 +21,22 @@ struct LaunchCtx {
         cfg.blockDim = block;
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchAttribute attr[2];
+        unsigned n = 0;
+        if (pdl) {
+            attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
+        if (cluster > 1) {
+            attr[n].id = cudaLaunchAttributeClusterDimension;
+            attr[n].val.clusterDim.x = (unsigned)cluster;
+            attr[n].val.clusterDim.y = 1;
+            attr[n].val.clusterDim.z = 1;
+            ++n;
+        }
         cfg.attrs = attr;
-        cfg.numAttrs = pdl ? 1 : 0;
+        cfg.numAttrs = n;
         return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
     }
 };
@@ -36,8 +48,10 @@ cudaError_t launch_router(const LaunchCtx& c, int T, int E, int K, const float* 
 cudaError_t launch_route_count(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
                                int renorm, int* ids, float* w, int* unit_cnt, uint32_t* unit_mask,
                                unsigned int* status_reset);
+// tile_pair may be null (then only meta[2] counts the pairs)
 cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
-                                int* padded_offsets, int* meta, int* tile_expert, int* route_of_row);
+                                int* padded_offsets, int* meta, int* tile_expert, int* tile_pair,
+                                int* route_of_row);
 cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base,
                            uint32_t* unit_mask, int* count, int* offsets, int* padded_offsets, int* meta,
                            int* tile_expert, int* row_of_route, int* route_of_row, unsigned int* status);
@@ -84,8 +98,9 @@ struct GemmParams {
     const uint8_t* sfb;          // B scales [E][N/128][kdim/64][512]
     int kdim;                    // reduction length (elements)
     int n;                       // output columns per expert (B rows per expert)
-    const int* meta;             // meta[1] = number of M tiles
+    const int* meta;             // meta[1] = number of M tiles, meta[2] = M-tile pairs
     const int* tile_expert;      // expert of each M tile
+    const int* tile_pair;        // (first M tile << 1) | has_second, per pair (pair kernel)
     const int* route_of_row;     // route of each padded row, -1 in pad rows
     int num_experts;             // E (bounds check of tile_expert)
     unsigned int* status;
@@ -115,5 +130,11 @@ cudaError_t launch_gemm_w4a16(const LaunchCtx& c, int epilogue, const CUtensorMa
 int gemm_nvf4_tile_n(int kdim, int n);
 cudaError_t launch_gemm_nvf4(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              const GemmParams& p, int num_sms, int tile_n);
+// gemm_nvf4_pair.cu — the same GEMMs on CTA pairs (256 x 256 pair tiles over
+// pairs of M tiles of one expert); needs n % 256 == 0 and a tmB box of 128
+// rows.  setup sizes the persistent grid for `device`.
+cudaError_t setup_gemm_pair_kernels(int device, int num_sms);
+cudaError_t launch_gemm_nvf4_pair(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                  const GemmParams& p, int device);
 
 }  // namespace moe

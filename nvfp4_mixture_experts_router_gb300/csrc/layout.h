@@ -103,6 +103,7 @@ inline moe_workspace_layout workspace_layout(moe_shape s, uint32_t flags) {
     L.row_of_route = take(4 * T * K);
     L.route_of_row = take(4 * cap);
     L.tile_expert = take(4 * (cap / kTileM));
+    L.tile_pair = take(4 * (cap / kTileM));
     if (mode != kModeW4A16) {
         L.g1 = take(4 * T);
         L.xq_codes = take(cap * H / 2);

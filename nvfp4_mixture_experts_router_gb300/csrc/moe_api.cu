@@ -26,7 +26,7 @@ std::mutex g_mu;
 DeviceState g_dev[64];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-moe_status device_state(int* sms) {
+moe_status device_state(int* sms, int* device = nullptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
@@ -42,7 +42,7 @@ moe_status device_state(int* sms) {
         } else if (major != 10 || minor != 3) {
             d.status = MOE_ERR_UNSUPPORTED;  // the binary carries sm_103a code only
         } else if (setup_routing_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess ||
-                   setup_gemm_w4a16_kernels() != cudaSuccess) {
+                   setup_gemm_w4a16_kernels() != cudaSuccess || setup_gemm_pair_kernels(dev, d.sms) != cudaSuccess) {
             d.status = MOE_ERR_CUDA;
         } else {
             d.status = MOE_OK;
@@ -60,6 +60,7 @@ moe_status device_state(int* sms) {
         }
     }
     *sms = d.sms;
+    if (device) *device = dev;
     return d.status;
 }
 
@@ -72,6 +73,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 moe_status validate_shape(moe_shape s, uint32_t flags) {
     if (flags & ~MOE_FLAGS_KNOWN) return MOE_ERR_INVALID_ARG;
+    if ((flags & MOE_GEMM_PAIRS_NEVER) && (flags & MOE_GEMM_PAIRS_ALWAYS)) return MOE_ERR_INVALID_ARG;
     if (act_of(flags) > 1 || mode_of(flags) > 2) return MOE_ERR_INVALID_ARG;
     if (s.T < 1 || s.T > (1 << 22)) return MOE_ERR_INVALID_ARG;
     if (s.H < 128 || s.H % 128 != 0 || s.H > 65536) return MOE_ERR_INVALID_ARG;
@@ -103,11 +105,20 @@ bool encode_operand_map(CUtensorMap* map, const void* base, uint64_t rows, uint6
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Run a W4A4 GEMM with `n` weight rows per expert on CTA pairs?  Only on
+// request: measured on every workload, the pair kernel's cross-CTA stage
+// handshake and its single (256-column) accumulator cost more than the
+// operand bytes it saves per SM.
+bool use_pair_gemm(moe_shape s, uint32_t flags, int n) {
+    (void)s;
+    return n % 256 == 0 && (flags & MOE_GEMM_PAIRS_ALWAYS) != 0;
+}
+
 }  // namespace
 
 extern "C" {
 
-const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.1 sm_103a (prepared v1, workspace v2)"; }
+const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.2 sm_103a (prepared v1, workspace v3)"; }
 
 size_t moe_nvfp4_prepared_bytes(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return 0;
@@ -167,8 +178,8 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         overlaps(y_bf16, y_bytes, router_logits, (size_t)s.T * s.E * 4))
         return MOE_ERR_INVALID_ARG;
 
-    int sms = 0;
-    st = device_state(&sms);
+    int sms = 0, device = 0;
+    st = device_state(&sms, &device);
     if (st != MOE_OK) return st;
 
     const PreparedLayout P = prepared_layout(s, flags);
@@ -204,7 +215,8 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     if (e != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
     e = launch_permute_scan(c, s.T, s.E, reinterpret_cast<int*>(wsp(W.unit_base)),
                             reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
-                            reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert, route_of_row);
+                            reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert,
+                            reinterpret_cast<int*>(wsp(W.tile_pair)), route_of_row);
     if (e != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
     // the quantize / gather kernel hands out the permuted rows itself
     RouteScatter rs;
@@ -290,13 +302,15 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
                           y_acc);
     if (e != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
-    const int tn1 = gemm_nvf4_tile_n(s.H, N1), tn2 = gemm_nvf4_tile_n(s.I, s.H);
+    const bool pair1 = use_pair_gemm(s, flags, N1), pair2 = use_pair_gemm(s, flags, s.H);
+    const int tn1 = pair1 ? 128 : gemm_nvf4_tile_n(s.H, N1), tn2 = pair2 ? 128 : gemm_nvf4_tile_n(s.I, s.H);
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
     if (!encode_operand_map(&tmA1, xq_codes, W.rows_cap, (uint64_t)s.H / 2) ||
         !encode_operand_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 128, tn1) ||
         !encode_operand_map(&tmA2, hq_codes, W.rows_cap, (uint64_t)s.I / 2) ||
         !encode_operand_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 128, tn2))
         return MOE_ERR_CUDA;
+    int* tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
 
     GemmParams g1p{};
     g1p.sfa = xq_sf;
@@ -305,6 +319,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     g1p.n = N1;
     g1p.meta = meta;
     g1p.tile_expert = tile_expert;
+    g1p.tile_pair = tile_pair;
     g1p.route_of_row = route_of_row;
     g1p.num_experts = s.E;
     g1p.status = status;
@@ -328,7 +343,8 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         g1p.out_sf = hq_sf;
         epi1 = kEpiFc1Quant;
     }
-    e = launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms, tn1);
+    e = pair1 ? launch_gemm_nvf4_pair(c, epi1, tmA1, tmB1, g1p, device)
+              : launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms, tn1);
     if (e != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
     if (per_token) {
         e = launch_quantize_h(c, W.rows_cap, s.I, meta, route_of_row, reinterpret_cast<const float*>(wsp(W.h_f32)),
@@ -344,6 +360,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     g2p.n = s.H;
     g2p.meta = meta;
     g2p.tile_expert = tile_expert;
+    g2p.tile_pair = tile_pair;
     g2p.route_of_row = route_of_row;
     g2p.num_experts = s.E;
     g2p.status = status;
@@ -368,7 +385,8 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         g2p.out_f32 = y_acc;
         epi2 = kEpiFc2Scatter;
     }
-    e = launch_gemm_nvf4(c, epi2, tmA2, tmB2, g2p, sms, tn2);
+    e = pair2 ? launch_gemm_nvf4_pair(c, epi2, tmA2, tmB2, g2p, device)
+              : launch_gemm_nvf4(c, epi2, tmA2, tmB2, g2p, sms, tn2);
     if (e != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
 
     if (det)

@@ -130,6 +130,7 @@ class MoEConfig:
     zipf_s: float = 1.1
     zipf_beta: float = 2.0
     w_std: float = 0.02
+    gemm_pairs: str = "auto"      # GEMM tile scheduling: "auto" | "never" | "always"
     extra: dict = field(default_factory=dict)
 
     @property
@@ -144,6 +145,10 @@ class MoEConfig:
             f |= 1 << 5
         if not self.renorm:
             f |= 1 << 6
+        if self.gemm_pairs == "never":
+            f |= 1 << 7
+        elif self.gemm_pairs == "always":
+            f |= 1 << 8
         return f
 
     def with_(self, **kw) -> "MoEConfig":

@@ -139,6 +139,14 @@ def check_routing(layer: api.MoELayer, ref: oracle.Result):
     tiles = layer.view("tile_expert", torch.int32, g.rows // 128).cpu().numpy()
     want = np.repeat(np.arange(E), (g.padded_offsets[1:] - g.padded_offsets[:-1]) // 128)
     assert np.array_equal(tiles, want), "tile -> expert map differs"
+    # pairs of consecutive M tiles of one expert: (first << 1) | has_second
+    pairs = []
+    for e in range(E):
+        t0, nt = g.padded_offsets[e] // 128, (g.padded_offsets[e + 1] - g.padded_offsets[e]) // 128
+        pairs += [((t0 + i) << 1) | int(i + 1 < nt) for i in range(0, nt, 2)]
+    assert meta[2] == len(pairs), "M-tile pair count differs"
+    got_pairs = layer.view("tile_pair", torch.int32, max(1, len(pairs))).cpu().numpy()[:len(pairs)]
+    assert np.array_equal(got_pairs, np.array(pairs, dtype=np.int32)), "M-tile pair map differs"
     return ror
 
 

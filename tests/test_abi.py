@@ -81,6 +81,9 @@ def test_invalid_arguments_rejected_before_cuda(L):
     assert f(s, 1 << 9, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, 3 << 2, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, 2, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    # contradictory GEMM scheduling hints
+    both = api.MOE_GEMM_PAIRS_NEVER | api.MOE_GEMM_PAIRS_ALWAYS
+    assert f(s, both, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     # null pointers
     assert f(s, 0, None, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, 0, A, B, None, A, A, A, W, wb, None, None) == api.MOE_ERR_INVALID_ARG

@@ -99,11 +99,37 @@ WIDE = [(384, 4096, 0, 0, False, False), (384, 4096, 1, 1, True, True), (4096, 3
 
 @pytest.mark.parametrize("H,I,mode,act,on_input,det", WIDE)
 def test_wide_tile_parity(H, I, mode, act, on_input, det):
-    """Reduction lengths >= 4096 select 256-wide weight tiles (two scale
-    movers); segments of 384 weight rows end in a 128-wide tail tile."""
+    """Reduction lengths >= 4096 select 256-wide weight tiles; segments of
+    384 weight rows end in a 128-wide tail tile."""
     c = synth.MoEConfig("wide", 40, H, I, 3, 2, act=act, mode=mode, router_on_input=on_input,
                         deterministic=det, seed=77 + mode + act, logits="normal")
     full_parity(c)
+
+
+PAIRS = []
+for T, H, I, E, K in [(1, 256, 128, 8, 2), (200, 256, 128, 8, 2), (300, 512, 256, 4, 2), (40, 256, 256, 16, 1),
+                      (333, 4096, 512, 4, 3)]:
+    for mode in (synth.MODE_PER_TENSOR, synth.MODE_PER_TOKEN):
+        for act in (0, 1):
+            for det in (False, True):
+                PAIRS.append((T, H, I, E, K, mode, act, det))
+
+
+@pytest.mark.parametrize("T,H,I,E,K,mode,act,det", PAIRS)
+def test_pair_gemm_parity(T, H, I, E, K, mode, act, det):
+    """GEMMs forced onto CTA pairs (256 x 256 tiles over two M tiles of one
+    expert): experts with an odd number of M tiles (half-filled pairs),
+    empty experts, one token, a reduction length of 4096, and ReLU2 shapes
+    whose FC1 (I = 128 rows) stays on single CTAs while FC2 runs on pairs."""
+    seed = (T * 17 + H + I * 3 + E * 5 + K + mode * 13 + act * 7 + det) % 1000
+    c = synth.MoEConfig("pair", T, H, I, E, K, act=act, mode=mode, router_on_input=act == 1, deterministic=det,
+                        seed=seed, logits="normal", gemm_pairs="always")
+    full_parity(c)
+
+
+def test_mid_config_parity_on_pairs():
+    """The mid workload with both GEMMs forced onto CTA pairs."""
+    full_parity(synth.config(1).with_(gemm_pairs="always"))
 
 
 def test_mid_config_parity():
