@@ -10,11 +10,19 @@
 // belongs to exactly one expert (tile_expert).
 //
 // Kernel design (one persistent CTA per SM), tile 128 routes x BN weight
-// rows, BN = 128 or 256:
-//   warp 0      TMA producer: per pipeline stage one 128x128-byte A tile and
-//               one BNx128-byte B tile (cp.async.bulk.tensor, 128-byte
-//               swizzle) plus the matching scale atoms of each operand
-//               (cp.async.bulk), all completing on one mbarrier.
+// rows, BN = 128 or 256, pipeline stage = 512 elements of K (two 128-byte
+// chunks of every operand row):
+//   warp 0      TMA producer: per stage ONE tensor copy of the A tile
+//               (128 rows x 2 chunks, 32 KB) and ONE of the B tile (BN rows x
+//               2 chunks), through 3-D tensor maps whose third dimension
+//               walks the 128-byte chunks of a row (128-byte swizzle; each
+//               chunk lands as its own swizzled [rows][128 B] tile), plus the
+//               matching scale atoms of each operand (cp.async.bulk).  The
+//               TMA unit costs about the same per copy instruction up to
+//               32 KB (measured: 16 KB boxes ~66 GB/s per SM from L2, 32 KB
+//               boxes ~131 GB/s), so two-chunk copies double the operand
+//               bytes an SM can pull in.  Rows whose length is not a
+//               multiple of 128 bytes use 2-D maps and one copy per chunk.
 //   warps 2-5   scale writers, one per tensor-memory lane quadrant: once a
 //               stage's scale atoms have landed (their own barrier, loaded
 //               ahead of the operand tiles), every lane reads its 16-byte
@@ -26,12 +34,9 @@
 //               copy-engine time per 512-byte atom, which capped a stage of
 //               eight atoms at ~800 cycles whatever the memory traffic.
 //   warp 1      allocates 512 tensor-memory columns; lane 0 issues, per
-//               stage, four 128xBNx64 block-scaled MMAs into an FP32
+//               stage, eight 128xBNx64 block-scaled MMAs into an FP32
 //               accumulator in tensor memory, then tcgen05.commit frees the
-//               stage.  The tcgen05 issue slot of this one thread is the
-//               scarce resource (~130 cycles per MMA measured), so scale
-//               copies come from another warp and BN = 256 doubles the
-//               weight bytes each MMA consumes.
+//               stage.
 //   warps 6..   epilogue: tcgen05.ld of the accumulator (warp w reads lanes
 //               32*(w%4)..+31, one output row per thread; with BN = 256 a
 //               second group of four warps takes columns 128..255), fused
@@ -55,27 +60,39 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBKBytes = 128;                 // 256 E2M1 elements per stage row
-constexpr int kTileBytesA = kBM * kBKBytes;   // 16 KB
-constexpr int kSfBytesA = 4 * 512;            // 4 scale atoms (128 rows x 64 elements each)
+constexpr int kChunkBytes = 128;              // one 128-byte chunk = 256 E2M1 elements of a row
+constexpr int kChunkBytesA = kBM * kChunkBytes;               // 16 KB
 constexpr uint32_t kTmemCols = 512;
 
+// BN = 128: stages of two chunks (3-stage ring); BN = 256: stages of one
+// chunk (4-stage ring; its 256-row B box is already a 32 KB copy).  The ring
+// turnaround (scale copies, scale writers, MMA commit) is a fixed latency per
+// slot, so the deeper ring wins where the copies are large anyway (measured
+// at K = 7168: 1087 us with four one-chunk stages, 1169 us with two
+// two-chunk stages).
 template <int BN>
 struct Cfg {
-    static constexpr int kStages = BN == 128 ? 6 : 4;
+    static constexpr int kChunks = BN == 128 ? 2 : 1;            // chunks per pipeline stage
+    static constexpr int kKbPerStage = 4 * kChunks;              // 64-element MMA k-blocks per stage
+    static constexpr int kTileBytesA = kChunks * kChunkBytesA;
+    static constexpr int kSfBytesA = kKbPerStage * 512;          // scale atoms (128 rows x 64 elements each)
+    static constexpr int kStages = BN == 128 ? 3 : 4;
     static constexpr int kAccBufs = BN == 128 ? 2 : 1;
     static constexpr int kEpiWarps = BN == 128 ? 4 : 8;
     static constexpr int kSfWarps = 4;                           // scale writers, one per lane quadrant
     static constexpr int kEpiWarp0 = 2 + kSfWarps;
     static constexpr int kNumThreads = (kEpiWarp0 + kEpiWarps) * 32;
     static constexpr int kRowBlocks = BN / 128;                  // 128-row scale blocks of B
-    static constexpr int kTileBytesB = BN * kBKBytes;
+    static constexpr int kChunkBytesB = BN * kChunkBytes;
+    static constexpr int kTileBytesB = kChunks * kChunkBytesB;
     static constexpr int kSfBytesB = kRowBlocks * kSfBytesA;
     static constexpr uint32_t kSfColBase = kAccBufs * BN;        // 256 either way
+    static constexpr uint32_t kSfColsA = 4 * kKbPerStage;
     static constexpr uint32_t kSfColsB = 4 * kRowBlocks;         // per 64-element k-block
-    static constexpr uint32_t kSfColsPerStage = 16 + 4 * kSfColsB;
+    static constexpr uint32_t kSfColsPerStage = kSfColsA + kKbPerStage * kSfColsB;
     static constexpr int kSmemBytes = kStages * (kTileBytesA + kTileBytesB + kSfBytesA + kSfBytesB) + 1024 + 256;
     static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct Smem {
@@ -100,9 +117,9 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     Smem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.a = base;
-    s.b = s.a + C::kStages * kTileBytesA;
+    s.b = s.a + C::kStages * C::kTileBytesA;
     s.sfa = s.b + C::kStages * C::kTileBytesB;
-    s.sfb = s.sfa + C::kStages * kSfBytesA;
+    s.sfb = s.sfa + C::kStages * C::kSfBytesA;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s.sfb + C::kStages * C::kSfBytesB);
     s.full = bars;
     s.sf_full = bars + C::kStages;
@@ -159,9 +176,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
     const int num_m_tiles = p.meta[1];
     const int n_tiles = (p.n + BN - 1) / BN;
     const int total = num_m_tiles * n_tiles;
-    const int kblocks = p.kdim / 64;          // 64-element MMA steps
-    const int kstages = (kblocks + 3) / 4;    // 4 MMA steps per stage
+    const int kblocks = p.kdim / 64;                          // 64-element MMA steps
+    constexpr int kKbPerStage = C::kKbPerStage, kChunks = C::kChunks;
+    const int kstages = (kblocks + kKbPerStage - 1) / kKbPerStage;
     const int rb_per_expert = p.n / 128;
+    const int row_chunks = (p.kdim / 2 + kChunkBytes - 1) / kChunkBytes;   // 128-byte chunks per row
 
     if (warp == 0) {
         if (lane == 0) {
@@ -184,20 +203,38 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
                     p.sfb + ((size_t)e * rb_per_expert + (size_t)n_tile * C::kRowBlocks) * kblocks * 512;
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
-                    const int nkb = min(4, kblocks - 4 * ks);
+                    const int nkb = min(kKbPerStage, kblocks - kKbPerStage * ks);
                     const uint32_t sf_bytes = (uint32_t)nkb * 512u;
                     // the small scale atoms first, on their own barrier, so the
-                    // scale movers can start while the operand tiles are in flight
+                    // scale writers can start while the operand tiles are in flight
                     mbar_arrive_expect_tx(&s.sf_full[stage], (uint32_t)(1 + nrb) * sf_bytes);
-                    bulk_load(s.sfa + stage * kSfBytesA, sfa_src + (size_t)ks * 4 * 512, sf_bytes,
+                    bulk_load(s.sfa + stage * C::kSfBytesA, sfa_src + (size_t)ks * kKbPerStage * 512, sf_bytes,
                               &s.sf_full[stage], pol);
                     for (int rb = 0; rb < nrb; ++rb)
-                        bulk_load(s.sfb + stage * C::kSfBytesB + rb * kSfBytesA,
-                                  sfb_src + ((size_t)rb * kblocks + (size_t)ks * 4) * 512, sf_bytes,
+                        bulk_load(s.sfb + stage * C::kSfBytesB + rb * C::kSfBytesA,
+                                  sfb_src + ((size_t)rb * kblocks + (size_t)ks * kKbPerStage) * 512, sf_bytes,
                                   &s.sf_full[stage], pol);
-                    mbar_arrive_expect_tx(&s.full[stage], kTileBytesA + C::kTileBytesB);
-                    tma_load_2d(s.a + stage * kTileBytesA, &tmA, &s.full[stage], ks * kBKBytes, a_row, pol);
-                    tma_load_2d(s.b + stage * C::kTileBytesB, &tmB, &s.full[stage], ks * kBKBytes, b_row, pol);
+                    uint8_t* a_dst = s.a + stage * C::kTileBytesA;
+                    uint8_t* b_dst = s.b + stage * C::kTileBytesB;
+                    const int c0 = kChunks * ks;
+                    if (p.chunk_maps) {
+                        // one copy per operand; a chunk past the row end is filled
+                        // with zeros and skipped by the MMAs
+                        mbar_arrive_expect_tx(&s.full[stage], C::kTileBytesA + C::kTileBytesB);
+                        tma_load_3d(a_dst, &tmA, &s.full[stage], 0, a_row, c0, pol);
+                        tma_load_3d(b_dst, &tmB, &s.full[stage], 0, b_row, c0, pol);
+                    } else {
+                        // rows of 64 + 128 j bytes: one 2-D copy per chunk that
+                        // starts inside the row
+                        const int nch = min(kChunks, row_chunks - c0);
+                        mbar_arrive_expect_tx(&s.full[stage], (uint32_t)nch * (kChunkBytesA + C::kChunkBytesB));
+                        for (int c = 0; c < nch; ++c) {
+                            tma_load_2d(a_dst + c * kChunkBytesA, &tmA, &s.full[stage], (c0 + c) * kChunkBytes, a_row,
+                                        pol);
+                            tma_load_2d(b_dst + c * C::kChunkBytesB, &tmB, &s.full[stage], (c0 + c) * kChunkBytes,
+                                        b_row, pol);
+                        }
+                    }
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -217,18 +254,22 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
-                    const int nkb = min(4, kblocks - 4 * ks);
+                    const int nkb = min(kKbPerStage, kblocks - kKbPerStage * ks);
                     const uint32_t sfa_t = tmem_base + C::kSfColBase + (uint32_t)stage * C::kSfColsPerStage;
-                    const uint32_t sfb_t = sfa_t + 16;
+                    const uint32_t sfb_t = sfa_t + C::kSfColsA;
                     // the scale writers' stores for this stage are done
                     if (!mbar_wait(&s.sf_ready[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
                     tc_fence_after();
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(s.a + stage * kTileBytesA));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(s.b + stage * C::kTileBytesB));
+                    const uint32_t a_s = smem_u32(s.a + stage * C::kTileBytesA);
+                    const uint32_t b_s = smem_u32(s.b + stage * C::kTileBytesB);
                     for (int j = 0; j < nkb; ++j) {
-                        // advance 32 bytes (64 E2M1) along K inside the swizzled 128-byte rows
-                        tc_mma_nvf4(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc, sfa_t + 4 * j,
-                                    sfb_t + C::kSfColsB * j, (ks | j) != 0);
+                        // chunk j / 4, then 32 bytes (64 E2M1) along K inside
+                        // its swizzled 128-byte rows
+                        const int c = j >> 2, jj = j & 3;
+                        const uint64_t adesc = sdesc_kmajor_sw128(a_s + c * kChunkBytesA) + 2u * jj;
+                        const uint64_t bdesc = sdesc_kmajor_sw128(b_s + c * C::kChunkBytesB) + 2u * jj;
+                        tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + C::kSfColsB * j,
+                                    (ks | j) != 0);
                     }
                     tc_commit(&s.empty[stage]);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -250,35 +291,42 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
                                 mbar_wait(&s.sf_full[stage], phase, s.abort, p.status, kStatusTimeoutMma)))
                     goto done;
                 const uint32_t sfa_t = tmem_base + C::kSfColBase + (uint32_t)stage * C::kSfColsPerStage;
-                const uint32_t sfb_t = sfa_t + 16;
-                uint32_t ra[16];
+                const uint32_t sfb_t = sfa_t + C::kSfColsA;
+                // per chunk (4 k-blocks): A scales 16 columns (k-block j: 4),
+                // B scales 16 (BN = 128) or 32 columns (k-block j: 8, row block
+                // 0 then row block 1)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(s.sfa + stage * kSfBytesA + j * 512 + lane * 16);
-                    ra[4 * j] = v.x; ra[4 * j + 1] = v.y; ra[4 * j + 2] = v.z; ra[4 * j + 3] = v.w;
-                }
-                tmem_st16(sfa_t + lane_off, ra);
-                if (C::kRowBlocks == 1) {
-                    uint32_t rb_[16];
+                for (int h = 0; h < kChunks; ++h) {
+                    uint32_t ra[16];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(s.sfb + stage * C::kSfBytesB + j * 512 + lane * 16);
-                        rb_[4 * j] = v.x; rb_[4 * j + 1] = v.y; rb_[4 * j + 2] = v.z; rb_[4 * j + 3] = v.w;
+                        const uint4 v = *reinterpret_cast<const uint4*>(s.sfa + stage * C::kSfBytesA +
+                                                                        (4 * h + j) * 512 + lane * 16);
+                        ra[4 * j] = v.x; ra[4 * j + 1] = v.y; ra[4 * j + 2] = v.z; ra[4 * j + 3] = v.w;
                     }
-                    tmem_st16(sfb_t + lane_off, rb_);
-                } else {
-                    // k-block j: 8 columns, row block 0 then row block 1
-                    uint32_t rb_[32];
+                    tmem_st16(sfa_t + lane_off + 16 * h, ra);
+                    if (C::kRowBlocks == 1) {
+                        uint32_t rb_[16];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int rb = 0; rb < 2; ++rb) {
+                        for (int j = 0; j < 4; ++j) {
                             const uint4 v = *reinterpret_cast<const uint4*>(s.sfb + stage * C::kSfBytesB +
-                                                                            rb * kSfBytesA + j * 512 + lane * 16);
-                            rb_[8 * j + 4 * rb] = v.x; rb_[8 * j + 4 * rb + 1] = v.y;
-                            rb_[8 * j + 4 * rb + 2] = v.z; rb_[8 * j + 4 * rb + 3] = v.w;
+                                                                            (4 * h + j) * 512 + lane * 16);
+                            rb_[4 * j] = v.x; rb_[4 * j + 1] = v.y; rb_[4 * j + 2] = v.z; rb_[4 * j + 3] = v.w;
                         }
-                    tmem_st32(sfb_t + lane_off, rb_);
+                        tmem_st16(sfb_t + lane_off + 16 * h, rb_);
+                    } else {
+                        uint32_t rb_[32];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int rb = 0; rb < 2; ++rb) {
+                                const uint4 v = *reinterpret_cast<const uint4*>(
+                                    s.sfb + stage * C::kSfBytesB + rb * C::kSfBytesA + (4 * h + j) * 512 + lane * 16);
+                                rb_[8 * j + 4 * rb] = v.x; rb_[8 * j + 4 * rb + 1] = v.y;
+                                rb_[8 * j + 4 * rb + 2] = v.z; rb_[8 * j + 4 * rb + 3] = v.w;
+                            }
+                        tmem_st32(sfb_t + lane_off + 32 * h, rb_);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();

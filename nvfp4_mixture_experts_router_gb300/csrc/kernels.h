@@ -97,6 +97,7 @@ struct GemmParams {
     const uint8_t* sfa;          // A scales [rows_cap/128][kdim/64][512]
     const uint8_t* sfb;          // B scales [E][N/128][kdim/64][512]
     int kdim;                    // reduction length (elements)
+    int chunk_maps;              // 1: tmA / tmB are 3-D chunk maps (rows of a multiple of 128 bytes)
     int n;                       // output columns per expert (B rows per expert)
     const int* meta;             // meta[1] = number of M tiles, meta[2] = M-tile pairs
     const int* tile_expert;      // expert of each M tile

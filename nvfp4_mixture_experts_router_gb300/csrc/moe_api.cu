@@ -103,6 +103,22 @@ bool encode_operand_map(CUtensorMap* map, const void* base, uint64_t rows, uint6
     return r == CUDA_SUCCESS;
 }
 
+// 3-D uint8 tensor map over a row-major [rows][row_bytes] array, row_bytes a
+// multiple of 128: x = byte inside a 128-byte chunk, y = row, z = chunk.  A
+// box of two chunks x box_rows rows lands in shared memory as two
+// consecutive 128-byte-swizzled [box_rows][128 B] tiles (one TMA copy for
+// what would otherwise be two).
+bool encode_chunk_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows) {
+    const cuuint64_t dims[3] = {128, rows, row_bytes / 128};
+    const cuuint64_t strides[2] = {row_bytes, 128};
+    const cuuint32_t box[3] = {128, box_rows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Run a W4A4 GEMM with `n` weight rows per expert on CTA pairs?  Only on
@@ -304,18 +320,30 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
 
     const bool pair1 = use_pair_gemm(s, flags, N1), pair2 = use_pair_gemm(s, flags, s.H);
     const int tn1 = pair1 ? 128 : gemm_nvf4_tile_n(s.H, N1), tn2 = pair2 ? 128 : gemm_nvf4_tile_n(s.I, s.H);
+    // single-CTA GEMMs with 128-wide tiles over rows of a multiple of 128
+    // bytes copy two chunks per TMA instruction (3-D maps); the others use
+    // 2-D maps
+    const bool ch1 = !pair1 && tn1 == 128 && (s.H / 2) % 128 == 0;
+    const bool ch2 = !pair2 && tn2 == 128 && (s.I / 2) % 128 == 0;
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
-    if (!encode_operand_map(&tmA1, xq_codes, W.rows_cap, (uint64_t)s.H / 2) ||
-        !encode_operand_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 128, tn1) ||
-        !encode_operand_map(&tmA2, hq_codes, W.rows_cap, (uint64_t)s.I / 2) ||
-        !encode_operand_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 128, tn2))
-        return MOE_ERR_CUDA;
+    const bool ok1 = ch1 ? (encode_chunk_map(&tmA1, xq_codes, W.rows_cap, (uint64_t)s.H / 2, 128) &&
+                            encode_chunk_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, tn1))
+                         : (encode_operand_map(&tmA1, xq_codes, W.rows_cap, (uint64_t)s.H / 2) &&
+                            encode_operand_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 128,
+                                               tn1));
+    const bool ok2 = ch2 ? (encode_chunk_map(&tmA2, hq_codes, W.rows_cap, (uint64_t)s.I / 2, 128) &&
+                            encode_chunk_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, tn2))
+                         : (encode_operand_map(&tmA2, hq_codes, W.rows_cap, (uint64_t)s.I / 2) &&
+                            encode_operand_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 128,
+                                               tn2));
+    if (!ok1 || !ok2) return MOE_ERR_CUDA;
     int* tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
 
     GemmParams g1p{};
     g1p.sfa = xq_sf;
     g1p.sfb = pw + P.w1_sf;
     g1p.kdim = s.H;
+    g1p.chunk_maps = ch1 ? 1 : 0;
     g1p.n = N1;
     g1p.meta = meta;
     g1p.tile_expert = tile_expert;
@@ -357,6 +385,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     g2p.sfa = hq_sf;
     g2p.sfb = pw + P.w2_sf;
     g2p.kdim = s.I;
+    g2p.chunk_maps = ch2 ? 1 : 0;
     g2p.n = s.H;
     g2p.meta = meta;
     g2p.tile_expert = tile_expert;

@@ -25,9 +25,9 @@ def test_dsv3_shape_T4096_deterministic():
 
 
 def test_dsv3_shape_T8192_on_cta_pairs():
-    """T=8192 at DSV3 shape: about 2.5 M tiles per expert, so both GEMMs run
-    on CTA pairs by default."""
-    r = fullsize_parity(synth.config(2, 8192), n_tokens=16)
+    """T=8192 at DSV3 shape (about 2.5 M tiles per expert) with both GEMMs
+    forced onto CTA pairs."""
+    r = fullsize_parity(synth.config(2, 8192).with_(gemm_pairs="always"), n_tokens=16)
     assert r["code_match"] >= 0.999
 
 
@@ -39,7 +39,7 @@ def test_w4a16_T4096():
 def test_prefill_T16384_zipf():
     """Prefill scale: T=16384, H=7168, I=2048, E=256, top-8, per-token
     scales, Zipf-skewed expert popularity (one expert takes most tokens,
-    others none); both GEMMs on CTA pairs."""
+    others none)."""
     import numpy as np
     import oracle
     c = synth.config(4)
