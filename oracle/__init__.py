@@ -345,25 +345,53 @@ def prepare_expert(layer: Layer, weights: WeightFn, e: int):
     return (p1.operand(), float(p1.G), p2.operand(), float(p2.G))
 
 
-def forward(layer: Layer, x_bf16: np.ndarray, logits: np.ndarray, bias: Optional[np.ndarray],
+def sanitize_routes(ids: np.ndarray, E: int) -> np.ndarray:
+    """Caller-supplied routing (FlashInfer PR #4366, "Motivation": the
+    wrapper takes precomputed top-K ids and weights).  Reading: a slot whose
+    id is outside [0, E) or repeats the id of an earlier kept slot of the same
+    token is dropped (id -1): it has no row and contributes nothing."""
+    ids = np.asarray(ids, dtype=np.int64)
+    T, K = ids.shape
+    out = np.full((T, K), -1, np.int32)
+    for t in range(T):
+        kept = set()
+        for k in range(K):
+            e = int(ids[t, k])
+            if 0 <= e < E and e not in kept:
+                kept.add(e)
+                out[t, k] = e
+    return out
+
+
+def forward(layer: Layer, x_bf16: np.ndarray, logits: Optional[np.ndarray], bias: Optional[np.ndarray],
             weights: WeightFn, G1: Optional[float] = None, G2: Optional[float] = None,
             tokens: Optional[Sequence[int]] = None, x_rows: Optional[np.ndarray] = None,
-            prepared: Optional[dict] = None) -> Result:
+            prepared: Optional[dict] = None, routing=None) -> Result:
     """Layer forward.
 
     x_bf16   BF16 bits [T, H] (or None when ``x_rows`` gives the rows of
              ``tokens`` only)
-    logits   float32 [T, E]; bias float32 [E] or None
+    logits   float32 [T, E]; bias float32 [E] or None (unused with ``routing``)
     weights  e -> (w1 bits [N1, H], w2 bits [H, I]) in checkpoint order
     G1, G2   per-tensor global scales (per-tensor W4A4 only)
     tokens   compute outputs for these tokens only (routing and grouping are
              always computed for all T)
     prepared optional cache dict e -> prepare_expert(...) result
+    routing  optional caller-supplied (ids int [T, K], weights float32
+             [T, K]) in place of the router: ids sanitized by
+             sanitize_routes, weights used as given
     """
     L = layer
-    T, E = logits.shape
-    assert E == L.E
-    ids, w = router(logits, bias, L.K, L.renorm)
+    if routing is None:
+        T, E = logits.shape
+        assert E == L.E
+        ids, w = router(logits, bias, L.K, L.renorm)
+    else:
+        E = L.E
+        ids = sanitize_routes(routing[0], E)
+        w = np.asarray(routing[1], dtype=np.float32).astype(np.float64)
+        T = ids.shape[0]
+        assert ids.shape == (T, L.K) and w.shape == (T, L.K)
     grp = group(ids, E)
     toks = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
     n_tok = len(toks)
@@ -392,7 +420,8 @@ def forward(layer: Layer, x_bf16: np.ndarray, logits: np.ndarray, bias: Optional
     by_expert: dict = {}
     for t in toks:
         for k in range(L.K):
-            by_expert.setdefault(int(ids[t, k]), []).append((int(t), k))
+            if ids[t, k] >= 0:
+                by_expert.setdefault(int(ids[t, k]), []).append((int(t), k))
 
     o_rows = np.zeros((n_tok * L.K, L.H), np.float64)
     h_out, hc_out, hs_out, g2_out, hb_out = {}, {}, {}, {}, {}

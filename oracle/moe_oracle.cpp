@@ -241,7 +241,8 @@ int64_t orc_group(int64_t T, int E, int K, const int32_t* ids, int pad,
                   int32_t* row_of_route, int32_t* route_of_row, int64_t rows_cap) {
     for (int e = 0; e < E; ++e) count[e] = 0;
     for (int64_t r = 0; r < T * K; ++r) {
-        if (ids[r] < 0 || ids[r] >= E) return -2;
+        if (ids[r] < 0) continue;          /* a dropped route has no row */
+        if (ids[r] >= E) return -2;
         count[ids[r]] += 1;
     }
     offsets[0] = 0;
@@ -257,6 +258,10 @@ int64_t orc_group(int64_t T, int E, int K, const int32_t* ids, int pad,
     for (int64_t t = 0; t < T; ++t)
         for (int k = 0; k < K; ++k) {
             const int e = ids[t * K + k];
+            if (e < 0) {
+                row_of_route[t * K + k] = -1;
+                continue;
+            }
             const int64_t row = next[e]++;
             row_of_route[t * K + k] = (int32_t)row;
             route_of_row[row] = (int32_t)(t * K + k);

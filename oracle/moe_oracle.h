@@ -70,7 +70,9 @@ void orc_router(int64_t T, int E, int K, const float* logits, const float* bias,
 /* Stable counting sort of routes by expert; expert segments padded to a
  * multiple of `pad` rows.  route r = t*K + k.  row_of_route gives the padded
  * row; route_of_row (length rows_cap) gets -1 in pad rows and past the end.
- * Returns the padded row total, or -1 if it exceeds rows_cap. */
+ * A negative id is a dropped route: it has no row (row_of_route -1).
+ * Returns the padded row total, -1 if it exceeds rows_cap, -2 if an id is
+ * >= E. */
 int64_t orc_group(int64_t T, int E, int K, const int32_t* ids, int pad,
                   int32_t* count, int32_t* offsets, int32_t* padded_offsets,
                   int32_t* row_of_route, int32_t* route_of_row, int64_t rows_cap);

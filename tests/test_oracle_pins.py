@@ -374,15 +374,25 @@ def test_input_side_relu2_is_post_activation():
 # quantized layer vs an independent per-token brute-force forward
 # ---------------------------------------------------------------------------
 
-def brute_forward(c, x, logits, bias, w1, w2, G1, G2, mode, on_input, act):
+def brute_forward(c, x, logits, bias, w1, w2, G1, G2, mode, on_input, act, routing=None):
     T, H, I, E, K = c.T, c.H, c.I, c.E, c.K
-    l = logits if bias is None else (logits + bias).astype(np.float32)
     y = np.zeros((T, H))
     xv = oracle.bf16_bits_to_f64(x)
+    if routing is None:
+        l = logits if bias is None else (logits + bias).astype(np.float32)
     for t in range(T):
-        order = sorted(range(E), key=lambda e: (-float(l[t, e]), e))[:K]
-        p = np.exp(l[t, order].astype(np.float64) - float(l[t, order[0]]))
-        p /= p.sum()
+        if routing is None:
+            order = sorted(range(E), key=lambda e: (-float(l[t, e]), e))[:K]
+            p = np.exp(l[t, order].astype(np.float64) - float(l[t, order[0]]))
+            p /= p.sum()
+        else:
+            # caller-supplied: walk the slots, keep in-range ids not seen before
+            order, p = [], []
+            for k in range(K):
+                e = int(routing[0][t, k])
+                if 0 <= e < E and e not in order:
+                    order.append(e)
+                    p.append(float(np.float32(routing[1][t, k])))
         if mode == 2:
             a = xv[t][None]
             g1 = np.float32(1.0)
@@ -441,6 +451,64 @@ def test_tiny_forward_matches_bruteforce(mode, on_input, act):
         G1v = G1 if mode == 0 else oracle.row_global_scale(xv)
         xc, xs = brute_quant_rows(xv, G1v)
         assert np.array_equal(res.x_codes, xc) and np.array_equal(res.x_sf, xs)
+
+
+def test_sanitize_routes_rule():
+    """Caller-supplied routing: per token the kept ids are distinct, in
+    range, each in-range id of the input is kept exactly once, at its first
+    slot; every other slot is dropped (-1)."""
+    rng = np.random.default_rng(11)
+    T, E, K = 300, 6, 4
+    ids = rng.integers(-3, E + 3, size=(T, K))
+    s = oracle.sanitize_routes(ids, E)
+    for t in range(T):
+        kept = [int(e) for e in s[t] if e >= 0]
+        assert len(kept) == len(set(kept))
+        assert set(kept) == {int(e) for e in ids[t] if 0 <= e < E}
+        for k in range(K):
+            first = 0 <= ids[t, k] < E and ids[t, k] not in ids[t, :k]
+            assert (s[t, k] == ids[t, k]) if first else (s[t, k] == -1)
+
+
+@pytest.mark.parametrize("mode,on_input,act", [(0, False, 0), (1, True, 0), (1, False, 1), (2, False, 1)])
+def test_routed_forward_matches_bruteforce(mode, on_input, act):
+    """Forward on caller-supplied ids and weights (with a repeated, an
+    out-of-range and a -1 id) against the per-token brute force."""
+    c, layer, x, logits, w1, w2 = _tiny(T=5, H=32, I=16, E=4, K=3, act=act, exact=False, mode=mode,
+                                        on_input=on_input, seed=40 + mode * 3 + act)
+    rng = np.random.default_rng(mode * 3 + act)
+    ids = np.stack([rng.permutation(4)[:3] for _ in range(5)]).astype(np.int32)
+    ids[1, 2] = ids[1, 0]
+    ids[3, 1] = 7
+    ids[4, 0] = -1
+    w = rng.uniform(0.05, 1.0, size=(5, 3)).astype(np.float32)
+    xv = oracle.bf16_bits_to_f64(x).astype(np.float32)
+    G1 = np.float32(np.abs(xv).max()) / np.float32(2688.0)
+    G2 = np.float32(0.02) / np.float32(2688.0) * np.float32(400.0)
+    res = oracle.forward(layer, x, None, None, lambda e: (w1[e], w2[e]), G1=G1, G2=G2, routing=(ids, w))
+    yb = brute_forward(c, x, None, None, w1, w2, G1, G2, mode, on_input, act, routing=(ids, w))
+    np.testing.assert_allclose(res.y64, yb, rtol=1e-9, atol=1e-12 * np.abs(yb).max())
+    assert (res.ids == -1).sum() == 3
+    flat = res.ids.reshape(-1)
+    assert np.array_equal(res.grouping.count, np.bincount(flat[flat >= 0], minlength=4))
+    assert (res.grouping.row_of_route[flat < 0] == -1).all()
+
+
+@pytest.mark.parametrize("on_input", [False, True])
+def test_dropped_route_equals_zero_weight_route(on_input):
+    """A dropped route contributes exactly what a route of weight 0 does."""
+    c, layer, x, logits, w1, w2 = _tiny(T=6, E=5, K=2, exact=False, mode=1, on_input=on_input, seed=9)
+    wf = lambda e: (w1[e], w2[e])
+    ids = np.array([[0, 1], [2, 3], [4, 0], [1, 2], [3, 4], [0, 2]], np.int32)
+    w = np.full((6, 2), 0.5, np.float32)
+    drop = ids.copy()
+    drop[[1, 4], 1] = drop[[1, 4], 0]
+    zw = w.copy()
+    zw[[1, 4], 1] = 0.0
+    a = oracle.forward(layer, x, None, None, wf, routing=(drop, w))
+    b = oracle.forward(layer, x, None, None, wf, routing=(ids, zw))
+    assert np.array_equal(a.y64, b.y64)
+    assert np.array_equal(a.y_bf16, b.y_bf16)
 
 
 def test_subset_forward_equals_full_forward():
