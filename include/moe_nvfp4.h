@@ -164,6 +164,32 @@ MOE_API moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags,
                              void* workspace, size_t workspace_bytes,
                              void* y_bf16, void* stream);
 
+/* The layer forward on caller-supplied routing instead of router logits
+ * [FlashInfer PR #4366, "Motivation": the fused-MoE wrapper takes the top-K
+ * expert ids and their final scales precomputed; "Existing SM120 status":
+ * they must be device tensors of the right dtype and shape].
+ *   topk_ids      [T][K] int32, device, 4-byte aligned: expert of slot k of
+ *                 token t.  An id outside [0, E), or repeating the id of an
+ *                 earlier kept slot of the same token, is a dropped route:
+ *                 it gets no row and contributes nothing (like a route of
+ *                 weight 0), and moe_nvfp4_last_device_status then reports
+ *                 MOE_ERR_INVALID_ARG.
+ *   topk_weights  [T][K] FP32, device, 4-byte aligned: used as given (no
+ *                 softmax, no renormalization), at the output reduction or
+ *                 on the FC2 input per MOE_ROUTER_W_ON_INPUT.
+ * Every other argument, the workspace and its layout are those of
+ * moe_nvfp4_forward; the workspace's topk_ids / topk_w regions receive the
+ * ids (dropped routes as -1) and the weights.  MOE_ROUTE_NO_RENORM is
+ * rejected (there is no router).  Neither routing array may overlap y or the
+ * workspace.  Errors as moe_nvfp4_forward.  Nothing is synchronized. */
+MOE_API moe_status moe_nvfp4_forward_routed(moe_shape s, uint32_t flags,
+                                            const void* x_bf16, const int32_t* topk_ids,
+                                            const float* topk_weights,
+                                            const float* act_scale_fc1, const float* act_scale_fc2,
+                                            const void* prepared,
+                                            void* workspace, size_t workspace_bytes,
+                                            void* y_bf16, void* stream);
+
 /* Same as moe_nvfp4_forward, and records caller-created CUDA events
  * (cudaEvent_t, created with timing enabled) on `stream` at the stage
  * boundaries, for per-stage timing:

@@ -46,8 +46,9 @@ class moe_shape(ctypes.Structure):
 
 
 _LAYOUT_FIELDS = ["rows_cap", "status", "topk_ids", "topk_w", "count", "offsets", "padded_offsets", "meta",
-                  "unit_base", "unit_mask", "row_of_route", "route_of_row", "tile_expert", "tile_pair", "g1", "xq_codes", "xq_sf", "h_f32",
-                  "g2", "hq_codes", "hq_sf", "x_bf16_perm", "h_bf16", "o_bf16", "y_acc", "total"]
+                  "unit_base", "unit_mask", "row_of_route", "route_of_row", "tile_expert", "tile_pair", "g1",
+                  "xq_codes", "xq_sf", "h_f32", "g2", "hq_codes", "hq_sf", "x_bf16_perm", "h_bf16", "o_bf16",
+                  "y_acc", "total"]
 
 
 class moe_workspace_layout(ctypes.Structure):
@@ -74,6 +75,7 @@ def lib():
             "moe_nvfp4_workspace_bytes": (sz, [S, u32]),
             "moe_nvfp4_workspace_layout": (ctypes.c_int, [S, u32, ctypes.POINTER(moe_workspace_layout)]),
             "moe_nvfp4_forward": (ctypes.c_int, [S, u32, P, P, P, P, P, P, P, sz, P, P]),
+            "moe_nvfp4_forward_routed": (ctypes.c_int, [S, u32, P, P, P, P, P, P, P, sz, P, P]),
             "moe_nvfp4_forward_staged": (ctypes.c_int, [S, u32, P, P, P, P, P, P, P, sz, P, P,
                                                         ctypes.POINTER(ctypes.c_void_p)]),
             "moe_nvfp4_forward_launches": (ctypes.c_int, [S, u32]),
@@ -92,6 +94,7 @@ def lib():
 
 EXPORTED = ["moe_nvfp4_version", "moe_nvfp4_prepared_bytes", "moe_nvfp4_prepare_weights",
             "moe_nvfp4_workspace_bytes", "moe_nvfp4_workspace_layout", "moe_nvfp4_forward",
+            "moe_nvfp4_forward_routed",
             "moe_nvfp4_forward_staged", "moe_nvfp4_forward_launches",
             "moe_nvfp4_last_device_status", "moe_nvfp4_debug_convert", "moe_nvfp4_route_noalloc"]
 EXPORTED.sort()
@@ -153,6 +156,25 @@ def moe_nvfp4_forward(s: moe_shape, flags: int, x_bf16: torch.Tensor, router_log
                                    _ptr(act_scale_fc1), _ptr(act_scale_fc2), _ptr(prepared), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _ptr(y_bf16), _stream(stream))
     _check("moe_nvfp4_forward", code)
+
+
+def moe_nvfp4_forward_routed(s: moe_shape, flags: int, x_bf16: torch.Tensor, topk_ids: torch.Tensor,
+                             topk_weights: torch.Tensor, act_scale_fc1: Optional[torch.Tensor],
+                             act_scale_fc2: Optional[torch.Tensor], prepared: torch.Tensor, workspace: torch.Tensor,
+                             y_bf16: torch.Tensor, stream=None) -> None:
+    """Forward on caller-supplied routing: topk_ids int32 [T, K], topk_weights
+    float32 [T, K] (CUDA, contiguous)."""
+    if topk_ids.dtype != torch.int32 or topk_weights.dtype != torch.float32:
+        raise TypeError("topk_ids must be int32 and topk_weights float32")
+    if not (topk_ids.is_contiguous() and topk_weights.is_contiguous()):
+        raise ValueError("topk_ids and topk_weights must be contiguous")
+    if tuple(topk_ids.shape) != (s.T, s.K) or tuple(topk_weights.shape) != (s.T, s.K):
+        raise ValueError(f"routing arrays must be [{s.T}, {s.K}]")
+    code = lib().moe_nvfp4_forward_routed(s, flags, _ptr(x_bf16), _ptr(topk_ids), _ptr(topk_weights),
+                                          _ptr(act_scale_fc1), _ptr(act_scale_fc2), _ptr(prepared),
+                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _ptr(y_bf16), _stream(stream))
+    _check("moe_nvfp4_forward_routed", code)
 
 
 def moe_nvfp4_forward_staged(s: moe_shape, flags: int, x_bf16, router_logits, router_bias, act_scale_fc1,
@@ -239,6 +261,13 @@ class MoELayer:
             y = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=x_bf16.device)
         moe_nvfp4_forward(self.shape, self.flags, x_bf16, logits, bias, g1, g2, self.prepared, self.workspace,
                           y, stream)
+        return y
+
+    def forward_routed(self, x_bf16, topk_ids, topk_weights, g1=None, g2=None, y=None, stream=None) -> torch.Tensor:
+        if y is None:
+            y = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=x_bf16.device)
+        moe_nvfp4_forward_routed(self.shape, self.flags, x_bf16, topk_ids, topk_weights, g1, g2, self.prepared,
+                                 self.workspace, y, stream)
         return y
 
     # -- views of the intermediates (tests / debugging) --

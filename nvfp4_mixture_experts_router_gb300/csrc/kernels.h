@@ -48,6 +48,10 @@ cudaError_t launch_router(const LaunchCtx& c, int T, int E, int K, const float* 
 cudaError_t launch_route_count(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
                                int renorm, int* ids, float* w, int* unit_cnt, uint32_t* unit_mask,
                                unsigned int* status_reset);
+// Caller-supplied ids / weights in place of the router (fused with the unit
+// masks); out-of-range or repeated ids become dropped routes (-1).
+cudaError_t launch_route_given(const LaunchCtx& c, int T, int E, int K, const int* ids_in, const float* w_in,
+                               int* ids, float* w, int* unit_cnt, uint32_t* unit_mask, unsigned int* status);
 // tile_pair may be null (then only meta[2] counts the pairs)
 cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
                                 int* padded_offsets, int* meta, int* tile_expert, int* tile_pair,

@@ -171,18 +171,34 @@ moe_status moe_nvfp4_prepare_weights(moe_shape s, uint32_t flags, const void* w1
                                       L.w2_codes, L.w2_sf));
 }
 
-static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, const float* router_logits,
-                               const float* router_bias, const float* act_scale_fc1, const float* act_scale_fc2,
-                               const void* prepared, void* workspace, size_t workspace_bytes, void* y_bf16,
-                               void* stream, void* const* events) {
+// Routing input of a forward: router logits (+ bias), or caller-supplied
+// top-K ids and weights.
+struct RoutingIn {
+    const float* logits = nullptr;
+    const float* bias = nullptr;
+    const int32_t* ids = nullptr;
+    const float* w = nullptr;
+};
+
+static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, const RoutingIn& rin,
+                               const float* act_scale_fc1, const float* act_scale_fc2, const void* prepared,
+                               void* workspace, size_t workspace_bytes, void* y_bf16, void* stream,
+                               void* const* events) {
     moe_status st = validate_shape(s, flags);
     if (st != MOE_OK) return st;
     const int mode = mode_of(flags);
-    if (!x_bf16 || !router_logits || !prepared || !workspace || !y_bf16) return MOE_ERR_INVALID_ARG;
-    if (!aligned(x_bf16, 16) || !aligned(router_logits, 16) || !aligned(y_bf16, 16) || !aligned(prepared, 256) ||
-        !aligned(workspace, 256))
+    const bool given = rin.ids != nullptr;
+    if (!x_bf16 || !prepared || !workspace || !y_bf16) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(y_bf16, 16) || !aligned(prepared, 256) || !aligned(workspace, 256))
         return MOE_ERR_INVALID_ARG;
-    if (router_bias && !aligned(router_bias, 4)) return MOE_ERR_INVALID_ARG;
+    if (given) {
+        // caller-supplied routing: no router, so its options do not apply
+        if (!rin.w || !aligned(rin.ids, 4) || !aligned(rin.w, 4) || (flags & MOE_ROUTE_NO_RENORM))
+            return MOE_ERR_INVALID_ARG;
+    } else {
+        if (!rin.logits || !aligned(rin.logits, 16)) return MOE_ERR_INVALID_ARG;
+        if (rin.bias && !aligned(rin.bias, 4)) return MOE_ERR_INVALID_ARG;
+    }
     if (mode == kModePerTensor) {
         if (!act_scale_fc1 || !act_scale_fc2 || !aligned(act_scale_fc1, 4) || !aligned(act_scale_fc2, 4))
             return MOE_ERR_INVALID_ARG;
@@ -190,8 +206,13 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     const moe_workspace_layout W = workspace_layout(s, flags);
     if (workspace_bytes < W.total) return MOE_ERR_WORKSPACE;
     const size_t y_bytes = (size_t)s.T * s.H * 2;
-    if (overlaps(y_bf16, y_bytes, workspace, W.total) || overlaps(y_bf16, y_bytes, x_bf16, y_bytes) ||
-        overlaps(y_bf16, y_bytes, router_logits, (size_t)s.T * s.E * 4))
+    if (overlaps(y_bf16, y_bytes, workspace, W.total) || overlaps(y_bf16, y_bytes, x_bf16, y_bytes))
+        return MOE_ERR_INVALID_ARG;
+    if (!given && overlaps(y_bf16, y_bytes, rin.logits, (size_t)s.T * s.E * 4)) return MOE_ERR_INVALID_ARG;
+    if (given && (overlaps(y_bf16, y_bytes, rin.ids, (size_t)s.T * s.K * 4) ||
+                  overlaps(y_bf16, y_bytes, rin.w, (size_t)s.T * s.K * 4) ||
+                  overlaps(workspace, W.total, rin.ids, (size_t)s.T * s.K * 4) ||
+                  overlaps(workspace, W.total, rin.w, (size_t)s.T * s.K * 4)))
         return MOE_ERR_INVALID_ARG;
 
     int sms = 0, device = 0;
@@ -225,9 +246,20 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     };
     if (!mark(0)) return MOE_ERR_CUDA;
 
-    e = launch_route_count(c, s.T, s.E, s.K, router_logits, router_bias, (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1,
-                           ids, topk_w, reinterpret_cast<int*>(wsp(W.unit_base)),
-                           reinterpret_cast<uint32_t*>(wsp(W.unit_mask)), status);
+    if (given) {
+        // the given-routing kernel reports bad ids in the status word, so the
+        // word is cleared before it rather than by it
+        if (cudaMemsetAsync(status, 0, 16, c.stream) != cudaSuccess) return MOE_ERR_CUDA;
+        LaunchCtx c0 = c;
+        c0.pdl = false;
+        e = launch_route_given(c0, s.T, s.E, s.K, rin.ids, rin.w, ids, topk_w,
+                               reinterpret_cast<int*>(wsp(W.unit_base)), reinterpret_cast<uint32_t*>(wsp(W.unit_mask)),
+                               status);
+    } else {
+        e = launch_route_count(c, s.T, s.E, s.K, rin.logits, rin.bias, (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1, ids,
+                               topk_w, reinterpret_cast<int*>(wsp(W.unit_base)),
+                               reinterpret_cast<uint32_t*>(wsp(W.unit_mask)), status);
+    }
     if (e != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
     e = launch_permute_scan(c, s.T, s.E, reinterpret_cast<int*>(wsp(W.unit_base)),
                             reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
@@ -431,8 +463,23 @@ moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags, const void* x_bf16, co
                              const float* router_bias, const float* act_scale_fc1, const float* act_scale_fc2,
                              const void* prepared, void* workspace, size_t workspace_bytes, void* y_bf16,
                              void* stream) {
-    return forward_impl(s, flags, x_bf16, router_logits, router_bias, act_scale_fc1, act_scale_fc2, prepared,
-                        workspace, workspace_bytes, y_bf16, stream, nullptr);
+    RoutingIn rin;
+    rin.logits = router_logits;
+    rin.bias = router_bias;
+    return forward_impl(s, flags, x_bf16, rin, act_scale_fc1, act_scale_fc2, prepared, workspace, workspace_bytes,
+                        y_bf16, stream, nullptr);
+}
+
+moe_status moe_nvfp4_forward_routed(moe_shape s, uint32_t flags, const void* x_bf16, const int32_t* topk_ids,
+                                    const float* topk_weights, const float* act_scale_fc1,
+                                    const float* act_scale_fc2, const void* prepared, void* workspace,
+                                    size_t workspace_bytes, void* y_bf16, void* stream) {
+    if (!topk_ids) return MOE_ERR_INVALID_ARG;
+    RoutingIn rin;
+    rin.ids = topk_ids;
+    rin.w = topk_weights;
+    return forward_impl(s, flags, x_bf16, rin, act_scale_fc1, act_scale_fc2, prepared, workspace, workspace_bytes,
+                        y_bf16, stream, nullptr);
 }
 
 moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags, const void* x_bf16, const float* router_logits,
@@ -442,8 +489,11 @@ moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags, const void* x_b
     if (!events) return MOE_ERR_INVALID_ARG;
     for (int i = 0; i < MOE_NUM_STAGE_EVENTS; ++i)
         if (!events[i]) return MOE_ERR_INVALID_ARG;
-    return forward_impl(s, flags, x_bf16, router_logits, router_bias, act_scale_fc1, act_scale_fc2, prepared,
-                        workspace, workspace_bytes, y_bf16, stream, events);
+    RoutingIn rin;
+    rin.logits = router_logits;
+    rin.bias = router_bias;
+    return forward_impl(s, flags, x_bf16, rin, act_scale_fc1, act_scale_fc2, prepared, workspace, workspace_bytes,
+                        y_bf16, stream, events);
 }
 
 int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags) {

@@ -166,6 +166,54 @@ __global__ void __launch_bounds__(256) permute_count_kernel(int T, int E, int K,
     pdl_launch_dependents();
 }
 
+// Caller-supplied routing [FlashInfer PR #4366, "Motivation": precomputed
+// top-K ids and weights] in place of the router, fused with step (1): warp w
+// of the block handles unit blockIdx.x*8+w, one lane per token.  Copies the
+// ids and weights into the workspace; an id outside [0, E) or repeating an
+// earlier kept id of the same token becomes -1 (a dropped route: no row, no
+// contribution) and sets kStatusBadExpert.  A repeat shows up as this
+// token's bit already set in the expert's unit mask.
+__global__ void __launch_bounds__(256) route_given_kernel(int T, int E, int K, const int* __restrict__ ids_in,
+                                                          const float* __restrict__ w_in, int* __restrict__ topk_ids,
+                                                          float* __restrict__ topk_w, int* __restrict__ unit_cnt,
+                                                          uint32_t* __restrict__ unit_mask, unsigned int* status) {
+    extern __shared__ uint32_t s_masks[];  // [8][E]
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int U = (T + kUnitTokens - 1) / kUnitTokens;
+    const int u = blockIdx.x * 8 + warp;
+    uint32_t* m = s_masks + warp * E;
+    for (int e = lane; e < E; e += 32) m[e] = 0u;
+    __syncwarp();
+    if (u < U) {
+        const int t = u * kUnitTokens + lane;
+        if (t < T) {
+            bool bad = false;
+            for (int k = 0; k < K; ++k) {
+                const size_t r = (size_t)t * K + k;
+                int e = ids_in[r];
+                if (e >= 0 && e < E) {
+                    // only this lane sets this bit, so the old value tells
+                    // whether an earlier slot of the token took expert e
+                    if (atomicOr(&m[e], 1u << lane) & (1u << lane)) e = -1;
+                } else {
+                    e = -1;
+                }
+                bad |= e < 0;
+                topk_ids[r] = e;
+                topk_w[r] = w_in[r];
+            }
+            if (bad) atomicOr(status, kStatusBadExpert);
+        }
+        __syncwarp();
+        for (int e = lane; e < E; e += 32) {
+            unit_cnt[(size_t)e * U + u] = __popc(m[e]);
+            unit_mask[(size_t)e * U + u] = m[e];
+        }
+    }
+    pdl_launch_dependents();
+}
+
 // (2) one block of 1024 threads: totals, offsets, padded offsets, per-unit
 // starting rows (in place of the counts), M-tile -> expert map, pad rows of
 // route_of_row set to -1.
@@ -339,9 +387,19 @@ cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* i
                     (const int*)unit_base, (const uint32_t*)unit_mask, row_of_route, route_of_row);
 }
 
+cudaError_t launch_route_given(const LaunchCtx& c, int T, int E, int K, const int* ids_in, const float* w_in,
+                               int* ids, float* w, int* unit_cnt, uint32_t* unit_mask, unsigned int* status) {
+    const int U = (T + kUnitTokens - 1) / kUnitTokens;
+    const size_t smem = (size_t)8 * E * sizeof(uint32_t);
+    return c.launch(route_given_kernel, dim3((U + 7) / 8), dim3(256), smem, T, E, K, ids_in, w_in, ids, w, unit_cnt,
+                    unit_mask, status);
+}
+
 cudaError_t setup_routing_kernels() {
     const int smem = 8 * 1024 * (int)sizeof(uint32_t);
-    return cudaFuncSetAttribute(permute_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const cudaError_t e = cudaFuncSetAttribute(permute_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(route_given_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 }  // namespace moe

@@ -41,12 +41,16 @@ __device__ __forceinline__ uint32_t pack_sf4(uint32_t s) {
 // Step 3 of the permutation for token t, lane k < K handling route t*K+k:
 // compute the route's padded row, record both directions of the map, and
 // return the row (0 for lanes >= K).
+// Returns the route's padded row, or -1 for lanes >= K and dropped routes.
 __device__ __forceinline__ int scatter_token_routes(int t, int T, int K, int lane, const RouteScatter& rs) {
-    if (lane >= K) return 0;
+    if (lane >= K) return -1;
     const int U = (T + kUnitTokens - 1) / kUnitTokens;
     const int r = t * K + lane;
     const int e = rs.topk_ids[r];
-    if (e < 0 || e >= rs.E) return 0;
+    if (e < 0 || e >= rs.E) {
+        rs.row_of_route[r] = -1;
+        return -1;
+    }
     const int row = route_row(t, e, U, rs.unit_base, rs.unit_mask);
     rs.row_of_route[r] = row;
     rs.route_of_row[row] = r;
@@ -122,6 +126,7 @@ __global__ void __launch_bounds__(1024) quantize_x_kernel(int T, int H, int K, c
         if (active) {
             for (int k = 0; k < K; ++k) {
                 const int row = s_rows[k];
+                if (row < 0) continue;
                 *reinterpret_cast<uint2*>(codes + (size_t)row * (H / 2) + 8 * b) = make_uint2(q[0], q[1]);
                 if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(row, b, H)) = word;
             }
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(256) gather_x_bf16_kernel(int T, int H, int K,
         if (c < H / 8) v = src[c];
         for (int k = 0; k < K; ++k) {
             const int row = __shfl_sync(0xffffffffu, my_row, k);
-            if (c < H / 8) reinterpret_cast<uint4*>(x_perm + (size_t)row * H)[c] = v;
+            if (c < H / 8 && row >= 0) reinterpret_cast<uint4*>(x_perm + (size_t)row * H)[c] = v;
         }
     }
     if (y_acc_zero) zero_row_f32(y_acc_zero + (size_t)t * H, H, lane);
@@ -228,6 +233,7 @@ __global__ void __launch_bounds__(128) finalize_det_kernel(int T, int H, int K, 
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int k = 0; k < K; ++k) {
             const int row = row_of_route[(size_t)t * K + k];
+            if (row < 0) continue;   // dropped route
             const float w = weight_on_output ? topk_w[(size_t)t * K + k] : 1.0f;
             const uint4 v = reinterpret_cast<const uint4*>(o + (size_t)row * H)[c];
             const uint32_t u[4] = {v.x, v.y, v.z, v.w};

@@ -475,11 +475,11 @@ def forward(layer: Layer, x_bf16: np.ndarray, logits: Optional[np.ndarray], bias
 
 
 def fc2_input_scale(layer: Layer, x_bf16, logits, bias, weights: WeightFn, G1: float,
-                    tokens: Optional[Sequence[int]] = None, prepared=None) -> np.float32:
+                    tokens: Optional[Sequence[int]] = None, prepared=None, routing=None) -> np.float32:
     """Per-tensor FC2-input calibration: amax of the float32 FC2 input over
     the given tokens' routes, divided by 2688."""
     res = forward(layer, x_bf16, logits, bias, weights, G1=G1, G2=1.0, tokens=tokens,
-                  prepared=prepared)
+                  prepared=prepared, routing=routing)
     amax = np.float32(0.0)
     for h in res.h.values():
         amax = max(amax, np.float32(np.max(np.abs(h.astype(np.float32)))) if h.size else 0)

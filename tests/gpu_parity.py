@@ -159,8 +159,9 @@ def check_x_quant(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray):
     toks = ref.tokens
     for k in range(K):
         rows = ror.reshape(T, K)[toks, k]
-        assert np.array_equal(codes[rows], ref.x_codes), f"x codes differ (slot {k})"
-        assert np.array_equal(sf_rowmajor(sfbuf, rows, H), ref.x_sf), f"x scales differ (slot {k})"
+        kept = rows >= 0                      # dropped routes (caller-supplied routing) have no row
+        assert np.array_equal(codes[rows[kept]], ref.x_codes[kept]), f"x codes differ (slot {k})"
+        assert np.array_equal(sf_rowmajor(sfbuf, rows[kept], H), ref.x_sf[kept]), f"x scales differ (slot {k})"
     if layer.flags & api.MOE_W4A4_PER_TOKEN:
         g1 = layer.view("g1", torch.float32, T).cpu().numpy()[toks]
         assert np.array_equal(g1, ref.G1), "per-token G1 differs"
@@ -309,6 +310,53 @@ def full_parity(c: synth.MoEConfig, tokens=None):
 # full-size workloads: everything that is cheap for the oracle on all tokens,
 # the expert MLPs on a seeded token sample
 # ---------------------------------------------------------------------------
+
+def routed_parity(c: synth.MoEConfig, ids: np.ndarray, w: np.ndarray, tokens=None):
+    """moe_nvfp4_forward_routed on caller-supplied ids / weights against the
+    oracle's forward on the same routing (ids sanitized by its stated rule)."""
+    inp = make_inputs(c)
+    routing = (ids, w)
+    wf = lambda e: (inp.w1_np[e], inp.w2_np[e])
+    G1 = G2 = None
+    if c.mode == synth.MODE_PER_TENSOR:
+        G1 = np.float32(oracle.tensor_global_scale(oracle.bf16_bits_to_f64(inp.x_np).astype(np.float32)))
+        G2 = np.float32(oracle.fc2_input_scale(oracle_layer(c), inp.x_np, None, None, wf, G1, tokens=tokens,
+                                               routing=routing))
+    layer = api.MoELayer.create(c.T, c.H, c.I, c.E, c.K, c.flags())
+    layer.prepare(inp.w1, inp.w2)
+    g1 = None if G1 is None else torch.tensor([G1], dtype=torch.float32, device="cuda")
+    g2 = None if G2 is None else torch.tensor([G2], dtype=torch.float32, device="cuda")
+    ids_t = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).cuda()
+    w_t = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).cuda()
+    y = layer.forward_routed(inp.x, ids_t, w_t, g1, g2)
+    torch.cuda.synchronize()
+    status = api.moe_nvfp4_last_device_status(layer.workspace)
+    prepared = {}
+    ref = oracle.forward(oracle_layer(c), inp.x_np, None, None, wf, G1=G1, G2=G2, tokens=tokens,
+                         prepared=prepared, routing=routing)
+    want_status = api.MOE_ERR_INVALID_ARG if (ref.ids < 0).any() else api.MOE_OK
+    assert status == want_status, f"device status {status}, expected {want_status}"
+    ror = check_routing(layer, ref)
+    if c.mode != synth.MODE_W4A16:
+        check_x_quant(layer, ref, ror)
+    frac, slack = check_fc2_input(layer, ref, ror, G2, prepared)
+    rel = check_y(y, ref, slack)
+    return dict(code_match=frac, y_rel_err=rel, layer=layer, y=y, ref=ref, inp=inp)
+
+
+def random_routing(T: int, E: int, K: int, seed: int, bad_frac: float = 0.0):
+    """Distinct ids per token and positive weights; with bad_frac > 0 some
+    slots get -1, an id >= E or a repeat of the token's slot 0."""
+    rng = np.random.default_rng(seed)
+    ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    w = rng.uniform(0.05, 1.0, size=(T, K)).astype(np.float32)
+    if bad_frac > 0:
+        bad = rng.random((T, K)) < bad_frac
+        kind = rng.integers(0, 3, size=(T, K))
+        for t, k in zip(*np.nonzero(bad)):
+            ids[t, k] = [-1, E + int(rng.integers(0, 5)), ids[t, 0] if k > 0 else -7][kind[t, k]]
+    return ids, w
+
 
 def check_x_quant_all(layer: api.MoELayer, x_np: np.ndarray, G1, ror: np.ndarray):
     """NVFP4 codes and scales of x for every token and every one of its K

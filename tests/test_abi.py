@@ -81,6 +81,13 @@ def test_invalid_arguments_rejected_before_cuda(L):
     assert f(s, 1 << 9, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, 3 << 2, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, 2, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    # caller-supplied routing: ids and weights required, no router options
+    fr = L.moe_nvfp4_forward_routed
+    assert fr(s, 0, A, None, B, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert fr(s, 0, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert fr(s, api.MOE_ROUTE_NO_RENORM, A, B, B, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert fr(s, 0, A, ctypes.c_void_p((1 << 30) + 2), B, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert fr(s, 0, A, W, B, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG   # ids inside the workspace
     # contradictory GEMM scheduling hints
     both = api.MOE_GEMM_PAIRS_NEVER | api.MOE_GEMM_PAIRS_ALWAYS
     assert f(s, both, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG

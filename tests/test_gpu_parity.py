@@ -127,6 +127,41 @@ def test_pair_gemm_parity(T, H, I, E, K, mode, act, det):
     full_parity(c)
 
 
+ROUTED = [(64, 256, 128, 8, 2, synth.MODE_PER_TENSOR, 0, False, False, 0.0, "auto"),
+          (200, 384, 256, 16, 4, synth.MODE_PER_TOKEN, 1, True, True, 0.1, "auto"),
+          (33, 256, 128, 8, 3, synth.MODE_W4A16, 1, False, False, 0.1, "auto"),
+          (300, 512, 256, 6, 2, synth.MODE_PER_TOKEN, 0, True, False, 0.05, "always"),
+          (129, 256, 256, 1, 1, synth.MODE_PER_TENSOR, 0, False, True, 0.0, "auto")]
+
+
+@pytest.mark.parametrize("T,H,I,E,K,mode,act,on_input,det,bad,pairs", ROUTED)
+def test_routed_forward_parity(T, H, I, E, K, mode, act, on_input, det, bad, pairs):
+    """Caller-supplied routing (moe_nvfp4_forward_routed): random distinct
+    ids with non-softmax weights, and slots with -1, out-of-range or repeated
+    ids that must be dropped and reported in the device status."""
+    from gpu_parity import random_routing, routed_parity
+    c = synth.MoEConfig("routed", T, H, I, E, K, act=act, mode=mode, router_on_input=on_input, deterministic=det,
+                        seed=T + E, logits="normal", gemm_pairs=pairs)
+    ids, w = random_routing(T, E, K, seed=T * 7 + K, bad_frac=bad)
+    routed_parity(c, ids, w)
+
+
+def test_routed_forward_equals_router_forward():
+    """Feeding the router's own ids and weights back through the routed
+    entry point reproduces the logits forward bit for bit (deterministic
+    finalize)."""
+    c = synth.MoEConfig("rr", 300, 256, 128, 16, 4, mode=synth.MODE_PER_TOKEN, deterministic=True, seed=21,
+                        logits="normal")
+    inp = make_inputs(c)
+    layer, y0 = run_gpu(inp, None, None)
+    ids = layer.view("topk_ids", torch.int32, c.T * c.K).view(c.T, c.K).clone()
+    w = layer.view("topk_w", torch.float32, c.T * c.K).view(c.T, c.K).clone()
+    y1 = layer.forward_routed(inp.x, ids, w)
+    torch.cuda.synchronize()
+    assert api.moe_nvfp4_last_device_status(layer.workspace) == api.MOE_OK
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
 def test_mid_config_parity_on_pairs():
     """The mid workload with both GEMMs forced onto CTA pairs."""
     full_parity(synth.config(1).with_(gemm_pairs="always"))
