@@ -70,6 +70,8 @@ def lib():
                 "orc_f32_to_bf16_n": (None, [P, P, i64]),
                 "orc_row_global_scale": (f32, [P, i64]),
                 "orc_quant_rows": (None, [P, i64, i64, P, P, P]),
+                "orc_quant_rows_4over6": (None, [P, i64, i64, P, P, P]),
+                "orc_row_global_scale_div": (f32, [P, i64, f32]),
                 "orc_dequant_rows": (None, [P, P, i64, i64, P]),
                 "orc_router": (None, [i64, i32, i32, P, P, i32, P, P]),
                 "orc_group": (i64, [i64, i32, i32, P, i32, P, P, P, P, P, i64]),
@@ -147,11 +149,18 @@ def f32_to_bf16_bits(v: np.ndarray) -> np.ndarray:
 # NVFP4 rows
 # ---------------------------------------------------------------------------
 
-def row_global_scale(x: np.ndarray) -> np.ndarray:
-    """Per-row amax/2688 (1 if the row is all zero), float32."""
+SCALE_DIV_4OVER6 = 1536.0     # 6 * 256: global scale under 4-over-6 with the 256 E4M3 bound
+
+
+def row_global_scale(x: np.ndarray, div: float = 2688.0) -> np.ndarray:
+    """Per-row amax/div (1 if the row is all zero), float32; div = 2688
+    (6 * 448) by default, 1536 (6 * 256) for 4-over-6 quantization."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     x2 = x.reshape(-1, x.shape[-1])
-    return np.array([lib().orc_row_global_scale(_p(np.ascontiguousarray(r)), r.size) for r in x2],
+    if div == 2688.0:
+        return np.array([lib().orc_row_global_scale(_p(np.ascontiguousarray(r)), r.size) for r in x2],
+                        dtype=np.float32)
+    return np.array([lib().orc_row_global_scale_div(_p(np.ascontiguousarray(r)), r.size, div) for r in x2],
                     dtype=np.float32)
 
 
@@ -161,16 +170,19 @@ def tensor_global_scale(x: np.ndarray) -> np.float32:
     return row_global_scale(x)[0]
 
 
-def quant_rows(x: np.ndarray, G) -> tuple:
+def quant_rows(x: np.ndarray, G, four_over_six: bool = False) -> tuple:
     """NVFP4-quantize rows of x (float32 [rows, n]) with per-row global scale
-    G (scalar or [rows]).  Returns (codes [rows, n/2] u8, sf [rows, n/16] u8)."""
+    G (scalar or [rows]); four_over_six picks, per block, the better of the
+    max-6 and max-4 scalings.  Returns (codes [rows, n/2] u8, sf [rows, n/16]
+    u8)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     rows, n = x.shape
     assert n % 16 == 0
     G = np.ascontiguousarray(np.broadcast_to(np.asarray(G, dtype=np.float32), (rows,)))
     codes = np.empty((rows, n // 2), dtype=np.uint8)
     sf = np.empty((rows, n // 16), dtype=np.uint8)
-    lib().orc_quant_rows(_p(x), rows, n, _p(G), _p(codes), _p(sf))
+    fn = lib().orc_quant_rows_4over6 if four_over_six else lib().orc_quant_rows
+    fn(_p(x), rows, n, _p(G), _p(codes), _p(sf))
     return codes, sf
 
 
@@ -312,6 +324,7 @@ class Layer:
     router_on_input: bool = False
     renorm: bool = True
     exact: bool = False    # FP64 with no quantization anywhere (pins only)
+    four_over_six: bool = False   # per-token W4A4: 4-over-6 activation quantization
 
 
 @dataclass
@@ -411,8 +424,8 @@ def forward(layer: Layer, x_bf16: np.ndarray, logits: Optional[np.ndarray], bias
             assert G1 is not None, "per-tensor mode needs the FC1 activation scale"
             G1_tok = np.full(n_tok, np.float32(G1), np.float32)
         else:
-            G1_tok = row_global_scale(x32)
-        x_codes, x_sf = quant_rows(x32, G1_tok)
+            G1_tok = row_global_scale(x32, SCALE_DIV_4OVER6 if L.four_over_six else SCALE_DIV)
+        x_codes, x_sf = quant_rows(x32, G1_tok, L.four_over_six)
         a_tok = dequant_rows(x_codes, x_sf)
 
     # routes of the selected tokens, grouped by expert
@@ -452,8 +465,8 @@ def forward(layer: Layer, x_bf16: np.ndarray, logits: Optional[np.ndarray], bias
                 assert G2 is not None, "per-tensor mode needs the FC2 activation scale"
                 g2 = np.full(len(routes), np.float32(G2), np.float32)
             else:
-                g2 = row_global_scale(h32)
-            hc, hs = quant_rows(h32, g2)
+                g2 = row_global_scale(h32, SCALE_DIV_4OVER6 if L.four_over_six else SCALE_DIV)
+            hc, hs = quant_rows(h32, g2, L.four_over_six)
             a2 = dequant_rows(hc, hs)
             alpha2 = g2.astype(np.float64) * gw2
         o = fc2(a2, alpha2, w2op)

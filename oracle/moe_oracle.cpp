@@ -179,6 +179,67 @@ void orc_quant_rows(const float* x, int64_t rows, int64_t n, const float* G,
         quant_row(x + r * n, n, G[r], codes + r * (n / 2), sf + r * (n / 16));
 }
 
+float orc_row_global_scale_div(const float* x, int64_t n, float div) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) amax = std::max(amax, std::fabs(x[i]));
+    if (amax == 0.0f) return 1.0f;
+    return amax / div;
+}
+
+/* ======================================================================
+ * 4-over-6 block quantization [FlashInfer PR #4366 post, "Performance
+ * benchmark": the per-token activation contract run with NVFP4_4OVER6,
+ * NVFP4_4OVER6_E4M3_USE_256 and NVFP4_4OVER6_ERR_MODE=MSE; the page gives
+ * only these switch names].  Reading: each 16-element block is quantized
+ * twice with the procedure above, once scaling the block maximum to 6 (the
+ * default) and once to 4 (scale amax/G/4), and keeps the candidate whose
+ * squared dequantization error is smaller (ties keep 6).  The error is
+ * computed in float32 with round-to-nearest-even at every step in a fixed
+ * order: d_i = x_i - (v_i * s) * G, err = (((d_0^2 + d_1^2) + d_2^2) ...),
+ * so that the choice is reproducible.  E4M3_USE_256: the per-row global
+ * scale is amax / (6 * 256) = amax / 1536, which keeps the larger max-4
+ * block scale (at most 384) inside the E4M3 range.
+ * ==================================================================== */
+static float block_candidate(const float* xb, float G, float t, float M, uint8_t* codes, uint8_t* s_out) {
+    const uint8_t s = orc_f32_to_e4m3(t / M);
+    const float sv = orc_e4m3_to_f32(s);
+    const float inv = (sv == 0.0f) ? 0.0f : 1.0f / (sv * G);
+    float err = 0.0f;
+    for (int i = 0; i < 16; i += 2) {
+        const uint8_t lo = orc_f32_to_e2m1(xb[i] * inv);
+        const uint8_t hi = orc_f32_to_e2m1(xb[i + 1] * inv);
+        codes[i / 2] = (uint8_t)(lo | (hi << 4));
+        const float d0 = xb[i] - (orc_e2m1_to_f32(lo) * sv) * G;
+        const float d1 = xb[i + 1] - (orc_e2m1_to_f32(hi) * sv) * G;
+        err = err + d0 * d0;
+        err = err + d1 * d1;
+    }
+    *s_out = s;
+    return err;
+}
+
+static void quant_row_4over6(const float* x, int64_t n, float G, uint8_t* codes, uint8_t* sf) {
+    for (int64_t b = 0; b < n / 16; ++b) {
+        const float* xb = x + 16 * b;
+        float amax = 0.0f;
+        for (int i = 0; i < 16; ++i) amax = std::max(amax, std::fabs(xb[i]));
+        const float t = amax / G;
+        uint8_t c6[8], c4[8], s6, s4;
+        const float e6 = block_candidate(xb, G, t, 6.0f, c6, &s6);
+        const float e4 = block_candidate(xb, G, t, 4.0f, c4, &s4);
+        const bool four = e4 < e6;
+        for (int i = 0; i < 8; ++i) codes[8 * b + i] = four ? c4[i] : c6[i];
+        sf[b] = four ? s4 : s6;
+    }
+}
+
+void orc_quant_rows_4over6(const float* x, int64_t rows, int64_t n, const float* G,
+                           uint8_t* codes, uint8_t* sf) {
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < rows; ++r)
+        quant_row_4over6(x + r * n, n, G[r], codes + r * (n / 2), sf + r * (n / 16));
+}
+
 void orc_dequant_rows(const uint8_t* codes, const uint8_t* sf, int64_t rows,
                       int64_t n, double* out) {
 #pragma omp parallel for schedule(static)

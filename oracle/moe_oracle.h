@@ -56,6 +56,12 @@ float orc_row_global_scale(const float* x, int64_t n);
 void orc_quant_rows(const float* x, int64_t rows, int64_t n, const float* G,
                     uint8_t* codes, uint8_t* sf);
 /* Decode q*s (without the global scale) into FP64, exact. */
+/* 4-over-6: per 16-element block, the better (float32 squared error) of
+ * scaling the block maximum to 6 or to 4; ties keep 6.  G as above. */
+void orc_quant_rows_4over6(const float* x, int64_t rows, int64_t n, const float* G,
+                           uint8_t* codes, uint8_t* sf);
+/* amax / div (1 for an all-zero row). */
+float orc_row_global_scale_div(const float* x, int64_t n, float div);
 void orc_dequant_rows(const uint8_t* codes, const uint8_t* sf, int64_t rows,
                       int64_t n, double* out);
 

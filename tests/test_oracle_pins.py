@@ -162,16 +162,17 @@ def test_golden_format_values():
 # NVFP4 rows
 # ---------------------------------------------------------------------------
 
-def brute_quant_rows(x, G):
+def brute_quant_rows(x, G, M=6.0):
     """Row quantization spelled out with numpy float32 steps and the
-    brute-force converters above."""
+    brute-force converters above; M = the E2M1 value the block maximum maps
+    to (6, or 4 for the 4-over-6 alternative)."""
     x = x.astype(np.float32)
     rows, n = x.shape
     G = np.broadcast_to(np.asarray(G, np.float32), (rows,)).astype(np.float32)
     xb = x.reshape(rows, n // 16, 16)
     amax = np.abs(xb).max(axis=2)
     t = (amax / G[:, None]).astype(np.float32)
-    s = brute_nearest((t / np.float32(6.0)).astype(np.float32), E4M3_MAG, 0x80)
+    s = brute_nearest((t / np.float32(M)).astype(np.float32), E4M3_MAG, 0x80)
     sv = E4M3_MAG[s & 0x7F].astype(np.float32)
     den = (sv * G[:, None]).astype(np.float32)
     with np.errstate(divide="ignore"):
@@ -236,6 +237,88 @@ def test_quant_error_bound():
     err = np.abs(x.astype(np.float64) - deq)
     assert (err <= bound).all()
     assert (np.sign(deq) * np.sign(x) >= 0).all()
+
+
+# ---------------------------------------------------------------------------
+# 4-over-6 block quantization
+# ---------------------------------------------------------------------------
+
+def _exact_blocks(rng, rows, n, top, must, G):
+    """Rows of exact NVFP4 values q*s*G (G a power of two, so every product
+    is exact): every block holds +-`top` and +-`must` and other grid values
+    no larger than `top`."""
+    s_codes = rng.integers(16, 0x70, (rows, n // 16)).astype(np.uint8)
+    allowed = [c for c in range(8) if E2M1_MAG[c] <= top]
+    q = rng.choice(allowed, (rows, n)).astype(np.uint8)
+    q[:, 0::16] = int(np.nonzero(E2M1_MAG == top)[0][0])
+    q[:, 1::16] = int(np.nonzero(E2M1_MAG == must)[0][0])
+    q |= (rng.random((rows, n)) < 0.5).astype(np.uint8) << 3
+    vals = E2M1_MAG[q & 7] * np.where(q & 8, -1, 1)
+    x64 = vals * E4M3_MAG[np.repeat(s_codes, 16, axis=1)] * float(G)
+    x = x64.astype(np.float32)
+    assert np.array_equal(x.astype(np.float64), x64)
+    return x, q, s_codes
+
+
+@pytest.mark.parametrize("G", [1.0, 2.0 ** -7, 2.0 ** 5])
+def test_4over6_picks_max4_for_exact_max4_blocks(G):
+    """Blocks of exact values with max |q| = 4 that contain a 3: the max-4
+    candidate reproduces them (zero error) while the max-6 one cannot (3 s
+    is off the grid scaled by 6/4), so 4-over-6 returns exactly q and s."""
+    rng = np.random.default_rng(21)
+    x, q, s_codes = _exact_blocks(rng, 24, 256, 4.0, 3.0, np.float32(G))
+    codes, sf = oracle.quant_rows(x, np.float32(G), four_over_six=True)
+    assert np.array_equal(sf, s_codes)
+    assert np.array_equal(codes, (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8))
+    c6, s6 = oracle.quant_rows(x, np.float32(G))
+    assert not np.array_equal(oracle.dequant_rows(c6, s6), oracle.dequant_rows(codes, sf))
+
+
+@pytest.mark.parametrize("G", [1.0, 2.0 ** -9])
+def test_4over6_keeps_max6_for_exact_max6_blocks(G):
+    """Blocks of exact values with max |q| = 6 that contain a 4 (off the
+    grid when scaled by 4/6): the max-6 candidate is exact and is kept."""
+    rng = np.random.default_rng(22)
+    x, q, s_codes = _exact_blocks(rng, 24, 256, 6.0, 4.0, np.float32(G))
+    codes, sf = oracle.quant_rows(x, np.float32(G), four_over_six=True)
+    assert np.array_equal(sf, s_codes)
+    assert np.array_equal(codes, (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8))
+
+
+def test_4over6_choice_matches_fp64_error():
+    """On random data each block gets the candidate with the smaller squared
+    error, computed here in float64 from the brute-force candidates; blocks
+    whose two errors are within float32 noise of each other may go either
+    way but must then equal one of the two candidates."""
+    rng = np.random.default_rng(23)
+    x = (rng.standard_normal((96, 512)) * np.exp2(rng.integers(-6, 6, (96, 32)).repeat(16, 1))).astype(np.float32)
+    G = oracle.row_global_scale(x, oracle.SCALE_DIV_4OVER6)
+    codes, sf = oracle.quant_rows(x, G, four_over_six=True)
+    cand = {}
+    for M in (6.0, 4.0):
+        c, s_ = brute_quant_rows(x, G, M)
+        deq = oracle.dequant_rows(c, s_) * G[:, None].astype(np.float64)
+        err = ((x.astype(np.float64) - deq) ** 2).reshape(96, 32, 16).sum(axis=2)
+        cand[M] = (c.reshape(96, 32, 8), s_.reshape(96, 32), err)
+    got_c, got_s = codes.reshape(96, 32, 8), sf.reshape(96, 32)
+    is6 = (got_s == cand[6.0][1]) & (got_c == cand[6.0][0]).all(axis=2)
+    is4 = (got_s == cand[4.0][1]) & (got_c == cand[4.0][0]).all(axis=2)
+    assert (is6 | is4).all()
+    e6, e4 = cand[6.0][2], cand[4.0][2]
+    clear = np.abs(e4 - e6) > 1e-4 * np.maximum(e4, e6)
+    assert (is4[clear & (e4 < e6)]).all() and (is6[clear & (e6 < e4)]).all()
+    assert (clear & (e4 < e6)).sum() > 100 and (clear & (e6 < e4)).sum() > 100   # both choices exercised
+
+
+def test_4over6_global_scale_bound():
+    """E4M3_USE_256: G = amax/1536, so the max-4 block scale stays <= 384
+    (E4M3 code 0x7C) and never saturates at 448."""
+    assert oracle.row_global_scale(np.full((1, 16), 1536.0, np.float32), oracle.SCALE_DIV_4OVER6)[0] == 1.0
+    rng = np.random.default_rng(24)
+    x = (rng.standard_normal((64, 1024)) * np.exp2(rng.integers(-30, 30, (64, 1)))).astype(np.float32)
+    G = oracle.row_global_scale(x, oracle.SCALE_DIV_4OVER6)
+    _, s4 = brute_quant_rows(x, G, 4.0)
+    assert (s4 & 0x7F).max() == 0x7C
 
 
 # ---------------------------------------------------------------------------
