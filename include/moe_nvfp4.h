@@ -88,7 +88,16 @@ typedef enum {
  * on every configuration so far.  Setting both is invalid. */
 #define MOE_GEMM_PAIRS_NEVER (1u << 7)
 #define MOE_GEMM_PAIRS_ALWAYS (1u << 8)
-#define MOE_FLAGS_KNOWN 0x1FFu
+/* bit 9: 4-over-6 activation quantization (per-token W4A4 only) [PR #4366
+ * post, "Performance benchmark": the per-token activation contract runs with
+ * NVFP4_4OVER6, NVFP4_4OVER6_E4M3_USE_256 and NVFP4_4OVER6_ERR_MODE=MSE].
+ * Every 16-element block of x and of the FC2 input is quantized with its
+ * maximum mapped to 6 and to 4; the candidate with the smaller float32
+ * squared dequantization error is kept (ties keep 6).  Per-row global
+ * scales become amax/1536 (6 * 256).  The decode, and so the GEMMs, are
+ * unchanged. */
+#define MOE_QUANT_4OVER6 (1u << 9)
+#define MOE_FLAGS_KNOWN 0x3FFu
 
 /* ---- shapes ---------------------------------------------------------------- */
 typedef struct {

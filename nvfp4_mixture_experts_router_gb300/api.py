@@ -32,6 +32,7 @@ MOE_FINALIZE_DETERMINISTIC = 1 << 5
 MOE_ROUTE_NO_RENORM = 1 << 6
 MOE_GEMM_PAIRS_NEVER = 1 << 7
 MOE_GEMM_PAIRS_ALWAYS = 1 << 8
+MOE_QUANT_4OVER6 = 1 << 9
 
 
 class MoEError(RuntimeError):

@@ -90,12 +90,65 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&v)[16], float G,
 __device__ __forceinline__ float global_scale_from_amax(float amax) {
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
 }
+// Under 4-over-6 quantization: amax / 1536 (6 * 256), so that the larger
+// max-4 block scale (at most 384) stays inside the E4M3 range.
+constexpr float kScaleDiv4over6 = 1536.0f;
+__device__ __forceinline__ float global_scale_from_amax_4over6(float amax) {
+    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, kScaleDiv4over6);
+}
 
-// E2M1 magnitudes, for dequantization.
+// E2M1 value of a 4-bit code (sign in bit 3), without a table in local
+// memory: magnitude codes 2..7 are 2^((c>>1)-1) * (1 + (c&1)/2), i.e. float32
+// exponent field 126 + (c>>1) and mantissa bit 22 = c&1; codes 0 and 1 are
+// 0 and 0.5.
 __device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
-    const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
-    const float m = mag[c & 7u];
-    return (c & 8u) ? -m : m;
+    const uint32_t m = c & 7u;
+    const float mag = m >= 2u ? __uint_as_float(((126u + (m >> 1)) << 23) | ((m & 1u) << 22)) : 0.5f * (float)m;
+    return (c & 8u) ? -mag : mag;
+}
+
+// One candidate of 4-over-6: the block quantized with its maximum mapped to
+// M (t = amax / G), and the float32 squared dequantization error summed in
+// element order (d_i = v_i - (e2m1_i * s) * G, every step rounded to nearest).
+__device__ __forceinline__ float quant_candidate16(const float (&v)[16], float G, float t, float M,
+                                                   uint32_t (&codes)[2], uint32_t& s_out) {
+    const uint32_t s = f32_to_e4m3(__fdiv_rn(t, M));
+    const float sv = e4m3_to_f32(s);
+    const float inv = (sv == 0.0f) ? 0.0f : __fdiv_rn(1.0f, __fmul_rn(sv, G));
+    float err = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int i = w * 8 + b * 2;
+            const uint32_t pair = f32x2_to_e2m1x2(__fmul_rn(v[i], inv), __fmul_rn(v[i + 1], inv));
+            word |= pair << (8 * b);
+            const float d0 = __fsub_rn(v[i], __fmul_rn(__fmul_rn(e2m1_to_f32(pair & 15u), sv), G));
+            const float d1 = __fsub_rn(v[i + 1], __fmul_rn(__fmul_rn(e2m1_to_f32(pair >> 4), sv), G));
+            err = __fadd_rn(err, __fmul_rn(d0, d0));
+            err = __fadd_rn(err, __fmul_rn(d1, d1));
+        }
+        codes[w] = word;
+    }
+    s_out = s;
+    return err;
+}
+
+// 4-over-6 block quantization: the max-6 and the max-4 candidates, keeping
+// the one with the smaller squared error (ties keep max-6).
+__device__ __forceinline__ uint32_t quant_block16_4over6(const float (&v)[16], float G, uint32_t (&codes)[2]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const float t = __fdiv_rn(amax, G);
+    uint32_t c6[2], c4[2], s6, s4;
+    const float e6 = quant_candidate16(v, G, t, 6.0f, c6, s6);
+    const float e4 = quant_candidate16(v, G, t, 4.0f, c4, s4);
+    const bool four = e4 < e6;
+    codes[0] = four ? c4[0] : c6[0];
+    codes[1] = four ? c4[1] : c6[1];
+    return four ? s4 : s6;
 }
 
 // Padded row of token t's route to expert e: the (expert, unit) starting row

@@ -77,8 +77,11 @@ cudaError_t launch_quantize_x(const LaunchCtx& c, int T, int H, int K, const voi
                               float* y_acc_zero);
 cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const void* x, const RouteScatter& rs,
                                  void* x_perm, float* y_acc_zero);
+// per_token (quantize_x): 0 caller's per-tensor scale, 1 per-token, 2 per-token
+// with 4-over-6 blocks; four_six (quantize_h): 4-over-6 blocks
 cudaError_t launch_quantize_h(const LaunchCtx& c, uint64_t rows_cap, int I, const int* meta,
-                              const int* route_of_row, const float* h, float* g2, uint8_t* codes, uint8_t* sf);
+                              const int* route_of_row, const float* h, float* g2, uint8_t* codes, uint8_t* sf,
+                              int four_six);
 cudaError_t launch_finalize_deterministic(const LaunchCtx& c, int T, int H, int K, const int* row_of_route,
                                           const float* topk_w, int weight_on_output, const void* o, void* y);
 cudaError_t launch_finalize_fused(const LaunchCtx& c, int T, int H, const float* y_acc, void* y);

@@ -74,6 +74,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 moe_status validate_shape(moe_shape s, uint32_t flags) {
     if (flags & ~MOE_FLAGS_KNOWN) return MOE_ERR_INVALID_ARG;
     if ((flags & MOE_GEMM_PAIRS_NEVER) && (flags & MOE_GEMM_PAIRS_ALWAYS)) return MOE_ERR_INVALID_ARG;
+    if ((flags & MOE_QUANT_4OVER6) && mode_of(flags) != kModePerToken) return MOE_ERR_INVALID_ARG;
     if (act_of(flags) > 1 || mode_of(flags) > 2) return MOE_ERR_INVALID_ARG;
     if (s.T < 1 || s.T > (1 << 22)) return MOE_ERR_INVALID_ARG;
     if (s.H < 128 || s.H % 128 != 0 || s.H > 65536) return MOE_ERR_INVALID_ARG;
@@ -346,8 +347,9 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     uint8_t* xq_sf = wsp(W.xq_sf);
     uint8_t* hq_codes = wsp(W.hq_codes);
     uint8_t* hq_sf = wsp(W.hq_sf);
-    e = launch_quantize_x(c, s.T, s.H, s.K, x_bf16, act_scale_fc1, per_token ? 1 : 0, g1, rs, xq_codes, xq_sf,
-                          y_acc);
+    const bool four_six = (flags & MOE_QUANT_4OVER6) != 0;
+    e = launch_quantize_x(c, s.T, s.H, s.K, x_bf16, act_scale_fc1, per_token ? (four_six ? 2 : 1) : 0, g1, rs,
+                          xq_codes, xq_sf, y_acc);
     if (e != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
     const bool pair1 = use_pair_gemm(s, flags, N1), pair2 = use_pair_gemm(s, flags, s.H);
@@ -408,7 +410,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     if (e != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
     if (per_token) {
         e = launch_quantize_h(c, W.rows_cap, s.I, meta, route_of_row, reinterpret_cast<const float*>(wsp(W.h_f32)),
-                              reinterpret_cast<float*>(wsp(W.g2)), hq_codes, hq_sf);
+                              reinterpret_cast<float*>(wsp(W.g2)), hq_codes, hq_sf, four_six ? 1 : 0);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     if (!mark(5)) return MOE_ERR_CUDA;

@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(1024) quantize_x_kernel(int T, int H, int K, c
         if (warp == 0) {
             float m = lane < (int)(blockDim.x >> 5) ? s_red[lane] : 0.0f;
             m = warp_max(m);
-            if (lane == 0) s_red[0] = global_scale_from_amax(m);
+            if (lane == 0) s_red[0] = per_token == 2 ? global_scale_from_amax_4over6(m) : global_scale_from_amax(m);
         }
         __syncthreads();
         G = s_red[0];
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(1024) quantize_x_kernel(int T, int H, int K, c
         const bool active = b < nblk;
         uint32_t q[2] = {0u, 0u};
         uint32_t s = 0;
-        if (active) s = quant_block16(v[i], G, q);
+        if (active) s = per_token == 2 ? quant_block16_4over6(v[i], G, q) : quant_block16(v[i], G, q);
         const uint32_t word = pack_sf4(s);
         if (active) {
             for (int k = 0; k < K; ++k) {
@@ -170,7 +170,8 @@ template <int kMaxPer>
 __global__ void __launch_bounds__(1024) quantize_h_kernel(int I, const int* __restrict__ meta,
                                                           const int* __restrict__ route_of_row,
                                                           const float* __restrict__ h, float* __restrict__ g2,
-                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                          int four_six) {
     __shared__ float s_red[32];
     pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(1024) quantize_h_kernel(int I, const int* __re
     if (warp == 0) {
         float m = lane < (int)(blockDim.x >> 5) ? s_red[lane] : 0.0f;
         m = warp_max(m);
-        if (lane == 0) s_red[0] = global_scale_from_amax(m);
+        if (lane == 0) s_red[0] = four_six ? global_scale_from_amax_4over6(m) : global_scale_from_amax(m);
     }
     __syncthreads();
     const float G = s_red[0];
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(1024) quantize_h_kernel(int I, const int* __re
         const bool active = b < nblk;
         uint32_t q[2] = {0u, 0u};
         uint32_t s = 0;
-        if (active) s = quant_block16(v[i], G, q);
+        if (active) s = four_six ? quant_block16_4over6(v[i], G, q) : quant_block16(v[i], G, q);
         const uint32_t word = pack_sf4(s);
         if (active) {
             *reinterpret_cast<uint2*>(codes + (size_t)row * (I / 2) + 8 * b) = make_uint2(q[0], q[1]);
@@ -393,15 +394,18 @@ cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const 
 }
 
 cudaError_t launch_quantize_h(const LaunchCtx& c, uint64_t rows_cap, int I, const int* meta,
-                              const int* route_of_row, const float* h, float* g2, uint8_t* codes, uint8_t* sf) {
+                              const int* route_of_row, const float* h, float* g2, uint8_t* codes, uint8_t* sf,
+                              int four_six) {
     const int per = (I / 16 + 1023) / 1024;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const uint64_t want = (uint64_t)sms * (2048 / row_threads(I));   // enough CTAs to fill every SM
     const dim3 grid((unsigned)(rows_cap < want ? rows_cap : want)), block(row_threads(I));
-    if (per <= 1) return c.launch(quantize_h_kernel<1>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf);
-    if (per <= 2) return c.launch(quantize_h_kernel<2>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf);
-    return c.launch(quantize_h_kernel<4>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf);
+    if (per <= 1)
+        return c.launch(quantize_h_kernel<1>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf, four_six);
+    if (per <= 2)
+        return c.launch(quantize_h_kernel<2>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf, four_six);
+    return c.launch(quantize_h_kernel<4>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf, four_six);
 }
 
 cudaError_t launch_finalize_deterministic(const LaunchCtx& c, int T, int H, int K, const int* row_of_route,

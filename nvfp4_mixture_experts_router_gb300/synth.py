@@ -131,6 +131,7 @@ class MoEConfig:
     zipf_beta: float = 2.0
     w_std: float = 0.02
     gemm_pairs: str = "auto"      # GEMM tile scheduling: "auto" | "never" | "always"
+    four_over_six: bool = False   # per-token W4A4: 4-over-6 activation quantization
     extra: dict = field(default_factory=dict)
 
     @property
@@ -149,6 +150,8 @@ class MoEConfig:
             f |= 1 << 7
         elif self.gemm_pairs == "always":
             f |= 1 << 8
+        if self.four_over_six:
+            f |= 1 << 9
         return f
 
     def with_(self, **kw) -> "MoEConfig":

@@ -93,7 +93,7 @@ def make_inputs(c: synth.MoEConfig, device="cuda") -> Inputs:
 
 def oracle_layer(c: synth.MoEConfig) -> oracle.Layer:
     return oracle.Layer(c.H, c.I, c.E, c.K, act=c.act, mode=c.mode, router_on_input=c.router_on_input,
-                        renorm=c.renorm)
+                        renorm=c.renorm, four_over_six=c.four_over_six)
 
 
 def scales_for(inp: Inputs, tokens=None):
@@ -363,8 +363,10 @@ def check_x_quant_all(layer: api.MoELayer, x_np: np.ndarray, G1, ror: np.ndarray
     permuted rows, bit for bit."""
     T, K, H = layer.T, layer.K, layer.H
     x32 = oracle.bf16_bits_to_f64(x_np).astype(np.float32)
-    G = oracle.row_global_scale(x32) if layer.flags & api.MOE_W4A4_PER_TOKEN else np.float32(G1)
-    codes_ref, sf_ref = oracle.quant_rows(x32, G)
+    four_six = bool(layer.flags & api.MOE_QUANT_4OVER6)
+    div = oracle.SCALE_DIV_4OVER6 if four_six else oracle.SCALE_DIV
+    G = oracle.row_global_scale(x32, div) if layer.flags & api.MOE_W4A4_PER_TOKEN else np.float32(G1)
+    codes_ref, sf_ref = oracle.quant_rows(x32, G, four_six)
     cap = layer.layout()["rows_cap"]
     codes = layer.view("xq_codes", torch.uint8, cap * H // 2).view(cap, H // 2)
     sfbuf = layer.view("xq_sf", torch.uint8, cap * H // 16).cpu().numpy()

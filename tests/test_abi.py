@@ -78,7 +78,10 @@ def test_invalid_arguments_rejected_before_cuda(L):
     W = ctypes.c_void_p(1 << 36)
     f = L.moe_nvfp4_forward
     # unknown flag bits, bad mode, bad activation
-    assert f(s, 1 << 9, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert f(s, 1 << 10, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    # 4-over-6 quantization only with per-token W4A4
+    assert f(s, api.MOE_QUANT_4OVER6, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert f(s, api.MOE_QUANT_4OVER6 | api.MOE_W4A16, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, 3 << 2, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, 2, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     # caller-supplied routing: ids and weights required, no router options

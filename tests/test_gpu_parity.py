@@ -162,6 +162,25 @@ def test_routed_forward_equals_router_forward():
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
 
 
+FOUR6 = [(64, 256, 128, 8, 2, 0, False, False), (200, 384, 256, 16, 4, 1, True, True),
+         (129, 512, 256, 4, 2, 0, True, False), (7, 4096, 384, 3, 2, 0, False, True)]
+
+
+@pytest.mark.parametrize("T,H,I,E,K,act,on_input,det", FOUR6)
+def test_4over6_parity(T, H, I, E, K, act, on_input, det):
+    """Per-token W4A4 with 4-over-6 block quantization of x and of the FC2
+    input: x codes / scales / G1 bit-exact, FC2-input codes >= 99.9 %."""
+    c = synth.MoEConfig("46", T, H, I, E, K, act=act, mode=synth.MODE_PER_TOKEN, router_on_input=on_input,
+                        deterministic=det, seed=T + H, logits="normal", four_over_six=True)
+    r = full_parity(c)
+    assert r["code_match"] >= 0.999
+
+
+def test_mid_config_parity_4over6():
+    """The mid workload under the 4-over-6 per-token activation contract."""
+    full_parity(synth.config(1).with_(four_over_six=True))
+
+
 def test_mid_config_parity_on_pairs():
     """The mid workload with both GEMMs forced onto CTA pairs."""
     full_parity(synth.config(1).with_(gemm_pairs="always"))
