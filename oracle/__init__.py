@@ -29,7 +29,7 @@ _lock = threading.Lock()
 _lib = None
 
 ACT_SWIGLU, ACT_RELU2 = 0, 1
-MODE_PER_TENSOR, MODE_PER_TOKEN, MODE_W4A16 = 0, 1, 2
+MODE_PER_TENSOR, MODE_PER_TOKEN, MODE_W4A16, MODE_MXFP8 = 0, 1, 2, 3
 PAD_ROWS = 128          # expert segments are padded to whole 128-row tiles
 SCALE_DIV = 2688.0      # 6 (largest E2M1) * 448 (largest E4M3)
 
@@ -71,6 +71,10 @@ def lib():
                 "orc_row_global_scale": (f32, [P, i64]),
                 "orc_quant_rows": (None, [P, i64, i64, P, P, P]),
                 "orc_quant_rows_4over6": (None, [P, i64, i64, P, P, P]),
+                "orc_mx_block_exp": (i32, [f32]),
+                "orc_quant_rows_mx": (None, [P, i64, i64, P, P]),
+                "orc_dequant_rows_mx": (None, [P, P, i64, i64, P]),
+                "orc_prepare_matrix_mx": (None, [P, i64, i64, P, P]),
                 "orc_row_global_scale_div": (f32, [P, i64, f32]),
                 "orc_dequant_rows": (None, [P, P, i64, i64, P]),
                 "orc_router": (None, [i64, i32, i32, P, P, i32, P, P]),
@@ -186,6 +190,32 @@ def quant_rows(x: np.ndarray, G, four_over_six: bool = False) -> tuple:
     return codes, sf
 
 
+def quant_rows_mx(x: np.ndarray) -> tuple:
+    """MXFP8-quantize rows of x (float32 [rows, n], n % 32 == 0): E4M3 codes
+    [rows, n] and E8M0 scales [rows, n/32]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, n = x.shape
+    assert n % 32 == 0
+    codes = np.empty((rows, n), dtype=np.uint8)
+    sf = np.empty((rows, n // 32), dtype=np.uint8)
+    lib().orc_quant_rows_mx(_p(x), rows, n, _p(codes), _p(sf))
+    return codes, sf
+
+
+def dequant_rows_mx(codes: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    """e4m3(code) * 2^(sf - 127) as float64 [rows, n]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    rows, n = codes.shape
+    out = np.empty((rows, n), np.float64)
+    lib().orc_dequant_rows_mx(_p(codes), _p(sf), rows, n, _p(out))
+    return out
+
+
+def mx_block_exp(amax: float) -> int:
+    return int(lib().orc_mx_block_exp(float(amax)))
+
+
 def dequant_rows(codes: np.ndarray, sf: np.ndarray) -> np.ndarray:
     """q*s as float64 [rows, n] (without the global scale)."""
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
@@ -257,6 +287,25 @@ class PreparedMatrix:
 
     def operand(self) -> np.ndarray:
         return dequant_rows(self.codes, self.sf)
+
+
+@dataclass
+class PreparedMatrixMX:
+    codes: np.ndarray   # [N, Kd] E4M3
+    sf: np.ndarray      # [N, Kd/32] E8M0
+    G: np.float32 = np.float32(1.0)
+
+    def operand(self) -> np.ndarray:
+        return dequant_rows_mx(self.codes, self.sf)
+
+
+def prepare_matrix_mx(w_bf16_bits: np.ndarray) -> PreparedMatrixMX:
+    w = np.ascontiguousarray(w_bf16_bits, dtype=np.uint16)
+    N, Kd = w.shape
+    codes = np.empty((N, Kd), np.uint8)
+    sf = np.empty((N, Kd // 32), np.uint8)
+    lib().orc_prepare_matrix_mx(_p(w), N, Kd, _p(codes), _p(sf))
+    return PreparedMatrixMX(codes, sf)
 
 
 def prepare_matrix(w_bf16_bits: np.ndarray) -> PreparedMatrix:
@@ -353,8 +402,9 @@ def prepare_expert(layer: Layer, weights: WeightFn, e: int):
     w1, w2 = weights(e)
     if layer.exact:
         return (bf16_bits_to_f64(w1), 1.0, bf16_bits_to_f64(w2), 1.0)
-    p1 = prepare_matrix(w1)
-    p2 = prepare_matrix(w2)
+    prep = prepare_matrix_mx if layer.mode == MODE_MXFP8 else prepare_matrix
+    p1 = prep(w1)
+    p2 = prep(w2)
     return (p1.operand(), float(p1.G), p2.operand(), float(p2.G))
 
 
@@ -419,6 +469,10 @@ def forward(layer: Layer, x_bf16: np.ndarray, logits: Optional[np.ndarray], bias
         x_codes = np.zeros((n_tok, L.H // 2), np.uint8)
         x_sf = np.zeros((n_tok, L.H // 16), np.uint8)
         a_tok = xv
+    elif L.mode == MODE_MXFP8:
+        G1_tok = np.ones(n_tok, np.float32)          # no global scale
+        x_codes, x_sf = quant_rows_mx(x32)
+        a_tok = dequant_rows_mx(x_codes, x_sf)
     else:
         if L.mode == MODE_PER_TENSOR:
             assert G1 is not None, "per-tensor mode needs the FC1 activation scale"
@@ -459,6 +513,11 @@ def forward(layer: Layer, x_bf16: np.ndarray, logits: Optional[np.ndarray], bias
             hb = f32_to_bf16_bits(h.astype(np.float32))
             a2 = bf16_bits_to_f64(hb)
             alpha2 = np.full(len(routes), gw2)
+        elif L.mode == MODE_MXFP8:
+            g2 = np.ones(len(routes), np.float32)
+            hc, hs = quant_rows_mx(h.astype(np.float32))
+            a2 = dequant_rows_mx(hc, hs)
+            alpha2 = np.ones(len(routes))
         else:
             h32 = h.astype(np.float32)
             if L.mode == MODE_PER_TENSOR:

@@ -353,6 +353,52 @@ float orc_prepare_matrix(const uint16_t* w_bf16, int64_t N, int64_t Kd,
 }
 
 /* ======================================================================
+ * MXFP8 (W8A8, block 32) [MegaMoE, "Our approach": an MXFP8 (W8A8) backend
+ * with 8-bit weights and activations and block-32 scaling].  The page names
+ * the format only.  Reading: the OCP Microscaling definition with E4M3
+ * elements and one E8M0 (power-of-two) scale per 32 consecutive elements
+ * along the reduction dimension: X = 2^(floor(log2(amax)) - 8), 8 being the
+ * exponent of the largest E4M3 normal (448 = 1.75 * 2^8); elements are
+ * E4M3_RN_satfinite(v / X) (the scaling by a power of two is exact); an
+ * all-zero block gets X = 2^-127 (code 0); the exponent is clamped to
+ * [-127, 127] (E8M0 codes 0..254, 255 is NaN).  There is no global scale.
+ * ==================================================================== */
+int orc_mx_block_exp(float amax) {
+    if (!(amax > 0.0f) || !std::isfinite(amax)) return -127;
+    int ex = 0;
+    std::frexp(amax, &ex);                 /* amax = m * 2^ex, m in [0.5, 1) */
+    const int e = (ex - 1) - 8;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+void orc_quant_rows_mx(const float* x, int64_t rows, int64_t n, uint8_t* codes, uint8_t* sf) {
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < n / 32; ++b) {
+            const float* xb = x + r * n + 32 * b;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(xb[i]));
+            const int e = orc_mx_block_exp(amax);
+            sf[r * (n / 32) + b] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; ++i) codes[r * n + 32 * b + i] = orc_f32_to_e4m3(std::ldexp(xb[i], -e));
+        }
+    }
+}
+
+void orc_dequant_rows_mx(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t n, double* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t i = 0; i < n; ++i)
+            out[r * n + i] = std::ldexp((double)orc_e4m3_to_f32(codes[r * n + i]), (int)sf[r * (n / 32) + i / 32] - 127);
+}
+
+void orc_prepare_matrix_mx(const uint16_t* w_bf16, int64_t N, int64_t Kd, uint8_t* codes, uint8_t* sf) {
+    std::vector<float> wf(N * Kd);
+    for (int64_t i = 0; i < N * Kd; ++i) wf[i] = (float)orc_bf16_to_f64(w_bf16[i]);
+    orc_quant_rows_mx(wf.data(), N, Kd, codes, sf);
+}
+
+/* ======================================================================
  * Expert MLP.  FC1 (gate|up), activation, optional input-side router
  * weight applied after the activation [PR4366, "Motivation": the flag
  * scales the post-activation FC2 input and never the FC1 pre-activation],

@@ -62,6 +62,12 @@ void orc_quant_rows_4over6(const float* x, int64_t rows, int64_t n, const float*
                            uint8_t* codes, uint8_t* sf);
 /* amax / div (1 for an all-zero row). */
 float orc_row_global_scale_div(const float* x, int64_t n, float div);
+/* MXFP8 rows: E4M3 codes [rows][n], E8M0 scales [rows][n/32] (block 32;
+ * scale 2^(floor(log2 amax) - 8), 2^-127 for an all-zero block). */
+int orc_mx_block_exp(float amax);
+void orc_quant_rows_mx(const float* x, int64_t rows, int64_t n, uint8_t* codes, uint8_t* sf);
+void orc_dequant_rows_mx(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t n, double* out);
+void orc_prepare_matrix_mx(const uint16_t* w_bf16, int64_t N, int64_t Kd, uint8_t* codes, uint8_t* sf);
 void orc_dequant_rows(const uint8_t* codes, const uint8_t* sf, int64_t rows,
                       int64_t n, double* out);
 

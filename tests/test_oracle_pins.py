@@ -240,6 +240,76 @@ def test_quant_error_bound():
 
 
 # ---------------------------------------------------------------------------
+# MXFP8 rows (E4M3 elements, E8M0 scale per 32)
+# ---------------------------------------------------------------------------
+
+def brute_quant_rows_mx(x):
+    """OCP MX quantization spelled out: shared exponent from frexp of the
+    block amax, elements by the brute-force nearest E4M3 search."""
+    x = x.astype(np.float32)
+    rows, n = x.shape
+    xb = x.reshape(rows, n // 32, 32).astype(np.float64)
+    amax = np.abs(xb).max(axis=2)
+    _, ex = np.frexp(amax)
+    e = np.where(amax > 0, ex - 1 - 8, -127).clip(-127, 127)
+    scaled = xb / np.exp2(e)[:, :, None]
+    codes = brute_nearest(scaled, E4M3_MAG, 0x80).reshape(rows, n)
+    return codes.astype(np.uint8), (e + 127).astype(np.uint8)
+
+
+def test_mx_quant_matches_bruteforce():
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal((64, 512)) * np.exp2(rng.integers(-30, 30, (64, 16)).repeat(32, 1))).astype(np.float32)
+    x[2, :32] = 0.0                                   # zero block -> scale 2^-127
+    x[4, 32:64] = -0.0
+    x[6, 64:96] = np.float32(511.0 * 2.0 ** 10)       # saturates: |v / X| = 511 > 448
+    x[8, 96] = np.float32(2.0 ** -140)                # subnormal float32 amax
+    c1, s1 = oracle.quant_rows_mx(x)
+    c2, s2 = brute_quant_rows_mx(x)
+    assert np.array_equal(s1, s2) and np.array_equal(c1, c2)
+    assert s1[2, 0] == 0 and (c1[2, :32] == 0).all()
+    assert (c1[6, 64:96] == 0x7E).all()               # 448
+    assert oracle.mx_block_exp(448.0) == 0 and oracle.mx_block_exp(256.0) == 0 and oracle.mx_block_exp(255.9) == -1
+
+
+def test_mx_roundtrip_exact_blocks():
+    """Blocks of exact values P * 2^e with max |P| in [256, 448] quantize to
+    themselves (scale exponent e and every E4M3 code recovered)."""
+    rng = np.random.default_rng(32)
+    rows, n = 32, 256
+    e = rng.integers(-100, 100, (rows, n // 32))
+    P = rng.integers(0, 0x7F, (rows, n)).astype(np.uint8) | ((rng.random((rows, n)) < 0.5).astype(np.uint8) << 7)
+    big = rng.integers(0x78, 0x7F, (rows, n // 32)).astype(np.uint8)       # 256 .. 448
+    P[:, ::32] = big | (P[:, ::32] & 0x80)
+    P[:, 1::32] = np.minimum(P[:, 1::32] & 0x7F, big) | (P[:, 1::32] & 0x80)
+    P = np.where((P & 0x7F) > np.repeat(big, 32, axis=1), (P & 0x80) | 0x30, P).astype(np.uint8)
+    vals = E4M3_MAG[P & 0x7F] * np.where(P & 0x80, -1.0, 1.0) * np.exp2(np.repeat(e, 32, axis=1))
+    x = vals.astype(np.float32)
+    assert np.array_equal(x.astype(np.float64), vals)
+    codes, sf = oracle.quant_rows_mx(x)
+    assert np.array_equal(sf.astype(int) - 127, e)
+    assert np.array_equal(codes & 0x7F, P & 0x7F)
+    nz = (P & 0x7F) != 0
+    assert np.array_equal(codes[nz], P[nz])
+    assert np.array_equal(oracle.dequant_rows_mx(codes, sf), vals)
+
+
+def test_mx_error_bound():
+    """|x - q X| <= ulp_E4M3(|x| / X) / 2 * X plus the excess above 448."""
+    rng = np.random.default_rng(33)
+    x = (rng.standard_normal((64, 1024)) * np.exp2(rng.integers(-20, 20, (64, 32)).repeat(32, 1))).astype(np.float32)
+    codes, sf = oracle.quant_rows_mx(x)
+    deq = oracle.dequant_rows_mx(codes, sf)
+    X = np.exp2(sf.astype(np.float64) - 127).repeat(32, axis=1)
+    v = np.abs(x.astype(np.float64)) / X
+    k = np.floor(np.log2(np.maximum(v, 2.0 ** -6)))
+    ulp = np.exp2(k - 3)                                # E4M3: 3 mantissa bits, subnormal step 2^-9
+    bound = (ulp / 2 + np.maximum(0, v - 448)) * X
+    assert (np.abs(x - deq) <= bound * (1 + 1e-12)).all()
+    assert (np.abs(x).reshape(64, 32, 32).max(axis=2) / np.exp2(sf.astype(np.float64) - 127) >= 256).all()
+
+
+# ---------------------------------------------------------------------------
 # 4-over-6 block quantization
 # ---------------------------------------------------------------------------
 
@@ -479,11 +549,25 @@ def brute_forward(c, x, logits, bias, w1, w2, G1, G2, mode, on_input, act, routi
         if mode == 2:
             a = xv[t][None]
             g1 = np.float32(1.0)
+        elif mode == 3:
+            xc, xs = brute_quant_rows_mx(xv[t][None].astype(np.float32))
+            a = _dq_mx(xc, xs)
+            g1 = np.float32(1.0)
         else:
             g1 = np.float32(G1) if mode == 0 else (np.float32(np.abs(xv[t]).max()) / np.float32(2688.0))
             xc, xs = brute_quant_rows(xv[t][None].astype(np.float32), g1)
             a = _dq(xc, xs)
         for k, e in enumerate(order):
+            if mode == 3:
+                wq1 = _dq_mx(*brute_quant_rows_mx(oracle.bf16_bits_to_f64(w1[e]).astype(np.float32)))
+                wq2 = _dq_mx(*brute_quant_rows_mx(oracle.bf16_bits_to_f64(w2[e]).astype(np.float32)))
+                h = _act(a @ wq1.T, I, act)
+                if on_input:
+                    h = h * p[k]
+                hc, hs = brute_quant_rows_mx(h.astype(np.float32))
+                o = _dq_mx(hc, hs) @ wq2.T
+                y[t] += (1.0 if on_input else p[k]) * o[0]
+                continue
             q1c, q1s, gw1 = _bprep(w1[e])
             q2c, q2s, gw2 = _bprep(w2[e])
             if mode == 2:
@@ -505,6 +589,11 @@ def brute_forward(c, x, logits, bias, w1, w2, G1, G2, mode, on_input, act, routi
     return y
 
 
+def _dq_mx(codes, sf):
+    v = E4M3_MAG[codes & 0x7F] * np.where(codes & 0x80, -1.0, 1.0)
+    return v * np.exp2(np.repeat(sf.astype(np.float64) - 127, 32, axis=1))
+
+
 def _dq(codes, sf):
     q = np.stack([codes & 15, codes >> 4], axis=-1).reshape(codes.shape[0], -1)
     v = E2M1_MAG[q & 7] * np.where(q & 8, -1.0, 1.0)
@@ -519,9 +608,10 @@ def _bprep(wbits):
 
 
 @pytest.mark.parametrize("mode,on_input,act", [(0, False, 0), (1, True, 0), (1, False, 1),
-                                               (2, False, 1), (2, True, 0), (0, True, 1)])
+                                               (2, False, 1), (2, True, 0), (0, True, 1), (3, False, 0),
+                                               (3, True, 1)])
 def test_tiny_forward_matches_bruteforce(mode, on_input, act):
-    c, layer, x, logits, w1, w2 = _tiny(T=4, H=32, I=16, E=4, K=2, act=act, exact=False,
+    c, layer, x, logits, w1, w2 = _tiny(T=4, H=32, I=32 if mode == 3 else 16, E=4, K=2, act=act, exact=False,
                                         mode=mode, on_input=on_input, seed=mode * 7 + act)
     bias = np.array([0.1, -0.2, 0.05, 0.0], np.float32)
     xv = oracle.bf16_bits_to_f64(x).astype(np.float32)
@@ -530,9 +620,12 @@ def test_tiny_forward_matches_bruteforce(mode, on_input, act):
     res = oracle.forward(layer, x, logits, bias, lambda e: (w1[e], w2[e]), G1=G1, G2=G2)
     yb = brute_forward(c, x, logits, bias, w1, w2, G1, G2, mode, on_input, act)
     np.testing.assert_allclose(res.y64, yb, rtol=1e-9, atol=1e-12 * np.abs(yb).max())
-    if mode != 2:
+    if mode in (0, 1):
         G1v = G1 if mode == 0 else oracle.row_global_scale(xv)
         xc, xs = brute_quant_rows(xv, G1v)
+        assert np.array_equal(res.x_codes, xc) and np.array_equal(res.x_sf, xs)
+    if mode == 3:
+        xc, xs = brute_quant_rows_mx(xv)
         assert np.array_equal(res.x_codes, xc) and np.array_equal(res.x_sf, xs)
 
 
