@@ -68,6 +68,11 @@ typedef enum {
 #define MOE_W4A4_PER_TENSOR (0u << 2) /* caller-supplied FP32 global scales   */
 #define MOE_W4A4_PER_TOKEN (1u << 2)  /* per-row amax/2688 global scales      */
 #define MOE_W4A16 (2u << 2)           /* BF16 activations, NVFP4 weights      */
+/* MXFP8 W8A8 [MegaMoE, "Our approach": 8-bit weights and activations with
+ * block-32 scaling]: E4M3 elements, one E8M0 (power-of-two) scale per 32
+ * elements along K, 2^(floor(log2 amax) - 8); no global scales (the
+ * act_scale arguments must be NULL).  Weights are prepared in this format. */
+#define MOE_W8A8_MXFP8 (3u << 2)
 #define MOE_MODE_MASK (3u << 2)
 /* bit 4: router weight applied to the FC2 input (after the activation,
  * before the FC2-input quantization or BF16 store) instead of at the output
@@ -109,14 +114,16 @@ typedef struct {
 } moe_shape;
 
 /* ---- weight preparation ------------------------------------------------------ */
-/* Size in bytes of the prepared-weight buffer for this shape and activation
- * (only the activation bits of `flags` matter).  0 if the shape is invalid. */
+/* Size in bytes of the prepared-weight buffer for this shape, activation and
+ * weight format (only the activation bits and whether the precision mode is
+ * MOE_W8A8_MXFP8 matter).  0 if the shape is invalid. */
 MOE_API size_t moe_nvfp4_prepared_bytes(moe_shape s, uint32_t flags);
 
-/* Quantize BF16 checkpoint weights to NVFP4 and reorder them into the
- * prepared layout consumed by moe_nvfp4_forward in every precision mode
- * ["MegaMoE", "Usage": weights accepted in checkpoint layout, quantized and
- * reordered by the layer; PR #5319 post: W4A4 and W4A16 share the layout].
+/* Quantize BF16 checkpoint weights to NVFP4 (or, with MOE_W8A8_MXFP8, to
+ * MXFP8) and reorder them into the prepared layout consumed by
+ * moe_nvfp4_forward ["MegaMoE", "Usage": weights accepted in checkpoint
+ * layout, quantized and reordered by the layer; PR #5319 post: W4A4 and
+ * W4A16 share the NVFP4 layout].
  *   w1_bf16  [E][N1][H] row-major, N1 = 2I for SwiGLU (rows 0..I-1 gate,
  *            I..2I-1 up), N1 = I for ReLU2.  16-byte aligned.
  *   w2_bf16  [E][H][I] row-major.  16-byte aligned.
@@ -131,6 +138,10 @@ MOE_API size_t moe_nvfp4_prepared_bytes(moe_shape s, uint32_t flags);
  *            so that every 128-row tile holds 64 gate rows then the 64
  *            matching up rows.  A 512-byte scale atom holds 128 rows x 4
  *            scales: byte (r%32)*16 + (r/32)*4 + j for row r, scale j.
+ *            MXFP8: Gw1 = Gw2 = 1, codes are E4M3 bytes ([E][N1][H],
+ *            [E][H][I]) and the scales E8M0 per 32 elements in the same atom
+ *            layout over 128 elements of K ([E][N1/128][H/128][512],
+ *            [E][H/128][I/128][512]).
  * Errors: MOE_ERR_INVALID_ARG (shape, flags, null/misaligned pointer),
  * MOE_ERR_WORKSPACE (prepared_bytes too small), MOE_ERR_CUDA.  Enqueues two
  * kernels on `stream`; the input buffers must stay valid until they finish. */

@@ -33,6 +33,7 @@ MOE_ROUTE_NO_RENORM = 1 << 6
 MOE_GEMM_PAIRS_NEVER = 1 << 7
 MOE_GEMM_PAIRS_ALWAYS = 1 << 8
 MOE_QUANT_4OVER6 = 1 << 9
+MOE_W8A8_MXFP8 = 3 << 2
 
 
 class MoEError(RuntimeError):
@@ -288,10 +289,12 @@ class MoELayer:
             return (v + 255) // 256 * 256
         N1 = 2 * self.I if (self.flags & 3) == MOE_ACT_SWIGLU else self.I
         E, H, I = self.E, self.H, self.I
+        mx = (self.flags & (3 << 2)) == MOE_W8A8_MXFP8
+        cd, sd = (1, 32) if mx else (2, 16)        # MXFP8: a byte per element, a scale per 32
         o = 0
         r = {}
-        for name, nbytes in [("gw1", 4 * E), ("gw2", 4 * E), ("w1_codes", E * N1 * H // 2),
-                             ("w1_sf", E * N1 * H // 16), ("w2_codes", E * H * I // 2), ("w2_sf", E * H * I // 16)]:
+        for name, nbytes in [("gw1", 4 * E), ("gw2", 4 * E), ("w1_codes", E * N1 * H // cd),
+                             ("w1_sf", E * N1 * H // sd), ("w2_codes", E * H * I // cd), ("w2_sf", E * H * I // sd)]:
             r[name] = (o, nbytes)
             o = up(o + nbytes)
         r["total"] = (o, 0)

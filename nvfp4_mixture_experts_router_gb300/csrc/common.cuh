@@ -44,6 +44,13 @@ __device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
     return r & 0xFFu;
 }
 
+// Two E4M3 codes (signed, satfinite): `lo` -> bits 0-7, `hi` -> bits 8-15.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Exact float value of an E4M3 code (finite codes; 0x7F/0xFF give NaN).
 __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
     uint32_t r;
@@ -105,6 +112,36 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
     const uint32_t m = c & 7u;
     const float mag = m >= 2u ? __uint_as_float(((126u + (m >> 1)) << 23) | ((m & 1u) << 22)) : 0.5f * (float)m;
     return (c & 8u) ? -mag : mag;
+}
+
+// MXFP8 (OCP MX, block 32, E4M3 elements, E8M0 scale): shared exponent
+// floor(log2 amax) - 8, clamped to [-127, 127]; -127 for an all-zero block.
+__device__ __forceinline__ int mx_block_exp(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    if (!(amax > 0.0f) || (b >> 23) >= 255u) return -127;
+    const int fl = (b >> 23) == 0 ? (31 - __clz((int)(b & 0x7FFFFFu))) - 149 : (int)(b >> 23) - 127;
+    return max(-127, min(127, fl - 8));
+}
+// 2^k as a float for k in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ float pow2f(int k) {
+    return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+// Quantize 32 consecutive values: 32 E4M3 codes (element 4w+b in byte b of
+// word w) and the returned E8M0 code e + 127.  v * 2^-e is an exact
+// power-of-two scaling.
+__device__ __forceinline__ uint32_t quant_block32_mx(const float (&v)[32], uint32_t (&codes)[8]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int e = mx_block_exp(amax);
+    const float sc = pow2f(-e);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(v[4 * w], sc), __fmul_rn(v[4 * w + 1], sc));
+        const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(v[4 * w + 2], sc), __fmul_rn(v[4 * w + 3], sc));
+        codes[w] = lo | (hi << 16);
+    }
+    return (uint32_t)(e + 127);
 }
 
 // One candidate of 4-over-6: the block quantized with its maximum mapped to
@@ -323,6 +360,15 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
     return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Instruction descriptor, block-scaled MMA kind::mxf8f6f4 with E4M3 A and B
+// (format code 0), UE8M0 scales (bit 23), scale-factor byte ids at bits
+// 29-30 (A) and 4-5 (B): with one scale per 32 elements (scale_vec::1X) the
+// four K = 32 MMAs of a 128-element chunk share one scale word per row and
+// pick byte `sf_id` of it.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
+    return ((uint32_t)sf_id << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
+           ((uint32_t)sf_id << 29);
+}
 // Instruction descriptor, kind::f16 with BF16 A/B (format 1) and FP32 D
 // (bits 4-5 = 1), K-major both.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
@@ -334,6 +380,16 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uin
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
         " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
@@ -439,6 +495,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Store 16 / 32 consecutive 32-bit columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -457,6 +523,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+// N consecutive columns, N in {4, 8, 16, 32}.
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
+    static_assert(N == 4 || N == 8 || N == 16 || N == 32, "tcgen05.st width");
+    if constexpr (N == 4) tmem_st4(taddr, r);
+    else if constexpr (N == 8) tmem_st8(taddr, r);
+    else if constexpr (N == 16) tmem_st16(taddr, r);
+    else tmem_st32(taddr, r);
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

@@ -51,7 +51,15 @@ __device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr
             col0 = n_tile * 128 + ch * 32;
         }
         if (route < 0) continue;
-        if (EPI == kEpiFc1Quant) {
+        if (EPI == kEpiFc1Mx) {
+            // one MXFP8 block per 32 columns: 32 E4M3 bytes and an E8M0 byte
+            uint32_t q[8];
+            const uint32_t sc = quant_block32_mx(h, q);
+            uint4* dst = reinterpret_cast<uint4*>(p.out_codes + (size_t)row * p.out_cols + col0);
+            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            p.out_sf[sf_offset_mx(row, col0 / 32, p.out_cols)] = (uint8_t)sc;
+        } else if (EPI == kEpiFc1Quant) {
             uint32_t q[4];
             float blk[16];
             uint32_t c2[2];

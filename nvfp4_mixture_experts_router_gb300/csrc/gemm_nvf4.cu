@@ -1,6 +1,11 @@
 // Grouped NVFP4 x NVFP4 GEMMs of the MoE layer on the 5th-generation tensor
 // cores (tcgen05.mma kind::mxf4nvf4, block-scaled with UE4M3 scales per 16
-// elements), with the FC1 and FC2 epilogues fused in.
+// elements), with the FC1 and FC2 epilogues fused in.  The same engine runs
+// the MXFP8 mode (KIND = 1: kind::mxf8f6f4, E4M3 elements, UE8M0 scales per
+// 32): a 128-byte chunk of a row holds 256 E2M1 or 128 E4M3 elements, four
+// 32-byte MMA steps either way; NVFP4 needs one 512-byte scale atom per MMA
+// step and 128 rows, MXFP8 one per chunk (its four MMAs pick bytes 0-3 of
+// each scale word through the scale-factor ids).
 //
 //   D[row, n] = sum_k A[row, k] * B_e[n, k]       (rows of expert e only)
 //
@@ -70,12 +75,13 @@ constexpr uint32_t kTmemCols = 512;
 // slot, so the deeper ring wins where the copies are large anyway (measured
 // at K = 7168: 1087 us with four one-chunk stages, 1169 us with two
 // two-chunk stages).
-template <int BN>
+template <int BN, int KIND>
 struct Cfg {
     static constexpr int kChunks = BN == 128 ? 2 : 1;            // chunks per pipeline stage
-    static constexpr int kKbPerStage = 4 * kChunks;              // 64-element MMA k-blocks per stage
+    static constexpr int kKbPerStage = 4 * kChunks;              // 32-byte MMA steps per stage
+    static constexpr int kAtoms = KIND == 0 ? kKbPerStage : kChunks;   // scale atoms per 128 rows and stage
     static constexpr int kTileBytesA = kChunks * kChunkBytesA;
-    static constexpr int kSfBytesA = kKbPerStage * 512;          // scale atoms (128 rows x 64 elements each)
+    static constexpr int kSfBytesA = kAtoms * 512;
     static constexpr int kStages = BN == 128 ? 3 : 4;
     static constexpr int kAccBufs = BN == 128 ? 2 : 1;
     static constexpr int kEpiWarps = BN == 128 ? 4 : 8;
@@ -87,9 +93,9 @@ struct Cfg {
     static constexpr int kTileBytesB = kChunks * kChunkBytesB;
     static constexpr int kSfBytesB = kRowBlocks * kSfBytesA;
     static constexpr uint32_t kSfColBase = kAccBufs * BN;        // 256 either way
-    static constexpr uint32_t kSfColsA = 4 * kKbPerStage;
-    static constexpr uint32_t kSfColsB = 4 * kRowBlocks;         // per 64-element k-block
-    static constexpr uint32_t kSfColsPerStage = kSfColsA + kKbPerStage * kSfColsB;
+    static constexpr uint32_t kSfColsA = 4 * kAtoms;
+    static constexpr uint32_t kSfColsB = 4 * kRowBlocks;         // per atom slot
+    static constexpr uint32_t kSfColsPerStage = kSfColsA + kAtoms * kSfColsB;
     static constexpr int kSmemBytes = kStages * (kTileBytesA + kTileBytesB + kSfBytesA + kSfBytesB) + 1024 + 256;
     static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -111,9 +117,9 @@ struct Smem {
     volatile int* abort;
 };
 
-template <int BN>
+template <int BN, int KIND>
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, KIND>;
     Smem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.a = base;
@@ -135,13 +141,13 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 
 }  // namespace
 
-template <int EPI, int BN>
-__global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
+template <int EPI, int BN, int KIND>
+__global__ void __launch_bounds__(Cfg<BN, KIND>::kNumThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmParams p) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, KIND>;
     extern __shared__ uint8_t smem_raw[];
-    const Smem s = carve<BN>(smem_raw);
+    const Smem s = carve<BN, KIND>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int no_abort = 0;
 
@@ -176,11 +182,13 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
     const int num_m_tiles = p.meta[1];
     const int n_tiles = (p.n + BN - 1) / BN;
     const int total = num_m_tiles * n_tiles;
-    const int kblocks = p.kdim / 64;                          // 64-element MMA steps
-    constexpr int kKbPerStage = C::kKbPerStage, kChunks = C::kChunks;
+    const int row_bytes = KIND == 0 ? p.kdim / 2 : p.kdim;
+    const int kblocks = row_bytes / 32;                       // 32-byte MMA steps
+    constexpr int kKbPerStage = C::kKbPerStage, kChunks = C::kChunks, kAtoms = C::kAtoms;
     const int kstages = (kblocks + kKbPerStage - 1) / kKbPerStage;
     const int rb_per_expert = p.n / 128;
-    const int row_chunks = (p.kdim / 2 + kChunkBytes - 1) / kChunkBytes;   // 128-byte chunks per row
+    const int row_chunks = (row_bytes + kChunkBytes - 1) / kChunkBytes;   // 128-byte chunks per row
+    const int atoms = KIND == 0 ? kblocks : row_chunks;      // scale atoms per 128 rows over all of K
 
     if (warp == 0) {
         if (lane == 0) {
@@ -198,21 +206,21 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
                 const int nrb = min(C::kRowBlocks, rb_per_expert - n_tile * C::kRowBlocks);
                 const int a_row = m_tile * kBM;
                 const int b_row = e * p.n + n_tile * BN;
-                const uint8_t* sfa_src = p.sfa + (size_t)m_tile * kblocks * 512;
+                const uint8_t* sfa_src = p.sfa + (size_t)m_tile * atoms * 512;
                 const uint8_t* sfb_src =
-                    p.sfb + ((size_t)e * rb_per_expert + (size_t)n_tile * C::kRowBlocks) * kblocks * 512;
+                    p.sfb + ((size_t)e * rb_per_expert + (size_t)n_tile * C::kRowBlocks) * atoms * 512;
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
-                    const int nkb = min(kKbPerStage, kblocks - kKbPerStage * ks);
-                    const uint32_t sf_bytes = (uint32_t)nkb * 512u;
+                    const int n_at = min(kAtoms, atoms - kAtoms * ks);
+                    const uint32_t sf_bytes = (uint32_t)n_at * 512u;
                     // the small scale atoms first, on their own barrier, so the
                     // scale writers can start while the operand tiles are in flight
                     mbar_arrive_expect_tx(&s.sf_full[stage], (uint32_t)(1 + nrb) * sf_bytes);
-                    bulk_load(s.sfa + stage * C::kSfBytesA, sfa_src + (size_t)ks * kKbPerStage * 512, sf_bytes,
+                    bulk_load(s.sfa + stage * C::kSfBytesA, sfa_src + (size_t)ks * kAtoms * 512, sf_bytes,
                               &s.sf_full[stage], pol);
                     for (int rb = 0; rb < nrb; ++rb)
                         bulk_load(s.sfb + stage * C::kSfBytesB + rb * C::kSfBytesA,
-                                  sfb_src + ((size_t)rb * kblocks + (size_t)ks * kKbPerStage) * 512, sf_bytes,
+                                  sfb_src + ((size_t)rb * atoms + (size_t)ks * kAtoms) * 512, sf_bytes,
                                   &s.sf_full[stage], pol);
                     uint8_t* a_dst = s.a + stage * C::kTileBytesA;
                     uint8_t* b_dst = s.b + stage * C::kTileBytesB;
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
                 const int n_tile = tile % n_tiles;
                 const int width = min(BN, p.n - n_tile * BN);
-                const uint32_t idesc = idesc_nvf4(kBM, width);
+                const uint32_t idesc = idesc_nvf4(kBM, width);   // NVFP4 (MXFP8 builds its own per MMA)
                 if (!mbar_wait(&s.acc_empty[acc], acc_phase ^ 1u, s.abort, p.status, kStatusTimeoutMma)) goto done;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -263,13 +271,17 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
                     const uint32_t a_s = smem_u32(s.a + stage * C::kTileBytesA);
                     const uint32_t b_s = smem_u32(s.b + stage * C::kTileBytesB);
                     for (int j = 0; j < nkb; ++j) {
-                        // chunk j / 4, then 32 bytes (64 E2M1) along K inside
-                        // its swizzled 128-byte rows
+                        // chunk j / 4, then 32 bytes (64 E2M1 / 32 E4M3) along K
+                        // inside its swizzled 128-byte rows
                         const int c = j >> 2, jj = j & 3;
                         const uint64_t adesc = sdesc_kmajor_sw128(a_s + c * kChunkBytesA) + 2u * jj;
                         const uint64_t bdesc = sdesc_kmajor_sw128(b_s + c * C::kChunkBytesB) + 2u * jj;
-                        tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + C::kSfColsB * j,
-                                    (ks | j) != 0);
+                        if (KIND == 0)
+                            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + C::kSfColsB * j,
+                                        (ks | j) != 0);
+                        else
+                            tc_mma_mxf8(d_tmem, adesc, bdesc, idesc_mxf8(kBM, width, jj), sfa_t + 4 * c,
+                                        sfb_t + C::kSfColsB * c, (ks | j) != 0);
                     }
                     tc_commit(&s.empty[stage]);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -292,41 +304,28 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
                     goto done;
                 const uint32_t sfa_t = tmem_base + C::kSfColBase + (uint32_t)stage * C::kSfColsPerStage;
                 const uint32_t sfb_t = sfa_t + C::kSfColsA;
-                // per chunk (4 k-blocks): A scales 16 columns (k-block j: 4),
-                // B scales 16 (BN = 128) or 32 columns (k-block j: 8, row block
-                // 0 then row block 1)
+                // A scales: atom a -> columns 4a..4a+3; B scales: atom a, row
+                // block rb -> columns 4 (a * kRowBlocks + rb) .. +3
+                {
+                    uint32_t ra[4 * kAtoms];
 #pragma unroll
-                for (int h = 0; h < kChunks; ++h) {
-                    uint32_t ra[16];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(s.sfa + stage * C::kSfBytesA +
-                                                                        (4 * h + j) * 512 + lane * 16);
-                        ra[4 * j] = v.x; ra[4 * j + 1] = v.y; ra[4 * j + 2] = v.z; ra[4 * j + 3] = v.w;
+                    for (int a = 0; a < kAtoms; ++a) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(s.sfa + stage * C::kSfBytesA + a * 512 +
+                                                                        lane * 16);
+                        ra[4 * a] = v.x; ra[4 * a + 1] = v.y; ra[4 * a + 2] = v.z; ra[4 * a + 3] = v.w;
                     }
-                    tmem_st16(sfa_t + lane_off + 16 * h, ra);
-                    if (C::kRowBlocks == 1) {
-                        uint32_t rb_[16];
+                    tmem_st_n<4 * kAtoms>(sfa_t + lane_off, ra);
+                    uint32_t rb_[4 * kAtoms * C::kRowBlocks];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(s.sfb + stage * C::kSfBytesB +
-                                                                            (4 * h + j) * 512 + lane * 16);
-                            rb_[4 * j] = v.x; rb_[4 * j + 1] = v.y; rb_[4 * j + 2] = v.z; rb_[4 * j + 3] = v.w;
+                    for (int a = 0; a < kAtoms; ++a)
+#pragma unroll
+                        for (int rb = 0; rb < C::kRowBlocks; ++rb) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(
+                                s.sfb + stage * C::kSfBytesB + rb * C::kSfBytesA + a * 512 + lane * 16);
+                            const int o = 4 * (a * C::kRowBlocks + rb);
+                            rb_[o] = v.x; rb_[o + 1] = v.y; rb_[o + 2] = v.z; rb_[o + 3] = v.w;
                         }
-                        tmem_st16(sfb_t + lane_off + 16 * h, rb_);
-                    } else {
-                        uint32_t rb_[32];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-#pragma unroll
-                            for (int rb = 0; rb < 2; ++rb) {
-                                const uint4 v = *reinterpret_cast<const uint4*>(
-                                    s.sfb + stage * C::kSfBytesB + rb * C::kSfBytesA + (4 * h + j) * 512 + lane * 16);
-                                rb_[8 * j + 4 * rb] = v.x; rb_[8 * j + 4 * rb + 1] = v.y;
-                                rb_[8 * j + 4 * rb + 2] = v.z; rb_[8 * j + 4 * rb + 3] = v.w;
-                            }
-                        tmem_st32(sfb_t + lane_off + 32 * h, rb_);
-                    }
+                    tmem_st_n<4 * kAtoms * C::kRowBlocks>(sfb_t + lane_off, rb_);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -355,7 +354,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kNumThreads, 1)
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + half * 128);
                 const int vtile = n_tile * C::kRowBlocks + half;   // index of this 128-column slice
-                if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32) epilogue_fc1<EPI>(p, taddr, row, route, e, vtile);
+                if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32 || EPI == kEpiFc1Mx)
+                    epilogue_fc1<EPI>(p, taddr, row, route, e, vtile);
                 else epilogue_fc2<EPI>(p, taddr, row, route, e, vtile);
             }
             tc_fence_before();
@@ -383,17 +383,22 @@ done:
     }
 }
 
+template <int EPI, int BN, int KIND>
+static cudaError_t set_smem_one() {
+    return cudaFuncSetAttribute(gemm_nvf4_kernel<EPI, BN, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<BN, KIND>::kSmemBytes);
+}
+
 template <int BN>
 static cudaError_t set_smem_all() {
     cudaError_t e;
-    const int b = Cfg<BN>::kSmemBytes;
-    if ((e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc1Quant, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, b)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc1F32, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, b)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc2Store, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, b)))
-        return e;
-    return cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiFc2Scatter, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+    if ((e = set_smem_one<kEpiFc1Quant, BN, 0>())) return e;
+    if ((e = set_smem_one<kEpiFc1F32, BN, 0>())) return e;
+    if ((e = set_smem_one<kEpiFc2Store, BN, 0>())) return e;
+    if ((e = set_smem_one<kEpiFc2Scatter, BN, 0>())) return e;
+    if ((e = set_smem_one<kEpiFc1Mx, BN, 1>())) return e;
+    if ((e = set_smem_one<kEpiFc2Store, BN, 1>())) return e;
+    return set_smem_one<kEpiFc2Scatter, BN, 1>();
 }
 
 cudaError_t setup_gemm_kernels() {
@@ -402,16 +407,30 @@ cudaError_t setup_gemm_kernels() {
     return set_smem_all<256>();
 }
 
+template <int EPI, int BN, int KIND>
+static cudaError_t launch_one(const LaunchCtx& c, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const GemmParams& p, int num_sms) {
+    using C = Cfg<BN, KIND>;
+    return c.launch(gemm_nvf4_kernel<EPI, BN, KIND>, dim3(num_sms), dim3(C::kNumThreads), (size_t)C::kSmemBytes, tmA,
+                    tmB, p);
+}
+
 template <int BN>
-static cudaError_t launch_bn(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const GemmParams& p, int num_sms) {
-    const dim3 grid(num_sms), block(Cfg<BN>::kNumThreads);
-    const size_t smem = Cfg<BN>::kSmemBytes;
+static cudaError_t launch_bn(const LaunchCtx& c, int epilogue, int kind, const CUtensorMap& tmA,
+                             const CUtensorMap& tmB, const GemmParams& p, int num_sms) {
+    if (kind == 0) {
+        switch (epilogue) {
+            case kEpiFc1Quant: return launch_one<kEpiFc1Quant, BN, 0>(c, tmA, tmB, p, num_sms);
+            case kEpiFc1F32: return launch_one<kEpiFc1F32, BN, 0>(c, tmA, tmB, p, num_sms);
+            case kEpiFc2Store: return launch_one<kEpiFc2Store, BN, 0>(c, tmA, tmB, p, num_sms);
+            case kEpiFc2Scatter: return launch_one<kEpiFc2Scatter, BN, 0>(c, tmA, tmB, p, num_sms);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (epilogue) {
-        case kEpiFc1Quant: return c.launch(gemm_nvf4_kernel<kEpiFc1Quant, BN>, grid, block, smem, tmA, tmB, p);
-        case kEpiFc1F32: return c.launch(gemm_nvf4_kernel<kEpiFc1F32, BN>, grid, block, smem, tmA, tmB, p);
-        case kEpiFc2Store: return c.launch(gemm_nvf4_kernel<kEpiFc2Store, BN>, grid, block, smem, tmA, tmB, p);
-        case kEpiFc2Scatter: return c.launch(gemm_nvf4_kernel<kEpiFc2Scatter, BN>, grid, block, smem, tmA, tmB, p);
+        case kEpiFc1Mx: return launch_one<kEpiFc1Mx, BN, 1>(c, tmA, tmB, p, num_sms);
+        case kEpiFc2Store: return launch_one<kEpiFc2Store, BN, 1>(c, tmA, tmB, p, num_sms);
+        case kEpiFc2Scatter: return launch_one<kEpiFc2Scatter, BN, 1>(c, tmA, tmB, p, num_sms);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -425,9 +444,9 @@ int gemm_nvf4_tile_n(int kdim, int n) {
 }
 
 cudaError_t launch_gemm_nvf4(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const GemmParams& p, int num_sms, int tile_n) {
-    return tile_n == 256 ? launch_bn<256>(c, epilogue, tmA, tmB, p, num_sms)
-                         : launch_bn<128>(c, epilogue, tmA, tmB, p, num_sms);
+                             const GemmParams& p, int num_sms, int tile_n, int kind) {
+    return tile_n == 256 ? launch_bn<256>(c, epilogue, kind, tmA, tmB, p, num_sms)
+                         : launch_bn<128>(c, epilogue, kind, tmA, tmB, p, num_sms);
 }
 
 }  // namespace moe

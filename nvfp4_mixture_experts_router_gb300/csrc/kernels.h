@@ -75,6 +75,9 @@ struct RouteScatter {
 cudaError_t launch_quantize_x(const LaunchCtx& c, int T, int H, int K, const void* x, const float* g1_in,
                               int per_token, float* g1_out, const RouteScatter& rs, uint8_t* codes, uint8_t* sf,
                               float* y_acc_zero);
+// MXFP8 mode: x quantized to E4M3 / E8M0 per 32 into the token's permuted rows
+cudaError_t launch_quantize_x_mx(const LaunchCtx& c, int T, int H, int K, const void* x, const RouteScatter& rs,
+                                 uint8_t* codes, uint8_t* sf, float* y_acc_zero);
 cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const void* x, const RouteScatter& rs,
                                  void* x_perm, float* y_acc_zero);
 // per_token (quantize_x): 0 caller's per-tensor scale, 1 per-token, 2 per-token
@@ -88,6 +91,9 @@ cudaError_t launch_finalize_fused(const LaunchCtx& c, int T, int H, const float*
 cudaError_t launch_prepare(cudaStream_t s, int E, int N1, int H, int I, int act, const void* w1, const void* w2,
                            uint8_t* prepared, uint64_t gw1, uint64_t gw2, uint64_t w1c, uint64_t w1s, uint64_t w2c,
                            uint64_t w2s);
+cudaError_t launch_prepare_mx(cudaStream_t s, int E, int N1, int H, int I, int act, const void* w1, const void* w2,
+                              uint8_t* prepared, uint64_t gw1, uint64_t gw2, uint64_t w1c, uint64_t w1s, uint64_t w2c,
+                              uint64_t w2s);
 cudaError_t launch_debug_convert(cudaStream_t s, const float* in, int64_t n, uint8_t* e4m3, uint8_t* e2m1);
 
 // gemm_nvf4.cu — grouped block-scaled GEMMs on tcgen05
@@ -96,7 +102,8 @@ enum GemmEpilogue : int {
     kEpiFc1F32 = 1,     // FC1: activation, route weight, FP32 store (per-token G2 later)
     kEpiFc2Store = 2,   // FC2: BF16 per-route rows (deterministic finalize)
     kEpiFc2Scatter = 3, // FC2: weighted FP32 atomic add into the token row (fused finalize)
-    kEpiFc1Bf16 = 4     // FC1 (W4A16): activation, route weight, BF16 store
+    kEpiFc1Bf16 = 4,    // FC1 (W4A16): activation, route weight, BF16 store
+    kEpiFc1Mx = 5       // FC1 (MXFP8): activation, route weight, MXFP8 requant (block 32)
 };
 
 struct GemmParams {
@@ -123,8 +130,8 @@ struct GemmParams {
     int weight_on_output;        // FC2 scatter: multiply o by the route weight
     const float* g2;             // FC1 quant: per-tensor FC2-input scale [1]
     int out_cols;                // width of the output row (I for FC1, H for FC2)
-    uint8_t* out_codes;          // FC1 quant: [rows_cap][I/2]
-    uint8_t* out_sf;             // FC1 quant: [rows_cap/128][I/64][512]
+    uint8_t* out_codes;          // FC1 quant: [rows_cap][I/2] (MXFP8: [rows_cap][I])
+    uint8_t* out_sf;             // FC1 quant: [rows_cap/128][I/64][512] (MXFP8: [..][I/128][512])
     float* out_f32;              // FC1 F32: [rows_cap][I]; FC2 scatter: y_acc [T][H]
                                  // (g_act == nullptr: no activation global scale, W4A16)
     __nv_bfloat16* out_bf16;     // FC2 store: [rows_cap][H]; FC1 BF16: [rows_cap][I]
@@ -134,10 +141,11 @@ cudaError_t setup_gemm_kernels();
 cudaError_t setup_gemm_w4a16_kernels();
 cudaError_t launch_gemm_w4a16(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmBq,
                               const GemmParams& p, int num_sms);
-// tile_n = gemm_nvf4_tile_n(kdim, n) (128 or 256); tmB's box must be tile_n rows high
+// tile_n = gemm_nvf4_tile_n(kdim, n) (128 or 256); tmB's box must be tile_n rows high.
+// kind 0: NVFP4 operands (kind::mxf4nvf4); 1: MXFP8 operands (kind::mxf8f6f4).
 int gemm_nvf4_tile_n(int kdim, int n);
 cudaError_t launch_gemm_nvf4(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const GemmParams& p, int num_sms, int tile_n);
+                             const GemmParams& p, int num_sms, int tile_n, int kind);
 // gemm_nvf4_pair.cu — the same GEMMs on CTA pairs (256 x 256 pair tiles over
 // pairs of M tiles of one expert); needs n % 256 == 0 and a tmB box of 128
 // rows.  setup sizes the persistent grid for `device`.

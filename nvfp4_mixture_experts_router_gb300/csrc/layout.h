@@ -24,7 +24,7 @@ MOE_HD uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
 
 MOE_HD int act_of(uint32_t flags) { return (int)(flags & MOE_ACT_MASK); }
 MOE_HD int mode_of(uint32_t flags) { return (int)((flags & MOE_MODE_MASK) >> 2); }
-constexpr int kModePerTensor = 0, kModePerToken = 1, kModeW4A16 = 2;
+constexpr int kModePerTensor = 0, kModePerToken = 1, kModeW4A16 = 2, kModeMxfp8 = 3;
 
 MOE_HD int n1_of(int I, uint32_t flags) { return act_of(flags) == MOE_ACT_SWIGLU ? 2 * I : I; }
 
@@ -44,6 +44,13 @@ MOE_HD uint64_t sf_offset(uint64_t r, uint64_t j, uint64_t cols) {
     return ((r >> 7) * (cols >> 6) + (j >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (j & 3u);
 }
 
+// The same atom layout for MXFP8 scales (one E8M0 per 32 elements): an
+// atom holds 128 rows x 4 scales covering 128 elements of K, so `j` (the
+// 32-element block) groups by four as above and `cols` counts elements.
+MOE_HD uint64_t sf_offset_mx(uint64_t r, uint64_t j, uint64_t cols) {
+    return ((r >> 7) * (cols >> 7) + (j >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (j & 3u);
+}
+
 // Prepared FC1 row of checkpoint row `r` (SwiGLU: rows [0, I) gate, [I, 2I) up).
 MOE_HD int prepared_w1_row(int r, int I, int act) {
     if (act != MOE_ACT_SWIGLU) return r;
@@ -57,14 +64,18 @@ struct PreparedLayout {
     uint64_t w1_codes_per_expert, w1_sf_per_expert, w2_codes_per_expert, w2_sf_per_expert;
 };
 
+// NVFP4 weights (every mode but MXFP8): half a byte per element and a scale
+// per 16; MXFP8 weights: a byte per element and a scale per 32.
 MOE_HD PreparedLayout prepared_layout(moe_shape s, uint32_t flags) {
     PreparedLayout L{};
     const uint64_t E = (uint64_t)s.E, H = (uint64_t)s.H, I = (uint64_t)s.I;
     const uint64_t N1 = (uint64_t)n1_of(s.I, flags);
-    L.w1_codes_per_expert = N1 * H / 2;
-    L.w1_sf_per_expert = N1 * H / 16;
-    L.w2_codes_per_expert = H * I / 2;
-    L.w2_sf_per_expert = H * I / 16;
+    const bool mx = mode_of(flags) == kModeMxfp8;
+    const uint64_t cdiv = mx ? 1 : 2, sdiv = mx ? 32 : 16;
+    L.w1_codes_per_expert = N1 * H / cdiv;
+    L.w1_sf_per_expert = N1 * H / sdiv;
+    L.w2_codes_per_expert = H * I / cdiv;
+    L.w2_sf_per_expert = H * I / sdiv;
     uint64_t o = 0;
     L.gw1 = o; o = align_up(o + 4 * E, 256);
     L.gw2 = o; o = align_up(o + 4 * E, 256);
@@ -104,7 +115,13 @@ inline moe_workspace_layout workspace_layout(moe_shape s, uint32_t flags) {
     L.route_of_row = take(4 * cap);
     L.tile_expert = take(4 * (cap / kTileM));
     L.tile_pair = take(4 * (cap / kTileM));
-    if (mode != kModeW4A16) {
+    if (mode == kModeMxfp8) {
+        // E4M3 codes, E8M0 scales per 32 (no global scales)
+        L.xq_codes = take(cap * H);
+        L.xq_sf = take(cap * H / 32);
+        L.hq_codes = take(cap * I);
+        L.hq_sf = take(cap * I / 32);
+    } else if (mode != kModeW4A16) {
         L.g1 = take(4 * T);
         L.xq_codes = take(cap * H / 2);
         L.xq_sf = take(cap * H / 16);

@@ -75,7 +75,7 @@ moe_status validate_shape(moe_shape s, uint32_t flags) {
     if (flags & ~MOE_FLAGS_KNOWN) return MOE_ERR_INVALID_ARG;
     if ((flags & MOE_GEMM_PAIRS_NEVER) && (flags & MOE_GEMM_PAIRS_ALWAYS)) return MOE_ERR_INVALID_ARG;
     if ((flags & MOE_QUANT_4OVER6) && mode_of(flags) != kModePerToken) return MOE_ERR_INVALID_ARG;
-    if (act_of(flags) > 1 || mode_of(flags) > 2) return MOE_ERR_INVALID_ARG;
+    if (act_of(flags) > 1) return MOE_ERR_INVALID_ARG;
     if (s.T < 1 || s.T > (1 << 22)) return MOE_ERR_INVALID_ARG;
     if (s.H < 128 || s.H % 128 != 0 || s.H > 65536) return MOE_ERR_INVALID_ARG;
     if (s.I < 128 || s.I % 128 != 0 || s.I > 65536) return MOE_ERR_INVALID_ARG;
@@ -167,9 +167,10 @@ moe_status moe_nvfp4_prepare_weights(moe_shape s, uint32_t flags, const void* w1
     st = device_state(&sms);
     if (st != MOE_OK) return st;
     const int N1 = n1_of(s.I, flags);
-    return cuda_status(launch_prepare(static_cast<cudaStream_t>(stream), s.E, N1, s.H, s.I, act_of(flags), w1_bf16,
-                                      w2_bf16, static_cast<uint8_t*>(prepared), L.gw1, L.gw2, L.w1_codes, L.w1_sf,
-                                      L.w2_codes, L.w2_sf));
+    auto prep = mode_of(flags) == kModeMxfp8 ? launch_prepare_mx : launch_prepare;
+    return cuda_status(prep(static_cast<cudaStream_t>(stream), s.E, N1, s.H, s.I, act_of(flags), w1_bf16, w2_bf16,
+                            static_cast<uint8_t*>(prepared), L.gw1, L.gw2, L.w1_codes, L.w1_sf, L.w2_codes,
+                            L.w2_sf));
 }
 
 // Routing input of a forward: router logits (+ bias), or caller-supplied
@@ -204,6 +205,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         if (!act_scale_fc1 || !act_scale_fc2 || !aligned(act_scale_fc1, 4) || !aligned(act_scale_fc2, 4))
             return MOE_ERR_INVALID_ARG;
     }
+    if (mode == kModeMxfp8 && (act_scale_fc1 || act_scale_fc2)) return MOE_ERR_INVALID_ARG;   // no global scales
     const moe_workspace_layout W = workspace_layout(s, flags);
     if (workspace_bytes < W.total) return MOE_ERR_WORKSPACE;
     const size_t y_bytes = (size_t)s.T * s.H * 2;
@@ -340,36 +342,40 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         return MOE_OK;
     }
 
-    // ---- W4A4 ----
+    // ---- W4A4 (NVFP4) and W8A8 (MXFP8) ----
+    const bool mx = mode == kModeMxfp8;
     const bool per_token = mode == kModePerToken;
-    float* g1 = reinterpret_cast<float*>(wsp(W.g1));
+    float* g1 = mx ? nullptr : reinterpret_cast<float*>(wsp(W.g1));
     uint8_t* xq_codes = wsp(W.xq_codes);
     uint8_t* xq_sf = wsp(W.xq_sf);
     uint8_t* hq_codes = wsp(W.hq_codes);
     uint8_t* hq_sf = wsp(W.hq_sf);
     const bool four_six = (flags & MOE_QUANT_4OVER6) != 0;
-    e = launch_quantize_x(c, s.T, s.H, s.K, x_bf16, act_scale_fc1, per_token ? (four_six ? 2 : 1) : 0, g1, rs,
-                          xq_codes, xq_sf, y_acc);
+    if (mx)
+        e = launch_quantize_x_mx(c, s.T, s.H, s.K, x_bf16, rs, xq_codes, xq_sf, y_acc);
+    else
+        e = launch_quantize_x(c, s.T, s.H, s.K, x_bf16, act_scale_fc1, per_token ? (four_six ? 2 : 1) : 0, g1, rs,
+                              xq_codes, xq_sf, y_acc);
     if (e != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
-    const bool pair1 = use_pair_gemm(s, flags, N1), pair2 = use_pair_gemm(s, flags, s.H);
+    // operand rows: NVFP4 half a byte per element, MXFP8 a byte
+    const uint64_t rbx = mx ? (uint64_t)s.H : (uint64_t)s.H / 2, rbh = mx ? (uint64_t)s.I : (uint64_t)s.I / 2;
+    const bool pair1 = !mx && use_pair_gemm(s, flags, N1), pair2 = !mx && use_pair_gemm(s, flags, s.H);
     const int tn1 = pair1 ? 128 : gemm_nvf4_tile_n(s.H, N1), tn2 = pair2 ? 128 : gemm_nvf4_tile_n(s.I, s.H);
     // single-CTA GEMMs with 128-wide tiles over rows of a multiple of 128
     // bytes copy two chunks per TMA instruction (3-D maps); the others use
     // 2-D maps
-    const bool ch1 = !pair1 && tn1 == 128 && (s.H / 2) % 128 == 0;
-    const bool ch2 = !pair2 && tn2 == 128 && (s.I / 2) % 128 == 0;
+    const bool ch1 = !pair1 && tn1 == 128 && rbx % 128 == 0;
+    const bool ch2 = !pair2 && tn2 == 128 && rbh % 128 == 0;
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
-    const bool ok1 = ch1 ? (encode_chunk_map(&tmA1, xq_codes, W.rows_cap, (uint64_t)s.H / 2, 128) &&
-                            encode_chunk_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, tn1))
-                         : (encode_operand_map(&tmA1, xq_codes, W.rows_cap, (uint64_t)s.H / 2) &&
-                            encode_operand_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 128,
-                                               tn1));
-    const bool ok2 = ch2 ? (encode_chunk_map(&tmA2, hq_codes, W.rows_cap, (uint64_t)s.I / 2, 128) &&
-                            encode_chunk_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, tn2))
-                         : (encode_operand_map(&tmA2, hq_codes, W.rows_cap, (uint64_t)s.I / 2) &&
-                            encode_operand_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 128,
-                                               tn2));
+    const bool ok1 = ch1 ? (encode_chunk_map(&tmA1, xq_codes, W.rows_cap, rbx, 128) &&
+                            encode_chunk_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, rbx, tn1))
+                         : (encode_operand_map(&tmA1, xq_codes, W.rows_cap, rbx) &&
+                            encode_operand_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, rbx, 128, tn1));
+    const bool ok2 = ch2 ? (encode_chunk_map(&tmA2, hq_codes, W.rows_cap, rbh, 128) &&
+                            encode_chunk_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, rbh, tn2))
+                         : (encode_operand_map(&tmA2, hq_codes, W.rows_cap, rbh) &&
+                            encode_operand_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, rbh, 128, tn2));
     if (!ok1 || !ok2) return MOE_ERR_CUDA;
     int* tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
 
@@ -392,7 +398,12 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     g1p.weight_on_input = on_input ? 1 : 0;
     g1p.out_cols = s.I;
     int epi1;
-    if (per_token) {
+    if (mx) {
+        g1p.g_act = nullptr;           // MXFP8: no activation global scale
+        g1p.out_codes = hq_codes;
+        g1p.out_sf = hq_sf;
+        epi1 = kEpiFc1Mx;
+    } else if (per_token) {
         g1p.g_act = g1;
         g1p.g_act_per_token = 1;
         g1p.out_f32 = reinterpret_cast<float*>(wsp(W.h_f32));
@@ -406,7 +417,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         epi1 = kEpiFc1Quant;
     }
     e = pair1 ? launch_gemm_nvf4_pair(c, epi1, tmA1, tmB1, g1p, device)
-              : launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms, tn1);
+              : launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms, tn1, mx ? 1 : 0);
     if (e != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
     if (per_token) {
         e = launch_quantize_h(c, W.rows_cap, s.I, meta, route_of_row, reinterpret_cast<const float*>(wsp(W.h_f32)),
@@ -433,7 +444,10 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     g2p.topk_w = topk_w;
     g2p.weight_on_output = on_input ? 0 : 1;
     g2p.out_cols = s.H;
-    if (per_token) {
+    if (mx) {
+        g2p.g_act = nullptr;
+        g2p.g_act_per_token = 0;
+    } else if (per_token) {
         g2p.g_act = reinterpret_cast<const float*>(wsp(W.g2));
         g2p.g_act_per_token = 2;
     } else {
@@ -449,7 +463,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         epi2 = kEpiFc2Scatter;
     }
     e = pair2 ? launch_gemm_nvf4_pair(c, epi2, tmA2, tmB2, g2p, device)
-              : launch_gemm_nvf4(c, epi2, tmA2, tmB2, g2p, sms, tn2);
+              : launch_gemm_nvf4(c, epi2, tmA2, tmB2, g2p, sms, tn2, mx ? 1 : 0);
     if (e != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
 
     if (det)

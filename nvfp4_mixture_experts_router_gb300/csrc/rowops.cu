@@ -139,6 +139,61 @@ __global__ void __launch_bounds__(1024) quantize_x_kernel(int T, int H, int K, c
     pdl_launch_dependents();
 }
 
+// MXFP8: x [T][H] BF16 -> E4M3 codes (a byte each) and E8M0 scales per 32
+// elements, written to each of the token's K permuted rows.  One CTA per
+// token, one thread per 32-element block (blocks are independent: no row
+// reduction); hands out the permuted rows and zeroes the token's row of the
+// fused-finalize accumulator like quantize_x_kernel.
+__global__ void __launch_bounds__(1024) quantize_x_mx_kernel(int T, int H, int K, const __nv_bfloat16* __restrict__ x,
+                                                             const RouteScatter rs, uint8_t* __restrict__ codes,
+                                                             uint8_t* __restrict__ sf, float* __restrict__ y_acc_zero) {
+    __shared__ int s_rows[32];
+    pdl_wait();
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (warp == 0) {
+        const int row = scatter_token_routes(t, T, K, lane, rs);
+        if (lane < K) s_rows[lane] = row;
+    }
+    __syncthreads();
+    const int nblk = H / 32;
+    const __nv_bfloat16* xr = x + (size_t)t * H;
+    for (int b0 = 0; b0 < nblk; b0 += blockDim.x) {      // uniform across the CTA
+        const int b = b0 + tid;
+        const bool active = b < nblk;
+        uint32_t q[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        uint32_t s = 0;
+        if (active) {
+            float v[32];
+            float h16[16];
+            load16_bf16(xr + 32 * b, h16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = h16[i];
+            load16_bf16(xr + 32 * b + 16, h16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[16 + i] = h16[i];
+            s = quant_block32_mx(v, q);
+        }
+        const uint32_t word = pack_sf4(s);
+        if (active) {
+            for (int k = 0; k < K; ++k) {
+                const int row = s_rows[k];
+                if (row < 0) continue;
+                uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)row * H + 32 * b);
+                dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+                dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+                if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset_mx(row, b, H)) = word;
+            }
+        }
+    }
+    if (y_acc_zero) {
+        float* yr = y_acc_zero + (size_t)t * H;
+        for (int c = tid * 4; c < H; c += blockDim.x * 4)
+            *reinterpret_cast<float4*>(yr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_launch_dependents();
+}
+
 // W4A16: copy each token's BF16 row to its K permuted rows.
 __global__ void __launch_bounds__(256) gather_x_bf16_kernel(int T, int H, int K, const __nv_bfloat16* __restrict__ x,
                                                             const RouteScatter rs,
@@ -315,6 +370,56 @@ __global__ void prep_scales_kernel(int E, const uint32_t* __restrict__ amax_bits
     }
 }
 
+// MXFP8 weights: one warp per weight row (W1 rows first, then W2 rows), one
+// lane per 32-element block; Gw1 = Gw2 = 1 (no global scales).
+__global__ void __launch_bounds__(256) prep_quant_mx_kernel(int E, int N1, int H, int I, int act,
+                                                            const __nv_bfloat16* __restrict__ w1,
+                                                            const __nv_bfloat16* __restrict__ w2,
+                                                            float* __restrict__ gw1, float* __restrict__ gw2,
+                                                            uint8_t* __restrict__ w1c, uint8_t* __restrict__ w1s,
+                                                            uint8_t* __restrict__ w2c, uint8_t* __restrict__ w2s) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gr = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gr < 2 * (int64_t)E && lane == 0) {
+        if (gr < E) gw1[gr] = 1.0f;
+        else gw2[gr - E] = 1.0f;
+    }
+    const int64_t rows1 = (int64_t)E * N1, rows2 = (int64_t)E * H;
+    if (gr >= rows1 + rows2) return;
+    const bool first = gr < rows1;
+    const int64_t r = first ? gr : gr - rows1;
+    const int Nrows = first ? N1 : H;
+    const int Kd = first ? H : I;
+    const int e = (int)(r / Nrows), rr = (int)(r % Nrows);
+    const __nv_bfloat16* src = first ? w1 + (size_t)r * H : w2 + (size_t)r * I;
+    const int prow = first ? prepared_w1_row(rr, I, act) : rr;
+    uint8_t* codes = first ? w1c + (size_t)e * N1 * H : w2c + (size_t)e * H * I;
+    uint8_t* sf = first ? w1s + (size_t)e * N1 * (H / 32) : w2s + (size_t)e * H * (I / 32);
+    for (int base = 0; base < Kd; base += 1024) {          // uniform across the warp
+        const int c = base + lane * 32;
+        const bool active = c < Kd;
+        uint32_t q[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        uint32_t s = 0;
+        if (active) {
+            float v[32], h16[16];
+            load16_bf16(src + c, h16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = h16[i];
+            load16_bf16(src + c + 16, h16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[16 + i] = h16[i];
+            s = quant_block32_mx(v, q);
+        }
+        const uint32_t word = pack_sf4(s);
+        if (active) {
+            uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)prow * Kd + c);
+            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset_mx(prow, c / 32, Kd)) = word;
+        }
+    }
+}
+
 // One warp per weight row (W1 rows first, then W2 rows).
 __global__ void __launch_bounds__(256) prep_quant_kernel(int E, int N1, int H, int I, int act,
                                                          const __nv_bfloat16* __restrict__ w1,
@@ -441,6 +546,24 @@ cudaError_t launch_prepare(cudaStream_t s, int E, int N1, int H, int I, int act,
         reinterpret_cast<const float*>(prepared + gw1), reinterpret_cast<const float*>(prepared + gw2),
         prepared + w1c, prepared + w1s, prepared + w2c, prepared + w2s);
     return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_mx(cudaStream_t s, int E, int N1, int H, int I, int act, const void* w1, const void* w2,
+                              uint8_t* prepared, uint64_t gw1, uint64_t gw2, uint64_t w1c, uint64_t w1s, uint64_t w2c,
+                              uint64_t w2s) {
+    const int64_t rows = (int64_t)E * (N1 + H);
+    prep_quant_mx_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+        E, N1, H, I, act, (const __nv_bfloat16*)w1, (const __nv_bfloat16*)w2, reinterpret_cast<float*>(prepared + gw1),
+        reinterpret_cast<float*>(prepared + gw2), prepared + w1c, prepared + w1s, prepared + w2c, prepared + w2s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_x_mx(const LaunchCtx& c, int T, int H, int K, const void* x, const RouteScatter& rs,
+                                 uint8_t* codes, uint8_t* sf, float* y_acc_zero) {
+    int threads = ((H / 32 + 31) / 32) * 32;
+    if (threads > 1024) threads = 1024;
+    return c.launch(quantize_x_mx_kernel, dim3(T), dim3(threads), 0, T, H, K, (const __nv_bfloat16*)x, rs, codes,
+                    sf, y_acc_zero);
 }
 
 cudaError_t launch_debug_convert(cudaStream_t s, const float* in, int64_t n, uint8_t* e4m3, uint8_t* e2m1) {

@@ -107,7 +107,7 @@ def normal_bf16(seed, stream, start, n, std, device="cpu"):
 # ---------------------------------------------------------------------------
 
 ACT_SWIGLU, ACT_RELU2 = 0, 1
-MODE_PER_TENSOR, MODE_PER_TOKEN, MODE_W4A16 = 0, 1, 2
+MODE_PER_TENSOR, MODE_PER_TOKEN, MODE_W4A16, MODE_MXFP8 = 0, 1, 2, 3
 
 
 @dataclass

@@ -51,6 +51,23 @@ def sf_rowmajor(buf: np.ndarray, rows: Sequence[int], cols: int) -> np.ndarray:
     return buf[off]
 
 
+def sf_rowmajor_mx(buf: np.ndarray, rows: Sequence[int], cols: int) -> np.ndarray:
+    """MXFP8 scales (one per 32) of the given rows, row-major [len(rows),
+    cols/32], from the atom layout [rows/128][cols/128][512]."""
+    r = np.asarray(rows, dtype=np.int64)[:, None]
+    j = np.arange(cols // 32, dtype=np.int64)[None, :]
+    off = ((r >> 7) * (cols >> 7) + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3)
+    return buf[off]
+
+
+def is_mx(layer) -> bool:
+    return (layer.flags & (3 << 2)) == api.MOE_W8A8_MXFP8
+
+
+def is_per_token(layer) -> bool:
+    return (layer.flags & (3 << 2)) == api.MOE_W4A4_PER_TOKEN
+
+
 def nibbles(codes: np.ndarray) -> np.ndarray:
     return np.stack([codes & 15, codes >> 4], axis=-1).reshape(codes.shape[0], -1)
 
@@ -154,15 +171,18 @@ def check_x_quant(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray):
     T, K, H = layer.T, layer.K, layer.H
     lay = layer.layout()
     cap = lay["rows_cap"]
-    codes = layer.view("xq_codes", torch.uint8, cap * H // 2).cpu().numpy().reshape(cap, H // 2)
-    sfbuf = layer.view("xq_sf", torch.uint8, cap * H // 16).cpu().numpy()
+    mx = is_mx(layer)
+    cb = H if mx else H // 2
+    codes = layer.view("xq_codes", torch.uint8, cap * cb).cpu().numpy().reshape(cap, cb)
+    sfbuf = layer.view("xq_sf", torch.uint8, cap * H // (32 if mx else 16)).cpu().numpy()
+    sf_of = sf_rowmajor_mx if mx else sf_rowmajor
     toks = ref.tokens
     for k in range(K):
         rows = ror.reshape(T, K)[toks, k]
         kept = rows >= 0                      # dropped routes (caller-supplied routing) have no row
         assert np.array_equal(codes[rows[kept]], ref.x_codes[kept]), f"x codes differ (slot {k})"
-        assert np.array_equal(sf_rowmajor(sfbuf, rows[kept], H), ref.x_sf[kept]), f"x scales differ (slot {k})"
-    if layer.flags & api.MOE_W4A4_PER_TOKEN:
+        assert np.array_equal(sf_of(sfbuf, rows[kept], H), ref.x_sf[kept]), f"x scales differ (slot {k})"
+    if is_per_token(layer):
         g1 = layer.view("g1", torch.float32, T).cpu().numpy()[toks]
         assert np.array_equal(g1, ref.G1), "per-token G1 differs"
 
@@ -194,15 +214,15 @@ class W2Colmax:
     """Per-expert (max_n |W2q[n, j]| over the oracle's dequantized FC2
     weight, Gw2), from an oracle `prepared` cache or computed on demand."""
 
-    def __init__(self, prepared=None, weights=None):
-        self.prepared, self.weights, self.cache = prepared, weights, {}
+    def __init__(self, prepared=None, weights=None, mx=False):
+        self.prepared, self.weights, self.mx, self.cache = prepared, weights, mx, {}
 
     def __getitem__(self, e):
         if e not in self.cache:
             if self.prepared is not None and e in self.prepared:
                 w2op, gw2 = self.prepared[e][2], self.prepared[e][3]
             else:
-                pm = oracle.prepare_matrix(self.weights(e)[1])
+                pm = (oracle.prepare_matrix_mx if self.mx else oracle.prepare_matrix)(self.weights(e)[1])
                 w2op, gw2 = pm.operand(), float(pm.G)
             self.cache[e] = (np.abs(w2op).max(axis=0), gw2)
         return self.cache[e]
@@ -217,11 +237,13 @@ def check_fc2_input(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray, G2
         prepared = W2Colmax(prepared)
     if (layer.flags & (3 << 2)) == api.MOE_W4A16:
         return _check_fc2_input_bf16(layer, ref, ror, prepared, slack)
+    if is_mx(layer):
+        return _check_fc2_input_mx(layer, ref, ror, prepared, slack)
     I, K = layer.I, layer.K
     cap = layer.layout()["rows_cap"]
     codes = layer.view("hq_codes", torch.uint8, cap * I // 2).cpu().numpy().reshape(cap, I // 2)
     sfbuf = layer.view("hq_sf", torch.uint8, cap * I // 16).cpu().numpy()
-    per_token = bool(layer.flags & api.MOE_W4A4_PER_TOKEN)
+    per_token = is_per_token(layer)
     g2_gpu = layer.view("g2", torch.float32, cap).cpu().numpy() if per_token else None
     routes = sorted(ref.h_codes)
     rows = ror[routes]
@@ -242,6 +264,37 @@ def check_fc2_input(layer: api.MoELayer, ref: oracle.Result, ror: np.ndarray, G2
         sg = np.repeat(_e4m3_values(got_sf[i]), 16)
         sr = np.repeat(_e4m3_values(ref.h_sf[r]), 16)
         d = np.abs(_e2m1_values(got[i]) * sg * g2g - _e2m1_values(want[i]) * sr * g2r)
+        wk = 1.0 if layer.flags & api.MOE_ROUTER_W_ON_INPUT else float(ref.w[t, k])
+        slack[pos[t]] += wk * gw2 * float(np.dot(d, colmax))
+    return frac, slack
+
+
+def _mx_values(codes: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    v = _e4m3_values(codes) * np.where(codes & 0x80, -1.0, 1.0)
+    return v * np.exp2(np.repeat(sf.astype(np.float64) - 127, 32, axis=-1))
+
+
+def _check_fc2_input_mx(layer, ref, ror, prepared, slack):
+    """MXFP8: E4M3 codes >= 99.9 % identical; a token whose FC2 input
+    differs gets the exact worst-case effect of the difference as slack."""
+    I, K = layer.I, layer.K
+    cap = layer.layout()["rows_cap"]
+    codes = layer.view("hq_codes", torch.uint8, cap * I).cpu().numpy().reshape(cap, I)
+    sfbuf = layer.view("hq_sf", torch.uint8, cap * I // 32).cpu().numpy()
+    routes = sorted(ref.h_codes)
+    rows = ror[routes]
+    got = codes[rows]
+    want = np.stack([ref.h_codes[r] for r in routes])
+    frac = float(np.mean(got == want))
+    assert_mostly_identical(got, want, "FC2-input codes")
+    got_sf = sf_rowmajor_mx(sfbuf, rows, I)
+    pos = {int(t): i for i, t in enumerate(ref.tokens)}
+    for i, r in enumerate(routes):
+        if np.array_equal(got[i], want[i]) and np.array_equal(got_sf[i], ref.h_sf[r]):
+            continue
+        t, k = divmod(r, K)
+        colmax, gw2 = prepared[int(ref.ids[t, k])]
+        d = np.abs(_mx_values(got[i], got_sf[i]) - _mx_values(want[i], ref.h_sf[r]))
         wk = 1.0 if layer.flags & api.MOE_ROUTER_W_ON_INPUT else float(ref.w[t, k])
         slack[pos[t]] += wk * gw2 * float(np.dot(d, colmax))
     return frac, slack
@@ -363,19 +416,24 @@ def check_x_quant_all(layer: api.MoELayer, x_np: np.ndarray, G1, ror: np.ndarray
     permuted rows, bit for bit."""
     T, K, H = layer.T, layer.K, layer.H
     x32 = oracle.bf16_bits_to_f64(x_np).astype(np.float32)
-    four_six = bool(layer.flags & api.MOE_QUANT_4OVER6)
-    div = oracle.SCALE_DIV_4OVER6 if four_six else oracle.SCALE_DIV
-    G = oracle.row_global_scale(x32, div) if layer.flags & api.MOE_W4A4_PER_TOKEN else np.float32(G1)
-    codes_ref, sf_ref = oracle.quant_rows(x32, G, four_six)
     cap = layer.layout()["rows_cap"]
-    codes = layer.view("xq_codes", torch.uint8, cap * H // 2).view(cap, H // 2)
-    sfbuf = layer.view("xq_sf", torch.uint8, cap * H // 16).cpu().numpy()
+    if is_mx(layer):
+        codes_ref, sf_ref = oracle.quant_rows_mx(x32)
+        cb, sf_of, per_sf = H, sf_rowmajor_mx, 32
+    else:
+        four_six = bool(layer.flags & api.MOE_QUANT_4OVER6)
+        div = oracle.SCALE_DIV_4OVER6 if four_six else oracle.SCALE_DIV
+        G = oracle.row_global_scale(x32, div) if is_per_token(layer) else np.float32(G1)
+        codes_ref, sf_ref = oracle.quant_rows(x32, G, four_six)
+        cb, sf_of, per_sf = H // 2, sf_rowmajor, 16
+    codes = layer.view("xq_codes", torch.uint8, cap * cb).view(cap, cb)
+    sfbuf = layer.view("xq_sf", torch.uint8, cap * H // per_sf).cpu().numpy()
     rr = ror.reshape(T, K)
     for k in range(K):
         rows = rr[:, k]
         got = codes[torch.as_tensor(rows, device=codes.device, dtype=torch.long)].cpu().numpy()
         assert np.array_equal(got, codes_ref), f"x codes differ (slot {k})"
-        assert np.array_equal(sf_rowmajor(sfbuf, rows, H), sf_ref), f"x scales differ (slot {k})"
+        assert np.array_equal(sf_of(sfbuf, rows, H), sf_ref), f"x scales differ (slot {k})"
 
 
 def fullsize_parity(c: synth.MoEConfig, n_tokens: int):
@@ -410,6 +468,6 @@ def fullsize_parity(c: synth.MoEConfig, n_tokens: int):
     ror = check_routing(layer, ref)
     if c.mode != synth.MODE_W4A16:
         check_x_quant_all(layer, x_np, G1, ror)
-    frac, slack = check_fc2_input(layer, ref, ror, G2, W2Colmax(None, weights))
+    frac, slack = check_fc2_input(layer, ref, ror, G2, W2Colmax(None, weights, mx=is_mx(layer)))
     rel = check_y(y, ref, slack)
     return dict(code_match=frac, y_rel_err=rel, flipped_tokens=int(np.sum(slack > 0)))

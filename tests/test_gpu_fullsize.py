@@ -31,6 +31,12 @@ def test_dsv3_shape_T8192_on_cta_pairs():
     assert r["code_match"] >= 0.999
 
 
+def test_dsv3_shape_T4096_mxfp8():
+    """The DSV3-like shape at T=4096 in MXFP8 W8A8 (E4M3, E8M0 per 32)."""
+    r = fullsize_parity(synth.config(2, 4096).with_(mode=synth.MODE_MXFP8), n_tokens=16)
+    assert r["code_match"] >= 0.999
+
+
 def test_w4a16_T4096():
     """W4A16: T=4096, H=4096, I=1536, E=128, top-8, ReLU2, fused finalize."""
     fullsize_parity(synth.config(3, 4096), n_tokens=24)

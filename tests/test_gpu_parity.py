@@ -181,6 +181,55 @@ def test_mid_config_parity_4over6():
     full_parity(synth.config(1).with_(four_over_six=True))
 
 
+@pytest.mark.parametrize("act", [0, 1])
+def test_prepare_weights_mxfp8_matches_oracle(act):
+    """MXFP8 weights: E4M3 codes and E8M0 scales per 32, bit-exact, in the
+    prepared (gate/up interleaved) row order."""
+    from gpu_parity import sf_rowmajor_mx
+    c = synth.MoEConfig("prepmx", 4, 384, 256, 3, 2, act=act, mode=synth.MODE_MXFP8, seed=19)
+    inp = make_inputs(c)
+    layer = api.MoELayer.create(c.T, c.H, c.I, c.E, c.K, c.flags())
+    layer.prepare(inp.w1, inp.w2)
+    torch.cuda.synchronize()
+    buf = layer.prepared.cpu().numpy()
+    reg = layer.prepared_regions()
+    N1, H, I, E = c.N1, c.H, c.I, c.E
+    assert (buf[reg["gw1"][0]:reg["gw1"][0] + 4 * E].view(np.float32) == 1.0).all()
+    canon = canonical_w1_rows(N1, I, act == 0)
+    for e in range(E):
+        p1 = oracle.prepare_matrix_mx(inp.w1_np[e])
+        p2 = oracle.prepare_matrix_mx(inp.w2_np[e])
+        o = reg["w1_codes"][0] + e * N1 * H
+        assert np.array_equal(buf[o:o + N1 * H].reshape(N1, H), p1.codes[canon])
+        o = reg["w1_sf"][0] + e * N1 * H // 32
+        assert np.array_equal(sf_rowmajor_mx(buf[o:o + N1 * H // 32], np.arange(N1), H), p1.sf[canon])
+        o = reg["w2_codes"][0] + e * H * I
+        assert np.array_equal(buf[o:o + H * I].reshape(H, I), p2.codes)
+        o = reg["w2_sf"][0] + e * H * I // 32
+        assert np.array_equal(sf_rowmajor_mx(buf[o:o + H * I // 32], np.arange(H), I), p2.sf)
+
+
+MXFP8 = [(1, 256, 128, 8, 2, 0, False, False), (7, 384, 256, 8, 2, 1, True, True),
+         (129, 256, 128, 8, 1, 0, True, False), (200, 512, 384, 16, 4, 1, False, False),
+         (40, 4096, 256, 3, 2, 0, False, True), (33, 256, 4096, 4, 3, 1, True, False)]
+
+
+@pytest.mark.parametrize("T,H,I,E,K,act,on_input,det", MXFP8)
+def test_mxfp8_parity(T, H, I, E, K, act, on_input, det):
+    """MXFP8 W8A8 (E4M3, E8M0 per 32) on the same engine: x codes / scales
+    bit-exact, FC2-input codes >= 99.9 %, y within the derived tolerance;
+    includes 256-wide tiles (K = 4096) and partial tiles."""
+    c = synth.MoEConfig("mx", T, H, I, E, K, act=act, mode=synth.MODE_MXFP8, router_on_input=on_input,
+                        deterministic=det, seed=T + I, logits="normal")
+    r = full_parity(c)
+    assert r["code_match"] >= 0.999
+
+
+def test_mid_config_parity_mxfp8():
+    """The mid workload's shapes and routing in MXFP8."""
+    full_parity(synth.config(1).with_(mode=synth.MODE_MXFP8))
+
+
 def test_mid_config_parity_on_pairs():
     """The mid workload with both GEMMs forced onto CTA pairs."""
     full_parity(synth.config(1).with_(gemm_pairs="always"))
