@@ -3,6 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload mid|tiny|dsv3|w4a16|prefill] [--tokens T]
+                    [--precision nvfp4|mxfp8] [--four-over-six] [--routing logits|given]
 
 A step is one full layer forward (router, permutation, activation
 quantization, FC1 + activation + requantization, FC2, finalize) over one
@@ -39,7 +40,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/s and NVFP4 TFLOPS (% of GB300 dense FP4 peak) vs tokens"
 L2_BYTES = 129 * 1024 * 1024
-FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense-rate ratio used to scale the measured bf16 peak
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense-rate ratios used to scale the measured bf16 peak
+FP8_OVER_BF16 = 4.5 / 2.25
 
 
 def parse():
@@ -51,20 +53,37 @@ def parse():
     p.add_argument("--workload", default="mid", choices=["tiny", "mid", "dsv3", "w4a16", "prefill"])
     p.add_argument("--tokens", type=int, default=None, help="token count (sweeps of dsv3 / w4a16)")
     p.add_argument("--stage-steps", type=int, default=200)
+    p.add_argument("--precision", default="nvfp4", choices=["nvfp4", "mxfp8"],
+                   help="mxfp8: the W4A4 workloads' shapes and routing in MXFP8 W8A8")
+    p.add_argument("--four-over-six", action="store_true",
+                   help="4-over-6 activation quantization (per-token W4A4 workloads)")
+    p.add_argument("--routing", default="logits", choices=["logits", "given"],
+                   help="given: caller-supplied top-K ids and weights (moe_nvfp4_forward_routed)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
 
-def workload_config(name, tokens):
+def workload_config(name, tokens, precision="nvfp4", four_over_six=False):
     from nvfp4_mixture_experts_router_gb300 import synth
     idx = {"tiny": 0, "mid": 1, "dsv3": 2, "w4a16": 3, "prefill": 4}[name]
-    return synth.config(idx, tokens)
+    c = synth.config(idx, tokens)
+    if precision == "mxfp8":
+        if c.mode == synth.MODE_W4A16:
+            raise SystemExit("--precision mxfp8 applies to the W4A4 workloads")
+        c = c.with_(mode=synth.MODE_MXFP8)
+    if four_over_six:
+        if c.mode != synth.MODE_PER_TOKEN:
+            raise SystemExit("--four-over-six needs a per-token W4A4 workload (mid, prefill)")
+        c = c.with_(four_over_six=True)
+    return c
 
 
 def describe(c):
     from nvfp4_mixture_experts_router_gb300 import synth
     act = "SwiGLU" if c.act == synth.ACT_SWIGLU else "ReLU2"
-    mode = {0: "W4A4 per-tensor", 1: "W4A4 per-token", 2: "W4A16"}[c.mode]
+    mode = {0: "W4A4 per-tensor", 1: "W4A4 per-token", 2: "W4A16", 3: "W8A8 MXFP8"}[c.mode]
+    if c.four_over_six:
+        mode += " 4-over-6"
     place = "router weight on FC2 input" if c.router_on_input else "router weight at output"
     fin = "deterministic finalize" if c.deterministic else "fused finalize"
     return f"{c.name}: T={c.T}, H={c.H}, I={c.I}, E={c.E}, top-{c.K}, {act}, {mode}, {place}, {fin}"
@@ -89,7 +108,8 @@ def stage_bytes(c, active):
     from nvfp4_mixture_experts_router_gb300 import synth
     T, H, I, E, K, N1 = c.T, c.H, c.I, c.E, c.K, c.N1
     R = T * K
-    nv = 0.5625                                  # NVFP4: 0.5 B code + 1/16 B scale per element
+    mx = c.mode == synth.MODE_MXFP8
+    nv = 1.03125 if mx else 0.5625               # MXFP8: 1 B + 1/32 B; NVFP4: 0.5 B code + 1/16 B scale
     w4a16 = c.mode == synth.MODE_W4A16
     per_token = c.mode == synth.MODE_PER_TOKEN
     a_elem = 2.0 if w4a16 else nv
@@ -214,7 +234,7 @@ class OracleRunner:
         from nvfp4_mixture_experts_router_gb300 import synth
         self.np, self.oracle, self.c = np, oracle, c
         self.layer = oracle.Layer(c.H, c.I, c.E, c.K, act=c.act, mode=c.mode, router_on_input=c.router_on_input,
-                                  renorm=c.renorm)
+                                  renorm=c.renorm, four_over_six=c.four_over_six)
         x = synth.gen_x(c, device)
         self.x_np = x.cpu().view(torch.int16).numpy().view(np.uint16)
         self.logits = synth.gen_logits(c, device, x).cpu().numpy()
@@ -358,9 +378,21 @@ def run_ours(args, c, world, rank, local):
         del tok
     y = torch.empty(c.T, c.H, dtype=torch.bfloat16, device=dev)
     ws = layer.workspace
+    given = args.routing == "given"
+    if given:
+        # caller-supplied routing: the ids and weights of one router pass,
+        # fed to moe_nvfp4_forward_routed every step
+        layer.prepared = preps[0]
+        layer.forward(x, logits, bias, g1, g2)
+        torch.cuda.synchronize()
+        ids = layer.view("topk_ids", torch.int32, c.T * c.K).view(c.T, c.K).clone()
+        wts = layer.view("topk_w", torch.float32, c.T * c.K).view(c.T, c.K).clone()
 
     def step(i, yy=y, xx=x, ll=logits):
-        api.moe_nvfp4_forward(s, flags, xx, ll, bias, g1, g2, preps[i % n_sets], ws, yy)
+        if given:
+            api.moe_nvfp4_forward_routed(s, flags, xx, ids, wts, g1, g2, preps[i % n_sets], ws, yy)
+        else:
+            api.moe_nvfp4_forward(s, flags, xx, ll, bias, g1, g2, preps[i % n_sets], ws, yy)
 
     for i in range(args.warmup):
         step(i)
@@ -410,14 +442,26 @@ def run_ours(args, c, world, rank, local):
     # end to end: host x/logits -> device, forward, y -> host, every step
     n_host = 2
     hx = [x.cpu().pin_memory() for _ in range(n_host)]
+    # the routing input of a step: logits, or the given ids and weights
+    # (copied straight into the tensors step() reads)
     hl = [logits.cpu().pin_memory() for _ in range(n_host)]
+    if given:
+        h_ids = [ids.cpu().pin_memory() for _ in range(n_host)]
+        h_wts = [wts.cpu().pin_memory() for _ in range(n_host)]
     hy = [torch.empty(c.T, c.H, dtype=torch.bfloat16).pin_memory() for _ in range(n_host)]
     dx = torch.empty_like(x)
     dl = torch.empty_like(logits)
+
+    def copy_routing(i):
+        if given:
+            ids.copy_(h_ids[i % n_host], non_blocking=True)
+            wts.copy_(h_wts[i % n_host], non_blocking=True)
+        else:
+            dl.copy_(hl[i % n_host], non_blocking=True)
     e2e_steps = args.steps
     for i in range(min(args.warmup, 5)):
         dx.copy_(hx[i % n_host], non_blocking=True)
-        dl.copy_(hl[i % n_host], non_blocking=True)
+        copy_routing(i)
         step(i, y, dx, dl)
         hy[i % n_host].copy_(y, non_blocking=True)
     torch.cuda.synchronize()
@@ -427,7 +471,7 @@ def run_ours(args, c, world, rank, local):
     e0.record()
     for i in range(e2e_steps):
         dx.copy_(hx[i % n_host], non_blocking=True)
-        dl.copy_(hl[i % n_host], non_blocking=True)
+        copy_routing(i)
         step(i, y, dx, dl)
         hy[i % n_host].copy_(y, non_blocking=True)
     e1.record()
@@ -438,7 +482,7 @@ def run_ours(args, c, world, rank, local):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
     e2e_value = world * c.T * e2e_steps / (e2e_ms / 1000.0)
-    h2d = c.T * c.H * 2 + c.T * c.E * 4
+    h2d = c.T * c.H * 2 + (c.T * c.K * 8 if given else c.T * c.E * 4)
     d2h = c.T * c.H * 2
 
     if rank != 0:
@@ -447,7 +491,9 @@ def run_ours(args, c, world, rank, local):
         return
 
     hbm, bf16, bf16s, peak_src = measured_peaks()
-    fp4_peak = bf16 * FP4_OVER_BF16
+    mx = c.mode == synth.MODE_MXFP8
+    ratio = FP8_OVER_BF16 if mx else FP4_OVER_BF16
+    fp4_peak = bf16 * ratio           # the dense peak of the GEMMs' input type (FP8 for MXFP8)
     flops = flops_per_step(c)
     dom = max(stage_ms, key=lambda k: stage_ms[k])
     dom_ms = stage_ms[dom]
@@ -472,7 +518,7 @@ def run_ours(args, c, world, rank, local):
                 "frac": round(achieved / fp4_peak, 4), "traffic": traffic_for(dom, args.workload),
                 "kernel": dom, "algorithmic_flops_per_launch": gemm_flops,
                 "mean_launch_us": round(dom_ms * 1000, 2),
-                "peak_source": f"{peak_src} bf16_tflops x {FP4_OVER_BF16:g} (nominal fp4/bf16 ratio)"}
+                "peak_source": f"{peak_src} bf16_tflops x {ratio:g} (nominal {'fp8' if mx else 'fp4'}/bf16 ratio)"}
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -486,7 +532,8 @@ def run_ours(args, c, world, rank, local):
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3/16) -> f32",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp8 (e4m3 x e8m0/32) -> f32" if mx else "nvfp4 (e2m1 x e4m3/16) -> f32",
         "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": describe(c), "T": c.T, "H": c.H, "I": c.I, "E": c.E, "K": c.K,
                    "l2": f"inputs larger than L2: {n_sets} prepared-weight copies "
@@ -494,6 +541,7 @@ def run_ours(args, c, world, rank, local):
                    "parallelism": f"replicas x{world}"},
         "tflops": round(tflops, 2), "pct_fp4_peak": round(100 * tflops / fp4_peak, 3),
         "fp4_peak_tflops": round(fp4_peak, 1),
+        "routing": args.routing + ("" if not given else " (stage times from the logits path)"),
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": api.moe_nvfp4_forward_launches(s, flags) * args.steps,
@@ -512,7 +560,7 @@ def run_ours(args, c, world, rank, local):
 def main():
     args = parse()
     world, rank, local = init_dist(args)
-    c = workload_config(args.workload, args.tokens)
+    c = workload_config(args.workload, args.tokens, args.precision, args.four_over_six)
     if args.impl == "reference":
         run_reference(args, c, world, rank)
     else:

@@ -68,7 +68,10 @@ __device__ __forceinline__ void zero_row_f32(float* p, int n, int lane) {
 // single read of the row; per-token mode reduces the row amax in the CTA and
 // derives G1 = amax/2688).  Also hands out the token's permuted rows (step 3
 // of the permutation) and zeroes its row of the fused-finalize accumulator.
-template <int kMaxPer>   // 16-element blocks per thread (rows up to kMaxPer * 16K elements)
+// kMaxPer: 16-element blocks per thread (rows up to kMaxPer * 16K elements);
+// kFourSix: 4-over-6 blocks (a compile-time choice, so that the default
+// kernels carry none of its code)
+template <int kMaxPer, bool kFourSix>
 __global__ void __launch_bounds__(1024) quantize_x_kernel(int T, int H, int K, const __nv_bfloat16* __restrict__ x,
                                                           const float* __restrict__ g1_in, int per_token,
                                                           float* __restrict__ g1_out, const RouteScatter rs,
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(1024) quantize_x_kernel(int T, int H, int K, c
         if (warp == 0) {
             float m = lane < (int)(blockDim.x >> 5) ? s_red[lane] : 0.0f;
             m = warp_max(m);
-            if (lane == 0) s_red[0] = per_token == 2 ? global_scale_from_amax_4over6(m) : global_scale_from_amax(m);
+            if (lane == 0) s_red[0] = kFourSix ? global_scale_from_amax_4over6(m) : global_scale_from_amax(m);
         }
         __syncthreads();
         G = s_red[0];
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(1024) quantize_x_kernel(int T, int H, int K, c
         const bool active = b < nblk;
         uint32_t q[2] = {0u, 0u};
         uint32_t s = 0;
-        if (active) s = per_token == 2 ? quant_block16_4over6(v[i], G, q) : quant_block16(v[i], G, q);
+        if (active) s = kFourSix ? quant_block16_4over6(v[i], G, q) : quant_block16(v[i], G, q);
         const uint32_t word = pack_sf4(s);
         if (active) {
             for (int k = 0; k < K; ++k) {
@@ -221,12 +224,11 @@ __global__ void __launch_bounds__(256) gather_x_bf16_kernel(int T, int H, int K,
 // Per-token W4A4: FC2 input row (FP32) -> G2 = amax/2688, NVFP4 codes/scales.
 // One CTA per row at a time (grid-stride over the padded rows, pad rows
 // skipped), one thread per 16-element block.
-template <int kMaxPer>
+template <int kMaxPer, bool kFourSix>
 __global__ void __launch_bounds__(1024) quantize_h_kernel(int I, const int* __restrict__ meta,
                                                           const int* __restrict__ route_of_row,
                                                           const float* __restrict__ h, float* __restrict__ g2,
-                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-                                                          int four_six) {
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
     __shared__ float s_red[32];
     pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(1024) quantize_h_kernel(int I, const int* __re
     if (warp == 0) {
         float m = lane < (int)(blockDim.x >> 5) ? s_red[lane] : 0.0f;
         m = warp_max(m);
-        if (lane == 0) s_red[0] = four_six ? global_scale_from_amax_4over6(m) : global_scale_from_amax(m);
+        if (lane == 0) s_red[0] = kFourSix ? global_scale_from_amax_4over6(m) : global_scale_from_amax(m);
     }
     __syncthreads();
     const float G = s_red[0];
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(1024) quantize_h_kernel(int I, const int* __re
         const bool active = b < nblk;
         uint32_t q[2] = {0u, 0u};
         uint32_t s = 0;
-        if (active) s = four_six ? quant_block16_4over6(v[i], G, q) : quant_block16(v[i], G, q);
+        if (active) s = kFourSix ? quant_block16_4over6(v[i], G, q) : quant_block16(v[i], G, q);
         const uint32_t word = pack_sf4(s);
         if (active) {
             *reinterpret_cast<uint2*>(codes + (size_t)row * (I / 2) + 8 * b) = make_uint2(q[0], q[1]);
@@ -487,9 +489,12 @@ cudaError_t launch_quantize_x(const LaunchCtx& c, int T, int H, int K, const voi
     const int per = (H / 16 + 1023) / 1024;
     const dim3 grid(T), block(row_threads(H));
     const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
-    if (per <= 1) return c.launch(quantize_x_kernel<1>, grid, block, 0, T, H, K, xb, g1_in, per_token, g1_out, rs, codes, sf, y_acc_zero);
-    if (per <= 2) return c.launch(quantize_x_kernel<2>, grid, block, 0, T, H, K, xb, g1_in, per_token, g1_out, rs, codes, sf, y_acc_zero);
-    return c.launch(quantize_x_kernel<4>, grid, block, 0, T, H, K, xb, g1_in, per_token, g1_out, rs, codes, sf, y_acc_zero);
+    // per_token 2 = per-token with 4-over-6 blocks
+#define MOE_QX(P, F) \
+    c.launch(quantize_x_kernel<P, F>, grid, block, 0, T, H, K, xb, g1_in, per_token, g1_out, rs, codes, sf, y_acc_zero)
+    if (per_token == 2) return per <= 1 ? MOE_QX(1, true) : per <= 2 ? MOE_QX(2, true) : MOE_QX(4, true);
+    return per <= 1 ? MOE_QX(1, false) : per <= 2 ? MOE_QX(2, false) : MOE_QX(4, false);
+#undef MOE_QX
 }
 
 cudaError_t launch_gather_x_bf16(const LaunchCtx& c, int T, int H, int K, const void* x, const RouteScatter& rs,
@@ -506,11 +511,10 @@ cudaError_t launch_quantize_h(const LaunchCtx& c, uint64_t rows_cap, int I, cons
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const uint64_t want = (uint64_t)sms * (2048 / row_threads(I));   // enough CTAs to fill every SM
     const dim3 grid((unsigned)(rows_cap < want ? rows_cap : want)), block(row_threads(I));
-    if (per <= 1)
-        return c.launch(quantize_h_kernel<1>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf, four_six);
-    if (per <= 2)
-        return c.launch(quantize_h_kernel<2>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf, four_six);
-    return c.launch(quantize_h_kernel<4>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf, four_six);
+#define MOE_QH(P, F) c.launch(quantize_h_kernel<P, F>, grid, block, 0, I, meta, route_of_row, h, g2, codes, sf)
+    if (four_six) return per <= 1 ? MOE_QH(1, true) : per <= 2 ? MOE_QH(2, true) : MOE_QH(4, true);
+    return per <= 1 ? MOE_QH(1, false) : per <= 2 ? MOE_QH(2, false) : MOE_QH(4, false);
+#undef MOE_QH
 }
 
 cudaError_t launch_finalize_deterministic(const LaunchCtx& c, int T, int H, int K, const int* row_of_route,
