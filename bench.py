@@ -142,6 +142,17 @@ def traffic_for(kernel, workload):
     return e.get("dram_bytes_per_launch")
 
 
+def traffic_key(args):
+    """Workload key of profiles/traffic.json (precision and quantization
+    variants have their own entries)."""
+    key = args.workload
+    if args.precision != "nvfp4":
+        key += "-" + args.precision
+    if args.four_over_six:
+        key += "-4over6"
+    return key
+
+
 def source_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_mixture_experts_router_gb300", "csrc")
@@ -509,13 +520,13 @@ def run_ours(args, c, world, rank, local):
     if bound == "hbm":
         achieved = sbytes[dom] / (dom_ms / 1000.0) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": traffic_for(dom, args.workload),
+                "frac": round(achieved / hbm, 4), "traffic": traffic_for(dom, traffic_key(args)),
                 "kernel": dom, "algorithmic_bytes_per_launch": int(sbytes[dom]),
                 "mean_launch_us": round(dom_ms * 1000, 2), "peak_source": f"{peak_src} hbm_gbs"}
     else:
         achieved = gemm_flops / (dom_ms / 1000.0) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / fp4_peak, 4), "traffic": traffic_for(dom, args.workload),
+                "frac": round(achieved / fp4_peak, 4), "traffic": traffic_for(dom, traffic_key(args)),
                 "kernel": dom, "algorithmic_flops_per_launch": gemm_flops,
                 "mean_launch_us": round(dom_ms * 1000, 2),
                 "peak_source": f"{peak_src} bf16_tflops x {ratio:g} (nominal {'fp8' if mx else 'fp4'}/bf16 ratio)"}
