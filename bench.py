@@ -4,6 +4,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload mid|tiny|dsv3|w4a16|prefill] [--tokens T]
                     [--precision nvfp4|mxfp8] [--four-over-six] [--routing logits|given]
+                    [--fused]
 
 A step is one full layer forward (router, permutation, activation
 quantization, FC1 + activation + requantization, FC2, finalize) over one
@@ -59,11 +60,13 @@ def parse():
                    help="4-over-6 activation quantization (per-token W4A4 workloads)")
     p.add_argument("--routing", default="logits", choices=["logits", "given"],
                    help="given: caller-supplied top-K ids and weights (moe_nvfp4_forward_routed)")
+    p.add_argument("--fused", action="store_true",
+                   help="the whole forward as one persistent kernel (MOE_FUSED_LAYER; W4A4, E <= 256)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
 
-def workload_config(name, tokens, precision="nvfp4", four_over_six=False):
+def workload_config(name, tokens, precision="nvfp4", four_over_six=False, fused=False):
     from nvfp4_mixture_experts_router_gb300 import synth
     idx = {"tiny": 0, "mid": 1, "dsv3": 2, "w4a16": 3, "prefill": 4}[name]
     c = synth.config(idx, tokens)
@@ -75,6 +78,10 @@ def workload_config(name, tokens, precision="nvfp4", four_over_six=False):
         if c.mode != synth.MODE_PER_TOKEN:
             raise SystemExit("--four-over-six needs a per-token W4A4 workload (mid, prefill)")
         c = c.with_(four_over_six=True)
+    if fused:
+        if c.mode not in (synth.MODE_PER_TENSOR, synth.MODE_PER_TOKEN) or c.E > 256:
+            raise SystemExit("--fused needs a W4A4 workload with E <= 256")
+        c = c.with_(fused=True)
     return c
 
 
@@ -84,6 +91,8 @@ def describe(c):
     mode = {0: "W4A4 per-tensor", 1: "W4A4 per-token", 2: "W4A16", 3: "W8A8 MXFP8"}[c.mode]
     if c.four_over_six:
         mode += " 4-over-6"
+    if c.fused:
+        mode += ", one persistent kernel"
     place = "router weight on FC2 input" if c.router_on_input else "router weight at output"
     fin = "deterministic finalize" if c.deterministic else "fused finalize"
     return f"{c.name}: T={c.T}, H={c.H}, I={c.I}, E={c.E}, top-{c.K}, {act}, {mode}, {place}, {fin}"
@@ -150,6 +159,8 @@ def traffic_key(args):
         key += "-" + args.precision
     if args.four_over_six:
         key += "-4over6"
+    if args.fused:
+        key += "-fused"
     return key
 
 
@@ -449,6 +460,14 @@ def run_ours(args, c, world, rank, local):
     count = layer.view("count", torch.int32, c.E).cpu()
     active = int((count > 0).sum())
     sbytes = stage_bytes(c, active)
+    if c.fused:
+        # one kernel: its time is the forward's, its algorithmic bytes the
+        # layer's irreducible traffic (routing input, x, the active experts'
+        # weights, y); the intermediates may stay in L2
+        stage_ms = {"fused_layer": sum(stage_ms.values())}
+        nv = 0.5625
+        sbytes = {"fused_layer": sbytes["router"] + c.T * c.H * 2 + active * (c.N1 * c.H + c.H * c.I) * nv +
+                  c.T * c.H * 2}
 
     # end to end: host x/logits -> device, forward, y -> host, every step
     n_host = 2
@@ -571,7 +590,7 @@ def run_ours(args, c, world, rank, local):
 def main():
     args = parse()
     world, rank, local = init_dist(args)
-    c = workload_config(args.workload, args.tokens, args.precision, args.four_over_six)
+    c = workload_config(args.workload, args.tokens, args.precision, args.four_over_six, args.fused)
     if args.impl == "reference":
         run_reference(args, c, world, rank)
     else:

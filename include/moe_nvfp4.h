@@ -102,7 +102,20 @@ typedef enum {
  * scales become amax/1536 (6 * 256).  The decode, and so the GEMMs, are
  * unchanged. */
 #define MOE_QUANT_4OVER6 (1u << 9)
-#define MOE_FLAGS_KNOWN 0x3FFu
+/* bit 10: the whole forward as one persistent kernel (one CTA per SM,
+ * cooperative launch) [MegaMoE, "Our approach": a single persistent kernel
+ * per forward pass runs the quantization, the grouped GEMMs and the
+ * combine]: routing, permutation, x quantization, FC1, the FC2-input
+ * quantization, FC2 and the finalize run as phases separated by grid-wide
+ * barriers, with the same arithmetic as the default launch sequence (same
+ * bits, up to the order of the fused finalize's FP32 additions).  Meant for
+ * small T, where launch and ramp-up latency dominate.  W4A4 modes only
+ * (per-tensor or per-token, optionally 4-over-6), E <= 256, 128-wide GEMM
+ * tiles; invalid with MOE_GEMM_PAIRS_ALWAYS.  Needs every SM free for one
+ * resident CTA (otherwise the launch fails: MOE_ERR_CUDA).  The staged entry
+ * point records all eight events around the one kernel. */
+#define MOE_FUSED_LAYER (1u << 10)
+#define MOE_FLAGS_KNOWN 0x7FFu
 
 /* ---- shapes ---------------------------------------------------------------- */
 typedef struct {
@@ -238,7 +251,8 @@ MOE_API int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags);
  * rows_cap = the padded-row capacity (a multiple of 128).               */
 typedef struct {
     uint64_t rows_cap;       /* padded-row capacity                          */
-    uint64_t status;         /* uint32[4]: [0] error bits of the last run    */
+    uint64_t status;         /* uint32[4]: [0] error bits of the last run,   */
+                             /*   [1] grid-barrier counter (fused layer)     */
     uint64_t topk_ids;       /* int32 [T][K]                                 */
     uint64_t topk_w;         /* f32   [T][K]                                 */
     uint64_t count;          /* int32 [E]   routes per expert                */
@@ -276,7 +290,8 @@ MOE_API moe_status moe_nvfp4_workspace_layout(moe_shape s, uint32_t flags,
 
 /* Debug: wait for `stream`, then read and clear the device status word that
  * the most recent forward on `workspace` left (each forward clears it first).
- * Returns MOE_OK; MOE_ERR_TIMEOUT if a kernel's bounded wait (1 s) gave up;
+ * Returns MOE_OK; MOE_ERR_TIMEOUT if a kernel's bounded wait (1 s) gave up
+ * (for the fused layer also a grid barrier, or a CTA that stopped early);
  * MOE_ERR_INVALID_ARG if a kernel met an out-of-range expert id; or
  * MOE_ERR_CUDA.  Synchronizes `stream`. */
 MOE_API moe_status moe_nvfp4_last_device_status(void* workspace, void* stream);

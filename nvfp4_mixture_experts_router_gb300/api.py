@@ -33,6 +33,7 @@ MOE_ROUTE_NO_RENORM = 1 << 6
 MOE_GEMM_PAIRS_NEVER = 1 << 7
 MOE_GEMM_PAIRS_ALWAYS = 1 << 8
 MOE_QUANT_4OVER6 = 1 << 9
+MOE_FUSED_LAYER = 1 << 10
 MOE_W8A8_MXFP8 = 3 << 2
 
 

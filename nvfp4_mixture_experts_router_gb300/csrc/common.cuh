@@ -20,6 +20,8 @@ constexpr uint32_t kStatusTimeoutMma = 1u << 1;
 constexpr uint32_t kStatusTimeoutEpilogue = 1u << 2;
 constexpr uint32_t kStatusBadExpert = 1u << 3;
 constexpr uint32_t kStatusBadRow = 1u << 4;
+constexpr uint32_t kStatusTimeoutGrid = 1u << 5;   // fused layer: a grid barrier gave up
+constexpr uint32_t kStatusGridAbort = 1u << 6;     // fused layer: a CTA stopped early
 
 // One bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;

@@ -153,4 +153,55 @@ cudaError_t setup_gemm_pair_kernels(int device, int num_sms);
 cudaError_t launch_gemm_nvf4_pair(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   const GemmParams& p, int device);
 
+// fused_layer.cu — the whole W4A4 forward as one cooperative persistent
+// kernel (one CTA per SM); E <= kFusedMaxExperts.
+constexpr int kFusedMaxExperts = 256;
+struct FusedParams {
+    int T, H, I, E, K;
+    // routing input: router logits (+ bias) or, when ids_in is set, given ids / weights
+    const float* logits;
+    const float* bias;
+    int renorm;
+    const int* ids_in;
+    const float* w_in;
+    // routing and permutation (workspace)
+    int* ids;
+    float* topk_w;
+    int* unit_base;
+    uint32_t* unit_mask;
+    int* count;
+    int* offsets;
+    int* padded_offsets;
+    int* meta;
+    int* tile_expert;
+    int* tile_pair;
+    int* row_of_route;
+    int* route_of_row;
+    // activations
+    const __nv_bfloat16* x;
+    int per_token;               // per-token G1 / G2 (else the caller's per-tensor scales)
+    const float* g1_in;          // per-tensor: the caller's FC1 input scale
+    float* g1;                   // per-token: [T]
+    uint8_t* xq_codes;
+    uint8_t* xq_sf;
+    float* h_f32;                // per-token: FC1 output before quantization
+    float* g2;                   // per-token: [rows_cap]
+    uint8_t* hq_codes;
+    uint8_t* hq_sf;
+    // output
+    int det;                     // deterministic finalize (FC2 stores BF16 rows)
+    int weight_on_output;
+    float* y_acc;                // fused finalize: [T][H] FP32
+    const __nv_bfloat16* o_bf16; // deterministic finalize: [rows_cap][H]
+    __nv_bfloat16* y;
+    GemmParams fc1, fc2;         // the two GEMMs (128-wide tiles)
+    unsigned int* status;        // status word (zeroed before the launch)
+    unsigned int* sync;          // grid-barrier counter (zeroed before the launch)
+};
+cudaError_t setup_fused_layer_kernel();
+// cooperative launch of num_sms CTAs; four_six: 4-over-6 blocks (per-token mode)
+cudaError_t launch_fused_layer(cudaStream_t stream, int num_sms, const CUtensorMap& tmA1, const CUtensorMap& tmB1,
+                               const CUtensorMap& tmA2, const CUtensorMap& tmB2, const FusedParams& fp,
+                               bool four_six);
+
 }  // namespace moe

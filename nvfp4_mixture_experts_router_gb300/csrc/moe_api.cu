@@ -42,7 +42,8 @@ moe_status device_state(int* sms, int* device = nullptr) {
         } else if (major != 10 || minor != 3) {
             d.status = MOE_ERR_UNSUPPORTED;  // the binary carries sm_103a code only
         } else if (setup_routing_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess ||
-                   setup_gemm_w4a16_kernels() != cudaSuccess || setup_gemm_pair_kernels(dev, d.sms) != cudaSuccess) {
+                   setup_gemm_w4a16_kernels() != cudaSuccess || setup_gemm_pair_kernels(dev, d.sms) != cudaSuccess ||
+                   setup_fused_layer_kernel() != cudaSuccess) {
             d.status = MOE_ERR_CUDA;
         } else {
             d.status = MOE_OK;
@@ -75,6 +76,13 @@ moe_status validate_shape(moe_shape s, uint32_t flags) {
     if (flags & ~MOE_FLAGS_KNOWN) return MOE_ERR_INVALID_ARG;
     if ((flags & MOE_GEMM_PAIRS_NEVER) && (flags & MOE_GEMM_PAIRS_ALWAYS)) return MOE_ERR_INVALID_ARG;
     if ((flags & MOE_QUANT_4OVER6) && mode_of(flags) != kModePerToken) return MOE_ERR_INVALID_ARG;
+    if (flags & MOE_FUSED_LAYER) {
+        // one persistent kernel: the NVFP4 activation modes, the router's
+        // register layout (E <= 256) and single-CTA GEMM tiles
+        const int m = mode_of(flags);
+        if ((m != kModePerTensor && m != kModePerToken) || s.E > kFusedMaxExperts || (flags & MOE_GEMM_PAIRS_ALWAYS))
+            return MOE_ERR_INVALID_ARG;
+    }
     if (act_of(flags) > 1) return MOE_ERR_INVALID_ARG;
     if (s.T < 1 || s.T > (1 << 22)) return MOE_ERR_INVALID_ARG;
     if (s.H < 128 || s.H % 128 != 0 || s.H > 65536) return MOE_ERR_INVALID_ARG;
@@ -182,6 +190,132 @@ struct RoutingIn {
     const float* w = nullptr;
 };
 
+// MOE_FUSED_LAYER: every step in one cooperative persistent launch.  The
+// operands and GemmParams are the default path's with 128-wide tiles.
+static moe_status forward_fused(moe_shape s, uint32_t flags, const void* x_bf16, const RoutingIn& rin,
+                                const float* act_scale_fc1, const float* act_scale_fc2, const PreparedLayout& P,
+                                const uint8_t* pw, const moe_workspace_layout& W, uint8_t* ws, void* y_bf16,
+                                int sms, cudaStream_t stream, void* const* events) {
+    auto wsp = [&](uint64_t off) { return ws + off; };
+    const bool per_token = mode_of(flags) == kModePerToken;
+    const bool det = (flags & MOE_FINALIZE_DETERMINISTIC) != 0;
+    const bool on_input = (flags & MOE_ROUTER_W_ON_INPUT) != 0;
+    const int N1 = n1_of(s.I, flags);
+    FusedParams f{};
+    f.T = s.T; f.H = s.H; f.I = s.I; f.E = s.E; f.K = s.K;
+    f.logits = rin.logits;
+    f.bias = rin.bias;
+    f.renorm = (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1;
+    f.ids_in = rin.ids;
+    f.w_in = rin.w;
+    f.ids = reinterpret_cast<int*>(wsp(W.topk_ids));
+    f.topk_w = reinterpret_cast<float*>(wsp(W.topk_w));
+    f.unit_base = reinterpret_cast<int*>(wsp(W.unit_base));
+    f.unit_mask = reinterpret_cast<uint32_t*>(wsp(W.unit_mask));
+    f.count = reinterpret_cast<int*>(wsp(W.count));
+    f.offsets = reinterpret_cast<int*>(wsp(W.offsets));
+    f.padded_offsets = reinterpret_cast<int*>(wsp(W.padded_offsets));
+    f.meta = reinterpret_cast<int*>(wsp(W.meta));
+    f.tile_expert = reinterpret_cast<int*>(wsp(W.tile_expert));
+    f.tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
+    f.row_of_route = reinterpret_cast<int*>(wsp(W.row_of_route));
+    f.route_of_row = reinterpret_cast<int*>(wsp(W.route_of_row));
+    f.x = static_cast<const __nv_bfloat16*>(x_bf16);
+    f.per_token = per_token ? 1 : 0;
+    f.g1_in = act_scale_fc1;
+    f.g1 = reinterpret_cast<float*>(wsp(W.g1));
+    f.xq_codes = wsp(W.xq_codes);
+    f.xq_sf = wsp(W.xq_sf);
+    f.h_f32 = per_token ? reinterpret_cast<float*>(wsp(W.h_f32)) : nullptr;
+    f.g2 = per_token ? reinterpret_cast<float*>(wsp(W.g2)) : nullptr;
+    f.hq_codes = wsp(W.hq_codes);
+    f.hq_sf = wsp(W.hq_sf);
+    f.det = det ? 1 : 0;
+    f.weight_on_output = on_input ? 0 : 1;
+    f.y_acc = det ? nullptr : reinterpret_cast<float*>(wsp(W.y_acc));
+    f.o_bf16 = det ? reinterpret_cast<const __nv_bfloat16*>(wsp(W.o_bf16)) : nullptr;
+    f.y = static_cast<__nv_bfloat16*>(y_bf16);
+    unsigned int* status = reinterpret_cast<unsigned int*>(wsp(W.status));
+    f.status = status;
+    f.sync = status + 1;
+
+    const uint64_t rbx = (uint64_t)s.H / 2, rbh = (uint64_t)s.I / 2;
+    const bool ch1 = rbx % 128 == 0, ch2 = rbh % 128 == 0;
+    CUtensorMap tmA1, tmB1, tmA2, tmB2;
+    const bool ok1 = ch1 ? (encode_chunk_map(&tmA1, f.xq_codes, W.rows_cap, rbx, 128) &&
+                            encode_chunk_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, rbx, 128))
+                         : (encode_operand_map(&tmA1, f.xq_codes, W.rows_cap, rbx) &&
+                            encode_operand_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, rbx));
+    const bool ok2 = ch2 ? (encode_chunk_map(&tmA2, f.hq_codes, W.rows_cap, rbh, 128) &&
+                            encode_chunk_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, rbh, 128))
+                         : (encode_operand_map(&tmA2, f.hq_codes, W.rows_cap, rbh) &&
+                            encode_operand_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, rbh));
+    if (!ok1 || !ok2) return MOE_ERR_CUDA;
+
+    GemmParams& a = f.fc1;
+    a.sfa = f.xq_sf;
+    a.sfb = pw + P.w1_sf;
+    a.kdim = s.H;
+    a.chunk_maps = ch1 ? 1 : 0;
+    a.n = N1;
+    a.meta = f.meta;
+    a.tile_expert = f.tile_expert;
+    a.tile_pair = f.tile_pair;
+    a.route_of_row = f.route_of_row;
+    a.num_experts = s.E;
+    a.status = status;
+    a.act = act_of(flags);
+    a.topk = s.K;
+    a.gw = reinterpret_cast<const float*>(pw + P.gw1);
+    a.topk_w = f.topk_w;
+    a.weight_on_input = on_input ? 1 : 0;
+    a.out_cols = s.I;
+    if (per_token) {
+        a.g_act = f.g1;
+        a.g_act_per_token = 1;
+        a.out_f32 = f.h_f32;
+    } else {
+        a.g_act = act_scale_fc1;
+        a.g2 = act_scale_fc2;
+        a.out_codes = f.hq_codes;
+        a.out_sf = f.hq_sf;
+    }
+    GemmParams& b = f.fc2;
+    b.sfa = f.hq_sf;
+    b.sfb = pw + P.w2_sf;
+    b.kdim = s.I;
+    b.chunk_maps = ch2 ? 1 : 0;
+    b.n = s.H;
+    b.meta = f.meta;
+    b.tile_expert = f.tile_expert;
+    b.tile_pair = f.tile_pair;
+    b.route_of_row = f.route_of_row;
+    b.num_experts = s.E;
+    b.status = status;
+    b.act = act_of(flags);
+    b.topk = s.K;
+    b.gw = reinterpret_cast<const float*>(pw + P.gw2);
+    b.topk_w = f.topk_w;
+    b.weight_on_output = on_input ? 0 : 1;
+    b.out_cols = s.H;
+    b.g_act = per_token ? f.g2 : act_scale_fc2;
+    b.g_act_per_token = per_token ? 2 : 0;
+    if (det) b.out_bf16 = reinterpret_cast<__nv_bfloat16*>(wsp(W.o_bf16));
+    else b.out_f32 = f.y_acc;
+
+    auto mark = [&](int i) -> bool {
+        return events == nullptr || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess;
+    };
+    if (!mark(0)) return MOE_ERR_CUDA;
+    // status word and grid-barrier counter start at zero
+    if (cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_fused_layer(stream, sms, tmA1, tmB1, tmA2, tmB2, f, (flags & MOE_QUANT_4OVER6) != 0) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    for (int i = 1; i < MOE_NUM_STAGE_EVENTS; ++i)
+        if (!mark(i)) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
 static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, const RoutingIn& rin,
                                const float* act_scale_fc1, const float* act_scale_fc2, const void* prepared,
                                void* workspace, size_t workspace_bytes, void* y_bf16, void* stream,
@@ -238,6 +372,10 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     const int act = act_of(flags);
     const int N1 = n1_of(s.I, flags);
     float* y_acc = det ? nullptr : reinterpret_cast<float*>(wsp(W.y_acc));
+
+    if (flags & MOE_FUSED_LAYER)
+        return forward_fused(s, flags, x_bf16, rin, act_scale_fc1, act_scale_fc2, P, pw, W, ws, y_bf16, sms,
+                             static_cast<cudaStream_t>(stream), events);
 
     LaunchCtx c;
     c.stream = static_cast<cudaStream_t>(stream);
@@ -514,6 +652,7 @@ moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags, const void* x_b
 
 int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return -1;
+    if (flags & MOE_FUSED_LAYER) return 1;
     // router + unit counts, scan, quantize or gather (+ row scatter), FC1, [FC2-input quant], FC2, finalize
     return 6 + (mode_of(flags) == kModePerToken ? 1 : 0);
 }
@@ -525,8 +664,9 @@ moe_status moe_nvfp4_last_device_status(void* workspace, void* stream) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return MOE_ERR_CUDA;
-    if (word & (kStatusTimeoutProducer | kStatusTimeoutMma | kStatusTimeoutEpilogue)) return MOE_ERR_TIMEOUT;
+    if (word & (kStatusTimeoutProducer | kStatusTimeoutMma | kStatusTimeoutEpilogue | kStatusTimeoutGrid)) return MOE_ERR_TIMEOUT;
     if (word & (kStatusBadExpert | kStatusBadRow)) return MOE_ERR_INVALID_ARG;
+    if (word & kStatusGridAbort) return MOE_ERR_TIMEOUT;   // raised only together with a reason above
     return MOE_OK;
 }
 

@@ -132,6 +132,7 @@ class MoEConfig:
     w_std: float = 0.02
     gemm_pairs: str = "auto"      # GEMM tile scheduling: "auto" | "never" | "always"
     four_over_six: bool = False   # per-token W4A4: 4-over-6 activation quantization
+    fused: bool = False           # W4A4: the whole forward as one persistent kernel
     extra: dict = field(default_factory=dict)
 
     @property
@@ -152,6 +153,8 @@ class MoEConfig:
             f |= 1 << 8
         if self.four_over_six:
             f |= 1 << 9
+        if self.fused:
+            f |= 1 << 10
         return f
 
     def with_(self, **kw) -> "MoEConfig":

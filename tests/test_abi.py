@@ -78,7 +78,16 @@ def test_invalid_arguments_rejected_before_cuda(L):
     W = ctypes.c_void_p(1 << 36)
     f = L.moe_nvfp4_forward
     # unknown flag bits, bad mode, bad activation
-    assert f(s, 1 << 10, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert f(s, 1 << 11, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    # the single-kernel layer: NVFP4 activation modes, E <= 256, single-CTA tiles
+    fu = api.MOE_FUSED_LAYER
+    assert f(s, fu | api.MOE_W4A16, A, B, None, None, None, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert f(s, fu | api.MOE_W8A8_MXFP8, A, B, None, None, None, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert f(s, fu | api.MOE_GEMM_PAIRS_ALWAYS, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    big = api.shape(16, 256, 128, 257, 2)
+    assert api.moe_nvfp4_workspace_bytes(big, fu) == 0 and api.moe_nvfp4_workspace_bytes(big, 0) > 0
+    assert api.moe_nvfp4_forward_launches(s, fu) == 1
+    assert api.moe_nvfp4_forward_launches(s, fu | api.MOE_W4A4_PER_TOKEN | api.MOE_QUANT_4OVER6) == 1
     # 4-over-6 quantization only with per-token W4A4
     assert f(s, api.MOE_QUANT_4OVER6, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, api.MOE_QUANT_4OVER6 | api.MOE_W4A16, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG

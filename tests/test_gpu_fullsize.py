@@ -59,3 +59,19 @@ def test_prefill_T16384_zipf():
 def test_dsv3_shape_single_token():
     """T=1 at DSV3 shape: eight experts with one route each."""
     fullsize_parity(synth.config(2, 1), n_tokens=1)
+
+
+@pytest.mark.parametrize("T", [1, 64])
+def test_dsv3_shape_single_kernel(T):
+    """The DSV3-like shape at decode token counts through the single
+    persistent kernel (MOE_FUSED_LAYER), per-tensor scales, deterministic
+    finalize."""
+    r = fullsize_parity(synth.config(2, T).with_(fused=True), n_tokens=min(T, 16))
+    assert r["code_match"] >= 0.999
+
+
+def test_prefill_T16384_single_kernel():
+    """The prefill workload (per-token scales, Zipf skew, fused finalize)
+    through the single persistent kernel: the same kernel at 16384 tokens."""
+    r = fullsize_parity(synth.config(4).with_(fused=True), n_tokens=16)
+    assert r["code_match"] >= 0.999

@@ -276,3 +276,86 @@ def test_all_tokens_to_one_expert():
     check_routing(layer, ref)
     check_y(y, ref, None)
     assert (ref.grouping.count[[3, 5]] == 300).all()
+
+
+FUSED = []
+for T, H, I, E, K in [(1, 256, 128, 8, 2), (7, 384, 256, 8, 2), (129, 256, 128, 8, 1), (40, 256, 256, 1, 1),
+                      (200, 384, 128, 16, 4), (64, 512, 256, 256, 8)]:
+    for mode in (synth.MODE_PER_TENSOR, synth.MODE_PER_TOKEN):
+        for act in (0, 1):
+            for on_input, det in ((False, False), (True, True)):
+                FUSED.append((T, H, I, E, K, mode, act, on_input, det))
+
+
+@pytest.mark.parametrize("T,H,I,E,K,mode,act,on_input,det", FUSED)
+def test_fused_layer_parity(T, H, I, E, K, mode, act, on_input, det):
+    """The whole forward as one persistent kernel (MOE_FUSED_LAYER) [MegaMoE
+    blog, "Our approach"]: routing, permutation and quantized operands
+    bit-exact against the oracle, output within the tolerance of the default
+    path; one token, partial tiles, rows of 192 bytes (2-D maps), a single
+    expert, and the maximum of 256 experts with top-8."""
+    seed = (T * 13 + H + I * 5 + E * 3 + K + mode * 17 + act * 7 + det) % 1000
+    c = synth.MoEConfig("fused", T, H, I, E, K, act=act, mode=mode, router_on_input=on_input, deterministic=det,
+                        seed=seed, logits="normal", fused=True)
+    full_parity(c)
+
+
+@pytest.mark.parametrize("T,act,det", [(64, 0, False), (200, 1, True)])
+def test_fused_layer_4over6_parity(T, act, det):
+    c = synth.MoEConfig("fused46", T, 384, 256, 16, 4, act=act, mode=synth.MODE_PER_TOKEN, deterministic=det,
+                        seed=T + 3, logits="normal", four_over_six=True, fused=True)
+    r = full_parity(c)
+    assert r["code_match"] >= 0.999
+
+
+@pytest.mark.parametrize("T,mode,bad", [(64, synth.MODE_PER_TENSOR, 0.0), (200, synth.MODE_PER_TOKEN, 0.1)])
+def test_fused_layer_routed_parity(T, mode, bad):
+    """Caller-supplied routing through the single kernel, with dropped slots."""
+    from gpu_parity import random_routing, routed_parity
+    c = synth.MoEConfig("fusedr", T, 256, 128, 16, 4, mode=mode, deterministic=True, seed=T + 9, logits="normal",
+                        fused=True)
+    ids, w = random_routing(T, 16, 4, seed=T * 5, bad_frac=bad)
+    routed_parity(c, ids, w)
+
+
+@pytest.mark.parametrize("mode,act", [(synth.MODE_PER_TENSOR, 0), (synth.MODE_PER_TOKEN, 1)])
+def test_fused_layer_equals_launch_sequence(mode, act):
+    """Same arithmetic as the default launch sequence: with the deterministic
+    finalize every intermediate and the output are bit-identical, and
+    repeated fused forwards (the barrier counter is reset per launch) give
+    the same bits."""
+    c = synth.MoEConfig("fq", 300, 512, 256, 32, 4, act=act, mode=mode, deterministic=True, seed=41 + mode,
+                        logits="normal")
+    inp = make_inputs(c)
+    G1, G2 = scales_for(inp) if mode == synth.MODE_PER_TENSOR else (None, None)
+    layer0, y0 = run_gpu(inp, G1, G2)
+    inp.c = c.with_(fused=True)
+    layer1, y1 = run_gpu(inp, G1, G2)
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    rows = int(layer0.view("meta", torch.int32, 4).cpu()[0])
+    for n in ["topk_ids", "topk_w", "row_of_route", "route_of_row", "tile_expert", "tile_pair", "meta"]:
+        nb = {"route_of_row": 4 * rows, "tile_expert": 4 * (rows // 128), "tile_pair": 4 * (rows // 128),
+              "meta": 12}.get(n, 4 * c.T * c.K)
+        assert torch.equal(layer0.view(n, torch.uint8, nb), layer1.view(n, torch.uint8, nb)), n
+    valid = layer0.view("route_of_row", torch.int32, rows) >= 0      # pad rows are never written
+    per_row = [("xq_codes", c.H // 2), ("hq_codes", c.I // 2)]
+    if mode == synth.MODE_PER_TOKEN:
+        per_row.append(("g2", 4))
+        assert torch.equal(layer0.view("g1", torch.uint8, 4 * c.T), layer1.view("g1", torch.uint8, 4 * c.T))
+    for n, width in per_row:
+        a = layer0.view(n, torch.uint8, rows * width).view(rows, width)[valid]
+        b = layer1.view(n, torch.uint8, rows * width).view(rows, width)[valid]
+        assert torch.equal(a, b), n
+    g1 = None if G1 is None else torch.tensor([G1], device="cuda")
+    g2 = None if G2 is None else torch.tensor([G2], device="cuda")
+    for _ in range(3):
+        y = layer1.forward(inp.x, inp.logits, inp.bias, g1, g2)
+        torch.cuda.synchronize()
+        assert api.moe_nvfp4_last_device_status(layer1.workspace) == api.MOE_OK
+        assert torch.equal(y.view(torch.int16), y1.view(torch.int16))
+
+
+def test_mid_config_parity_fused():
+    """The mid workload (T=512, H=2048, I=768, E=64, top-6, per-token) as
+    one persistent kernel."""
+    full_parity(synth.config(1).with_(fused=True))
