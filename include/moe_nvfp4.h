@@ -281,7 +281,7 @@ typedef struct {
     uint64_t total;          /* workspace bytes                              */
 } moe_workspace_layout;
 
-#define MOE_WORKSPACE_VERSION 3
+#define MOE_WORKSPACE_VERSION 4
 
 /* Fill `out` with the workspace layout for this shape and flags.  Regions a
  * mode does not use have offset UINT64_MAX.  Pure host call, no CUDA. */

@@ -544,6 +544,17 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Fire-and-forget FP32 vector reduction into global memory (red, no
+// returned value).  Stated explicitly: the same float4 atomicAdd was
+// measured to become a returning atomic in one kernel and a reduction in
+// another, and the returning form halved the throughput of the scatter
+// epilogue.
+__device__ __forceinline__ void red_add_f32x4(float4* addr, float a, float b, float c, float d) {
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -124,8 +124,8 @@ __device__ __forceinline__ void epilogue_fc2(const GemmParams& p, uint32_t taddr
             float4* dst = reinterpret_cast<float4*>(p.out_f32 + (size_t)token * p.out_cols + col0);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                atomicAdd(dst + i, make_float4(o[4 * i] * alpha, o[4 * i + 1] * alpha, o[4 * i + 2] * alpha,
-                                               o[4 * i + 3] * alpha));
+                red_add_f32x4(dst + i, o[4 * i] * alpha, o[4 * i + 1] * alpha, o[4 * i + 2] * alpha,
+                              o[4 * i + 3] * alpha);
         }
     }
 }

@@ -8,24 +8,39 @@
 // One CTA per SM (cooperative launch, so that every CTA is resident) with the
 // grouped GEMM's warp roles and shared-memory pipeline (gemm_nvf4.cuh,
 // 128-wide tiles) and grid-wide barriers between the phases:
-//   1 router or given ids + per-unit expert masks  (units of 32 tokens)
-//   2 scan: offsets, tile map, pairs, unit rows     (CTA 0)
-//   3 x quantization + row scatter + y_acc zeroing  (tokens)
+//   1 routes + per-unit expert token masks   (one warp per token; masks by
+//                                             atomicOr, zeroed before launch)
+//   2 scan, redundantly in every CTA: expert totals, offsets, padded offsets
+//     and tile pairs in shared memory; the per-expert outputs (unit starting
+//     rows, tile map, pair list, pad rows) spread over the grid
+//   3 x quantization + row scatter + y_acc zeroing (a CTA per token when
+//                                             T <= grid, else a warp per token)
 //   4 FC1 tiles (SwiGLU / ReLU2, route weight, requant or FP32 store)
-//   5 per-token FC2-input quantization              (rows; per-token mode)
+//   5 per-token FC2-input quantization        (one warp per row)
 //   6 FC2 tiles (BF16 per-route rows or FP32 scatter)
-//   7 finalize                                      (tokens / elements)
+//   7 finalize                                (grid-stride over elements)
+// Phases 2 and 3 share one barrier interval when T <= 32 * kDirectUnits:
+// a token's row is then its expert's padded offset (in every CTA's shared
+// memory) plus the population counts of at most kDirectUnits unit masks.
 // Every phase computes what the kernel of the default path for that step
 // computes, with the same device arithmetic, so both paths give the same
 // bits (up to the order of the fused finalize's FP32 atomic additions).
 // The GEMM pipeline position carries over from FC1 to FC2.
 //
+// The row phases hand work out per warp over the whole grid (1 CTA per SM
+// leaves only ten warps per SM, so per-CTA rows with CTA-wide reductions
+// were latency-bound: a first version spent 33 us quantizing the mid
+// workload's FC2 input, against 10 us for the standalone kernel), except
+// that a token's x row is spread over a whole CTA when T is below the grid
+// size (a single warp walking a 7168-wide row took ~14 dependent memory
+// round trips), and every load loop keeps two blocks per thread in flight.
+//
 // A grid barrier is a counter (zeroed before the launch) that each CTA
 // increments once per barrier (release) and polls (acquire); the generic ->
 // async proxy fences around it make the operands written by the previous
 // phase visible to the TMA copies of the next.  Data written inside the
-// kernel is read with plain or L2 (.cg) loads, never through the read-only
-// path.  Every wait is bounded (1 s): a CTA that gives up raises
+// kernel by other CTAs is read with L2 (.cg) loads, never through the
+// read-only path.  Every wait is bounded (1 s): a CTA that gives up raises
 // kStatusGridAbort, and the others stop at their next barrier.
 #include "gemm_nvf4.cuh"
 #include "kernels.h"
@@ -39,6 +54,7 @@ using FC = grouped::Cfg<128, 0>;   // one pipeline configuration for both GEMMs
 constexpr int kFusedThreads = FC::kNumThreads;
 constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr int kFusedEpl = kFusedMaxExperts / 32;   // router: experts per lane
+constexpr int kDirectUnits = 4;                    // phases 2 + 3 fused up to 4 units of 32 tokens
 
 __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
     unsigned int v;
@@ -49,6 +65,9 @@ __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
 // next phase read global data and overwrite shared scratch written by the
 // generic proxy before
 __device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+__device__ __forceinline__ int global_warp() { return blockIdx.x * kFusedWarps + (threadIdx.x >> 5); }
+__device__ __forceinline__ int num_warps() { return gridDim.x * kFusedWarps; }
 
 // Grid-wide barrier number n (1, 2, ...).  Returns false (and sets the CTA's
 // abort flag) if this CTA arrives failed or another CTA has failed.
@@ -83,67 +102,94 @@ __device__ bool grid_barrier(const FusedParams& fp, unsigned int n, volatile int
     return s_ok != 0;
 }
 
-// Phase 1: per unit of 32 tokens (one unit per CTA at a time) the routes and
-// the unit's token mask of every expert (route_count_kernel /
-// route_given_kernel).
-__device__ void phase_route(const FusedParams& fp, uint32_t* s_mask) {
-    const int U = (fp.T + kUnitTokens - 1) / kUnitTokens;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        for (int e = threadIdx.x; e < fp.E; e += blockDim.x) s_mask[e] = 0u;
-        __syncthreads();
-        if (fp.ids_in == nullptr) {
-            for (int j = warp; j < kUnitTokens; j += kFusedWarps) {   // one warp per token
-                const int t = u * kUnitTokens + j;
-                if (t < fp.T) {
-                    const int e = route_token<kFusedEpl>(t, fp.E, fp.K, fp.logits, fp.bias, fp.renorm, fp.ids,
-                                                         fp.topk_w);
-                    if (e >= 0) atomicOr(&s_mask[e], 1u << j);
-                }
-            }
-        } else if (warp == 0) {                                        // one lane per token
-            const int t = u * kUnitTokens + lane;
-            if (t < fp.T) {
-                bool bad = false;
-                for (int k = 0; k < fp.K; ++k) {
-                    const size_t r = (size_t)t * fp.K + k;
-                    int e = fp.ids_in[r];
-                    if (e >= 0 && e < fp.E) {
-                        // a repeat of an earlier kept id finds its bit set
-                        if (atomicOr(&s_mask[e], 1u << lane) & (1u << lane)) e = -1;
-                    } else {
-                        e = -1;
-                    }
-                    bad |= e < 0;
-                    fp.ids[r] = e;
-                    fp.topk_w[r] = fp.w_in[r];
-                }
-                if (bad) atomicOr(fp.status, kStatusBadExpert);
-            }
-        }
-        __syncthreads();
-        for (int e = threadIdx.x; e < fp.E; e += blockDim.x) {
-            const uint32_t m = s_mask[e];
-            fp.unit_base[(size_t)e * U + u] = __popc(m);
-            fp.unit_mask[(size_t)e * U + u] = m;
-        }
-        __syncthreads();
+__device__ __forceinline__ void load16_bf16_plain(const __nv_bfloat16* p, float (&v)[16]) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
+    const uint4 b = *reinterpret_cast<const uint4*>(p + 8);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
 }
 
-// Phase 2 (CTA 0): per-expert totals, exclusive offsets of the counts, the
-// 128-padded counts and the M-tile pairs; the per-(expert, unit) starting
-// rows in place of the counts; tile map, pair list and -1 in the pad rows
-// (permute_scan_kernel).
+__device__ __forceinline__ void load16_f32_cg(const float* p, float (&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 q = __ldcg(reinterpret_cast<const float4*>(p) + i);
+        v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+    }
+}
+
+// Scales of four consecutive blocks (four consecutive lanes) packed into the
+// first lane's word; every lane of the warp takes part.
+__device__ __forceinline__ uint32_t pack_sf4_fused(uint32_t s) {
+    const uint32_t s1 = __shfl_down_sync(0xffffffffu, s, 1);
+    const uint32_t s2 = __shfl_down_sync(0xffffffffu, s, 2);
+    const uint32_t s3 = __shfl_down_sync(0xffffffffu, s, 3);
+    return s | (s1 << 8) | (s2 << 16) | (s3 << 24);
+}
+
+// Phase 1: the routes of every token and the unit token masks of every
+// expert (route_count_kernel / route_given_kernel).  Router: one warp per
+// token.  Given ids: one warp per unit of 32 tokens, one lane per token,
+// slots in order, so that a repeat of an earlier kept id finds its bit set.
+__device__ void phase_route(const FusedParams& fp) {
+    const int U = (fp.T + kUnitTokens - 1) / kUnitTokens;
+    const int lane = threadIdx.x & 31;
+    if (fp.ids_in == nullptr) {
+        for (int t = global_warp(); t < fp.T; t += num_warps()) {
+            const int e = route_token<kFusedEpl>(t, fp.E, fp.K, fp.logits, fp.bias, fp.renorm, fp.ids, fp.topk_w);
+            if (e >= 0) atomicOr(fp.unit_mask + (size_t)e * U + t / kUnitTokens, 1u << (t % kUnitTokens));
+        }
+        return;
+    }
+    for (int u = global_warp(); u < U; u += num_warps()) {
+        const int t = u * kUnitTokens + lane;
+        if (t >= fp.T) continue;
+        bool bad = false;
+        for (int k = 0; k < fp.K; ++k) {
+            const size_t r = (size_t)t * fp.K + k;
+            int e = fp.ids_in[r];
+            if (e >= 0 && e < fp.E) {
+                if (atomicOr(fp.unit_mask + (size_t)e * U + u, 1u << lane) & (1u << lane)) e = -1;
+            } else {
+                e = -1;
+            }
+            bad |= e < 0;
+            fp.ids[r] = e;
+            fp.topk_w[r] = fp.w_in[r];
+        }
+        if (bad) atomicOr(fp.status, kStatusBadExpert);
+    }
+}
+
+// Phase 2 (permute_scan_kernel), in every CTA: the per-expert totals (the
+// population counts of the unit masks), exclusive scans of the counts, the
+// 128-padded counts and the M-tile pairs into shared memory (s_cnt, s_pad,
+// s_pair); CTA 0 publishes count / offsets / padded_offsets / meta.  Then
+// the per-expert outputs, expert e on CTA e % grid: the per-(expert, unit)
+// starting rows, the tile map, the pair list and -1 in the pad rows.
 __device__ void phase_scan(const FusedParams& fp, int* s_cnt, int* s_pad, int* s_pair) {
     const int U = (fp.T + kUnitTokens - 1) / kUnitTokens;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int e = warp; e < fp.E; e += kFusedWarps) {
-        int sum = 0;
-        for (int u = lane; u < U; u += 32) sum += fp.unit_base[(size_t)e * U + u];
+    if (U < 32) {
+        // few units: a thread per expert, its loads independent (a warp per
+        // expert would chain E / 10 dependent L2 round trips per warp)
+        for (int e = threadIdx.x; e < fp.E; e += blockDim.x) {
+            int sum = 0;
+#pragma unroll 4
+            for (int u = 0; u < U; ++u) sum += __popc(__ldcg(fp.unit_mask + (size_t)e * U + u));
+            s_cnt[e] = sum;
+        }
+    } else {
+        for (int e = warp; e < fp.E; e += kFusedWarps) {
+            int sum = 0;
+            for (int u = lane; u < U; u += 32) sum += __popc(__ldcg(fp.unit_mask + (size_t)e * U + u));
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) s_cnt[e] = sum;
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (lane == 0) s_cnt[e] = sum;
+        }
     }
     __syncthreads();
     if (warp == 0) {
@@ -162,30 +208,35 @@ __device__ void phase_scan(const FusedParams& fp, int* s_cnt, int* s_pad, int* s
                 if (lane >= o) { ic += a; ip += b; iq += d; }
             }
             if (e < fp.E) {
-                fp.count[e] = c;
-                fp.offsets[e] = cc + ic - c;
-                fp.padded_offsets[e] = cp + ip - p;
                 s_pad[e] = cp + ip - p;
                 s_pair[e] = cq + iq - q;
+                if (blockIdx.x == 0) {
+                    fp.count[e] = c;
+                    fp.offsets[e] = cc + ic - c;
+                    fp.padded_offsets[e] = cp + ip - p;
+                }
             }
             cc += __shfl_sync(0xffffffffu, ic, 31);
             cp += __shfl_sync(0xffffffffu, ip, 31);
             cq += __shfl_sync(0xffffffffu, iq, 31);
         }
         if (lane == 0) {
-            fp.offsets[fp.E] = cc;
-            fp.padded_offsets[fp.E] = cp;
-            fp.meta[0] = cp;
-            fp.meta[1] = cp / kTileM;
-            fp.meta[2] = cq;
+            s_pad[fp.E] = cp;
+            if (blockIdx.x == 0) {
+                fp.offsets[fp.E] = cc;
+                fp.padded_offsets[fp.E] = cp;
+                fp.meta[0] = cp;
+                fp.meta[1] = cp / kTileM;
+                fp.meta[2] = cq;
+            }
         }
     }
     __syncthreads();
-    for (int e = warp; e < fp.E; e += kFusedWarps) {
+    for (int e = blockIdx.x + gridDim.x * warp; e < fp.E; e += gridDim.x * kFusedWarps) {
         int carry = s_pad[e];
         for (int u0 = 0; u0 < U; u0 += 32) {
             const int u = u0 + lane;
-            const int v = u < U ? fp.unit_base[(size_t)e * U + u] : 0;
+            const int v = u < U ? __popc(__ldcg(fp.unit_mask + (size_t)e * U + u)) : 0;
             int incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -206,159 +257,217 @@ __device__ void phase_scan(const FusedParams& fp, int* s_cnt, int* s_pad, int* s
     }
 }
 
-__device__ __forceinline__ void load16_bf16_plain(const __nv_bfloat16* p, float (&v)[16]) {
-    const uint4 a = *reinterpret_cast<const uint4*>(p);
-    const uint4 b = *reinterpret_cast<const uint4*>(p + 8);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+// Rows of token t's routes (step 3 of the permutation), lane k < K of the
+// calling warp taking route t*K+k; records both directions of the map and
+// returns the row (-1 for a dropped route and for lanes >= K).  direct: the
+// scan's unit starting rows are not published yet; the row is the expert's
+// padded offset (s_pad) plus the counts of the token's earlier units.
+__device__ __forceinline__ int token_route_row(const FusedParams& fp, int t, const int* s_pad, bool direct) {
+    const int lane = threadIdx.x & 31;
+    if (lane >= fp.K) return -1;
+    const int U = (fp.T + kUnitTokens - 1) / kUnitTokens;
+    const int r = t * fp.K + lane;
+    const int e = __ldcg(fp.ids + r);
+    int row = -1;
+    if (e >= 0 && e < fp.E) {
+        const int u = t / kUnitTokens;
+        const size_t idx = (size_t)e * U + u;
+        const uint32_t below = (1u << (t % kUnitTokens)) - 1u;
+        int start;
+        if (direct) {
+            start = s_pad[e];
+            for (int v = 0; v < u; ++v) start += __popc(__ldcg(fp.unit_mask + (size_t)e * U + v));
+        } else {
+            start = __ldcg(fp.unit_base + idx);
+        }
+        row = start + __popc(__ldcg(fp.unit_mask + idx) & below);
+        fp.route_of_row[row] = r;
+    }
+    fp.row_of_route[r] = row;
+    return row;
+}
+
+// Largest |x| of token t's row over the blocks g, g + kGroup, ... (two
+// blocks per thread in flight).
+template <int kGroup>
+__device__ __forceinline__ float token_row_amax(const FusedParams& fp, int t, int g) {
+    const int nblk = fp.H / 16;
+    const __nv_bfloat16* xr = fp.x + (size_t)t * fp.H;
+    float amax = 0.0f;
+    for (int b0 = g; b0 < nblk; b0 += 2 * kGroup) {
+        float v[2][16];
+        const bool second = b0 + kGroup < nblk;
+        load16_bf16_plain(xr + 16 * b0, v[0]);
+        if (second) load16_bf16_plain(xr + 16 * (b0 + kGroup), v[1]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[0][j]));
+        if (second) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[1][j]));
+        }
+    }
+    return amax;
+}
+
+// NVFP4 codes and scales of token t's x row written to its K rows (rows[],
+// shared memory) by a group of kGroup threads (a warp or the CTA), thread g
+// of the group on blocks g, g + kGroup, ...; two blocks per thread in
+// flight per step (explicit: the byte stores could alias x, so the compiler
+// would not move a later load above them).
+template <bool kFourSix, int kGroup>
+__device__ __forceinline__ void quantize_token_row(const FusedParams& fp, int t, int g, float G, const int* rows) {
+    const int H = fp.H, K = fp.K, nblk = H / 16, lane = threadIdx.x & 31;
+    const __nv_bfloat16* xr = fp.x + (size_t)t * H;
+    for (int b0 = 0; b0 < nblk; b0 += 2 * kGroup) {   // uniform across the group
+        float v[2][16];
+        bool act[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int b = b0 + i * kGroup + g;
+            act[i] = b < nblk;
+            if (act[i]) load16_bf16_plain(xr + 16 * b, v[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            if (b0 + i * kGroup >= nblk) break;           // uniform: the group's first block
+            const int b = b0 + i * kGroup + g;
+            uint32_t q[2] = {0u, 0u};
+            uint32_t s = 0;
+            if (act[i]) s = kFourSix ? quant_block16_4over6(v[i], G, q) : quant_block16(v[i], G, q);
+            const uint32_t word = pack_sf4_fused(s);
+            if (!act[i]) continue;
+            for (int k = 0; k < K; ++k) {
+                const int row = rows[k];
+                if (row < 0) continue;
+                *reinterpret_cast<uint2*>(fp.xq_codes + (size_t)row * (H / 2) + 8 * b) = make_uint2(q[0], q[1]);
+                if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(fp.xq_sf + sf_offset(row, b, H)) = word;
+            }
+        }
     }
 }
 
-// Scales of four consecutive blocks (four consecutive lanes) packed into the
-// first lane's word.
-__device__ __forceinline__ uint32_t pack_sf4_fused(uint32_t s) {
-    const uint32_t s1 = __shfl_down_sync(0xffffffffu, s, 1);
-    const uint32_t s2 = __shfl_down_sync(0xffffffffu, s, 2);
-    const uint32_t s3 = __shfl_down_sync(0xffffffffu, s, 3);
-    return s | (s1 << 8) | (s2 << 16) | (s3 << 24);
-}
-
-// CTA-wide maximum of v (every thread gets it); s_red holds kFusedWarps floats.
-__device__ __forceinline__ float cta_max(float v, float* s_red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = warp_max(v);
-    if (lane == 0) s_red[warp] = v;
-    __syncthreads();
-    float m = lane < kFusedWarps ? s_red[lane] : 0.0f;
-    m = warp_max(m);
-    __syncthreads();                                   // s_red is reused
-    return m;
-}
-
-// Phase 3: x quantization into the token's K permuted rows, the row scatter
-// (step 3 of the permutation) and the zeroing of the token's fused-finalize
-// accumulator row (quantize_x_kernel).
+// Phase 3 (quantize_x_kernel): the token's rows, the per-token G1 from the
+// row amax (per-token mode), the NVFP4 codes and scales in each of the K
+// rows, the zeroing of the fused-finalize accumulator row.  A CTA per token
+// when the tokens fit the grid (small T: the row's blocks spread over 320
+// threads), else a warp per token.  s_rows: [kFusedWarps][32], s_red:
+// [kFusedWarps].
 template <bool kFourSix>
-__device__ void phase_quantize_x(const FusedParams& fp, int* s_rows, float* s_red) {
-    const int U = (fp.T + kUnitTokens - 1) / kUnitTokens;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int H = fp.H, K = fp.K, nblk = H / 16;
-    for (int t = blockIdx.x; t < fp.T; t += gridDim.x) {
-        if (warp == 0 && lane < K) {
-            const int r = t * K + lane;
-            const int e = fp.ids[r];
-            int row = -1;
-            if (e >= 0 && e < fp.E) {
-                const size_t idx = (size_t)e * U + t / kUnitTokens;
-                const uint32_t below = (1u << (t % kUnitTokens)) - 1u;
-                row = __ldcg(fp.unit_base + idx) + __popc(__ldcg(fp.unit_mask + idx) & below);
-                fp.route_of_row[row] = r;
-            }
-            fp.row_of_route[r] = row;
-            s_rows[lane] = row;
+__device__ void phase_quantize_x(const FusedParams& fp, const int* s_pad, bool direct, int* s_rows, float* s_red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int H = fp.H;
+    if (fp.T <= (int)gridDim.x) {
+        const int t = blockIdx.x;
+        if (t >= fp.T) return;                           // uniform across the CTA
+        if (warp == 0) {
+            const int row = token_route_row(fp, t, s_pad, direct);
+            if (lane < fp.K) s_rows[lane] = row;
         }
-        const __nv_bfloat16* xr = fp.x + (size_t)t * H;
         float G;
         if (fp.per_token) {
-            float amax = 0.0f;
-            for (int b = tid; b < nblk; b += blockDim.x) {
-                float v[16];
-                load16_bf16_plain(xr + 16 * b, v);
+            float amax = warp_max(token_row_amax<kFusedThreads>(fp, t, threadIdx.x));
+            if (lane == 0) s_red[warp] = amax;
+            __syncthreads();
+            amax = s_red[0];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
-            }
-            const float m = cta_max(amax, s_red);
-            G = kFourSix ? global_scale_from_amax_4over6(m) : global_scale_from_amax(m);
-            if (tid == 0) fp.g1[t] = G;
+            for (int w = 1; w < kFusedWarps; ++w) amax = fmaxf(amax, s_red[w]);
+            G = kFourSix ? global_scale_from_amax_4over6(amax) : global_scale_from_amax(amax);
+            if (threadIdx.x == 0) fp.g1[t] = G;
         } else {
             G = __ldg(fp.g1_in);
-            __syncthreads();                                // s_rows
+            __syncthreads();                             // s_rows
         }
-        for (int b0 = 0; b0 < nblk; b0 += blockDim.x) {   // uniform across the CTA
-            const int b = b0 + tid;
-            const bool active = b < nblk;
-            uint32_t q[2] = {0u, 0u};
-            uint32_t s = 0;
-            if (active) {
-                float v[16];
-                load16_bf16_plain(xr + 16 * b, v);
-                s = kFourSix ? quant_block16_4over6(v, G, q) : quant_block16(v, G, q);
-            }
-            const uint32_t word = pack_sf4_fused(s);
-            if (active) {
-                for (int k = 0; k < K; ++k) {
-                    const int row = s_rows[k];
-                    if (row < 0) continue;
-                    *reinterpret_cast<uint2*>(fp.xq_codes + (size_t)row * (H / 2) + 8 * b) = make_uint2(q[0], q[1]);
-                    if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(fp.xq_sf + sf_offset(row, b, H)) = word;
-                }
-            }
-        }
+        quantize_token_row<kFourSix, kFusedThreads>(fp, t, threadIdx.x, G, s_rows);
         if (!fp.det) {
             float* yr = fp.y_acc + (size_t)t * H;
-            for (int c = tid * 4; c < H; c += blockDim.x * 4)
+            for (int c = threadIdx.x * 4; c < H; c += kFusedThreads * 4)
                 *reinterpret_cast<float4*>(yr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        __syncthreads();                                    // s_rows is reused by the next token
+        return;
+    }
+    int* rows = s_rows + warp * 32;
+    for (int t = global_warp(); t < fp.T; t += num_warps()) {
+        const int row = token_route_row(fp, t, s_pad, direct);
+        if (lane < fp.K) rows[lane] = row;
+        __syncwarp();
+        float G;
+        if (fp.per_token) {
+            const float amax = warp_max(token_row_amax<32>(fp, t, lane));
+            G = kFourSix ? global_scale_from_amax_4over6(amax) : global_scale_from_amax(amax);
+            if (lane == 0) fp.g1[t] = G;
+        } else {
+            G = __ldg(fp.g1_in);
+        }
+        quantize_token_row<kFourSix, 32>(fp, t, lane, G, rows);
+        if (!fp.det) {
+            float* yr = fp.y_acc + (size_t)t * H;
+            for (int c = lane * 4; c < H; c += 128) *reinterpret_cast<float4*>(yr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncwarp();                                    // rows is reused by the next token
     }
 }
 
-// Phase 5 (per-token mode): each valid FC2 input row -> G2 = amax / 2688
-// (or / 1536 with 4-over-6 blocks) and NVFP4 codes and scales
-// (quantize_h_kernel).
+// Phase 5 (per-token mode; quantize_h_kernel), one warp per padded row: the
+// valid FC2 input rows -> G2 = amax / 2688 (or / 1536 with 4-over-6 blocks)
+// and NVFP4 codes and scales; two blocks per lane in flight per step.
 template <bool kFourSix>
-__device__ void phase_quantize_h(const FusedParams& fp, float* s_red) {
-    const int tid = threadIdx.x, lane = tid & 31;
+__device__ void phase_quantize_h(const FusedParams& fp) {
+    const int lane = threadIdx.x & 31;
     const int I = fp.I, nblk = I / 16;
-    const int rows = fp.meta[0];
-    for (int row = blockIdx.x; row < rows; row += gridDim.x) {
-        if (fp.route_of_row[row] < 0) continue;   // pad row (uniform across the CTA)
+    const int rows = __ldcg(fp.meta);
+    for (int row = global_warp(); row < rows; row += num_warps()) {
+        if (__ldcg(fp.route_of_row + row) < 0) continue;   // pad row (uniform across the warp)
         const float* hr = fp.h_f32 + (size_t)row * I;
         float amax = 0.0f;
-        for (int b = tid; b < nblk; b += blockDim.x) {
-            const float4* p4 = reinterpret_cast<const float4*>(hr + 16 * b);
+        for (int b0 = lane; b0 < nblk; b0 += 64) {
+            float v[2][16];
+            const bool second = b0 + 32 < nblk;
+            load16_f32_cg(hr + 16 * b0, v[0]);
+            if (second) load16_f32_cg(hr + 16 * (b0 + 32), v[1]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 q = p4[j];
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(q.x), fabsf(q.y)), fmaxf(fabsf(q.z), fabsf(q.w))));
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[0][j]));
+            if (second) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[1][j]));
             }
         }
-        const float m = cta_max(amax, s_red);
-        const float G = kFourSix ? global_scale_from_amax_4over6(m) : global_scale_from_amax(m);
-        if (tid == 0) fp.g2[row] = G;
-        for (int b0 = 0; b0 < nblk; b0 += blockDim.x) {
-            const int b = b0 + tid;
-            const bool active = b < nblk;
-            uint32_t q[2] = {0u, 0u};
-            uint32_t s = 0;
-            if (active) {
-                float v[16];
-                const float4* p4 = reinterpret_cast<const float4*>(hr + 16 * b);
+        amax = warp_max(amax);
+        const float G = kFourSix ? global_scale_from_amax_4over6(amax) : global_scale_from_amax(amax);
+        if (lane == 0) fp.g2[row] = G;
+        for (int b0 = 0; b0 < nblk; b0 += 64) {        // uniform across the warp
+            float v[2][16];
+            bool act[2];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 x4 = p4[j];
-                    v[4 * j] = x4.x; v[4 * j + 1] = x4.y; v[4 * j + 2] = x4.z; v[4 * j + 3] = x4.w;
-                }
-                s = kFourSix ? quant_block16_4over6(v, G, q) : quant_block16(v, G, q);
+            for (int i = 0; i < 2; ++i) {
+                const int b = b0 + 32 * i + lane;
+                act[i] = b < nblk;
+                if (act[i]) load16_f32_cg(hr + 16 * b, v[i]);
             }
-            const uint32_t word = pack_sf4_fused(s);
-            if (active) {
-                *reinterpret_cast<uint2*>(fp.hq_codes + (size_t)row * (I / 2) + 8 * b) = make_uint2(q[0], q[1]);
-                if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(fp.hq_sf + sf_offset(row, b, I)) = word;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                if (b0 + 32 * i >= nblk) break;
+                const int b = b0 + 32 * i + lane;
+                uint32_t q[2] = {0u, 0u};
+                uint32_t s = 0;
+                if (act[i]) s = kFourSix ? quant_block16_4over6(v[i], G, q) : quant_block16(v[i], G, q);
+                const uint32_t word = pack_sf4_fused(s);
+                if (act[i]) {
+                    *reinterpret_cast<uint2*>(fp.hq_codes + (size_t)row * (I / 2) + 8 * b) = make_uint2(q[0], q[1]);
+                    if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(fp.hq_sf + sf_offset(row, b, I)) = word;
+                }
             }
         }
     }
 }
 
-// Phase 7: finalize (finalize_fused_kernel / finalize_det_kernel).
+// Phase 7 (finalize_fused_kernel / finalize_det_kernel), grid-stride over
+// groups of 8 output elements.
 __device__ void phase_finalize(const FusedParams& fp) {
-    const int H = fp.H, K = fp.K;
+    const int H = fp.H, K = fp.K, H8 = H / 8;
+    const int64_t n8 = (int64_t)fp.T * H8;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
     if (!fp.det) {
-        const int64_t n8 = (int64_t)fp.T * H / 8;
-        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += step) {
             const float4 a = __ldcg(reinterpret_cast<const float4*>(fp.y_acc) + 2 * i);
             const float4 b = __ldcg(reinterpret_cast<const float4*>(fp.y_acc) + 2 * i + 1);
             const __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
@@ -369,29 +478,28 @@ __device__ void phase_finalize(const FusedParams& fp) {
         }
         return;
     }
-    for (int t = blockIdx.x; t < fp.T; t += gridDim.x) {
-        for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int k = 0; k < K; ++k) {
-                const int row = fp.row_of_route[(size_t)t * K + k];
-                if (row < 0) continue;   // dropped route
-                const float w = fp.weight_on_output ? fp.topk_w[(size_t)t * K + k] : 1.0f;
-                const uint4 v = __ldcg(reinterpret_cast<const uint4*>(fp.o_bf16 + (size_t)row * H) + c);
-                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += step) {
+        const int t = (int)(i / H8), c = (int)(i % H8);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < K; ++k) {
+            const int row = __ldcg(fp.row_of_route + (size_t)t * K + k);
+            if (row < 0) continue;   // dropped route
+            const float w = fp.weight_on_output ? __ldcg(fp.topk_w + (size_t)t * K + k) : 1.0f;
+            const uint4 v = __ldcg(reinterpret_cast<const uint4*>(fp.o_bf16 + (size_t)row * H) + c);
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = fmaf(w, __uint_as_float(u[i] << 16), acc[2 * i]);
-                    acc[2 * i + 1] = fmaf(w, __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
-                }
+            for (int j = 0; j < 4; ++j) {
+                acc[2 * j] = fmaf(w, __uint_as_float(u[j] << 16), acc[2 * j]);
+                acc[2 * j + 1] = fmaf(w, __uint_as_float(u[j] & 0xFFFF0000u), acc[2 * j + 1]);
             }
-            uint32_t out[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-                out[i] = *reinterpret_cast<const uint32_t*>(&b);
-            }
-            reinterpret_cast<uint4*>(fp.y + (size_t)t * H)[c] = make_uint4(out[0], out[1], out[2], out[3]);
         }
+        uint32_t out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+            out[j] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        reinterpret_cast<uint4*>(fp.y)[i] = make_uint4(out[0], out[1], out[2], out[3]);
     }
 }
 
@@ -403,15 +511,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                        const __grid_constant__ FusedParams fp) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ int s_rows[32];
-    __shared__ float s_red[32];
+    __shared__ int s_rows[kFusedWarps * 32];
+    __shared__ float s_red[kFusedWarps];
     const grouped::Smem s = grouped::carve<128, 0>(smem_raw);
-    // the operand ring is idle until FC1: phases 1 and 2 keep their
-    // per-expert scratch in it
-    uint32_t* s_mask = reinterpret_cast<uint32_t*>(s.a);
-    int* s_cnt = reinterpret_cast<int*>(s.a) + kFusedMaxExperts;
-    int* s_pad = s_cnt + kFusedMaxExperts;
-    int* s_pair = s_pad + kFusedMaxExperts;
+    // the operand ring is idle until FC1: the scan keeps its per-expert
+    // tables in it (the TMA copies of FC1 start after a grid barrier, whose
+    // proxy fence orders these generic writes before them)
+    int* s_cnt = reinterpret_cast<int*>(s.a);
+    int* s_pad = s_cnt + kFusedMaxExperts;          // E + 1 entries
+    int* s_pair = s_pad + kFusedMaxExperts + 1;
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tmA1);
         prefetch_tensormap(&tmB1);
@@ -421,15 +529,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const uint32_t tmem_base = grouped::gemm_init<128, 0>(s);
     grouped::RingState rs;
     unsigned int nb = 0;
+    const bool direct = (fp.T + kUnitTokens - 1) / kUnitTokens <= kDirectUnits;
 
-    phase_route(fp, s_mask);
+    phase_route(fp);
     bool ok = grid_barrier(fp, ++nb, s.abort);
     if (ok) {
-        if (blockIdx.x == 0) phase_scan(fp, s_cnt, s_pad, s_pair);
-        ok = grid_barrier(fp, ++nb, s.abort);
+        phase_scan(fp, s_cnt, s_pad, s_pair);
+        if (!direct) ok = grid_barrier(fp, ++nb, s.abort);
     }
     if (ok) {
-        phase_quantize_x<kFourSix>(fp, s_rows, s_red);
+        phase_quantize_x<kFourSix>(fp, s_pad, direct, s_rows, s_red);
         ok = grid_barrier(fp, ++nb, s.abort);
     }
     if (ok) {
@@ -438,7 +547,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         ok = grid_barrier(fp, ++nb, s.abort);   // fails if the tile loop set the abort flag
     }
     if (ok && fp.per_token) {
-        phase_quantize_h<kFourSix>(fp, s_red);
+        phase_quantize_h<kFourSix>(fp);
         ok = grid_barrier(fp, ++nb, s.abort);
     }
     if (ok) {

@@ -103,6 +103,9 @@ inline moe_workspace_layout workspace_layout(moe_shape s, uint32_t flags) {
     uint64_t o = 0;
     auto take = [&](uint64_t bytes) { uint64_t at = o; o = align_up(o + bytes, 256); return at; };
     L.status = take(16);
+    // the unit masks follow the status word: the single-kernel forward
+    // zeroes both with one memset before its launch
+    L.unit_mask = take(4 * E * units);
     L.topk_ids = take(4 * T * K);
     L.topk_w = take(4 * T * K);
     L.count = take(4 * E);
@@ -110,7 +113,6 @@ inline moe_workspace_layout workspace_layout(moe_shape s, uint32_t flags) {
     L.padded_offsets = take(4 * (E + 1));
     L.meta = take(16);
     L.unit_base = take(4 * E * units);
-    L.unit_mask = take(4 * E * units);
     L.row_of_route = take(4 * T * K);
     L.route_of_row = take(4 * cap);
     L.tile_expert = take(4 * (cap / kTileM));

@@ -143,7 +143,7 @@ bool use_pair_gemm(moe_shape s, uint32_t flags, int n) {
 
 extern "C" {
 
-const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.2 sm_103a (prepared v1, workspace v3)"; }
+const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.3 sm_103a (prepared v1, workspace v4)"; }
 
 size_t moe_nvfp4_prepared_bytes(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return 0;
@@ -307,8 +307,11 @@ static moe_status forward_fused(moe_shape s, uint32_t flags, const void* x_bf16,
         return events == nullptr || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess;
     };
     if (!mark(0)) return MOE_ERR_CUDA;
-    // status word and grid-barrier counter start at zero
-    if (cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    // status word, grid-barrier counter and the unit masks (built by
+    // atomicOr) start at zero; the masks follow the status word
+    const uint64_t units = ((uint64_t)s.T + kUnitTokens - 1) / kUnitTokens;
+    const size_t zero_bytes = (size_t)(W.unit_mask + 4 * (uint64_t)s.E * units - W.status);
+    if (W.unit_mask < W.status || cudaMemsetAsync(status, 0, zero_bytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_fused_layer(stream, sms, tmA1, tmB1, tmA2, tmB2, f, (flags & MOE_QUANT_4OVER6) != 0) != cudaSuccess)
         return MOE_ERR_CUDA;
     for (int i = 1; i < MOE_NUM_STAGE_EVENTS; ++i)
