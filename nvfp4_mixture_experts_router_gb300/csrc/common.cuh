@@ -555,6 +555,54 @@ __device__ __forceinline__ void red_add_f32x4(float4* addr, float a, float b, fl
                  : "memory");
 }
 
+// Deterministic finalize of 8 output elements: acc = sum over the K routes
+// of token t, k ascending, of w'_k * o[row(t, k)][8c .. 8c+8) with FP32 fma
+// (w' = the router weight on the output side, else 1; dropped routes,
+// row -1, skipped).  The rows are loaded four at a time (L2 loads: the
+// inputs may come from other CTAs of the same kernel).
+__device__ __forceinline__ void finalize_det_group(int t, int c, int H, int K, const int* row_of_route,
+                                                   const float* topk_w, int weight_on_output,
+                                                   const __nv_bfloat16* o, float (&acc)[8]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int k0 = 0; k0 < K; k0 += 4) {
+        int row[4];
+        float w[4];
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = k0 + j;
+            row[j] = k < K ? __ldcg(row_of_route + (size_t)t * K + k) : -1;
+            w[j] = (k < K && weight_on_output) ? __ldcg(topk_w + (size_t)t * K + k) : 1.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[j] = row[j] >= 0 ? __ldcg(reinterpret_cast<const uint4*>(o + (size_t)row[j] * H) + c)
+                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (row[j] < 0) continue;
+            const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(w[j], __uint_as_float(u[i] << 16), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(w[j], __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
+            }
+        }
+    }
+}
+
+// Eight FP32 values rounded to BF16 (nearest even), packed in order.
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&a)[8]) {
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
+        out[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -480,26 +480,9 @@ __device__ void phase_finalize(const FusedParams& fp) {
     }
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += step) {
         const int t = (int)(i / H8), c = (int)(i % H8);
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int k = 0; k < K; ++k) {
-            const int row = __ldcg(fp.row_of_route + (size_t)t * K + k);
-            if (row < 0) continue;   // dropped route
-            const float w = fp.weight_on_output ? __ldcg(fp.topk_w + (size_t)t * K + k) : 1.0f;
-            const uint4 v = __ldcg(reinterpret_cast<const uint4*>(fp.o_bf16 + (size_t)row * H) + c);
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                acc[2 * j] = fmaf(w, __uint_as_float(u[j] << 16), acc[2 * j]);
-                acc[2 * j + 1] = fmaf(w, __uint_as_float(u[j] & 0xFFFF0000u), acc[2 * j + 1]);
-            }
-        }
-        uint32_t out[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
-            out[j] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-        reinterpret_cast<uint4*>(fp.y)[i] = make_uint4(out[0], out[1], out[2], out[3]);
+        float acc[8];
+        finalize_det_group(t, c, H, K, fp.row_of_route, fp.topk_w, fp.weight_on_output, fp.o_bf16, acc);
+        reinterpret_cast<uint4*>(fp.y)[i] = pack_bf16x8(acc);
     }
 }
 

@@ -281,33 +281,21 @@ __global__ void __launch_bounds__(1024) quantize_h_kernel(int I, const int* __re
 
 // Deterministic finalize: y[t] = BF16( sum_k w'_k * o[row(t,k)] ), k in
 // ascending order, FP32 accumulation; w' = router weight (output side) or 1.
-__global__ void __launch_bounds__(128) finalize_det_kernel(int T, int H, int K, const int* __restrict__ row_of_route,
+// One thread per 8 output elements of a token (the whole grid shares the
+// T x H/8 groups, so a few tokens still spread over many SMs); the K rows
+// are loaded four at a time to keep loads in flight.
+__global__ void __launch_bounds__(256) finalize_det_kernel(int T, int H, int K, const int* __restrict__ row_of_route,
                                                            const float* __restrict__ topk_w, int weight_on_output,
                                                            const __nv_bfloat16* __restrict__ o,
                                                            __nv_bfloat16* __restrict__ y) {
     pdl_wait();
-    const int t = blockIdx.x;
-    for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int k = 0; k < K; ++k) {
-            const int row = row_of_route[(size_t)t * K + k];
-            if (row < 0) continue;   // dropped route
-            const float w = weight_on_output ? topk_w[(size_t)t * K + k] : 1.0f;
-            const uint4 v = reinterpret_cast<const uint4*>(o + (size_t)row * H)[c];
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = fmaf(w, __uint_as_float(u[i] << 16), acc[2 * i]);
-                acc[2 * i + 1] = fmaf(w, __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
-            }
-        }
-        uint32_t out[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-            out[i] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-        reinterpret_cast<uint4*>(y + (size_t)t * H)[c] = make_uint4(out[0], out[1], out[2], out[3]);
+    const int H8 = H / 8;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < (int64_t)T * H8) {
+        const int t = (int)(i / H8), c = (int)(i % H8);
+        float acc[8];
+        finalize_det_group(t, c, H, K, row_of_route, topk_w, weight_on_output, o, acc);
+        reinterpret_cast<uint4*>(y)[i] = pack_bf16x8(acc);
     }
     pdl_launch_dependents();
 }
@@ -519,8 +507,9 @@ cudaError_t launch_quantize_h(const LaunchCtx& c, uint64_t rows_cap, int I, cons
 
 cudaError_t launch_finalize_deterministic(const LaunchCtx& c, int T, int H, int K, const int* row_of_route,
                                           const float* topk_w, int weight_on_output, const void* o, void* y) {
-    return c.launch(finalize_det_kernel, dim3(T), dim3(128), 0, T, H, K, row_of_route, topk_w, weight_on_output,
-                    (const __nv_bfloat16*)o, (__nv_bfloat16*)y);
+    const int64_t groups = (int64_t)T * (H / 8);
+    return c.launch(finalize_det_kernel, dim3((unsigned)((groups + 255) / 256)), dim3(256), 0, T, H, K, row_of_route,
+                    topk_w, weight_on_output, (const __nv_bfloat16*)o, (__nv_bfloat16*)y);
 }
 
 cudaError_t launch_finalize_fused(const LaunchCtx& c, int T, int H, const float* y_acc, void* y) {
