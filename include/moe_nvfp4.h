@@ -115,7 +115,18 @@ typedef enum {
  * resident CTA (otherwise the launch fails: MOE_ERR_CUDA).  The staged entry
  * point records all eight events around the one kernel. */
 #define MOE_FUSED_LAYER (1u << 10)
-#define MOE_FLAGS_KNOWN 0x7FFu
+/* bits 11-12: GEMM operand orientation (W4A4 launch sequence; results are
+ * the same either way up to FP32 accumulation order).  The swapped
+ * orientation puts the expert's weights on the MMA's M side and 64 of its
+ * routes on the N side, so that experts with few routes do not stream
+ * 128-row activation tiles that are mostly padding.  Default: swapped when
+ * the mean number of routes per expert holding any (T*K / min(E, T*K)) is
+ * at most 64 and T*K >= 64.  MOE_GEMM_SWAP_NEVER / _ALWAYS force a choice; setting both,
+ * or _ALWAYS with MOE_GEMM_PAIRS_ALWAYS, MOE_FUSED_LAYER or a non-W4A4 mode,
+ * is invalid. */
+#define MOE_GEMM_SWAP_NEVER (1u << 11)
+#define MOE_GEMM_SWAP_ALWAYS (1u << 12)
+#define MOE_FLAGS_KNOWN 0x1FFFu
 
 /* ---- shapes ---------------------------------------------------------------- */
 typedef struct {
@@ -259,7 +270,8 @@ typedef struct {
     uint64_t offsets;        /* int32 [E+1] exclusive prefix of count        */
     uint64_t padded_offsets; /* int32 [E+1] prefix of count rounded up to 128*/
     uint64_t meta;           /* int32 [4]: [0] padded rows, [1] M tiles,     */
-                             /*   [2] M-tile pairs (tile_pair entries)       */
+                             /*   [2] M-tile pairs (tile_pair entries),      */
+                             /*   [3] occupied halves (tile_half entries)    */
     uint64_t unit_base;      /* int32 [E][ceil(T/32)] per-unit starting rows */
     uint64_t unit_mask;      /* uint32 [E][ceil(T/32)] per-unit token masks  */
     uint64_t row_of_route;   /* int32 [T*K] padded row of route t*K+k        */
@@ -267,6 +279,8 @@ typedef struct {
     uint64_t tile_expert;    /* int32 [rows_cap/128] expert of each M tile   */
     uint64_t tile_pair;      /* int32 [rows_cap/128] M-tile pairs of one     */
                              /*   expert: (first tile << 1) | has_second     */
+    uint64_t tile_half;      /* int32 [2*rows_cap/128] 64-row halves of M    */
+                             /*   tiles holding routes: (M tile << 1) | half */
     uint64_t g1;             /* f32   [T] FC1-input global scale per token   */
     uint64_t xq_codes;       /* u8    [rows_cap][H/2] permuted x codes       */
     uint64_t xq_sf;          /* u8    [rows_cap/128][H/64][512] x scales     */
@@ -281,7 +295,7 @@ typedef struct {
     uint64_t total;          /* workspace bytes                              */
 } moe_workspace_layout;
 
-#define MOE_WORKSPACE_VERSION 4
+#define MOE_WORKSPACE_VERSION 5
 
 /* Fill `out` with the workspace layout for this shape and flags.  Regions a
  * mode does not use have offset UINT64_MAX.  Pure host call, no CUDA. */

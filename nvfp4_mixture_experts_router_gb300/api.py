@@ -34,6 +34,8 @@ MOE_GEMM_PAIRS_NEVER = 1 << 7
 MOE_GEMM_PAIRS_ALWAYS = 1 << 8
 MOE_QUANT_4OVER6 = 1 << 9
 MOE_FUSED_LAYER = 1 << 10
+MOE_GEMM_SWAP_NEVER = 1 << 11
+MOE_GEMM_SWAP_ALWAYS = 1 << 12
 MOE_W8A8_MXFP8 = 3 << 2
 
 
@@ -49,7 +51,7 @@ class moe_shape(ctypes.Structure):
 
 
 _LAYOUT_FIELDS = ["rows_cap", "status", "topk_ids", "topk_w", "count", "offsets", "padded_offsets", "meta",
-                  "unit_base", "unit_mask", "row_of_route", "route_of_row", "tile_expert", "tile_pair", "g1",
+                  "unit_base", "unit_mask", "row_of_route", "route_of_row", "tile_expert", "tile_pair", "tile_half", "g1",
                   "xq_codes", "xq_sf", "h_f32", "g2", "hq_codes", "hq_sf", "x_bf16_perm", "h_bf16", "o_bf16",
                   "y_acc", "total"]
 

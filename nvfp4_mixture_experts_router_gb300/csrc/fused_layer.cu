@@ -170,7 +170,7 @@ __device__ void phase_route(const FusedParams& fp) {
 // s_pair); CTA 0 publishes count / offsets / padded_offsets / meta.  Then
 // the per-expert outputs, expert e on CTA e % grid: the per-(expert, unit)
 // starting rows, the tile map, the pair list and -1 in the pad rows.
-__device__ void phase_scan(const FusedParams& fp, int* s_cnt, int* s_pad, int* s_pair) {
+__device__ void phase_scan(const FusedParams& fp, int* s_cnt, int* s_pad, int* s_pair, int* s_half) {
     const int U = (fp.T + kUnitTokens - 1) / kUnitTokens;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (U < 32) {
@@ -193,23 +193,26 @@ __device__ void phase_scan(const FusedParams& fp, int* s_cnt, int* s_pad, int* s
     }
     __syncthreads();
     if (warp == 0) {
-        int cc = 0, cp = 0, cq = 0;   // running totals of the earlier 32-expert groups
+        int cc = 0, cp = 0, cq = 0, ch = 0;   // running totals of the earlier 32-expert groups
         for (int e0 = 0; e0 < fp.E; e0 += 32) {
             const int e = e0 + lane;
             const int c = e < fp.E ? s_cnt[e] : 0;
             const int p = (c + kTileM - 1) / kTileM * kTileM;
             const int q = (p / kTileM + 1) / 2;
-            int ic = c, ip = p, iq = q;
+            const int hv = (c + kTileM / 2 - 1) / (kTileM / 2);
+            int ic = c, ip = p, iq = q, ih = hv;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int a = __shfl_up_sync(0xffffffffu, ic, o);
                 const int b = __shfl_up_sync(0xffffffffu, ip, o);
                 const int d = __shfl_up_sync(0xffffffffu, iq, o);
-                if (lane >= o) { ic += a; ip += b; iq += d; }
+                const int f = __shfl_up_sync(0xffffffffu, ih, o);
+                if (lane >= o) { ic += a; ip += b; iq += d; ih += f; }
             }
             if (e < fp.E) {
                 s_pad[e] = cp + ip - p;
                 s_pair[e] = cq + iq - q;
+                s_half[e] = ch + ih - hv;
                 if (blockIdx.x == 0) {
                     fp.count[e] = c;
                     fp.offsets[e] = cc + ic - c;
@@ -219,6 +222,7 @@ __device__ void phase_scan(const FusedParams& fp, int* s_cnt, int* s_pad, int* s
             cc += __shfl_sync(0xffffffffu, ic, 31);
             cp += __shfl_sync(0xffffffffu, ip, 31);
             cq += __shfl_sync(0xffffffffu, iq, 31);
+            ch += __shfl_sync(0xffffffffu, ih, 31);
         }
         if (lane == 0) {
             s_pad[fp.E] = cp;
@@ -228,6 +232,7 @@ __device__ void phase_scan(const FusedParams& fp, int* s_cnt, int* s_pad, int* s
                 fp.meta[0] = cp;
                 fp.meta[1] = cp / kTileM;
                 fp.meta[2] = cq;
+                fp.meta[3] = ch;
             }
         }
     }
@@ -254,6 +259,8 @@ __device__ void phase_scan(const FusedParams& fp, int* s_cnt, int* s_pad, int* s
         const int nt = pcnt / kTileM;
         for (int i = lane; 2 * i < nt; i += 32)
             fp.tile_pair[s_pair[e] + i] = ((r0 / kTileM + 2 * i) << 1) | (2 * i + 1 < nt ? 1 : 0);
+        const int nh = (cnt + kTileM / 2 - 1) / (kTileM / 2);
+        for (int j = lane; j < nh; j += 32) fp.tile_half[s_half[e] + j] = ((r0 / kTileM + (j >> 1)) << 1) | (j & 1);
     }
 }
 
@@ -503,6 +510,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     int* s_cnt = reinterpret_cast<int*>(s.a);
     int* s_pad = s_cnt + kFusedMaxExperts;          // E + 1 entries
     int* s_pair = s_pad + kFusedMaxExperts + 1;
+    int* s_half = s_pair + kFusedMaxExperts;
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tmA1);
         prefetch_tensormap(&tmB1);
@@ -517,7 +525,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     phase_route(fp);
     bool ok = grid_barrier(fp, ++nb, s.abort);
     if (ok) {
-        phase_scan(fp, s_cnt, s_pad, s_pair);
+        phase_scan(fp, s_cnt, s_pad, s_pair, s_half);
         if (!direct) ok = grid_barrier(fp, ++nb, s.abort);
     }
     if (ok) {

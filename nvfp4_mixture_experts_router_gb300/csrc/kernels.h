@@ -52,9 +52,9 @@ cudaError_t launch_route_count(const LaunchCtx& c, int T, int E, int K, const fl
 // masks); out-of-range or repeated ids become dropped routes (-1).
 cudaError_t launch_route_given(const LaunchCtx& c, int T, int E, int K, const int* ids_in, const float* w_in,
                                int* ids, float* w, int* unit_cnt, uint32_t* unit_mask, unsigned int* status);
-// tile_pair may be null (then only meta[2] counts the pairs)
+// tile_pair / tile_half may be null (then only meta[2] / meta[3] count them)
 cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
-                                int* padded_offsets, int* meta, int* tile_expert, int* tile_pair,
+                                int* padded_offsets, int* meta, int* tile_expert, int* tile_pair, int* tile_half,
                                 int* route_of_row);
 cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base,
                            uint32_t* unit_mask, int* count, int* offsets, int* padded_offsets, int* meta,
@@ -116,6 +116,7 @@ struct GemmParams {
     const int* meta;             // meta[1] = number of M tiles, meta[2] = M-tile pairs
     const int* tile_expert;      // expert of each M tile
     const int* tile_pair;        // (first M tile << 1) | has_second, per pair (pair kernel)
+    const int* tile_half;        // (M tile << 1) | half, per occupied 64-row half (swapped GEMM; meta[3] entries)
     const int* route_of_row;     // route of each padded row, -1 in pad rows
     int num_experts;             // E (bounds check of tile_expert)
     unsigned int* status;
@@ -153,6 +154,17 @@ cudaError_t setup_gemm_pair_kernels(int device, int num_sms);
 cudaError_t launch_gemm_nvf4_pair(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   const GemmParams& p, int device);
 
+// gemm_swap.cu — the W4A4 GEMMs with the weights on the MMA's M side (128
+// rows per operand, two operands per tile) and 64 routes on its N side, for
+// experts with few routes.  tmW: 3-D map over the prepared weights
+// (row bytes, 128 rows, blocks of 128 rows), box 128 B x 64 x 2; tmX: 2-D
+// map over the activation codes, box 128 B x 64 rows.  gated: FC1 SwiGLU
+// (needs n % 256 == 0).  Epilogues kEpiFc1Quant / kEpiFc1F32 / kEpiFc2Store /
+// kEpiFc2Scatter.
+cudaError_t setup_gemm_swap_kernels();
+cudaError_t launch_gemm_swap(const LaunchCtx& c, int epilogue, bool gated, const CUtensorMap& tmW,
+                             const CUtensorMap& tmX, const GemmParams& p, int num_sms);
+
 // fused_layer.cu — the whole W4A4 forward as one cooperative persistent
 // kernel (one CTA per SM); E <= kFusedMaxExperts.
 constexpr int kFusedMaxExperts = 256;
@@ -175,6 +187,7 @@ struct FusedParams {
     int* meta;
     int* tile_expert;
     int* tile_pair;
+    int* tile_half;
     int* row_of_route;
     int* route_of_row;
     // activations

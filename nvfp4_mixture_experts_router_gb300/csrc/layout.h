@@ -117,6 +117,7 @@ inline moe_workspace_layout workspace_layout(moe_shape s, uint32_t flags) {
     L.route_of_row = take(4 * cap);
     L.tile_expert = take(4 * (cap / kTileM));
     L.tile_pair = take(4 * (cap / kTileM));
+    L.tile_half = take(4 * 2 * (cap / kTileM));
     if (mode == kModeMxfp8) {
         // E4M3 codes, E8M0 scales per 32 (no global scales)
         L.xq_codes = take(cap * H);

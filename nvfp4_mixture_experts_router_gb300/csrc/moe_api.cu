@@ -43,7 +43,7 @@ moe_status device_state(int* sms, int* device = nullptr) {
             d.status = MOE_ERR_UNSUPPORTED;  // the binary carries sm_103a code only
         } else if (setup_routing_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess ||
                    setup_gemm_w4a16_kernels() != cudaSuccess || setup_gemm_pair_kernels(dev, d.sms) != cudaSuccess ||
-                   setup_fused_layer_kernel() != cudaSuccess) {
+                   setup_fused_layer_kernel() != cudaSuccess || setup_gemm_swap_kernels() != cudaSuccess) {
             d.status = MOE_ERR_CUDA;
         } else {
             d.status = MOE_OK;
@@ -76,6 +76,11 @@ moe_status validate_shape(moe_shape s, uint32_t flags) {
     if (flags & ~MOE_FLAGS_KNOWN) return MOE_ERR_INVALID_ARG;
     if ((flags & MOE_GEMM_PAIRS_NEVER) && (flags & MOE_GEMM_PAIRS_ALWAYS)) return MOE_ERR_INVALID_ARG;
     if ((flags & MOE_QUANT_4OVER6) && mode_of(flags) != kModePerToken) return MOE_ERR_INVALID_ARG;
+    if ((flags & MOE_GEMM_SWAP_NEVER) && (flags & MOE_GEMM_SWAP_ALWAYS)) return MOE_ERR_INVALID_ARG;
+    if ((flags & MOE_GEMM_SWAP_ALWAYS) &&
+        ((mode_of(flags) != kModePerTensor && mode_of(flags) != kModePerToken) ||
+         (flags & (MOE_GEMM_PAIRS_ALWAYS | MOE_FUSED_LAYER))))
+        return MOE_ERR_INVALID_ARG;
     if (flags & MOE_FUSED_LAYER) {
         // one persistent kernel: the NVFP4 activation modes, the router's
         // register layout (E <= 256) and single-CTA GEMM tiles
@@ -128,6 +133,39 @@ bool encode_chunk_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_
     return r == CUDA_SUCCESS;
 }
 
+// 3-D uint8 tensor map over prepared weight codes [rows][row_bytes] viewed
+// as [rows/128 blocks][128 rows][row_bytes], box 128 B x 64 rows x 2 blocks
+// (the swapped-orientation GEMM's weight operands).
+bool encode_swap_weight_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes) {
+    const cuuint64_t dims[3] = {row_bytes, 128, rows / 128};
+    const cuuint64_t strides[2] = {row_bytes, 128 * row_bytes};
+    const cuuint32_t box[3] = {128, 64, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Run the W4A4 GEMMs in the swapped orientation?  When asked to, or by
+// default when the experts that hold routes hold at most 64 on average
+// (their 128-row activation tiles would be half padding or more) and there
+// are at least 64 routes in all.  With fewer (a decode step of one token,
+// the 16-token tiny case) every CTA runs a single tile and the standard
+// kernel's 256-wide tile has the shorter fixed latency (measured on GB300:
+// T = 1 at the DSV3 shape 68.6 us standard vs 72.3 us swapped; T = 16
+// 452.7 vs 440.8; the mid workload 77.8 vs 74.9; T = 4096: 128 routes per
+// expert, standard).
+constexpr int64_t kSwapMaxRoutesPerExpert = 64;
+constexpr int64_t kSwapMinRoutes = 64;
+bool use_swap_gemm(moe_shape s, uint32_t flags) {
+    if (flags & MOE_GEMM_SWAP_ALWAYS) return true;
+    if (flags & (MOE_GEMM_SWAP_NEVER | MOE_GEMM_PAIRS_ALWAYS)) return false;
+    const int64_t routes = (int64_t)s.T * s.K;
+    const int64_t busy = routes < s.E ? routes : s.E;
+    return routes >= kSwapMinRoutes && routes <= kSwapMaxRoutesPerExpert * busy;
+}
+
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Run a W4A4 GEMM with `n` weight rows per expert on CTA pairs?  Only on
@@ -143,7 +181,7 @@ bool use_pair_gemm(moe_shape s, uint32_t flags, int n) {
 
 extern "C" {
 
-const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.3 sm_103a (prepared v1, workspace v4)"; }
+const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.4 sm_103a (prepared v1, workspace v5)"; }
 
 size_t moe_nvfp4_prepared_bytes(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return 0;
@@ -218,6 +256,7 @@ static moe_status forward_fused(moe_shape s, uint32_t flags, const void* x_bf16,
     f.meta = reinterpret_cast<int*>(wsp(W.meta));
     f.tile_expert = reinterpret_cast<int*>(wsp(W.tile_expert));
     f.tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
+    f.tile_half = reinterpret_cast<int*>(wsp(W.tile_half));
     f.row_of_route = reinterpret_cast<int*>(wsp(W.row_of_route));
     f.route_of_row = reinterpret_cast<int*>(wsp(W.route_of_row));
     f.x = static_cast<const __nv_bfloat16*>(x_bf16);
@@ -408,7 +447,8 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     e = launch_permute_scan(c, s.T, s.E, reinterpret_cast<int*>(wsp(W.unit_base)),
                             reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
                             reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert,
-                            reinterpret_cast<int*>(wsp(W.tile_pair)), route_of_row);
+                            reinterpret_cast<int*>(wsp(W.tile_pair)), reinterpret_cast<int*>(wsp(W.tile_half)),
+                            route_of_row);
     if (e != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
     // the quantize / gather kernel hands out the permuted rows itself
     RouteScatter rs;
@@ -501,7 +541,9 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
 
     // operand rows: NVFP4 half a byte per element, MXFP8 a byte
     const uint64_t rbx = mx ? (uint64_t)s.H : (uint64_t)s.H / 2, rbh = mx ? (uint64_t)s.I : (uint64_t)s.I / 2;
-    const bool pair1 = !mx && use_pair_gemm(s, flags, N1), pair2 = !mx && use_pair_gemm(s, flags, s.H);
+    const bool swap = !mx && use_swap_gemm(s, flags);
+    const bool pair1 = !mx && !swap && use_pair_gemm(s, flags, N1),
+               pair2 = !mx && !swap && use_pair_gemm(s, flags, s.H);
     const int tn1 = pair1 ? 128 : gemm_nvf4_tile_n(s.H, N1), tn2 = pair2 ? 128 : gemm_nvf4_tile_n(s.I, s.H);
     // single-CTA GEMMs with 128-wide tiles over rows of a multiple of 128
     // bytes copy two chunks per TMA instruction (3-D maps); the others use
@@ -509,16 +551,21 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     const bool ch1 = !pair1 && tn1 == 128 && rbx % 128 == 0;
     const bool ch2 = !pair2 && tn2 == 128 && rbh % 128 == 0;
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
-    const bool ok1 = ch1 ? (encode_chunk_map(&tmA1, xq_codes, W.rows_cap, rbx, 128) &&
+    const bool ok1 = swap ? (encode_operand_map(&tmA1, xq_codes, W.rows_cap, rbx, 128, 64) &&
+                             encode_swap_weight_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, rbx))
+                   : ch1 ? (encode_chunk_map(&tmA1, xq_codes, W.rows_cap, rbx, 128) &&
                             encode_chunk_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, rbx, tn1))
                          : (encode_operand_map(&tmA1, xq_codes, W.rows_cap, rbx) &&
                             encode_operand_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, rbx, 128, tn1));
-    const bool ok2 = ch2 ? (encode_chunk_map(&tmA2, hq_codes, W.rows_cap, rbh, 128) &&
+    const bool ok2 = swap ? (encode_operand_map(&tmA2, hq_codes, W.rows_cap, rbh, 128, 64) &&
+                             encode_swap_weight_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, rbh))
+                   : ch2 ? (encode_chunk_map(&tmA2, hq_codes, W.rows_cap, rbh, 128) &&
                             encode_chunk_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, rbh, tn2))
                          : (encode_operand_map(&tmA2, hq_codes, W.rows_cap, rbh) &&
                             encode_operand_map(&tmB2, pw + P.w2_codes, (uint64_t)s.E * s.H, rbh, 128, tn2));
     if (!ok1 || !ok2) return MOE_ERR_CUDA;
     int* tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
+    int* tile_half = reinterpret_cast<int*>(wsp(W.tile_half));
 
     GemmParams g1p{};
     g1p.sfa = xq_sf;
@@ -529,6 +576,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     g1p.meta = meta;
     g1p.tile_expert = tile_expert;
     g1p.tile_pair = tile_pair;
+    g1p.tile_half = tile_half;
     g1p.route_of_row = route_of_row;
     g1p.num_experts = s.E;
     g1p.status = status;
@@ -557,8 +605,9 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         g1p.out_sf = hq_sf;
         epi1 = kEpiFc1Quant;
     }
-    e = pair1 ? launch_gemm_nvf4_pair(c, epi1, tmA1, tmB1, g1p, device)
-              : launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms, tn1, mx ? 1 : 0);
+    e = swap    ? launch_gemm_swap(c, epi1, act == MOE_ACT_SWIGLU, tmB1, tmA1, g1p, sms)
+        : pair1 ? launch_gemm_nvf4_pair(c, epi1, tmA1, tmB1, g1p, device)
+                : launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms, tn1, mx ? 1 : 0);
     if (e != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
     if (per_token) {
         e = launch_quantize_h(c, W.rows_cap, s.I, meta, route_of_row, reinterpret_cast<const float*>(wsp(W.h_f32)),
@@ -576,6 +625,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     g2p.meta = meta;
     g2p.tile_expert = tile_expert;
     g2p.tile_pair = tile_pair;
+    g2p.tile_half = tile_half;
     g2p.route_of_row = route_of_row;
     g2p.num_experts = s.E;
     g2p.status = status;
@@ -603,8 +653,9 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         g2p.out_f32 = y_acc;
         epi2 = kEpiFc2Scatter;
     }
-    e = pair2 ? launch_gemm_nvf4_pair(c, epi2, tmA2, tmB2, g2p, device)
-              : launch_gemm_nvf4(c, epi2, tmA2, tmB2, g2p, sms, tn2, mx ? 1 : 0);
+    e = swap    ? launch_gemm_swap(c, epi2, false, tmB2, tmA2, g2p, sms)
+        : pair2 ? launch_gemm_nvf4_pair(c, epi2, tmA2, tmB2, g2p, device)
+                : launch_gemm_nvf4(c, epi2, tmA2, tmB2, g2p, sms, tn2, mx ? 1 : 0);
     if (e != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
 
     if (det)

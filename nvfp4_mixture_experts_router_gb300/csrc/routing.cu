@@ -156,11 +156,13 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
                                                             int* __restrict__ padded_offsets, int* __restrict__ meta,
                                                             int* __restrict__ tile_expert,
                                                             int* __restrict__ tile_pair,
+                                                            int* __restrict__ tile_half,
                                                             int* __restrict__ route_of_row) {
     __shared__ int s_cnt[1024];
     __shared__ int s_pad[1024];
     __shared__ int s_pair[1024];
-    __shared__ int s_warp[3][32];
+    __shared__ int s_half[1024];
+    __shared__ int s_warp[4][32];
     pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int U = (T + kUnitTokens - 1) / kUnitTokens;
@@ -173,45 +175,52 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
         if (lane == 0) s_cnt[e] = s;
     }
     __syncthreads();
-    // exclusive scans over experts of the count, the padded count and the
-    // number of M-tile pairs (ceil(tiles / 2))
+    // exclusive scans over experts of the count, the padded count, the
+    // number of M-tile pairs (ceil(tiles / 2)) and the number of 64-row
+    // halves holding routes (ceil(count / 64))
     const int c = tid < E ? s_cnt[tid] : 0;
     const int p = tid < E ? (c + kTileM - 1) / kTileM * kTileM : 0;
     const int q = (p / kTileM + 1) / 2;
-    int ic = c, ip = p, iq = q;
+    const int hv = (c + kTileM / 2 - 1) / (kTileM / 2);
+    int ic = c, ip = p, iq = q, ih = hv;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int a = __shfl_up_sync(0xffffffffu, ic, o);
         const int b = __shfl_up_sync(0xffffffffu, ip, o);
         const int d = __shfl_up_sync(0xffffffffu, iq, o);
-        if (lane >= o) { ic += a; ip += b; iq += d; }
+        const int f = __shfl_up_sync(0xffffffffu, ih, o);
+        if (lane >= o) { ic += a; ip += b; iq += d; ih += f; }
     }
-    if (lane == 31) { s_warp[0][warp] = ic; s_warp[1][warp] = ip; s_warp[2][warp] = iq; }
+    if (lane == 31) { s_warp[0][warp] = ic; s_warp[1][warp] = ip; s_warp[2][warp] = iq; s_warp[3][warp] = ih; }
     __syncthreads();
     if (warp == 0) {
-        int a = s_warp[0][lane], b = s_warp[1][lane], d = s_warp[2][lane];
+        int a = s_warp[0][lane], b = s_warp[1][lane], d = s_warp[2][lane], f = s_warp[3][lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int x = __shfl_up_sync(0xffffffffu, a, o);
             const int y = __shfl_up_sync(0xffffffffu, b, o);
             const int z = __shfl_up_sync(0xffffffffu, d, o);
-            if (lane >= o) { a += x; b += y; d += z; }
+            const int w = __shfl_up_sync(0xffffffffu, f, o);
+            if (lane >= o) { a += x; b += y; d += z; f += w; }
         }
         s_warp[0][lane] = a;
         s_warp[1][lane] = b;
         s_warp[2][lane] = d;
+        s_warp[3][lane] = f;
     }
     __syncthreads();
     const int base_c = warp > 0 ? s_warp[0][warp - 1] : 0;
     const int base_p = warp > 0 ? s_warp[1][warp - 1] : 0;
     const int base_q = warp > 0 ? s_warp[2][warp - 1] : 0;
-    const int ex_c = base_c + ic - c, ex_p = base_p + ip - p, ex_q = base_q + iq - q;
+    const int base_h = warp > 0 ? s_warp[3][warp - 1] : 0;
+    const int ex_c = base_c + ic - c, ex_p = base_p + ip - p, ex_q = base_q + iq - q, ex_h = base_h + ih - hv;
     if (tid < E) {
         count[tid] = c;
         offsets[tid] = ex_c;
         padded_offsets[tid] = ex_p;
         s_pad[tid] = ex_p;
         s_pair[tid] = ex_q;
+        s_half[tid] = ex_h;
     }
     if (tid == E - 1) {
         offsets[E] = ex_c + c;
@@ -219,6 +228,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
         meta[0] = ex_p + p;
         meta[1] = (ex_p + p) / kTileM;
         meta[2] = ex_q + q;
+        meta[3] = ex_h + hv;
     }
     __syncthreads();
     // per-(expert, unit) starting rows, tile map, pad rows
@@ -247,6 +257,11 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
             const int nt = pcnt / kTileM;
             for (int i = lane; 2 * i < nt; i += 32)
                 tile_pair[s_pair[e] + i] = ((r0 / kTileM + 2 * i) << 1) | (2 * i + 1 < nt ? 1 : 0);
+        }
+        if (tile_half != nullptr) {
+            // the 64-row halves of this expert's M tiles that hold routes, in order
+            const int nh = (cnt + kTileM / 2 - 1) / (kTileM / 2);
+            for (int j = lane; j < nh; j += 32) tile_half[s_half[e] + j] = ((r0 / kTileM + (j >> 1)) << 1) | (j & 1);
         }
     }
     pdl_launch_dependents();
@@ -298,10 +313,10 @@ cudaError_t launch_route_count(const LaunchCtx& c, int T, int E, int K, const fl
 }
 
 cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
-                                int* padded_offsets, int* meta, int* tile_expert, int* tile_pair,
+                                int* padded_offsets, int* meta, int* tile_expert, int* tile_pair, int* tile_half,
                                 int* route_of_row) {
     return c.launch(permute_scan_kernel, dim3(1), dim3(1024), 0, T, E, unit_base, count, offsets, padded_offsets,
-                    meta, tile_expert, tile_pair, route_of_row);
+                    meta, tile_expert, tile_pair, tile_half, route_of_row);
 }
 
 cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base,
@@ -313,7 +328,7 @@ cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* i
     err = c.launch(permute_count_kernel, dim3((U + 7) / 8), dim3(256), smem, T, E, K, ids, unit_base, unit_mask,
                    status);
     if (err != cudaSuccess) return err;
-    err = launch_permute_scan(c, T, E, unit_base, count, offsets, padded_offsets, meta, tile_expert, nullptr,
+    err = launch_permute_scan(c, T, E, unit_base, count, offsets, padded_offsets, meta, tile_expert, nullptr, nullptr,
                               route_of_row);
     if (err != cudaSuccess) return err;
     const int64_t routes = (int64_t)T * K;

@@ -133,6 +133,7 @@ class MoEConfig:
     gemm_pairs: str = "auto"      # GEMM tile scheduling: "auto" | "never" | "always"
     four_over_six: bool = False   # per-token W4A4: 4-over-6 activation quantization
     fused: bool = False           # W4A4: the whole forward as one persistent kernel
+    gemm_swap: str = "auto"       # W4A4 GEMM orientation: "auto" | "never" | "always"
     extra: dict = field(default_factory=dict)
 
     @property
@@ -155,6 +156,10 @@ class MoEConfig:
             f |= 1 << 9
         if self.fused:
             f |= 1 << 10
+        if self.gemm_swap == "never":
+            f |= 1 << 11
+        elif self.gemm_swap == "always":
+            f |= 1 << 12
         return f
 
     def with_(self, **kw) -> "MoEConfig":

@@ -164,6 +164,14 @@ def check_routing(layer: api.MoELayer, ref: oracle.Result):
     assert meta[2] == len(pairs), "M-tile pair count differs"
     got_pairs = layer.view("tile_pair", torch.int32, max(1, len(pairs))).cpu().numpy()[:len(pairs)]
     assert np.array_equal(got_pairs, np.array(pairs, dtype=np.int32)), "M-tile pair map differs"
+    # 64-row halves of the M tiles that hold routes, expert by expert, in order
+    halves = []
+    for e in range(E):
+        for j in range((int(g.count[e]) + 63) // 64):
+            halves.append(((int(g.padded_offsets[e]) // 128 + j // 2) << 1) | (j & 1))
+    assert meta[3] == len(halves), "occupied-half count differs"
+    got_halves = layer.view("tile_half", torch.int32, max(1, len(halves))).cpu().numpy()[:len(halves)]
+    assert np.array_equal(got_halves, np.array(halves, dtype=np.int32)), "occupied-half list differs"
     return ror
 
 

@@ -82,15 +82,43 @@ for T, H, I, E, K in [(1, 256, 128, 8, 2), (7, 384, 256, 8, 2), (129, 256, 128, 
                     MATRIX.append((T, H, I, E, K, mode, act, on_input, det))
 
 
-@pytest.mark.parametrize("T,H,I,E,K,mode,act,on_input,det", MATRIX)
-def test_matrix_parity(T, H, I, E, K, mode, act, on_input, det):
+MATRIX_ORIENT = [m + (sw,) for m in MATRIX for sw in (("never", "always") if m[5] != synth.MODE_W4A16 else ("auto",))]
+
+
+@pytest.mark.parametrize("T,H,I,E,K,mode,act,on_input,det,swap", MATRIX_ORIENT)
+def test_matrix_parity(T, H, I, E, K, mode, act, on_input, det, swap):
     """Token count x activation x placement x finalize x scaling mode x top-K
     x experts (the axes of the wrapper accuracy matrix, FlashInfer PR #4366,
-    "Tests"), small shapes with partial tiles, H=384 and empty experts."""
+    "Tests"), small shapes with partial tiles, H=384 and empty experts; the
+    W4A4 GEMMs in both operand orientations."""
     seed = (T * 31 + H + I + E * 7 + K * 3 + mode * 11 + act * 5 + on_input * 2 + det) % 1000
     c = synth.MoEConfig("m", T, H, I, E, K, act=act, mode=mode, router_on_input=on_input, deterministic=det,
-                        seed=seed, logits="normal")
+                        seed=seed, logits="normal", gemm_swap=swap)
     full_parity(c)
+
+
+SWAP = [(300, 512, 256, 4, 2, 0, 0, False, False),     # ~150 routes per expert: both 64-route halves
+        (300, 512, 256, 4, 2, 1, 1, True, True),
+        (97, 384, 384, 6, 3, 0, 1, False, True),       # ReLU2, I = 384: a 128-row tail weight tile
+        (97, 384, 384, 6, 3, 1, 0, True, False),       # rows of 192 bytes: a half K chunk
+        (1, 7168, 2048, 16, 8, 0, 0, False, True),     # one token, DSV3 widths
+        (64, 1024, 512, 256, 8, 1, 0, True, False)]    # E = 256, mostly one route per expert
+
+
+@pytest.mark.parametrize("T,H,I,E,K,mode,act,on_input,det", SWAP)
+def test_swapped_gemm_parity(T, H, I, E, K, mode, act, on_input, det):
+    """The W4A4 GEMMs with the weights on the MMA's M side (forced)."""
+    seed = (T * 7 + H + I * 3 + E + K + mode * 5 + act * 3 + det) % 1000
+    c = synth.MoEConfig("swap", T, H, I, E, K, act=act, mode=mode, router_on_input=on_input, deterministic=det,
+                        seed=seed, logits="normal", gemm_swap="always")
+    r = full_parity(c)
+    assert r["code_match"] >= 0.999
+
+
+@pytest.mark.parametrize("swap", ["never", "always"])
+def test_mid_config_parity_orientations(swap):
+    """The mid workload with the GEMM orientation forced either way."""
+    full_parity(synth.config(1).with_(gemm_swap=swap))
 
 
 WIDE = [(384, 4096, 0, 0, False, False), (384, 4096, 1, 1, True, True), (4096, 384, 0, 1, True, False),
@@ -332,10 +360,11 @@ def test_fused_layer_equals_launch_sequence(mode, act):
     inp.c = c.with_(fused=True)
     layer1, y1 = run_gpu(inp, G1, G2)
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
-    rows = int(layer0.view("meta", torch.int32, 4).cpu()[0])
-    for n in ["topk_ids", "topk_w", "row_of_route", "route_of_row", "tile_expert", "tile_pair", "meta"]:
-        nb = {"route_of_row": 4 * rows, "tile_expert": 4 * (rows // 128), "tile_pair": 4 * (rows // 128),
-              "meta": 12}.get(n, 4 * c.T * c.K)
+    meta0 = layer0.view("meta", torch.int32, 4).cpu()
+    rows, halves = int(meta0[0]), int(meta0[3])
+    for n in ["topk_ids", "topk_w", "row_of_route", "route_of_row", "tile_expert", "tile_pair", "tile_half", "meta"]:
+        nb = {"route_of_row": 4 * rows, "tile_expert": 4 * (rows // 128), "tile_pair": 4 * (int(meta0[2])),
+              "tile_half": 4 * halves, "meta": 16}.get(n, 4 * c.T * c.K)
         assert torch.equal(layer0.view(n, torch.uint8, nb), layer1.view(n, torch.uint8, nb)), n
     valid = layer0.view("route_of_row", torch.int32, rows) >= 0      # pad rows are never written
     per_row = [("xq_codes", c.H // 2), ("hq_codes", c.I // 2)]
