@@ -166,13 +166,31 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
     pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int U = (T + kUnitTokens - 1) / kUnitTokens;
-    // totals per expert
-    for (int e = warp; e < E; e += 32) {
-        int s = 0;
-        for (int u = lane; u < U; u += 32) s += unit_base[(size_t)e * U + u];
+    // totals per expert.  Up to kSmallU units (T <= 512): a thread per
+    // expert holds its unit counts in registers (independent loads) and
+    // later writes the unit starting rows from them; a warp per expert
+    // would chain E/32 dependent round trips per warp, twice.
+    constexpr int kSmallU = 16;
+    const bool small = U <= kSmallU;
+    int ucnt[kSmallU];
+    if (small) {
+        if (tid < E) {
+            int sum = 0;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) s_cnt[e] = s;
+            for (int u = 0; u < kSmallU; ++u) {
+                ucnt[u] = u < U ? unit_base[(size_t)tid * U + u] : 0;
+                sum += ucnt[u];
+            }
+            s_cnt[tid] = sum;
+        }
+    } else {
+        for (int e = warp; e < E; e += 32) {
+            int s = 0;
+            for (int u = lane; u < U; u += 32) s += unit_base[(size_t)e * U + u];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) s_cnt[e] = s;
+        }
     }
     __syncthreads();
     // exclusive scans over experts of the count, the padded count, the
@@ -232,9 +250,17 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
     }
     __syncthreads();
     // per-(expert, unit) starting rows, tile map, pad rows
+    if (small && tid < E) {
+        int run = s_pad[tid];
+#pragma unroll
+        for (int u = 0; u < kSmallU; ++u) {
+            if (u < U) unit_base[(size_t)tid * U + u] = run;
+            run += ucnt[u];
+        }
+    }
     for (int e = warp; e < E; e += 32) {
         int carry = s_pad[e];
-        for (int u0 = 0; u0 < U; u0 += 32) {
+        for (int u0 = 0; !small && u0 < U; u0 += 32) {
             const int u = u0 + lane;
             const int v = u < U ? unit_base[(size_t)e * U + u] : 0;
             int incl = v;
