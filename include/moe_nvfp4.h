@@ -238,7 +238,8 @@ MOE_API moe_status moe_nvfp4_forward_routed(moe_shape s, uint32_t flags,
  * (cudaEvent_t, created with timing enabled) on `stream` at the stage
  * boundaries, for per-stage timing:
  *   events[0] before the router, [1] after the router, [2] after the
- *   permutation, [3] after the activation quantization (W4A4) or gather
+ *   permutation (recorded right after [1] when T <= 32: one launch does
+ *   both), [3] after the activation quantization (W4A4) or gather
  *   (W4A16), [4] after FC1, [5] after the FC2-input quantization (recorded
  *   right after [4] when the mode has none), [6] after FC2, [7] after the
  *   finalize.  MOE_NUM_STAGE_EVENTS events, none NULL.
@@ -254,7 +255,10 @@ MOE_API moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags,
                                             void* y_bf16, void* stream, void* const* events);
 
 /* Number of kernel launches one moe_nvfp4_forward enqueues for this shape
- * and flags (-1 if invalid).  Pure host call. */
+ * and flags (-1 if invalid): 6 (7 with per-token scales), one fewer for
+ * T <= 32 (router and permutation scan in one launch), 1 for
+ * MOE_FUSED_LAYER.  moe_nvfp4_forward_routed always launches the scan
+ * separately.  Pure host call. */
 MOE_API int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags);
 
 /* Byte offsets of the intermediates inside the workspace (for tests and

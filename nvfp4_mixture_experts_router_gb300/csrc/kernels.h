@@ -52,6 +52,12 @@ cudaError_t launch_route_count(const LaunchCtx& c, int T, int E, int K, const fl
 // masks); out-of-range or repeated ids become dropped routes (-1).
 cudaError_t launch_route_given(const LaunchCtx& c, int T, int E, int K, const int* ids_in, const float* w_in,
                                int* ids, float* w, int* unit_cnt, uint32_t* unit_mask, unsigned int* status);
+// T <= 32 (one unit of tokens): router, unit masks and the scan in one
+// block (the outputs of launch_route_count + launch_permute_scan)
+cudaError_t launch_route_scan_small(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
+                                    int renorm, int* ids, float* w, int* unit_base, uint32_t* unit_mask, int* count,
+                                    int* offsets, int* padded_offsets, int* meta, int* tile_expert, int* tile_pair,
+                                    int* tile_half, int* route_of_row, unsigned int* status_reset);
 // tile_pair / tile_half may be null (then only meta[2] / meta[3] count them)
 cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
                                 int* padded_offsets, int* meta, int* tile_expert, int* tile_pair, int* tile_half,

@@ -438,18 +438,29 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         e = launch_route_given(c0, s.T, s.E, s.K, rin.ids, rin.w, ids, topk_w,
                                reinterpret_cast<int*>(wsp(W.unit_base)), reinterpret_cast<uint32_t*>(wsp(W.unit_mask)),
                                status);
+    } else if (s.T <= kUnitTokens) {
+        // one unit of tokens: router and scan in one block
+        e = launch_route_scan_small(c, s.T, s.E, s.K, rin.logits, rin.bias, (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1,
+                                    ids, topk_w, reinterpret_cast<int*>(wsp(W.unit_base)),
+                                    reinterpret_cast<uint32_t*>(wsp(W.unit_mask)), reinterpret_cast<int*>(wsp(W.count)),
+                                    reinterpret_cast<int*>(wsp(W.offsets)), reinterpret_cast<int*>(wsp(W.padded_offsets)),
+                                    meta, tile_expert, reinterpret_cast<int*>(wsp(W.tile_pair)),
+                                    reinterpret_cast<int*>(wsp(W.tile_half)), route_of_row, status);
     } else {
         e = launch_route_count(c, s.T, s.E, s.K, rin.logits, rin.bias, (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1, ids,
                                topk_w, reinterpret_cast<int*>(wsp(W.unit_base)),
                                reinterpret_cast<uint32_t*>(wsp(W.unit_mask)), status);
     }
     if (e != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
-    e = launch_permute_scan(c, s.T, s.E, reinterpret_cast<int*>(wsp(W.unit_base)),
-                            reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
-                            reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert,
-                            reinterpret_cast<int*>(wsp(W.tile_pair)), reinterpret_cast<int*>(wsp(W.tile_half)),
-                            route_of_row);
-    if (e != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
+    if (given || s.T > kUnitTokens) {
+        e = launch_permute_scan(c, s.T, s.E, reinterpret_cast<int*>(wsp(W.unit_base)),
+                                reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
+                                reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert,
+                                reinterpret_cast<int*>(wsp(W.tile_pair)), reinterpret_cast<int*>(wsp(W.tile_half)),
+                                route_of_row);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (!mark(2)) return MOE_ERR_CUDA;
     // the quantize / gather kernel hands out the permuted rows itself
     RouteScatter rs;
     rs.topk_ids = ids;
@@ -707,6 +718,8 @@ moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags, const void* x_b
 int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return -1;
     if (flags & MOE_FUSED_LAYER) return 1;
+    // T <= 32: router and scan in one launch
+    if (s.T <= kUnitTokens) return 5 + (mode_of(flags) == kModePerToken ? 1 : 0);
     // router + unit counts, scan, quantize or gather (+ row scatter), FC1, [FC2-input quant], FC2, finalize
     return 6 + (mode_of(flags) == kModePerToken ? 1 : 0);
 }

@@ -148,16 +148,115 @@ __global__ void __launch_bounds__(256) route_given_kernel(int T, int E, int K, c
     pdl_launch_dependents();
 }
 
+// Outputs of the permutation scan (step 2).  tile_pair / tile_half may be
+// null (then only meta[2] / meta[3] count them).
+struct ScanOut {
+    int* count;
+    int* offsets;
+    int* padded_offsets;
+    int* meta;
+    int* tile_expert;
+    int* tile_pair;
+    int* tile_half;
+    int* route_of_row;
+};
+
+// By a block of 1024 threads, given the per-expert route counts s_cnt[E]:
+// exclusive scans over experts of the count, the 128-padded count, the
+// number of M-tile pairs (ceil(tiles / 2)) and the number of 64-row halves
+// holding routes (ceil(count / 64)); publishes count / offsets /
+// padded_offsets / meta and leaves the padded offsets, pair and half
+// offsets in shared memory (ends with a block barrier).
+__device__ __forceinline__ void scan_experts_block(int E, const int* s_cnt, int* s_pad, int* s_pair, int* s_half,
+                                                   int (*s_warp)[32], const ScanOut& o) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = tid < E ? s_cnt[tid] : 0;
+    const int p = tid < E ? (c + kTileM - 1) / kTileM * kTileM : 0;
+    const int q = (p / kTileM + 1) / 2;
+    const int hv = (c + kTileM / 2 - 1) / (kTileM / 2);
+    int ic = c, ip = p, iq = q, ih = hv;
+#pragma unroll
+    for (int k = 1; k < 32; k <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, ic, k);
+        const int b = __shfl_up_sync(0xffffffffu, ip, k);
+        const int d = __shfl_up_sync(0xffffffffu, iq, k);
+        const int f = __shfl_up_sync(0xffffffffu, ih, k);
+        if (lane >= k) { ic += a; ip += b; iq += d; ih += f; }
+    }
+    if (lane == 31) { s_warp[0][warp] = ic; s_warp[1][warp] = ip; s_warp[2][warp] = iq; s_warp[3][warp] = ih; }
+    __syncthreads();
+    if (warp == 0) {
+        int a = s_warp[0][lane], b = s_warp[1][lane], d = s_warp[2][lane], f = s_warp[3][lane];
+#pragma unroll
+        for (int k = 1; k < 32; k <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, a, k);
+            const int y = __shfl_up_sync(0xffffffffu, b, k);
+            const int z = __shfl_up_sync(0xffffffffu, d, k);
+            const int w = __shfl_up_sync(0xffffffffu, f, k);
+            if (lane >= k) { a += x; b += y; d += z; f += w; }
+        }
+        s_warp[0][lane] = a;
+        s_warp[1][lane] = b;
+        s_warp[2][lane] = d;
+        s_warp[3][lane] = f;
+    }
+    __syncthreads();
+    const int base_c = warp > 0 ? s_warp[0][warp - 1] : 0;
+    const int base_p = warp > 0 ? s_warp[1][warp - 1] : 0;
+    const int base_q = warp > 0 ? s_warp[2][warp - 1] : 0;
+    const int base_h = warp > 0 ? s_warp[3][warp - 1] : 0;
+    const int ex_c = base_c + ic - c, ex_p = base_p + ip - p, ex_q = base_q + iq - q, ex_h = base_h + ih - hv;
+    if (tid < E) {
+        o.count[tid] = c;
+        o.offsets[tid] = ex_c;
+        o.padded_offsets[tid] = ex_p;
+        s_pad[tid] = ex_p;
+        s_pair[tid] = ex_q;
+        s_half[tid] = ex_h;
+    }
+    if (tid == E - 1) {
+        o.offsets[E] = ex_c + c;
+        o.padded_offsets[E] = ex_p + p;
+        o.meta[0] = ex_p + p;
+        o.meta[1] = (ex_p + p) / kTileM;
+        o.meta[2] = ex_q + q;
+        o.meta[3] = ex_h + hv;
+    }
+    __syncthreads();
+}
+
+// Per-expert outputs of the scan, a warp per expert: -1 in the pad rows of
+// its segment, the M-tile -> expert map, its M-tile pairs and its occupied
+// 64-row halves.
+__device__ __forceinline__ void expert_outputs_block(int E, const int* s_cnt, const int* s_pad, const int* s_pair,
+                                                     const int* s_half, const ScanOut& o) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int e = warp; e < E; e += nwarps) {
+        const int cnt = s_cnt[e];
+        const int pcnt = (cnt + kTileM - 1) / kTileM * kTileM;
+        const int r0 = s_pad[e];
+        for (int r = r0 + cnt + lane; r < r0 + pcnt; r += 32) o.route_of_row[r] = -1;
+        for (int tl = r0 / kTileM + lane; tl < (r0 + pcnt) / kTileM; tl += 32) o.tile_expert[tl] = e;
+        if (o.tile_pair != nullptr) {
+            // pairs of consecutive M tiles of this expert; an odd count leaves
+            // the last tile alone
+            const int nt = pcnt / kTileM;
+            for (int i = lane; 2 * i < nt; i += 32)
+                o.tile_pair[s_pair[e] + i] = ((r0 / kTileM + 2 * i) << 1) | (2 * i + 1 < nt ? 1 : 0);
+        }
+        if (o.tile_half != nullptr) {
+            // the 64-row halves of this expert's M tiles that hold routes, in order
+            const int nh = (cnt + kTileM / 2 - 1) / (kTileM / 2);
+            for (int j = lane; j < nh; j += 32) o.tile_half[s_half[e] + j] = ((r0 / kTileM + (j >> 1)) << 1) | (j & 1);
+        }
+    }
+}
+
 // (2) one block of 1024 threads: totals, offsets, padded offsets, per-unit
 // starting rows (in place of the counts), M-tile -> expert map, pad rows of
 // route_of_row set to -1.
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* __restrict__ unit_base /* [E][U] */,
-                                                            int* __restrict__ count, int* __restrict__ offsets,
-                                                            int* __restrict__ padded_offsets, int* __restrict__ meta,
-                                                            int* __restrict__ tile_expert,
-                                                            int* __restrict__ tile_pair,
-                                                            int* __restrict__ tile_half,
-                                                            int* __restrict__ route_of_row) {
+                                                            const ScanOut o) {
     __shared__ int s_cnt[1024];
     __shared__ int s_pad[1024];
     __shared__ int s_pair[1024];
@@ -193,63 +292,8 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
         }
     }
     __syncthreads();
-    // exclusive scans over experts of the count, the padded count, the
-    // number of M-tile pairs (ceil(tiles / 2)) and the number of 64-row
-    // halves holding routes (ceil(count / 64))
-    const int c = tid < E ? s_cnt[tid] : 0;
-    const int p = tid < E ? (c + kTileM - 1) / kTileM * kTileM : 0;
-    const int q = (p / kTileM + 1) / 2;
-    const int hv = (c + kTileM / 2 - 1) / (kTileM / 2);
-    int ic = c, ip = p, iq = q, ih = hv;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, ic, o);
-        const int b = __shfl_up_sync(0xffffffffu, ip, o);
-        const int d = __shfl_up_sync(0xffffffffu, iq, o);
-        const int f = __shfl_up_sync(0xffffffffu, ih, o);
-        if (lane >= o) { ic += a; ip += b; iq += d; ih += f; }
-    }
-    if (lane == 31) { s_warp[0][warp] = ic; s_warp[1][warp] = ip; s_warp[2][warp] = iq; s_warp[3][warp] = ih; }
-    __syncthreads();
-    if (warp == 0) {
-        int a = s_warp[0][lane], b = s_warp[1][lane], d = s_warp[2][lane], f = s_warp[3][lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, a, o);
-            const int y = __shfl_up_sync(0xffffffffu, b, o);
-            const int z = __shfl_up_sync(0xffffffffu, d, o);
-            const int w = __shfl_up_sync(0xffffffffu, f, o);
-            if (lane >= o) { a += x; b += y; d += z; f += w; }
-        }
-        s_warp[0][lane] = a;
-        s_warp[1][lane] = b;
-        s_warp[2][lane] = d;
-        s_warp[3][lane] = f;
-    }
-    __syncthreads();
-    const int base_c = warp > 0 ? s_warp[0][warp - 1] : 0;
-    const int base_p = warp > 0 ? s_warp[1][warp - 1] : 0;
-    const int base_q = warp > 0 ? s_warp[2][warp - 1] : 0;
-    const int base_h = warp > 0 ? s_warp[3][warp - 1] : 0;
-    const int ex_c = base_c + ic - c, ex_p = base_p + ip - p, ex_q = base_q + iq - q, ex_h = base_h + ih - hv;
-    if (tid < E) {
-        count[tid] = c;
-        offsets[tid] = ex_c;
-        padded_offsets[tid] = ex_p;
-        s_pad[tid] = ex_p;
-        s_pair[tid] = ex_q;
-        s_half[tid] = ex_h;
-    }
-    if (tid == E - 1) {
-        offsets[E] = ex_c + c;
-        padded_offsets[E] = ex_p + p;
-        meta[0] = ex_p + p;
-        meta[1] = (ex_p + p) / kTileM;
-        meta[2] = ex_q + q;
-        meta[3] = ex_h + hv;
-    }
-    __syncthreads();
-    // per-(expert, unit) starting rows, tile map, pad rows
+    scan_experts_block(E, s_cnt, s_pad, s_pair, s_half, s_warp, o);
+    // per-(expert, unit) starting rows
     if (small && tid < E) {
         int run = s_pad[tid];
 #pragma unroll
@@ -258,38 +302,61 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
             run += ucnt[u];
         }
     }
-    for (int e = warp; e < E; e += 32) {
+    for (int e = warp; !small && e < E; e += 32) {
         int carry = s_pad[e];
-        for (int u0 = 0; !small && u0 < U; u0 += 32) {
+        for (int u0 = 0; u0 < U; u0 += 32) {
             const int u = u0 + lane;
             const int v = u < U ? unit_base[(size_t)e * U + u] : 0;
             int incl = v;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int a = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += a;
+            for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                const int a = __shfl_up_sync(0xffffffffu, incl, o2);
+                if (lane >= o2) incl += a;
             }
             if (u < U) unit_base[(size_t)e * U + u] = carry + incl - v;
             carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        const int cnt = s_cnt[e];
-        const int pcnt = (cnt + kTileM - 1) / kTileM * kTileM;
-        const int r0 = s_pad[e];
-        for (int r = r0 + cnt + lane; r < r0 + pcnt; r += 32) route_of_row[r] = -1;
-        for (int tl = r0 / kTileM + lane; tl < (r0 + pcnt) / kTileM; tl += 32) tile_expert[tl] = e;
-        if (tile_pair != nullptr) {
-            // pairs of consecutive M tiles of this expert; an odd count leaves
-            // the last tile alone
-            const int nt = pcnt / kTileM;
-            for (int i = lane; 2 * i < nt; i += 32)
-                tile_pair[s_pair[e] + i] = ((r0 / kTileM + 2 * i) << 1) | (2 * i + 1 < nt ? 1 : 0);
-        }
-        if (tile_half != nullptr) {
-            // the 64-row halves of this expert's M tiles that hold routes, in order
-            const int nh = (cnt + kTileM / 2 - 1) / (kTileM / 2);
-            for (int j = lane; j < nh; j += 32) tile_half[s_half[e] + j] = ((r0 / kTileM + (j >> 1)) << 1) | (j & 1);
-        }
     }
+    expert_outputs_block(E, s_cnt, s_pad, s_pair, s_half, o);
+    pdl_launch_dependents();
+}
+
+// Steps (1) and (2) in one block for T <= 32 (a single unit of tokens):
+// the router (a warp per token), the expert token masks in shared memory,
+// their counts and the scan, without the masks' round trip through memory
+// and the second launch.  Same outputs as route_count_kernel followed by
+// permute_scan_kernel.
+template <int EPL>
+__global__ void __launch_bounds__(1024) route_scan_small_kernel(int T, int E, int K, const float* __restrict__ logits,
+                                                                const float* __restrict__ bias, int renorm,
+                                                                int* __restrict__ topk_ids, float* __restrict__ topk_w,
+                                                                int* __restrict__ unit_base, uint32_t* __restrict__ unit_mask,
+                                                                const ScanOut o, unsigned int* status_reset) {
+    __shared__ uint32_t s_mask[1024];
+    __shared__ int s_cnt[1024];
+    __shared__ int s_pad[1024];
+    __shared__ int s_pair[1024];
+    __shared__ int s_half[1024];
+    __shared__ int s_warp[4][32];
+    pdl_wait();
+    if (status_reset && threadIdx.x == 0) *status_reset = 0u;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int e = tid; e < E; e += blockDim.x) s_mask[e] = 0u;
+    __syncthreads();
+    if (warp < T) {
+        const int e = route_token<EPL>(warp, E, K, logits, bias, renorm, topk_ids, topk_w);
+        if (e >= 0) atomicOr(&s_mask[e], 1u << warp);
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        const uint32_t m = s_mask[e];
+        unit_mask[e] = m;            // [E][1]
+        s_cnt[e] = __popc(m);
+    }
+    __syncthreads();
+    scan_experts_block(E, s_cnt, s_pad, s_pair, s_half, s_warp, o);
+    for (int e = tid; e < E; e += blockDim.x) unit_base[e] = s_pad[e];   // one unit: its start is the segment's
+    expert_outputs_block(E, s_cnt, s_pad, s_pair, s_half, o);
     pdl_launch_dependents();
 }
 
@@ -341,8 +408,18 @@ cudaError_t launch_route_count(const LaunchCtx& c, int T, int E, int K, const fl
 cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
                                 int* padded_offsets, int* meta, int* tile_expert, int* tile_pair, int* tile_half,
                                 int* route_of_row) {
-    return c.launch(permute_scan_kernel, dim3(1), dim3(1024), 0, T, E, unit_base, count, offsets, padded_offsets,
-                    meta, tile_expert, tile_pair, tile_half, route_of_row);
+    const ScanOut o{count, offsets, padded_offsets, meta, tile_expert, tile_pair, tile_half, route_of_row};
+    return c.launch(permute_scan_kernel, dim3(1), dim3(1024), 0, T, E, unit_base, o);
+}
+
+cudaError_t launch_route_scan_small(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
+                                    int renorm, int* ids, float* w, int* unit_base, uint32_t* unit_mask, int* count,
+                                    int* offsets, int* padded_offsets, int* meta, int* tile_expert, int* tile_pair,
+                                    int* tile_half, int* route_of_row, unsigned int* status_reset) {
+    if (T > kUnitTokens) return cudaErrorInvalidValue;
+    const ScanOut o{count, offsets, padded_offsets, meta, tile_expert, tile_pair, tile_half, route_of_row};
+    MOE_EPL_DISPATCH(E, route_scan_small_kernel, dim3(1), dim3(1024), 0, T, E, K, logits, bias, renorm, ids, w,
+                     unit_base, unit_mask, o, status_reset);
 }
 
 cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base,

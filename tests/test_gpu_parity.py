@@ -388,3 +388,16 @@ def test_mid_config_parity_fused():
     """The mid workload (T=512, H=2048, I=768, E=64, top-6, per-token) as
     one persistent kernel."""
     full_parity(synth.config(1).with_(fused=True))
+
+
+@pytest.mark.parametrize("T,E,K,bias,renorm", [(1, 256, 8, "none", True), (20, 64, 6, "normal", False),
+                                               (32, 256, 8, "zipf", True), (33, 16, 4, "normal", True)])
+def test_small_T_router_and_scan(T, E, K, bias, renorm):
+    """T <= 32 runs the router and the permutation scan in one block
+    (T = 33 the two launches): ids, weights, offsets, tile, pair and half
+    lists bit for bit, with a logit bias and the full-softmax weights."""
+    c = synth.MoEConfig("small", T, 256, 128, E, K, mode=synth.MODE_PER_TOKEN, seed=T + E, logits="normal",
+                        bias=bias, renorm=renorm)
+    full_parity(c)
+    s = api.shape(T, 256, 128, E, K)
+    assert api.moe_nvfp4_forward_launches(s, c.flags()) == (6 if T <= 32 else 7)
