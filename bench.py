@@ -4,7 +4,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload mid|tiny|dsv3|w4a16|prefill] [--tokens T]
                     [--precision nvfp4|mxfp8] [--four-over-six] [--routing logits|given]
-                    [--fused] [--gemm auto|standard|swapped]
+                    [--fused] [--gemm auto|standard|swapped|pairs]
 
 A step is one full layer forward (router, permutation, activation
 quantization, FC1 + activation + requantization, FC2, finalize) over one
@@ -62,8 +62,8 @@ def parse():
                    help="given: caller-supplied top-K ids and weights (moe_nvfp4_forward_routed)")
     p.add_argument("--fused", action="store_true",
                    help="the whole forward as one persistent kernel (MOE_FUSED_LAYER; W4A4, E <= 256)")
-    p.add_argument("--gemm", default="auto", choices=["auto", "standard", "swapped"],
-                   help="W4A4 GEMM operand orientation (default: by routes per expert)")
+    p.add_argument("--gemm", default="auto", choices=["auto", "standard", "swapped", "pairs"],
+                   help="W4A4 GEMM variant: operand orientation (default: by routes per expert) or CTA pairs")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -84,7 +84,9 @@ def workload_config(name, tokens, precision="nvfp4", four_over_six=False, fused=
         if c.mode not in (synth.MODE_PER_TENSOR, synth.MODE_PER_TOKEN) or c.E > 256:
             raise SystemExit("--fused needs a W4A4 workload with E <= 256")
         c = c.with_(fused=True)
-    if gemm != "auto":
+    if gemm == "pairs":
+        c = c.with_(gemm_pairs="always", gemm_swap="never")
+    elif gemm != "auto":
         c = c.with_(gemm_swap="always" if gemm == "swapped" else "never")
     return c
 

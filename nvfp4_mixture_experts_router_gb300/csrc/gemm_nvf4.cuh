@@ -148,6 +148,25 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 
 // Pipeline position of one role thread; carried from one gemm_tiles call to
 // the next when a kernel runs several GEMMs on one pipeline.
+// Tile index -> (M tile, N tile).  Default: N tiles fastest over the whole
+// output width.  With slabs of n_slab N tiles (p.n_slab > 0), the width is
+// walked slab by slab and every M tile runs within a slab before the next:
+// the fused-finalize scatter then keeps adding into one slab of the output
+// accumulator, which stays in L2 when the accumulator as a whole does not.
+__device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int n_tiles, int num_m_tiles, int& m_tile,
+                                            int& n_tile) {
+    if (p.n_slab <= 0) {
+        m_tile = tile / n_tiles;
+        n_tile = tile % n_tiles;
+        return;
+    }
+    const int per_slab = num_m_tiles * p.n_slab;
+    const int slab = tile / per_slab, rem = tile % per_slab;
+    const int width = min(p.n_slab, n_tiles - slab * p.n_slab);   // the last slab may be narrower
+    m_tile = rem / width;
+    n_tile = slab * p.n_slab + rem % width;
+}
+
 struct RingState {
     int stage = 0;
     uint32_t phase = 0;
@@ -209,10 +228,14 @@ __device__ __forceinline__ bool gemm_tiles(const Smem& s, uint32_t tmem_base, co
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_normal();
+            // slabs: the activation rows are re-read once per slab; evict them
+            // first so that the slab of the accumulator stays in L2
+            const uint64_t pol_a = p.n_slab > 0 ? policy_evict_first() : pol;
             int stage = rs.stage;
             uint32_t phase = rs.phase;
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-                const int m_tile = tile / n_tiles, n_tile = tile % n_tiles;
+                int m_tile, n_tile;
+                decode_tile(p, tile, n_tiles, num_m_tiles, m_tile, n_tile);
                 const int e = p.tile_expert[m_tile];
                 if (e < 0 || e >= p.num_experts) {
                     atomicOr(p.status, kStatusBadExpert);
@@ -245,7 +268,7 @@ __device__ __forceinline__ bool gemm_tiles(const Smem& s, uint32_t tmem_base, co
                         // one copy per operand; a chunk past the row end is filled
                         // with zeros and skipped by the MMAs
                         mbar_arrive_expect_tx(&s.full[stage], C::kTileBytesA + C::kTileBytesB);
-                        tma_load_3d(a_dst, tmA, &s.full[stage], 0, a_row, c0, pol);
+                        tma_load_3d(a_dst, tmA, &s.full[stage], 0, a_row, c0, pol_a);
                         tma_load_3d(b_dst, tmB, &s.full[stage], 0, b_row, c0, pol);
                     } else {
                         // rows of 64 + 128 j bytes: one 2-D copy per chunk that
@@ -254,7 +277,7 @@ __device__ __forceinline__ bool gemm_tiles(const Smem& s, uint32_t tmem_base, co
                         mbar_arrive_expect_tx(&s.full[stage], (uint32_t)nch * (kChunkBytesA + C::kChunkBytesB));
                         for (int c = 0; c < nch; ++c) {
                             tma_load_2d(a_dst + c * kChunkBytesA, tmA, &s.full[stage], (c0 + c) * kChunkBytes, a_row,
-                                        pol);
+                                        pol_a);
                             tma_load_2d(b_dst + c * C::kChunkBytesB, tmB, &s.full[stage], (c0 + c) * kChunkBytes,
                                         b_row, pol);
                         }
@@ -272,7 +295,8 @@ __device__ __forceinline__ bool gemm_tiles(const Smem& s, uint32_t tmem_base, co
             int acc = rs.acc;
             uint32_t acc_phase = rs.acc_phase;
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-                const int n_tile = tile % n_tiles;
+                int m_tile, n_tile;
+                decode_tile(p, tile, n_tiles, num_m_tiles, m_tile, n_tile);
                 const int width = min(BN, p.n - n_tile * BN);
                 const uint32_t idesc = idesc_nvf4(kBM, width);   // NVFP4 (MXFP8 builds its own per MMA)
                 if (!mbar_wait(&s.acc_empty[acc], acc_phase ^ 1u, s.abort, p.status, kStatusTimeoutMma)) return false;
@@ -363,7 +387,8 @@ __device__ __forceinline__ bool gemm_tiles(const Smem& s, uint32_t tmem_base, co
         int acc = rs.acc;
         uint32_t acc_phase = rs.acc_phase;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const int m_tile = tile / n_tiles, n_tile = tile % n_tiles;
+            int m_tile, n_tile;
+            decode_tile(p, tile, n_tiles, num_m_tiles, m_tile, n_tile);
             const int e = p.tile_expert[m_tile];
             if (e < 0 || e >= p.num_experts) break;
             // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction

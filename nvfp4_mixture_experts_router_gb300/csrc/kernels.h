@@ -119,6 +119,7 @@ struct GemmParams {
     int kdim;                    // reduction length (elements)
     int chunk_maps;              // 1: tmA / tmB are 3-D chunk maps (rows of a multiple of 128 bytes)
     int n;                       // output columns per expert (B rows per expert)
+    int n_slab;                  // > 0: walk the output width in slabs of n_slab N tiles (standard kernel)
     const int* meta;             // meta[1] = number of M tiles, meta[2] = M-tile pairs
     const int* tile_expert;      // expert of each M tile
     const int* tile_pair;        // (first M tile << 1) | has_second, per pair (pair kernel)

@@ -75,3 +75,12 @@ def test_prefill_T16384_single_kernel():
     through the single persistent kernel: the same kernel at 16384 tokens."""
     r = fullsize_parity(synth.config(4).with_(fused=True), n_tokens=16)
     assert r["code_match"] >= 0.999
+
+
+def test_fc2_output_slabs():
+    """Fused finalize with an accumulator beyond half the L2 (T x H x 4 B =
+    73 MB): FC2 walks its output width in slabs (51 and 5 N tiles here, a
+    narrower last slab) so a token's reductions stay in L2; same results."""
+    c = synth.MoEConfig("slab", 2560, 7168, 256, 8, 2, mode=synth.MODE_PER_TOKEN, seed=12, logits="normal")
+    r = fullsize_parity(c, n_tokens=24)
+    assert r["code_match"] >= 0.999
