@@ -64,11 +64,14 @@ def parse():
                    help="the whole forward as one persistent kernel (MOE_FUSED_LAYER; W4A4, E <= 256)")
     p.add_argument("--gemm", default="auto", choices=["auto", "standard", "swapped", "pairs"],
                    help="W4A4 GEMM variant: operand orientation (default: by routes per expert) or CTA pairs")
+    p.add_argument("--finalize", default="config", choices=["config", "fused", "deterministic"],
+                   help="finalize mode: the workload's own (default), the FC2-epilogue scatter or the fixed-order kernel")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
 
-def workload_config(name, tokens, precision="nvfp4", four_over_six=False, fused=False, gemm="auto"):
+def workload_config(name, tokens, precision="nvfp4", four_over_six=False, fused=False, gemm="auto",
+                    finalize="config"):
     from nvfp4_mixture_experts_router_gb300 import synth
     idx = {"tiny": 0, "mid": 1, "dsv3": 2, "w4a16": 3, "prefill": 4}[name]
     c = synth.config(idx, tokens)
@@ -88,6 +91,8 @@ def workload_config(name, tokens, precision="nvfp4", four_over_six=False, fused=
         c = c.with_(gemm_pairs="always", gemm_swap="never")
     elif gemm != "auto":
         c = c.with_(gemm_swap="always" if gemm == "swapped" else "never")
+    if finalize != "config":
+        c = c.with_(deterministic=finalize == "deterministic")
     return c
 
 
@@ -143,7 +148,7 @@ def stage_bytes(c, active):
 
 def traffic_for(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+    on the current source of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(path))
@@ -152,7 +157,7 @@ def traffic_for(kernel, workload):
     e = d.get(f"{workload}:{kernel}")
     if not e:
         return None
-    if e.get("source_sha") != source_sha():
+    if e.get("source_sha") != source_sha(e.get("source")):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -167,15 +172,32 @@ def traffic_key(args):
         key += "-4over6"
     if args.fused:
         key += "-fused"
+    if args.finalize != "config":
+        key += "-" + args.finalize
     return key
 
 
-def source_sha():
-    h = hashlib.sha256()
+def source_sha(unit=None):
+    """Hash of the kernel sources: one translation unit of csrc/ and every
+    header it includes (transitively), or all of csrc/ when unit is None."""
     csrc = os.path.join(ROOT, "nvfp4_mixture_experts_router_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    if unit is None:
+        files = [os.path.join(csrc, f) for f in sorted(os.listdir(csrc)) if f.endswith((".cu", ".cuh", ".h"))]
+    else:
+        files, todo = [], [os.path.join(csrc, unit)]
+        while todo:
+            f = os.path.normpath(todo.pop())
+            if f in files or not os.path.exists(f):
+                continue
+            files.append(f)
+            for line in open(f, encoding="utf-8", errors="replace"):
+                line = line.strip()
+                if line.startswith("#include \""):
+                    todo.append(os.path.join(os.path.dirname(f), line.split('"')[1]))
+        files.sort()
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -596,7 +618,8 @@ def run_ours(args, c, world, rank, local):
 def main():
     args = parse()
     world, rank, local = init_dist(args)
-    c = workload_config(args.workload, args.tokens, args.precision, args.four_over_six, args.fused, args.gemm)
+    c = workload_config(args.workload, args.tokens, args.precision, args.four_over_six, args.fused, args.gemm,
+                        args.finalize)
     if args.impl == "reference":
         run_reference(args, c, world, rank)
     else:
