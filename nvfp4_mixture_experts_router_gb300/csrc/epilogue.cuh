@@ -94,9 +94,51 @@ __device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr
     }
 }
 
-template <int EPI>
+// Row segments through a per-warp shared-memory block.  After the
+// tensor-memory load, lane r holds the words of route row r, so a global
+// access issued straight from registers sends the 32 lanes to 32 different
+// rows, 16 bytes each: every 32-byte L2 sector of a red or a store then
+// carries half a sector.  Here each warp writes COLS words of its 32 rows
+// into its block, row by row, and reads them back with COLS/4 lanes per row,
+// so that one instruction covers whole COLS*4-byte segments of 32*4/COLS
+// rows.  The 16-byte slots of a row are XOR-swizzled so that both the
+// row-wise writes and the segment-wise reads are free of bank conflicts
+// (a quarter warp touches eight distinct 16-byte bank groups either way).
+// op(r, w0, v) gets row r of the warp, the word offset w0 of v in the row's
+// NW words and the four words v; it runs on every lane (shuffles allowed).
+template <int COLS, int NW, class Op>
+__device__ __forceinline__ void staged_rows(uint32_t* stg, const uint32_t (&w)[NW], Op op) {
+    static_assert(COLS == 8 || COLS == 16, "staging block of 8 or 16 words per row");
+    static_assert(NW % COLS == 0, "whole staging blocks");
+    constexpr int NQ = COLS / 4;          // 16-byte slots per row
+    constexpr int RPL = 8 / NQ;           // rows per 128 bytes of the block
+    constexpr int RPI = 32 / NQ;          // rows per read instruction
+    const int lane = threadIdx.x & 31;
+    uint4* blk = reinterpret_cast<uint4*>(stg);
+#pragma unroll
+    for (int sc = 0; sc < NW / COLS; ++sc) {
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < NQ; ++j)
+            blk[lane * NQ + (j ^ ((lane / RPL) % NQ))] =
+                make_uint4(w[sc * COLS + 4 * j], w[sc * COLS + 4 * j + 1], w[sc * COLS + 4 * j + 2],
+                           w[sc * COLS + 4 * j + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+            const int r = i * RPI + lane / NQ, q = lane % NQ;
+            op(r, sc * COLS + 4 * q, blk[r * NQ + (q ^ ((r / RPL) % NQ))]);
+        }
+    }
+    __syncwarp();
+}
+
+// COLS > 0: the scatter and the BF16 store go through staged_rows with the
+// warp's staging block stg (32 rows x COLS words); COLS = 0 writes straight
+// from registers.
+template <int EPI, int COLS = 0>
 __device__ __forceinline__ void epilogue_fc2(const GemmParams& p, uint32_t taddr, int row, int route, int e,
-                                             int n_tile) {
+                                             int n_tile, uint32_t* stg = nullptr) {
     const float g_act = p.g_act_per_token == 2 ? p.g_act[row] : (p.g_act ? p.g_act[0] : 1.0f);
     float alpha = __fmul_rn(g_act, p.gw[e]);
     int token = 0;
@@ -108,8 +150,37 @@ __device__ __forceinline__ void epilogue_fc2(const GemmParams& p, uint32_t taddr
         float o[32];
         tmem_ld32(taddr + ch * 32, o);
         tmem_ld_wait();
-        if (route < 0) continue;
         const int col0 = n_tile * 128 + ch * 32;
+        if constexpr (COLS > 0) {
+            // every lane takes part (shuffles); rows without a route write nothing
+            if constexpr (EPI == kEpiFc2Store) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * i] * alpha, o[2 * i + 1] * alpha);
+                    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+                }
+                const int row0 = row - (threadIdx.x & 31);
+                staged_rows<COLS>(stg, w, [&](int r, int w0, uint4 v) {
+                    if (__shfl_sync(0xffffffffu, route, r) >= 0)
+                        *reinterpret_cast<uint4*>(p.out_bf16 + (size_t)(row0 + r) * p.out_cols + col0 + 2 * w0) = v;
+                });
+            } else {
+                uint32_t w[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * alpha);
+                const int tk_lane = route >= 0 ? token : -1;
+                staged_rows<COLS>(stg, w, [&](int r, int w0, uint4 v) {
+                    const int tk = __shfl_sync(0xffffffffu, tk_lane, r);
+                    if (tk >= 0)
+                        red_add_f32x4(reinterpret_cast<float4*>(p.out_f32 + (size_t)tk * p.out_cols + col0 + w0),
+                                      __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                                      __uint_as_float(v.w));
+                });
+            }
+            continue;
+        }
+        if (route < 0) continue;
         if (EPI == kEpiFc2Store) {
             uint32_t w[16];
 #pragma unroll

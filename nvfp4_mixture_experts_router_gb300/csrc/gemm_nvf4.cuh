@@ -102,7 +102,12 @@ struct Cfg {
     static constexpr uint32_t kSfColsA = 4 * kAtoms;
     static constexpr uint32_t kSfColsB = 4 * kRowBlocks;         // per atom slot
     static constexpr uint32_t kSfColsPerStage = kSfColsA + kAtoms * kSfColsB;
-    static constexpr int kSmemBytes = kStages * (kTileBytesA + kTileBytesB + kSfBytesA + kSfBytesB) + 1024 + 256;
+    // FC2 epilogue staging (one block of 32 rows x kStgCols words per
+    // epilogue warp; 8 KB either way)
+    static constexpr int kStgCols = 64 / kEpiWarps;
+    static constexpr int kStgBytes = kEpiWarps * 32 * kStgCols * 4;
+    static constexpr int kSmemBytes =
+        kStages * (kTileBytesA + kTileBytesB + kSfBytesA + kSfBytesB) + kStgBytes + 1024 + 256;
     static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -112,6 +117,7 @@ struct Smem {
     uint8_t* b;
     uint8_t* sfa;
     uint8_t* sfb;
+    uint32_t* stg;
     uint64_t* full;
     uint64_t* sf_full;
     uint64_t* empty;
@@ -132,7 +138,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     s.b = s.a + C::kStages * C::kTileBytesA;
     s.sfa = s.b + C::kStages * C::kTileBytesB;
     s.sfb = s.sfa + C::kStages * C::kSfBytesA;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.sfb + C::kStages * C::kSfBytesB);
+    s.stg = reinterpret_cast<uint32_t*>(s.sfb + C::kStages * C::kSfBytesB);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.stg) + C::kStgBytes);
     s.full = bars;
     s.sf_full = bars + C::kStages;
     s.empty = bars + 2 * C::kStages;
@@ -405,7 +412,9 @@ __device__ __forceinline__ bool gemm_tiles(const Smem& s, uint32_t tmem_base, co
                 const int vtile = n_tile * C::kRowBlocks + half;   // index of this 128-column slice
                 if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32 || EPI == kEpiFc1Mx)
                     epilogue_fc1<EPI>(p, taddr, row, route, e, vtile);
-                else epilogue_fc2<EPI>(p, taddr, row, route, e, vtile);
+                else
+                    epilogue_fc2<EPI, C::kStgCols>(p, taddr, row, route, e, vtile,
+                                                   s.stg + (warp - C::kEpiWarp0) * 32 * C::kStgCols);
             }
             tc_fence_before();
             mbar_arrive(&s.acc_empty[acc]);

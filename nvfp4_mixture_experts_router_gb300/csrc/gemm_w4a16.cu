@@ -40,13 +40,17 @@ constexpr int kConvWarps = 4;
 constexpr int kNumThreads = (6 + kConvWarps) * 32;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kAccCols = 128;
-constexpr int kSmemBytes = kStages * (kTileBytesA + kTileBytesB + kTileBytesQ + kSfBytes) + 1024 + 256;
+constexpr int kStgCols = 8;                           // FC2 epilogue staging, words per row
+constexpr int kStgBytes = 4 * 32 * kStgCols * 4;      // one block per epilogue warp
+constexpr int kSmemBytes = kStages * (kTileBytesA + kTileBytesB + kTileBytesQ + kSfBytes) + kStgBytes + 1024 + 256;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Smem {
     uint8_t* a;
     uint8_t* b;
     uint8_t* q;
     uint8_t* sf;
+    uint32_t* stg;
     uint64_t* full;
     uint64_t* conv;
     uint64_t* empty;
@@ -64,7 +68,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     s.b = s.a + kStages * kTileBytesA;
     s.q = s.b + kStages * kTileBytesB;
     s.sf = s.q + kStages * kTileBytesQ;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.sf + kStages * kSfBytes);
+    s.stg = reinterpret_cast<uint32_t*>(s.sf + kStages * kSfBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.stg) + kStgBytes);
     s.full = bars;
     s.conv = bars + kStages;
     s.empty = bars + 2 * kStages;
@@ -240,7 +245,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int route = p.route_of_row[row];
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kAccCols;
             if (EPI == kEpiFc1Bf16) epilogue_fc1<EPI>(p, taddr, row, route, e, n_tile);
-            else epilogue_fc2<EPI>(p, taddr, row, route, e, n_tile);
+            else epilogue_fc2<EPI, kStgCols>(p, taddr, row, route, e, n_tile, s.stg + q * 32 * kStgCols);
             tc_fence_before();
             mbar_arrive(&s.acc_empty[acc]);
             acc ^= 1;
