@@ -270,6 +270,24 @@ def init_dist(args):
     return world, rank, local
 
 
+def max_over_ranks(x, world, device):
+    """The largest value of x over all ranks (x itself on a single rank);
+    the timed region's duration is the slowest replica's."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens, steps, ms):
+    """Whole-job throughput: the tokens every replica processed in `steps`
+    steps over the slowest replica's time `ms` (milliseconds)."""
+    return world * tokens * steps / (ms / 1000.0)
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
@@ -470,12 +488,9 @@ def run_ours(args, c, world, rank, local):
     ms = ev0.elapsed_time(ev1)
     if rank == 0:
         clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     ms_per_step = ms / args.steps
-    value = world * c.T * args.steps / (ms / 1000.0)
+    value = job_tokens_per_s(world, c.T, args.steps, ms)
 
     # per-stage durations (stage events; programmatic dependent launch off)
     nst = min(args.stage_steps, max(args.steps, 1))
@@ -535,11 +550,8 @@ def run_ours(args, c, world, rank, local):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * c.T * e2e_steps / (e2e_ms / 1000.0)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = job_tokens_per_s(world, c.T, e2e_steps, e2e_ms)
     h2d = c.T * c.H * 2 + (c.T * c.K * 8 if given else c.T * c.E * 4)
     d2h = c.T * c.H * 2
 
