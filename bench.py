@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="mid", choices=["tiny", "mid", "dsv3", "w4a16", "prefill"])
     p.add_argument("--tokens", type=int, default=None, help="token count (sweeps of dsv3 / w4a16)")
+    p.add_argument("--experts", type=int, default=None,
+                   help="expert count in place of the workload's (same shapes and distributions otherwise; "
+                        "fewer experts = more rows per expert, a compute-bound GEMM at a small footprint)")
     p.add_argument("--stage-steps", type=int, default=200)
     p.add_argument("--precision", default="nvfp4", choices=["nvfp4", "mxfp8"],
                    help="mxfp8: the W4A4 workloads' shapes and routing in MXFP8 W8A8")
@@ -71,10 +74,14 @@ def parse():
 
 
 def workload_config(name, tokens, precision="nvfp4", four_over_six=False, fused=False, gemm="auto",
-                    finalize="config"):
+                    finalize="config", experts=None):
     from nvfp4_mixture_experts_router_gb300 import synth
     idx = {"tiny": 0, "mid": 1, "dsv3": 2, "w4a16": 3, "prefill": 4}[name]
     c = synth.config(idx, tokens)
+    if experts is not None:
+        if not (c.K <= experts <= 1024):
+            raise SystemExit(f"--experts must lie in [{c.K}, 1024]")
+        c = c.with_(E=experts, name=c.name.replace(f"_E{c.E}_", f"_E{experts}_"))
     if precision == "mxfp8":
         if c.mode == synth.MODE_W4A16:
             raise SystemExit("--precision mxfp8 applies to the W4A4 workloads")
@@ -174,6 +181,10 @@ def traffic_key(args):
         key += "-fused"
     if args.finalize != "config":
         key += "-" + args.finalize
+    if args.experts is not None:
+        key += f"-E{args.experts}"
+    if args.tokens is not None:
+        key += f"-T{args.tokens}"
     return key
 
 
@@ -631,7 +642,7 @@ def main():
     args = parse()
     world, rank, local = init_dist(args)
     c = workload_config(args.workload, args.tokens, args.precision, args.four_over_six, args.fused, args.gemm,
-                        args.finalize)
+                        args.finalize, args.experts)
     if args.impl == "reference":
         run_reference(args, c, world, rank)
     else:
