@@ -467,9 +467,10 @@ def run_ours(args, c, world, rank, local):
         ids = layer.view("topk_ids", torch.int32, c.T * c.K).view(c.T, c.K).clone()
         wts = layer.view("topk_w", torch.float32, c.T * c.K).view(c.T, c.K).clone()
 
-    def step(i, yy=y, xx=x, ll=logits):
+    def step(i, yy=y, xx=x, ll=logits, ii=None, ww=None):
         if given:
-            api.moe_nvfp4_forward_routed(s, flags, xx, ids, wts, g1, g2, preps[i % n_sets], ws, yy)
+            api.moe_nvfp4_forward_routed(s, flags, xx, ids if ii is None else ii, wts if ww is None else ww,
+                                         g1, g2, preps[i % n_sets], ws, yy)
         else:
             api.moe_nvfp4_forward(s, flags, xx, ll, bias, g1, g2, preps[i % n_sets], ws, yy)
 
@@ -523,44 +524,117 @@ def run_ours(args, c, world, rank, local):
         sbytes = {"fused_layer": sbytes["router"] + c.T * c.H * 2 + active * (c.N1 * c.H + c.H * c.I) * nv +
                   c.T * c.H * 2}
 
-    # end to end: host x/logits -> device, forward, y -> host, every step
-    n_host = 2
-    hx = [x.cpu().pin_memory() for _ in range(n_host)]
-    # the routing input of a step: logits, or the given ids and weights
-    # (copied straight into the tensors step() reads)
-    hl = [logits.cpu().pin_memory() for _ in range(n_host)]
+    # end to end through the C ABI: every step copies its inputs (x and the
+    # logits, or the given ids and weights) from pinned host memory, runs the
+    # forward and copies y back to pinned host memory.  Pipelined as a user
+    # of the library would: two device slots, the host-to-device copy of
+    # step i+1 and the device-to-host copy of step i-1 on their own streams
+    # while step i computes; events keep a slot from being overwritten
+    # before the step that uses it is done.
+    n_slot = 2
+    hx = [x.cpu().pin_memory() for _ in range(n_slot)]
+    hl = [logits.cpu().pin_memory() for _ in range(n_slot)]
     if given:
-        h_ids = [ids.cpu().pin_memory() for _ in range(n_host)]
-        h_wts = [wts.cpu().pin_memory() for _ in range(n_host)]
-    hy = [torch.empty(c.T, c.H, dtype=torch.bfloat16).pin_memory() for _ in range(n_host)]
-    dx = torch.empty_like(x)
-    dl = torch.empty_like(logits)
+        h_ids = [ids.cpu().pin_memory() for _ in range(n_slot)]
+        h_wts = [wts.cpu().pin_memory() for _ in range(n_slot)]
+        d_ids = [torch.empty_like(ids) for _ in range(n_slot)]
+        d_wts = [torch.empty_like(wts) for _ in range(n_slot)]
+    hy = [torch.empty(c.T, c.H, dtype=torch.bfloat16).pin_memory() for _ in range(n_slot)]
+    dx = [torch.empty_like(x) for _ in range(n_slot)]
+    dl = [torch.empty_like(logits) for _ in range(n_slot)]
+    dy = [torch.empty_like(y) for _ in range(n_slot)]
+    cs, ds = torch.cuda.Stream(), torch.cuda.Stream()
+    h2d_done = [torch.cuda.Event() for _ in range(n_slot)]
+    fwd_done = [torch.cuda.Event() for _ in range(n_slot)]
+    d2h_done = [torch.cuda.Event() for _ in range(n_slot)]
 
-    def copy_routing(i):
-        if given:
-            ids.copy_(h_ids[i % n_host], non_blocking=True)
-            wts.copy_(h_wts[i % n_host], non_blocking=True)
-        else:
-            dl.copy_(hl[i % n_host], non_blocking=True)
-    e2e_steps = args.steps
-    for i in range(min(args.warmup, 5)):
-        dx.copy_(hx[i % n_host], non_blocking=True)
-        copy_routing(i)
-        step(i, y, dx, dl)
-        hy[i % n_host].copy_(y, non_blocking=True)
+    def e2e_step(i, ms):
+        b = i % n_slot
+        with torch.cuda.stream(cs):
+            if i >= n_slot:
+                cs.wait_event(fwd_done[b])         # step i - 2 has read slot b's inputs
+            dx[b].copy_(hx[b], non_blocking=True)
+            if given:
+                d_ids[b].copy_(h_ids[b], non_blocking=True)
+                d_wts[b].copy_(h_wts[b], non_blocking=True)
+            else:
+                dl[b].copy_(hl[b], non_blocking=True)
+            h2d_done[b].record(cs)
+        ms.wait_event(h2d_done[b])
+        if i >= n_slot:
+            ms.wait_event(d2h_done[b])             # step i - 2's y has left slot b
+        with torch.cuda.stream(ms):
+            if given:
+                step(i, dy[b], dx[b], None, d_ids[b], d_wts[b])
+            else:
+                step(i, dy[b], dx[b], dl[b])
+        fwd_done[b].record(ms)
+        with torch.cuda.stream(ds):
+            ds.wait_event(fwd_done[b])
+            hy[b].copy_(dy[b], non_blocking=True)
+            d2h_done[b].record(ds)
+
+    def e2e_steps_on(ms, n):
+        # fork the copy streams from ms, run n steps, join them back into ms
+        fork = torch.cuda.Event()
+        fork.record(ms)
+        cs.wait_event(fork)
+        ds.wait_event(fork)
+        for i in range(n):
+            e2e_step(i, ms)
+        for ev in d2h_done[:min(n, n_slot)]:
+            ms.wait_event(ev)
+        join = torch.cuda.Event()
+        join.record(cs)
+        ms.wait_event(join)
+
+    # A group of steps is captured once into a CUDA graph and replayed, so
+    # that the host enqueues one graph per group instead of every copy,
+    # event and kernel (at small T the host's launch rate would otherwise
+    # bound the step); without a graph the same calls are enqueued directly.
+    # Consecutive replays do not overlap (the first copy of a group waits
+    # for the last step of the previous one), so a group is long: 64 steps.
+    group = 64
+    reps = max(1, -(-args.steps // group))
+    e2e_steps = reps * group
+    e2e_graph = None
+    main = torch.cuda.current_stream()
+    e2e_steps_on(main, group)                        # warm-up, outside any capture
     torch.cuda.synchronize()
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(main)
+        with torch.cuda.graph(g, stream=cap):
+            e2e_steps_on(cap, group)
+        torch.cuda.synchronize()
+        for _ in range(min(args.warmup, 3)):
+            g.replay()
+        torch.cuda.synchronize()
+        e2e_graph = g
+        e2e_mode = f"steps replayed from a CUDA graph of {group} pipelined steps"
+    except Exception as exc:                       # capture refused: enqueue the calls directly
+        torch.cuda.synchronize()
+        e2e_mode = f"pipelined steps enqueued directly (graph capture failed: {type(exc).__name__})"
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(e2e_steps):
-        dx.copy_(hx[i % n_host], non_blocking=True)
-        copy_routing(i)
-        step(i, y, dx, dl)
-        hy[i % n_host].copy_(y, non_blocking=True)
-    e1.record()
+    e0.record(main)
+    for _ in range(reps):
+        if e2e_graph is not None:
+            e2e_graph.replay()
+        else:
+            e2e_steps_on(main, group)
+    e1.record(main)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
+    # the pipelined steps returned the layer's output (the fused finalize's
+    # reduction order may differ from run to run, hence a tolerance)
+    y_ref = y.float().cpu()
+    y_e2e = hy[(e2e_steps - 1) % n_slot].float()
+    tol = 0.02 * float(y_ref.pow(2).mean().sqrt()) + 0.01 * float(y_ref.abs().max())
+    if not bool(torch.isfinite(y_e2e).all()) or float((y_e2e - y_ref).abs().max()) > tol:
+        raise RuntimeError("end-to-end output differs from the device-timed forward's")
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     e2e_value = job_tokens_per_s(world, c.T, e2e_steps, e2e_ms)
     h2d = c.T * c.H * 2 + (c.T * c.K * 8 if given else c.T * c.E * 4)
@@ -624,7 +698,9 @@ def run_ours(args, c, world, rank, local):
         "fp4_peak_tflops": round(fp4_peak, 1),
         "routing": args.routing + ("" if not given else " (stage times from the logits path)"),
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "pipeline": "2 device slots; the H2D copy of step i+1 and the D2H copy of step i-1 run on two "
+                            "copy streams while step i computes; " + e2e_mode},
         "gpu_launches": api.moe_nvfp4_forward_launches(s, flags) * args.steps,
         "roofline": roof,
         "stages_us": {k: round(v * 1000, 2) for k, v in stage_ms.items()},
