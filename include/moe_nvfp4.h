@@ -53,7 +53,7 @@ extern "C" {
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,   /* bad shape, flag, null or misaligned pointer */
-    MOE_ERR_UNSUPPORTED = 2,   /* valid request the library or device cannot run */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid request this build/device cannot run  */
     MOE_ERR_WORKSPACE = 3,     /* buffer smaller than the *_bytes() query     */
     MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed                  */
     MOE_ERR_TIMEOUT = 5        /* a device-side wait gave up (see status word)*/
