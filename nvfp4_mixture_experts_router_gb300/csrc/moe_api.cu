@@ -156,7 +156,7 @@ bool encode_swap_weight_map(CUtensorMap* map, const void* base, uint64_t rows, u
 // T = 1 at the DSV3 shape 68.6 us standard vs 72.3 us swapped; T = 16
 // 452.7 vs 440.8; the mid workload 77.8 vs 74.9; T = 4096: 128 routes per
 // expert, standard).
-constexpr uint64_t kSlabAccBytes = 64ull << 20;   // FC2 accumulator slice kept in L2 (of 129 MB)
+constexpr uint64_t kSlabAccBytes = 48ull << 20;   // FC2 accumulator slice kept in L2 (of 129 MB)
 constexpr int64_t kSwapMaxRoutesPerExpert = 64;
 constexpr int64_t kSwapMinRoutes = 64;
 bool use_swap_gemm(moe_shape s, uint32_t flags) {
@@ -665,7 +665,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         g2p.out_f32 = y_acc;
         epi2 = kEpiFc2Scatter;
         // an accumulator beyond half the L2: walk FC2's output width in slabs
-        // whose accumulator slice stays in L2 (T x slab x 4 B <= 64 MB), so
+        // whose accumulator slice stays in L2 (T x slab x 4 B <= 48 MB), so
         // that a token's K reductions do not each go through HBM
         const uint64_t slab_bytes_per_tile = (uint64_t)s.T * (uint64_t)tn2 * 4u;
         if (!swap && !pair2 && (uint64_t)s.T * s.H * 4u > kSlabAccBytes) {
