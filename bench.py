@@ -605,7 +605,9 @@ def run_ours(args, c, world, rank, local):
         g = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream()
         cap.wait_stream(main)
-        with torch.cuda.graph(g, stream=cap):
+        # thread-local capture: CUDA calls of other threads (NCCL's watchdog
+        # under torchrun) are not affected by it
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
             e2e_steps_on(cap, group)
         torch.cuda.synchronize()
         for _ in range(min(args.warmup, 3)):
