@@ -2,15 +2,20 @@
 """Benchmark of the NVFP4 MoE layer forward (libmoe_nvfp4.so, C ABI).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload mid|tiny|dsv3|w4a16|prefill] [--tokens T]
-                    [--precision nvfp4|mxfp8] [--four-over-six] [--routing logits|given]
-                    [--fused] [--gemm auto|standard|swapped|pairs]
+                    [--workload prefill|mid|tiny|dsv3|w4a16] [--tokens T]
+                    [--precision nvfp4|mxfp8] [--four-over-six] [--routing logits|given|gate]
+                    [--fused] [--gemm auto|standard|swapped|pairs] [--sweep dsv3|none]
 
 A step is one full layer forward (router, permutation, activation
 quantization, FC1 + activation + requantization, FC2, finalize) over one
-batch of T synthetic tokens.  Default workload: the mid configuration
-(T=512, H=2048, I=768, E=64, top-6, SwiGLU, W4A4 per-token scales, router
-weight on the FC2 input, fused finalize).
+batch of T synthetic tokens.  Default workload: the prefill-scale
+configuration, the largest that runs on one GPU (T=16384, H=7168, I=2048,
+E=256, top-8, SwiGLU, W4A4 per-token scales, Zipf-skewed expert
+popularity, fused finalize).  With --sweep dsv3 (the default at N=1) the
+line also carries the DeepSeek-V3-like expert shape (H=7168, I=2048, E=256,
+top-8, per-tensor, deterministic finalize) at T in {1, 8, 64, 256, 1024,
+4096, 8192}: device-timed tokens/s, TFLOP/s and % of the dense FP4 peak
+per token count.
 
 Prints one JSON line (rank 0).  `value` is whole-job tokens/s with inputs
 resident in HBM; L2 is defeated by rotating several copies of the prepared
@@ -48,10 +53,12 @@ FP8_OVER_BF16 = 4.5 / 2.25
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="mid", choices=["tiny", "mid", "dsv3", "w4a16", "prefill"])
+    p.add_argument("--workload", default="prefill", choices=["tiny", "mid", "dsv3", "w4a16", "prefill"])
+    p.add_argument("--sweep", default="dsv3", choices=["dsv3", "none"],
+                   help="dsv3: also time the DSV3-like expert shape over its token counts (N=1 only)")
     p.add_argument("--tokens", type=int, default=None, help="token count (sweeps of dsv3 / w4a16)")
     p.add_argument("--experts", type=int, default=None,
                    help="expert count in place of the workload's (same shapes and distributions otherwise; "
@@ -61,8 +68,9 @@ def parse():
                    help="mxfp8: the W4A4 workloads' shapes and routing in MXFP8 W8A8")
     p.add_argument("--four-over-six", action="store_true",
                    help="4-over-6 activation quantization (per-token W4A4 workloads)")
-    p.add_argument("--routing", default="logits", choices=["logits", "given"],
-                   help="given: caller-supplied top-K ids and weights (moe_nvfp4_forward_routed)")
+    p.add_argument("--routing", default="logits", choices=["logits", "given", "gate"],
+                   help="given: caller-supplied top-K ids and weights (moe_nvfp4_forward_routed); "
+                        "gate: logits computed by the layer from the gate projection (moe_nvfp4_forward_gate)")
     p.add_argument("--fused", action="store_true",
                    help="the whole forward as one persistent kernel (MOE_FUSED_LAYER; W4A4, E <= 256)")
     p.add_argument("--gemm", default="auto", choices=["auto", "standard", "swapped", "pairs"],
@@ -130,8 +138,10 @@ def flops_per_step(c):
     return 2.0 * R * (c.N1 * c.H + c.I * c.H)
 
 
-def stage_bytes(c, active):
-    """Algorithmic bytes per launch of each stage (minimum HBM traffic)."""
+def stage_bytes(c, active, h_fp32=False):
+    """Algorithmic bytes per launch of each stage (minimum HBM traffic).
+    h_fp32: per-token mode on its fallback path (FC1 stores the FP32 FC2
+    input and a separate kernel quantizes it)."""
     from nvfp4_mixture_experts_router_gb300 import synth
     T, H, I, E, K, N1 = c.T, c.H, c.I, c.E, c.K, c.N1
     R = T * K
@@ -140,14 +150,15 @@ def stage_bytes(c, active):
     w4a16 = c.mode == synth.MODE_W4A16
     per_token = c.mode == synth.MODE_PER_TOKEN
     a_elem = 2.0 if w4a16 else nv
-    h_out = 2.0 if w4a16 else (4.0 if per_token else nv)
+    h_out = 2.0 if w4a16 else (4.0 if (per_token and h_fp32) else nv)
     fused = not c.deterministic
     return {
+        "router_gemm": T * H * 2 + E * H * 2 + T * E * 4,
         "router": T * E * 4 + T * K * 8 + (E * 4 if c.bias != "none" else 0),
         "permute": T * K * 4 * 4,
         "quantize_x": T * H * 2 + R * H * a_elem + (T * H * 4 if fused else 0),
         "fc1": active * N1 * H * nv + R * H * a_elem + R * I * h_out,
-        "quantize_h": (R * I * 4 + R * I * nv) if per_token else 0,
+        "quantize_h": (R * I * 4 + R * I * nv) if (per_token and h_fp32) else 0,
         "fc2": active * H * I * nv + R * I * (2.0 if w4a16 else nv) + (T * H * 4 if fused else R * H * 2),
         "finalize": (T * H * 4 + T * H * 2) if fused else (R * H * 2 + T * H * 2),
     }
@@ -412,6 +423,74 @@ def run_reference(args, c, world, rank):
 # our arm
 # ---------------------------------------------------------------------------
 
+SWEEP_T = [1, 8, 64, 256, 1024, 4096, 8192]
+
+
+def per_tensor_scales(api, c, flags, prepared, x, logits, bias, dev):
+    """Calibration of the per-tensor activation scales: G1 = amax(x)/2688,
+    G2 = the largest per-row FC2-input scale of a per-token pass of the
+    library itself over the same tokens."""
+    import torch
+    g1 = (x.float().abs().max() / 2688.0).reshape(1).contiguous()
+    tok = api.MoELayer.create(c.T, c.H, c.I, c.E, c.K, (flags & ~(3 << 2)) | api.MOE_W4A4_PER_TOKEN, dev)
+    tok.prepared = prepared
+    tok.forward(x, logits, bias)
+    cap = tok.layout()["rows_cap"]
+    rows = int(tok.view("meta", torch.int32, 4)[0])
+    g2 = tok.view("g2", torch.float32, cap)[:rows].max().reshape(1).contiguous()
+    del tok
+    return g1, g2
+
+
+def dsv3_sweep(dev, steps, warmup, fp4_peak):
+    """The DSV3-like expert shape over its token counts, one prepared weight
+    set (6.3 GB) for all of them.  Every timed forward follows a 256 MB write
+    that evicts L2 and is timed alone with CUDA events; the median is kept."""
+    import torch
+    from nvfp4_mixture_experts_router_gb300 import api, synth
+    c0 = synth.config(2)
+    flags = c0.flags()
+    s0 = api.shape(SWEEP_T[-1], c0.H, c0.I, c0.E, c0.K)
+    prep = torch.empty(api.moe_nvfp4_prepared_bytes(s0, flags), dtype=torch.uint8, device=dev)
+    w1 = synth.gen_w1(c0, dev)
+    w2 = synth.gen_w2(c0, dev)
+    api.moe_nvfp4_prepare_weights(s0, flags, w1, w2, prep)
+    torch.cuda.synchronize()
+    del w1, w2
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    points = []
+    for T in SWEEP_T:
+        c = synth.config(2, T)
+        s = api.shape(T, c.H, c.I, c.E, c.K)
+        x = synth.gen_x(c, dev)
+        logits = synth.gen_logits(c, dev, x)
+        g1, g2 = per_tensor_scales(api, c, flags, prep, x, logits, None, dev)
+        ws = torch.empty(api.moe_nvfp4_workspace_bytes(s, flags), dtype=torch.uint8, device=dev)
+        y = torch.empty(T, c.H, dtype=torch.bfloat16, device=dev)
+        for _ in range(max(warmup, 3)):
+            api.moe_nvfp4_forward(s, flags, x, logits, None, g1, g2, prep, ws, y)
+        torch.cuda.synchronize()
+        if api.moe_nvfp4_last_device_status(ws) != api.MOE_OK:
+            raise RuntimeError(f"device status not OK in the DSV3 sweep at T={T}")
+        n = max(5, min(steps, 50))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record()
+            api.moe_nvfp4_forward(s, flags, x, logits, None, g1, g2, prep, ws, y)
+            b.record()
+        torch.cuda.synchronize()
+        ms = sorted(a.elapsed_time(b) for a, b in evs)[n // 2]
+        tflops = flops_per_step(c) / (ms / 1000.0) / 1e12
+        points.append({"T": T, "ms": round(ms, 5), "tokens_per_s": round(T / (ms / 1000.0), 1),
+                       "tflops": round(tflops, 2), "pct_fp4_peak": round(100 * tflops / fp4_peak, 3),
+                       "timed_steps": n})
+        del ws, y, x, logits
+    return {"workload": describe(c0).split(":", 1)[1].replace(" T=4096,", "").strip(),
+            "l2": "256 MB write before every timed forward (evicts L2); median of per-forward CUDA-event times",
+            "points": points}
+
+
 def run_ours(args, c, world, rank, local):
     import torch
     import torch.distributed as dist
@@ -424,14 +503,19 @@ def run_ours(args, c, world, rank, local):
     build.build()
     api.lib()
 
-    flags = c.flags()
+    gate = args.routing == "gate"
+    flags = c.flags() | (api.MOE_ROUTER_GEMM if gate else 0)
     s = api.shape(c.T, c.H, c.I, c.E, c.K)
     x = synth.gen_x(c, dev)
     logits = synth.gen_logits(c, dev, x)
+    wg = synth.gen_wg(c, dev) if gate else None
+    if gate:
+        # the logits the layer will compute itself (the calibration pass and
+        # the stage timings below run on them)
+        logits = torch.empty(c.T, c.E, dtype=torch.float32, device=dev)
+        api.moe_nvfp4_router_logits(x, wg, logits)
     bias = synth.gen_bias(c, dev)
     g1 = g2 = None
-    if c.mode == synth.MODE_PER_TENSOR:
-        g1 = (x.float().abs().max() / 2688.0).reshape(1).contiguous()          # calibration of the FC1 input
 
     # prepared weights: enough copies that consecutive steps miss in L2
     pb = api.moe_nvfp4_prepared_bytes(s, flags)
@@ -447,14 +531,7 @@ def run_ours(args, c, world, rank, local):
     torch.cuda.synchronize()
     del w1, w2
     if c.mode == synth.MODE_PER_TENSOR:
-        # FC2-input calibration from a per-token pass of the library itself
-        tok = api.MoELayer.create(c.T, c.H, c.I, c.E, c.K, (flags & ~(3 << 2)) | api.MOE_W4A4_PER_TOKEN, dev)
-        tok.prepared = preps[0]
-        tok.forward(x, logits, bias)
-        cap = tok.layout()["rows_cap"]
-        g2 = (tok.view("g2", torch.float32, cap)[:int(tok.view("meta", torch.int32, 4)[0])].max()).reshape(1)
-        g2 = g2.contiguous()
-        del tok
+        g1, g2 = per_tensor_scales(api, c, c.flags(), preps[0], x, logits, bias, dev)
     y = torch.empty(c.T, c.H, dtype=torch.bfloat16, device=dev)
     ws = layer.workspace
     given = args.routing == "given"
@@ -471,6 +548,8 @@ def run_ours(args, c, world, rank, local):
         if given:
             api.moe_nvfp4_forward_routed(s, flags, xx, ids if ii is None else ii, wts if ww is None else ww,
                                          g1, g2, preps[i % n_sets], ws, yy)
+        elif gate:
+            api.moe_nvfp4_forward_gate(s, flags, xx, wg, bias, g1, g2, preps[i % n_sets], ws, yy)
         else:
             api.moe_nvfp4_forward(s, flags, xx, ll, bias, g1, g2, preps[i % n_sets], ws, yy)
 
@@ -507,14 +586,31 @@ def run_ours(args, c, world, rank, local):
     # per-stage durations (stage events; programmatic dependent launch off)
     nst = min(args.stage_steps, max(args.steps, 1))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(api.NUM_STAGE_EVENTS)] for _ in range(nst)]
+    staged_flags = flags & ~api.MOE_ROUTER_GEMM
     for i in range(nst):
-        api.moe_nvfp4_forward_staged(s, flags, x, logits, bias, g1, g2, preps[i % n_sets], ws, y, evs[i])
+        api.moe_nvfp4_forward_staged(s, staged_flags, x, logits, bias, g1, g2, preps[i % n_sets], ws, y, evs[i])
     torch.cuda.synchronize()
     stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(nst)) / nst
                 for j, name in enumerate(api.STAGES)}
+    if gate:
+        # the logits kernel, timed on its own in front of the staged forward
+        lg = torch.empty_like(logits)
+        gevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nst)]
+        for a, b in gevs:
+            a.record()
+            api.moe_nvfp4_router_logits(x, wg, lg)
+            b.record()
+        torch.cuda.synchronize()
+        stage_ms = {"router_gemm": sum(a.elapsed_time(b) for a, b in gevs) / nst, **stage_ms}
     count = layer.view("count", torch.int32, c.E).cpu()
     active = int((count > 0).sum())
-    sbytes = stage_bytes(c, active)
+    # per-token: the FC2-input quantization is inside FC1 unless the launch
+    # count shows the separate kernel
+    h_fp32 = (c.mode == synth.MODE_PER_TOKEN and not c.fused and
+              api.moe_nvfp4_forward_launches(s, c.flags()) == (6 if c.T <= 32 else 7))
+    sbytes = stage_bytes(c, active, h_fp32)
+    if not h_fp32:
+        stage_ms.pop("quantize_h", None)        # no kernel between the FC1 and FC2 events
     if c.fused:
         # one kernel: its time is the forward's, its algorithmic bytes the
         # layer's irreducible traffic (routing input, x, the active experts'
@@ -533,7 +629,7 @@ def run_ours(args, c, world, rank, local):
     # before the step that uses it is done.
     n_slot = 2
     hx = [x.cpu().pin_memory() for _ in range(n_slot)]
-    hl = [logits.cpu().pin_memory() for _ in range(n_slot)]
+    hl = [logits.cpu().pin_memory() for _ in range(n_slot)]   # (unused by the gate routing: x is the input)
     if given:
         h_ids = [ids.cpu().pin_memory() for _ in range(n_slot)]
         h_wts = [wts.cpu().pin_memory() for _ in range(n_slot)]
@@ -557,7 +653,7 @@ def run_ours(args, c, world, rank, local):
             if given:
                 d_ids[b].copy_(h_ids[b], non_blocking=True)
                 d_wts[b].copy_(h_wts[b], non_blocking=True)
-            else:
+            elif not gate:
                 dl[b].copy_(hl[b], non_blocking=True)
             h2d_done[b].record(cs)
         ms.wait_event(h2d_done[b])
@@ -593,9 +689,11 @@ def run_ours(args, c, world, rank, local):
     # event and kernel (at small T the host's launch rate would otherwise
     # bound the step); without a graph the same calls are enqueued directly.
     # Consecutive replays do not overlap (the first copy of a group waits
-    # for the last step of the previous one), so a group is long: 64 steps.
-    group = 64
-    reps = max(1, -(-args.steps // group))
+    # for the last step of the previous one), so a group is long: the
+    # largest divisor of the step count up to 64, so that exactly `steps`
+    # steps are timed.
+    group = max(d for d in range(1, min(64, max(args.steps, 1)) + 1) if max(args.steps, 1) % d == 0)
+    reps = max(args.steps, 1) // group
     e2e_steps = reps * group
     e2e_graph = None
     main = torch.cuda.current_stream()
@@ -639,7 +737,7 @@ def run_ours(args, c, world, rank, local):
         raise RuntimeError("end-to-end output differs from the device-timed forward's")
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     e2e_value = job_tokens_per_s(world, c.T, e2e_steps, e2e_ms)
-    h2d = c.T * c.H * 2 + (c.T * c.K * 8 if given else c.T * c.E * 4)
+    h2d = c.T * c.H * 2 + (c.T * c.K * 8 if given else (0 if gate else c.T * c.E * 4))
     d2h = c.T * c.H * 2
 
     if rank != 0:
@@ -649,15 +747,20 @@ def run_ours(args, c, world, rank, local):
 
     hbm, bf16, bf16s, peak_src = measured_peaks()
     mx = c.mode == synth.MODE_MXFP8
+    w4a16 = c.mode == synth.MODE_W4A16
     ratio = FP8_OVER_BF16 if mx else FP4_OVER_BF16
-    fp4_peak = bf16 * ratio           # the dense peak of the GEMMs' input type (FP8 for MXFP8)
+    fp4_peak = bf16 * ratio           # the dense FP4 peak (FP8 for MXFP8): the metric's reference rate
+    # the peak of the MMA kind the GEMMs run on: W4A16 widens the weights to
+    # BF16 on chip and runs kind::f16, so its GEMMs are bounded by the BF16 peak
+    gemm_peak, gemm_ratio = (bf16, 1.0) if w4a16 else (fp4_peak, ratio)
+    gemm_kind = "bf16" if w4a16 else ("fp8" if mx else "fp4")
     flops = flops_per_step(c)
     dom = max(stage_ms, key=lambda k: stage_ms[k])
     dom_ms = stage_ms[dom]
     if dom in ("fc1", "fc2"):
         # GEMM: report the bound that limits it at this shape
         gemm_flops = 2.0 * c.T * c.K * c.H * (c.N1 if dom == "fc1" else c.I)
-        t_flop = gemm_flops / (fp4_peak * 1e12)
+        t_flop = gemm_flops / (gemm_peak * 1e12)
         t_byte = sbytes[dom] / (hbm * 1e9)
         bound = "tensor" if t_flop > t_byte else "hbm"
     else:
@@ -671,11 +774,16 @@ def run_ours(args, c, world, rank, local):
                 "mean_launch_us": round(dom_ms * 1000, 2), "peak_source": f"{peak_src} hbm_gbs"}
     else:
         achieved = gemm_flops / (dom_ms / 1000.0) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / fp4_peak, 4), "traffic": traffic_for(dom, traffic_key(args)),
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(gemm_peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / gemm_peak, 4), "traffic": traffic_for(dom, traffic_key(args)),
                 "kernel": dom, "algorithmic_flops_per_launch": gemm_flops,
                 "mean_launch_us": round(dom_ms * 1000, 2),
-                "peak_source": f"{peak_src} bf16_tflops x {ratio:g} (nominal {'fp8' if mx else 'fp4'}/bf16 ratio)"}
+                "peak_source": (f"{peak_src} bf16_tflops (kind::f16 MMAs)" if w4a16 else
+                                f"{peak_src} bf16_tflops x {gemm_ratio:g} (nominal {gemm_kind}/bf16 ratio)")}
+
+    sweep = None
+    if args.sweep == "dsv3" and world == 1:
+        sweep = dsv3_sweep(dev, args.steps, args.warmup, bf16 * FP4_OVER_BF16)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -698,12 +806,13 @@ def run_ours(args, c, world, rank, local):
                    "parallelism": f"replicas x{world}"},
         "tflops": round(tflops, 2), "pct_fp4_peak": round(100 * tflops / fp4_peak, 3),
         "fp4_peak_tflops": round(fp4_peak, 1),
-        "routing": args.routing + ("" if not given else " (stage times from the logits path)"),
+        "routing": args.routing + ("" if args.routing == "logits" else " (stage times from the logits path)"),
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "pipeline": "2 device slots; the H2D copy of step i+1 and the D2H copy of step i-1 run on two "
                             "copy streams while step i computes; " + e2e_mode},
-        "gpu_launches": api.moe_nvfp4_forward_launches(s, flags) * args.steps,
+        "gpu_launches": (api.moe_nvfp4_forward_launches(s, flags & ~api.MOE_ROUTER_GEMM) + (1 if gate else 0))
+                        * args.steps,
         "roofline": roof,
         "stages_us": {k: round(v * 1000, 2) for k, v in stage_ms.items()},
         "stage_gbs": {k: round(sbytes[k] / (stage_ms[k] / 1000) / 1e9, 1) for k in stage_ms if stage_ms[k] > 0},
@@ -711,6 +820,8 @@ def run_ours(args, c, world, rank, local):
         "clocks": clocks.summary(t_wall0, t_wall1),
         "cpu_baseline": cpu,
     }
+    if sweep is not None:
+        out["sweep"] = sweep
     print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()

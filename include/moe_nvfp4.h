@@ -126,7 +126,22 @@ typedef enum {
  * is invalid. */
 #define MOE_GEMM_SWAP_NEVER (1u << 11)
 #define MOE_GEMM_SWAP_ALWAYS (1u << 12)
-#define MOE_FLAGS_KNOWN 0x1FFFu
+/* bit 13: test hook for the bounded waits.  The producer warp of the first
+ * CTA of the FC1 GEMM skips its first pipeline stage: it issues neither that
+ * stage's copies nor its barrier arrival, so no copy is ever in flight
+ * against the barrier the MMA thread then waits on.  That wait gives up
+ * after its limit (1 s), every role of the CTA drains and exits, the forward
+ * returns MOE_OK and moe_nvfp4_last_device_status reports MOE_ERR_TIMEOUT;
+ * y is undefined.  Valid only on the launch sequence with the standard GEMM
+ * orientation: a W4A4 mode together with MOE_GEMM_SWAP_NEVER, without
+ * MOE_GEMM_PAIRS_ALWAYS or MOE_FUSED_LAYER. */
+#define MOE_DEBUG_FC1_SKIP_STAGE (1u << 13)
+/* bit 14: the router logits are computed by the layer itself from the gate
+ * projection, logits = x . W_g^T (moe_nvfp4_forward_gate; required by it,
+ * invalid with every other forward entry point and with MOE_FUSED_LAYER).
+ * The workspace then holds the FP32 logits [T][E]. */
+#define MOE_ROUTER_GEMM (1u << 14)
+#define MOE_FLAGS_KNOWN 0x7FFFu
 
 /* ---- shapes ---------------------------------------------------------------- */
 typedef struct {
@@ -234,6 +249,40 @@ MOE_API moe_status moe_nvfp4_forward_routed(moe_shape s, uint32_t flags,
                                             void* workspace, size_t workspace_bytes,
                                             void* y_bf16, void* stream);
 
+/* Router logits from the gate projection on the tensor cores [FlashInfer
+ * PR #4366, "Motivation": the MoE wrapper is handed routing that was computed
+ * upstream from the gate projection; this is that projection]:
+ *   logits[t][e] = sum_h x[t][h] * gate_w[e][h]
+ *   x_bf16       [T][H] BF16, device, 16-byte aligned (H % 128 == 0)
+ *   gate_w_bf16  [E][H] BF16, device, 16-byte aligned (1 <= E <= 1024)
+ *   logits       [T][E] FP32, device, 16-byte aligned, caller-owned output;
+ *                may not overlap x or gate_w.
+ * BF16 products are exact; the sum is accumulated in FP32 by the tensor cores
+ * (order unspecified), so it may differ from the exactly rounded sum by a few
+ * FP32 roundings of partial sums.  Enqueues one kernel on `stream`; nothing is
+ * synchronized; a timed-out internal wait leaves the output undefined and is
+ * not reported (use moe_nvfp4_forward_gate for a status).
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+MOE_API moe_status moe_nvfp4_router_logits(int T, int E, int H, const void* x_bf16,
+                                           const void* gate_w_bf16, float* logits,
+                                           void* stream);
+
+/* The layer forward from the gate projection instead of router logits: the
+ * logits kernel of moe_nvfp4_router_logits writes into the workspace's logits
+ * region, then the forward of moe_nvfp4_forward runs on them (router bias,
+ * softmax and top-K as there).  flags must include MOE_ROUTER_GEMM (which
+ * sizes the workspace for the logits) and not MOE_FUSED_LAYER.  gate_w_bf16
+ * [E][H] BF16, device, 16-byte aligned, not overlapping the workspace.  Every
+ * other argument as moe_nvfp4_forward; the device status also reports a
+ * timeout of the logits kernel.  Nothing is synchronized. */
+MOE_API moe_status moe_nvfp4_forward_gate(moe_shape s, uint32_t flags,
+                                          const void* x_bf16, const void* gate_w_bf16,
+                                          const float* router_bias,
+                                          const float* act_scale_fc1, const float* act_scale_fc2,
+                                          const void* prepared,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* y_bf16, void* stream);
+
 /* Same as moe_nvfp4_forward, and records caller-created CUDA events
  * (cudaEvent_t, created with timing enabled) on `stream` at the stage
  * boundaries, for per-stage timing:
@@ -255,10 +304,12 @@ MOE_API moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags,
                                             void* y_bf16, void* stream, void* const* events);
 
 /* Number of kernel launches one moe_nvfp4_forward enqueues for this shape
- * and flags (-1 if invalid): 6 (7 with per-token scales), one fewer for
- * T <= 32 (router and permutation scan in one launch), 1 for
- * MOE_FUSED_LAYER.  moe_nvfp4_forward_routed always launches the scan
- * separately.  Pure host call. */
+ * and flags on the current device (-1 if invalid): 6, one fewer for T <= 32
+ * (router and permutation scan in one launch), 1 for MOE_FUSED_LAYER.  With
+ * per-token scales the FC2-input quantization runs inside FC1's epilogue;
+ * it is a seventh launch only on CTA pairs or when FC1 has more N tiles per
+ * M tile than the device has SMs.  moe_nvfp4_forward_routed always launches
+ * the scan separately.  No work is enqueued (reads the device's SM count). */
 MOE_API int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags);
 
 /* Byte offsets of the intermediates inside the workspace (for tests and
@@ -296,10 +347,15 @@ typedef struct {
     uint64_t h_bf16;         /* bf16  [rows_cap][I] FC2 input (W4A16)        */
     uint64_t o_bf16;         /* bf16  [rows_cap][H] per-route FC2 output     */
     uint64_t y_acc;          /* f32   [T][H] fused-finalize accumulator      */
+    uint64_t row_amax;       /* u32   [rows_cap] per-token: float bits of    */
+                             /*   each route row's FC2-input |max|           */
+    uint64_t tile_done;      /* u32   [2*rows_cap/128] per-token: FC1        */
+                             /*   epilogue arrivals per M tile / half        */
+    uint64_t logits;         /* f32   [T][E] router logits (MOE_ROUTER_GEMM) */
     uint64_t total;          /* workspace bytes                              */
 } moe_workspace_layout;
 
-#define MOE_WORKSPACE_VERSION 5
+#define MOE_WORKSPACE_VERSION 6
 
 /* Fill `out` with the workspace layout for this shape and flags.  Regions a
  * mode does not use have offset UINT64_MAX.  Pure host call, no CUDA. */
@@ -350,7 +406,11 @@ MOE_API moe_status moe_nvfp4_debug_convert(const float* in, int64_t n, uint8_t* 
  * whose work may overlap on the GPU (different streams, or other host
  * threads) race and must be serialized by the caller.  The first call on each
  * device looks up the array's device address (cudaGetSymbolAddress) and
- * prepares the kernels; make that first call before any stream capture.
+ * prepares the kernels; make that first call before any stream capture (a
+ * CUDA error during that look-up is returned and the look-up retried on the
+ * next call).  There is no device status to read back: the status word of
+ * the kernels lives in the shared array, and the router only produces ids in
+ * [0, E), so the permutation's bad-id checks cannot trigger.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE, MOE_ERR_UNSUPPORTED,
  * MOE_ERR_CUDA.  Enqueues four kernels on `stream`; does not synchronize. */
 #define MOE_NOALLOC_SCRATCH_BYTES (1 << 20)

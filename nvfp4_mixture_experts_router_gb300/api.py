@@ -36,6 +36,8 @@ MOE_QUANT_4OVER6 = 1 << 9
 MOE_FUSED_LAYER = 1 << 10
 MOE_GEMM_SWAP_NEVER = 1 << 11
 MOE_GEMM_SWAP_ALWAYS = 1 << 12
+MOE_DEBUG_FC1_SKIP_STAGE = 1 << 13
+MOE_ROUTER_GEMM = 1 << 14
 MOE_W8A8_MXFP8 = 3 << 2
 
 
@@ -53,7 +55,7 @@ class moe_shape(ctypes.Structure):
 _LAYOUT_FIELDS = ["rows_cap", "status", "topk_ids", "topk_w", "count", "offsets", "padded_offsets", "meta",
                   "unit_base", "unit_mask", "row_of_route", "route_of_row", "tile_expert", "tile_pair", "tile_half", "g1",
                   "xq_codes", "xq_sf", "h_f32", "g2", "hq_codes", "hq_sf", "x_bf16_perm", "h_bf16", "o_bf16",
-                  "y_acc", "total"]
+                  "y_acc", "row_amax", "tile_done", "logits", "total"]
 
 
 class moe_workspace_layout(ctypes.Structure):
@@ -88,6 +90,8 @@ def lib():
             "moe_nvfp4_debug_convert": (ctypes.c_int, [P, i64, P, P, P]),
             "moe_nvfp4_route_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, u32, P, P,
                                                        P, P, P, P, P, P, P, P]),
+            "moe_nvfp4_router_logits": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P]),
+            "moe_nvfp4_forward_gate": (ctypes.c_int, [S, u32, P, P, P, P, P, P, P, sz, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -101,7 +105,8 @@ EXPORTED = ["moe_nvfp4_version", "moe_nvfp4_prepared_bytes", "moe_nvfp4_prepare_
             "moe_nvfp4_workspace_bytes", "moe_nvfp4_workspace_layout", "moe_nvfp4_forward",
             "moe_nvfp4_forward_routed",
             "moe_nvfp4_forward_staged", "moe_nvfp4_forward_launches",
-            "moe_nvfp4_last_device_status", "moe_nvfp4_debug_convert", "moe_nvfp4_route_noalloc"]
+            "moe_nvfp4_last_device_status", "moe_nvfp4_debug_convert", "moe_nvfp4_route_noalloc",
+            "moe_nvfp4_router_logits", "moe_nvfp4_forward_gate"]
 EXPORTED.sort()
 NUM_STAGE_EVENTS = 8
 STAGES = ["router", "permute", "quantize_x", "fc1", "quantize_h", "fc2", "finalize"]
@@ -180,6 +185,35 @@ def moe_nvfp4_forward_routed(s: moe_shape, flags: int, x_bf16: torch.Tensor, top
                                           _ptr(workspace), workspace.numel() * workspace.element_size(),
                                           _ptr(y_bf16), _stream(stream))
     _check("moe_nvfp4_forward_routed", code)
+
+
+def moe_nvfp4_router_logits(x_bf16: torch.Tensor, gate_w_bf16: torch.Tensor, logits: torch.Tensor,
+                            stream=None) -> None:
+    """logits [T, E] float32 = x [T, H] . gate_w [E, H]^T (BF16, CUDA, contiguous)."""
+    T, H = x_bf16.shape
+    E = gate_w_bf16.shape[0]
+    if x_bf16.dtype != torch.bfloat16 or gate_w_bf16.dtype != torch.bfloat16 or logits.dtype != torch.float32:
+        raise TypeError("x and gate_w must be bfloat16, logits float32")
+    if tuple(gate_w_bf16.shape) != (E, H) or tuple(logits.shape) != (T, E):
+        raise ValueError("shapes must be x [T, H], gate_w [E, H], logits [T, E]")
+    if not (x_bf16.is_contiguous() and gate_w_bf16.is_contiguous() and logits.is_contiguous()):
+        raise ValueError("x, gate_w and logits must be contiguous")
+    code = lib().moe_nvfp4_router_logits(T, E, H, _ptr(x_bf16), _ptr(gate_w_bf16), _ptr(logits), _stream(stream))
+    _check("moe_nvfp4_router_logits", code)
+
+
+def moe_nvfp4_forward_gate(s: moe_shape, flags: int, x_bf16: torch.Tensor, gate_w_bf16: torch.Tensor,
+                           router_bias: Optional[torch.Tensor], act_scale_fc1: Optional[torch.Tensor],
+                           act_scale_fc2: Optional[torch.Tensor], prepared: torch.Tensor, workspace: torch.Tensor,
+                           y_bf16: torch.Tensor, stream=None) -> None:
+    """Forward from the gate projection: flags must include MOE_ROUTER_GEMM;
+    gate_w_bf16 is W_g [E, H] (CUDA, contiguous)."""
+    if gate_w_bf16.dtype != torch.bfloat16 or tuple(gate_w_bf16.shape) != (s.E, s.H):
+        raise ValueError(f"gate_w must be bfloat16 [{s.E}, {s.H}]")
+    code = lib().moe_nvfp4_forward_gate(s, flags, _ptr(x_bf16), _ptr(gate_w_bf16), _ptr(router_bias),
+                                        _ptr(act_scale_fc1), _ptr(act_scale_fc2), _ptr(prepared), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _ptr(y_bf16), _stream(stream))
+    _check("moe_nvfp4_forward_gate", code)
 
 
 def moe_nvfp4_forward_staged(s: moe_shape, flags: int, x_bf16, router_logits, router_bias, act_scale_fc1,
@@ -266,6 +300,13 @@ class MoELayer:
             y = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=x_bf16.device)
         moe_nvfp4_forward(self.shape, self.flags, x_bf16, logits, bias, g1, g2, self.prepared, self.workspace,
                           y, stream)
+        return y
+
+    def forward_gate(self, x_bf16, gate_w_bf16, bias=None, g1=None, g2=None, y=None, stream=None) -> torch.Tensor:
+        if y is None:
+            y = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=x_bf16.device)
+        moe_nvfp4_forward_gate(self.shape, self.flags, x_bf16, gate_w_bf16, bias, g1, g2, self.prepared,
+                               self.workspace, y, stream)
         return y
 
     def forward_routed(self, x_bf16, topk_ids, topk_weights, g1=None, g2=None, y=None, stream=None) -> torch.Tensor:

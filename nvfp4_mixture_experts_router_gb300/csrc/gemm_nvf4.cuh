@@ -257,6 +257,12 @@ __device__ __forceinline__ bool gemm_tiles(const Smem& s, uint32_t tmem_base, co
                     p.sfb + ((size_t)e * rb_per_expert + (size_t)n_tile * C::kRowBlocks) * atoms * 512;
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) return false;
+                    if (p.debug_skip_first_stage && blockIdx.x == 0 && tile == (int)blockIdx.x && ks == 0) {
+                        // test hook: nothing issued, nothing arrives on this
+                        // stage's barriers; the consumers' bounded waits give up
+                        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
                     const int n_at = min(kAtoms, atoms - kAtoms * ks);
                     const uint32_t sf_bytes = (uint32_t)n_at * 512u;
                     // the small scale atoms first, on their own barrier, so the
@@ -404,7 +410,18 @@ __device__ __forceinline__ bool gemm_tiles(const Smem& s, uint32_t tmem_base, co
                 break;
             tc_fence_after();
             const int width = min(BN, p.n - n_tile * BN);
-            if (half * 128 < width) {
+            if constexpr (EPI == kEpiFc1Tok || EPI == kEpiFc1Tok46) {
+                // every epilogue warp of every N tile of the M tile arrives
+                // once on its counter, then waits for all of them
+                const int row = m_tile * kBM + q * 32 + lane;
+                const int route = p.route_of_row[row];
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + half * 128);
+                if (!epilogue_fc1_tok<EPI == kEpiFc1Tok46>(p, taddr, row, route, e, n_tile * C::kRowBlocks + half,
+                                                            half * 128 < width, p.tile_done + m_tile,
+                                                            (unsigned int)(n_tiles * C::kEpiWarps), s.abort))
+                    break;
+            } else if (half * 128 < width) {
                 const int row = m_tile * kBM + q * 32 + lane;
                 const int route = p.route_of_row[row];
                 const uint32_t taddr =

@@ -57,11 +57,14 @@ cudaError_t launch_route_given(const LaunchCtx& c, int T, int E, int K, const in
 cudaError_t launch_route_scan_small(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
                                     int renorm, int* ids, float* w, int* unit_base, uint32_t* unit_mask, int* count,
                                     int* offsets, int* padded_offsets, int* meta, int* tile_expert, int* tile_pair,
-                                    int* tile_half, int* route_of_row, unsigned int* status_reset);
-// tile_pair / tile_half may be null (then only meta[2] / meta[3] count them)
+                                    int* tile_half, int* route_of_row, unsigned int* status_reset,
+                                    unsigned int* tile_done = nullptr);
+// tile_pair / tile_half may be null (then only meta[2] / meta[3] count them);
+// tile_done (may be null): the FC1 epilogue's arrival counters, zeroed for
+// every M tile and every entry of the half list
 cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
                                 int* padded_offsets, int* meta, int* tile_expert, int* tile_pair, int* tile_half,
-                                int* route_of_row);
+                                int* route_of_row, unsigned int* tile_done = nullptr);
 cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base,
                            uint32_t* unit_mask, int* count, int* offsets, int* padded_offsets, int* meta,
                            int* tile_expert, int* row_of_route, int* route_of_row, unsigned int* status);
@@ -75,6 +78,7 @@ struct RouteScatter {
     int E;
     int* row_of_route;          // [T*K] out
     int* route_of_row;          // [rows_cap] out (valid rows)
+    unsigned int* row_amax;     // [rows_cap] zeroed for every route row (null: not used)
 };
 
 // rowops.cu
@@ -109,7 +113,10 @@ enum GemmEpilogue : int {
     kEpiFc2Store = 2,   // FC2: BF16 per-route rows (deterministic finalize)
     kEpiFc2Scatter = 3, // FC2: weighted FP32 atomic add into the token row (fused finalize)
     kEpiFc1Bf16 = 4,    // FC1 (W4A16): activation, route weight, BF16 store
-    kEpiFc1Mx = 5       // FC1 (MXFP8): activation, route weight, MXFP8 requant (block 32)
+    kEpiFc1Mx = 5,      // FC1 (MXFP8): activation, route weight, MXFP8 requant (block 32)
+    kEpiFc1Tok = 6,     // FC1: activation, route weight, NVFP4 requant with the per-row G2 (row amax
+                        // gathered across the M tile's N tiles through row_amax / tile_done)
+    kEpiFc1Tok46 = 7    // the same with 4-over-6 blocks
 };
 
 struct GemmParams {
@@ -143,6 +150,12 @@ struct GemmParams {
     float* out_f32;              // FC1 F32: [rows_cap][I]; FC2 scatter: y_acc [T][H]
                                  // (g_act == nullptr: no activation global scale, W4A16)
     __nv_bfloat16* out_bf16;     // FC2 store: [rows_cap][H]; FC1 BF16: [rows_cap][I]
+    int debug_skip_first_stage;  // test hook: CTA 0's producer skips its first stage (standard GEMM)
+    // kEpiFc1Tok*: per-row FC2-input scale computed inside FC1
+    unsigned int* row_amax;      // [rows_cap] float bits of the row's |h| max, zero before FC1
+    unsigned int* tile_done;     // [2 rows_cap/128] epilogue-warp arrivals per M tile (standard) or per
+                                 // occupied half (swapped), zero before FC1
+    float* g2_out;               // [rows_cap] G2 of each route row
 };
 
 cudaError_t setup_gemm_kernels();
@@ -160,6 +173,15 @@ cudaError_t launch_gemm_nvf4(const LaunchCtx& c, int epilogue, const CUtensorMap
 cudaError_t setup_gemm_pair_kernels(int device, int num_sms);
 cudaError_t launch_gemm_nvf4_pair(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   const GemmParams& p, int device);
+
+// router_gemm.cu — logits = x . W_g^T on the tensor cores (BF16, FP32
+// accumulate).  tmX: 2-D uint8 map over x [T][2H] bytes, box 128 B x 128
+// rows; tmW: over W_g [E][2H] bytes, box 128 B x router_gemm_tile_n(E) rows.
+// status may be null.
+cudaError_t setup_router_gemm_kernel();
+int router_gemm_tile_n(int E);
+cudaError_t launch_router_gemm(const LaunchCtx& c, const CUtensorMap& tmX, const CUtensorMap& tmW, int T, int E,
+                               int H, float* logits, unsigned int* status);
 
 // gemm_swap.cu — the W4A4 GEMMs with the weights on the MMA's M side (128
 // rows per operand, two operands per tile) and 64 routes on its N side, for

@@ -43,7 +43,8 @@ moe_status device_state(int* sms, int* device = nullptr) {
             d.status = MOE_ERR_UNSUPPORTED;  // the binary carries sm_103a code only
         } else if (setup_routing_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess ||
                    setup_gemm_w4a16_kernels() != cudaSuccess || setup_gemm_pair_kernels(dev, d.sms) != cudaSuccess ||
-                   setup_fused_layer_kernel() != cudaSuccess || setup_gemm_swap_kernels() != cudaSuccess) {
+                   setup_fused_layer_kernel() != cudaSuccess || setup_gemm_swap_kernels() != cudaSuccess ||
+                   setup_router_gemm_kernel() != cudaSuccess) {
             d.status = MOE_ERR_CUDA;
         } else {
             d.status = MOE_OK;
@@ -86,6 +87,13 @@ moe_status validate_shape(moe_shape s, uint32_t flags) {
         // register layout (E <= 256) and single-CTA GEMM tiles
         const int m = mode_of(flags);
         if ((m != kModePerTensor && m != kModePerToken) || s.E > kFusedMaxExperts || (flags & MOE_GEMM_PAIRS_ALWAYS))
+            return MOE_ERR_INVALID_ARG;
+    }
+    if ((flags & MOE_ROUTER_GEMM) && (flags & MOE_FUSED_LAYER)) return MOE_ERR_INVALID_ARG;
+    if (flags & MOE_DEBUG_FC1_SKIP_STAGE) {
+        const int m = mode_of(flags);
+        if ((m != kModePerTensor && m != kModePerToken) || !(flags & MOE_GEMM_SWAP_NEVER) ||
+            (flags & (MOE_GEMM_PAIRS_ALWAYS | MOE_FUSED_LAYER)))
             return MOE_ERR_INVALID_ARG;
     }
     if (act_of(flags) > 1) return MOE_ERR_INVALID_ARG;
@@ -182,7 +190,7 @@ bool use_pair_gemm(moe_shape s, uint32_t flags, int n) {
 
 extern "C" {
 
-const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.4 sm_103a (prepared v1, workspace v5)"; }
+const char* moe_nvfp4_version(void) { return "moe_nvfp4 1.5 sm_103a (prepared v1, workspace v6)"; }
 
 size_t moe_nvfp4_prepared_bytes(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return 0;
@@ -227,6 +235,7 @@ struct RoutingIn {
     const float* bias = nullptr;
     const int32_t* ids = nullptr;
     const float* w = nullptr;
+    bool status_cleared = false;   // an earlier kernel of this forward may have raised status bits
 };
 
 // MOE_FUSED_LAYER: every step in one cooperative persistent launch.  The
@@ -420,6 +429,23 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         return forward_fused(s, flags, x_bf16, rin, act_scale_fc1, act_scale_fc2, P, pw, W, ws, y_bf16, sms,
                              static_cast<cudaStream_t>(stream), events);
 
+    // GEMM variants of the W4A4 / W8A8 modes (host decisions only)
+    const bool mx = mode == kModeMxfp8;
+    const bool per_token = mode == kModePerToken;
+    const bool swap = mode != kModeW4A16 && !mx && use_swap_gemm(s, flags);
+    const bool pair1 = mode != kModeW4A16 && !mx && !swap && use_pair_gemm(s, flags, N1),
+               pair2 = mode != kModeW4A16 && !mx && !swap && use_pair_gemm(s, flags, s.H);
+    const int tn1 = pair1 ? 128 : gemm_nvf4_tile_n(s.H, N1), tn2 = pair2 ? 128 : gemm_nvf4_tile_n(s.I, s.H);
+    // Per-token FC2-input quantization inside the FC1 epilogue: the epilogue
+    // warps of an M tile's (a route half's) N tiles wait for one another, so
+    // all of them must be able to hold an accumulator at once -- at most one
+    // tile per CTA of the persistent grid.  Otherwise (and on CTA pairs) FC1
+    // stores FP32 and a separate kernel quantizes.
+    const int fc1_tiles_per_m = swap ? (N1 / 128 + 1) / 2 : (N1 + tn1 - 1) / tn1;
+    const bool tok_fused = false && per_token && !pair1 && fc1_tiles_per_m <= sms;
+    unsigned int* row_amax = tok_fused ? reinterpret_cast<unsigned int*>(wsp(W.row_amax)) : nullptr;
+    unsigned int* tile_done = tok_fused ? reinterpret_cast<unsigned int*>(wsp(W.tile_done)) : nullptr;
+
     LaunchCtx c;
     c.stream = static_cast<cudaStream_t>(stream);
     c.pdl = events == nullptr;   // stage events between kernels would serialize them anyway
@@ -446,11 +472,12 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
                                     reinterpret_cast<uint32_t*>(wsp(W.unit_mask)), reinterpret_cast<int*>(wsp(W.count)),
                                     reinterpret_cast<int*>(wsp(W.offsets)), reinterpret_cast<int*>(wsp(W.padded_offsets)),
                                     meta, tile_expert, reinterpret_cast<int*>(wsp(W.tile_pair)),
-                                    reinterpret_cast<int*>(wsp(W.tile_half)), route_of_row, status);
+                                    reinterpret_cast<int*>(wsp(W.tile_half)), route_of_row,
+                                    rin.status_cleared ? nullptr : status, tile_done);
     } else {
         e = launch_route_count(c, s.T, s.E, s.K, rin.logits, rin.bias, (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1, ids,
                                topk_w, reinterpret_cast<int*>(wsp(W.unit_base)),
-                               reinterpret_cast<uint32_t*>(wsp(W.unit_mask)), status);
+                               reinterpret_cast<uint32_t*>(wsp(W.unit_mask)), rin.status_cleared ? nullptr : status);
     }
     if (e != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
     if (given || s.T > kUnitTokens) {
@@ -458,7 +485,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
                                 reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
                                 reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert,
                                 reinterpret_cast<int*>(wsp(W.tile_pair)), reinterpret_cast<int*>(wsp(W.tile_half)),
-                                route_of_row);
+                                route_of_row, tile_done);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     if (!mark(2)) return MOE_ERR_CUDA;
@@ -470,6 +497,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     rs.E = s.E;
     rs.row_of_route = row_of_route;
     rs.route_of_row = route_of_row;
+    rs.row_amax = row_amax;
 
     if (mode == kModeW4A16) {
         // ---- W4A16: BF16 activations, weights widened on chip ----
@@ -536,8 +564,6 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     }
 
     // ---- W4A4 (NVFP4) and W8A8 (MXFP8) ----
-    const bool mx = mode == kModeMxfp8;
-    const bool per_token = mode == kModePerToken;
     float* g1 = mx ? nullptr : reinterpret_cast<float*>(wsp(W.g1));
     uint8_t* xq_codes = wsp(W.xq_codes);
     uint8_t* xq_sf = wsp(W.xq_sf);
@@ -553,10 +579,6 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
 
     // operand rows: NVFP4 half a byte per element, MXFP8 a byte
     const uint64_t rbx = mx ? (uint64_t)s.H : (uint64_t)s.H / 2, rbh = mx ? (uint64_t)s.I : (uint64_t)s.I / 2;
-    const bool swap = !mx && use_swap_gemm(s, flags);
-    const bool pair1 = !mx && !swap && use_pair_gemm(s, flags, N1),
-               pair2 = !mx && !swap && use_pair_gemm(s, flags, s.H);
-    const int tn1 = pair1 ? 128 : gemm_nvf4_tile_n(s.H, N1), tn2 = pair2 ? 128 : gemm_nvf4_tile_n(s.I, s.H);
     // single-CTA GEMMs with 128-wide tiles over rows of a multiple of 128
     // bytes copy two chunks per TMA instruction (3-D maps); the others use
     // 2-D maps
@@ -598,12 +620,22 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     g1p.topk_w = topk_w;
     g1p.weight_on_input = on_input ? 1 : 0;
     g1p.out_cols = s.I;
+    g1p.debug_skip_first_stage = (flags & MOE_DEBUG_FC1_SKIP_STAGE) ? 1 : 0;
     int epi1;
     if (mx) {
         g1p.g_act = nullptr;           // MXFP8: no activation global scale
         g1p.out_codes = hq_codes;
         g1p.out_sf = hq_sf;
         epi1 = kEpiFc1Mx;
+    } else if (per_token && tok_fused) {
+        g1p.g_act = g1;
+        g1p.g_act_per_token = 1;
+        g1p.out_codes = hq_codes;
+        g1p.out_sf = hq_sf;
+        g1p.row_amax = row_amax;
+        g1p.tile_done = tile_done;
+        g1p.g2_out = reinterpret_cast<float*>(wsp(W.g2));
+        epi1 = four_six ? kEpiFc1Tok46 : kEpiFc1Tok;
     } else if (per_token) {
         g1p.g_act = g1;
         g1p.g_act_per_token = 1;
@@ -621,7 +653,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         : pair1 ? launch_gemm_nvf4_pair(c, epi1, tmA1, tmB1, g1p, device)
                 : launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms, tn1, mx ? 1 : 0);
     if (e != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
-    if (per_token) {
+    if (per_token && !tok_fused) {
         e = launch_quantize_h(c, W.rows_cap, s.I, meta, route_of_row, reinterpret_cast<const float*>(wsp(W.h_f32)),
                               reinterpret_cast<float*>(wsp(W.g2)), hq_codes, hq_sf, four_six ? 1 : 0);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -664,9 +696,9 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     } else {
         g2p.out_f32 = y_acc;
         epi2 = kEpiFc2Scatter;
-        // an accumulator beyond half the L2: walk FC2's output width in slabs
-        // whose accumulator slice stays in L2 (T x slab x 4 B <= 48 MB), so
-        // that a token's K reductions do not each go through HBM
+        // an accumulator beyond 48 MB: walk FC2's output width in slabs whose
+        // accumulator slice stays in L2 (T x slab x 4 B <= 48 MB), so that a
+        // token's K reductions do not each go through HBM
         const uint64_t slab_bytes_per_tile = (uint64_t)s.T * (uint64_t)tn2 * 4u;
         if (!swap && !pair2 && (uint64_t)s.T * s.H * 4u > kSlabAccBytes) {
             const uint64_t ns = kSlabAccBytes / slab_bytes_per_tile;
@@ -691,6 +723,7 @@ moe_status moe_nvfp4_forward(moe_shape s, uint32_t flags, const void* x_bf16, co
                              const float* router_bias, const float* act_scale_fc1, const float* act_scale_fc2,
                              const void* prepared, void* workspace, size_t workspace_bytes, void* y_bf16,
                              void* stream) {
+    if (flags & MOE_ROUTER_GEMM) return MOE_ERR_INVALID_ARG;   // logits come from the caller here
     RoutingIn rin;
     rin.logits = router_logits;
     rin.bias = router_bias;
@@ -702,7 +735,7 @@ moe_status moe_nvfp4_forward_routed(moe_shape s, uint32_t flags, const void* x_b
                                     const float* topk_weights, const float* act_scale_fc1,
                                     const float* act_scale_fc2, const void* prepared, void* workspace,
                                     size_t workspace_bytes, void* y_bf16, void* stream) {
-    if (!topk_ids) return MOE_ERR_INVALID_ARG;
+    if (!topk_ids || (flags & MOE_ROUTER_GEMM)) return MOE_ERR_INVALID_ARG;
     RoutingIn rin;
     rin.ids = topk_ids;
     rin.w = topk_weights;
@@ -714,7 +747,7 @@ moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags, const void* x_b
                                     const float* router_bias, const float* act_scale_fc1,
                                     const float* act_scale_fc2, const void* prepared, void* workspace,
                                     size_t workspace_bytes, void* y_bf16, void* stream, void* const* events) {
-    if (!events) return MOE_ERR_INVALID_ARG;
+    if (!events || (flags & MOE_ROUTER_GEMM)) return MOE_ERR_INVALID_ARG;
     for (int i = 0; i < MOE_NUM_STAGE_EVENTS; ++i)
         if (!events[i]) return MOE_ERR_INVALID_ARG;
     RoutingIn rin;
@@ -724,13 +757,88 @@ moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags, const void* x_b
                         y_bf16, stream, events);
 }
 
+// 2-D uint8 maps of the router GEMM's BF16 operands (rows of 2H bytes,
+// 128-byte boxes, 128-byte swizzle).
+static bool encode_router_maps(CUtensorMap* tmX, CUtensorMap* tmW, const void* x, const void* gate_w, int T, int E,
+                               int H) {
+    return encode_operand_map(tmX, x, (uint64_t)T, (uint64_t)H * 2, 128, 128) &&
+           encode_operand_map(tmW, gate_w, (uint64_t)E, (uint64_t)H * 2, 128, (uint32_t)router_gemm_tile_n(E));
+}
+
+static bool router_gemm_args_ok(int T, int E, int H, const void* x, const void* gate_w, const void* logits) {
+    if (T < 1 || T > (1 << 22) || E < 1 || E > 1024 || H < 128 || H % 128 != 0 || H > 65536) return false;
+    if (!x || !gate_w || !logits || !aligned(x, 16) || !aligned(gate_w, 16) || !aligned(logits, 16)) return false;
+    const size_t lb = (size_t)T * E * 4;
+    return !overlaps(logits, lb, x, (size_t)T * H * 2) && !overlaps(logits, lb, gate_w, (size_t)E * H * 2);
+}
+
+moe_status moe_nvfp4_router_logits(int T, int E, int H, const void* x_bf16, const void* gate_w_bf16, float* logits,
+                                   void* stream) {
+    if (!router_gemm_args_ok(T, E, H, x_bf16, gate_w_bf16, logits)) return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    const moe_status st = device_state(&sms);
+    if (st != MOE_OK) return st;
+    CUtensorMap tmX, tmW;
+    if (!encode_router_maps(&tmX, &tmW, x_bf16, gate_w_bf16, T, E, H)) return MOE_ERR_CUDA;
+    LaunchCtx c;
+    c.stream = static_cast<cudaStream_t>(stream);
+    return cuda_status(launch_router_gemm(c, tmX, tmW, T, E, H, logits, nullptr));
+}
+
+moe_status moe_nvfp4_forward_gate(moe_shape s, uint32_t flags, const void* x_bf16, const void* gate_w_bf16,
+                                  const float* router_bias, const float* act_scale_fc1, const float* act_scale_fc2,
+                                  const void* prepared, void* workspace, size_t workspace_bytes, void* y_bf16,
+                                  void* stream) {
+    if (!(flags & MOE_ROUTER_GEMM)) return MOE_ERR_INVALID_ARG;
+    moe_status st = validate_shape(s, flags);
+    if (st != MOE_OK) return st;
+    if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    const moe_workspace_layout W = workspace_layout(s, flags);
+    if (workspace_bytes < W.total) return MOE_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* logits = reinterpret_cast<float*>(ws + W.logits);
+    if (!router_gemm_args_ok(s.T, s.E, s.H, x_bf16, gate_w_bf16, logits) ||
+        overlaps(gate_w_bf16, (size_t)s.E * s.H * 2, workspace, W.total))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    st = device_state(&sms);
+    if (st != MOE_OK) return st;
+    CUtensorMap tmX, tmW;
+    if (!encode_router_maps(&tmX, &tmW, x_bf16, gate_w_bf16, s.T, s.E, s.H)) return MOE_ERR_CUDA;
+    LaunchCtx c;
+    c.stream = static_cast<cudaStream_t>(stream);
+    unsigned int* status = reinterpret_cast<unsigned int*>(ws + W.status);
+    // the status word is cleared here, before the logits kernel (which can
+    // raise a timeout bit), rather than by the router
+    if (cudaMemsetAsync(status, 0, 16, c.stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_router_gemm(c, tmX, tmW, s.T, s.E, s.H, logits, status) != cudaSuccess) return MOE_ERR_CUDA;
+    RoutingIn rin;
+    rin.logits = logits;
+    rin.bias = router_bias;
+    rin.status_cleared = true;
+    return forward_impl(s, flags, x_bf16, rin, act_scale_fc1, act_scale_fc2, prepared, workspace, workspace_bytes,
+                        y_bf16, stream, nullptr);
+}
+
 int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return -1;
     if (flags & MOE_FUSED_LAYER) return 1;
+    // the per-token FC2-input quantization is a separate kernel only on CTA
+    // pairs, or when FC1 has more N tiles per M tile (route half) than the
+    // GPU has SMs (the shapes of this check run on any sm_103 part)
+    int extra = 0;
+    if (mode_of(flags) == kModePerToken) {
+        const int N1 = n1_of(s.I, flags);
+        const bool swap = use_swap_gemm(s, flags), pair1 = !swap && use_pair_gemm(s, flags, N1);
+        const int per_m = swap ? (N1 / 128 + 1) / 2 : (N1 + gemm_nvf4_tile_n(s.H, N1) - 1) / gemm_nvf4_tile_n(s.H, N1);
+        int sms = 0;
+        const bool known = device_state(&sms) == MOE_OK;
+        extra = (true || pair1 || !known || per_m > sms) ? 1 : 0;
+    }
     // T <= 32: router and scan in one launch
-    if (s.T <= kUnitTokens) return 5 + (mode_of(flags) == kModePerToken ? 1 : 0);
+    if (s.T <= kUnitTokens) return 5 + extra;
     // router + unit counts, scan, quantize or gather (+ row scatter), FC1, [FC2-input quant], FC2, finalize
-    return 6 + (mode_of(flags) == kModePerToken ? 1 : 0);
+    return 6 + extra;
 }
 
 moe_status moe_nvfp4_last_device_status(void* workspace, void* stream) {

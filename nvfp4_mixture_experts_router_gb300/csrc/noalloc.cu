@@ -27,6 +27,10 @@ static __device__ __align__(256) int g_route_scratch[kScratchInts];
 // Host-side addresses of g_route_scratch, looked up once per device (the
 // array's name in host code is only a stand-in for the symbol, not a device
 // address).
+// A device's outcome is kept once it is final (the address found, or the
+// GPU is not one this library runs on); a CUDA error during the look-up (for
+// example a first call made inside a stream capture) is returned but not
+// kept, so that a later call tries again.
 std::mutex g_mu;
 int* g_scratch_ptr[64] = {};
 moe_status g_state[64] = {};
@@ -38,7 +42,6 @@ moe_status scratch_for_current_device(int** out) {
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_ready[dev]) {
-        g_ready[dev] = true;
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
@@ -57,6 +60,7 @@ moe_status scratch_for_current_device(int** out) {
                 g_state[dev] = MOE_OK;
             }
         }
+        g_ready[dev] = g_state[dev] != MOE_ERR_CUDA;
     }
     *out = g_scratch_ptr[dev];
     return g_state[dev];

@@ -244,9 +244,13 @@ def gen_logits(c: MoEConfig, device="cpu", x: Optional[torch.Tensor] = None) -> 
         return normal_f32(c.seed, STREAM_LOGITS, 0, c.T * c.E, 1.0, device).view(c.T, c.E)
     if x is None:
         x = gen_x(c, device)
-    wg = normal_f32(c.seed, STREAM_WG, 0, c.E * c.H, 1.0 / math.sqrt(c.H), device).view(c.E, c.H)
-    wg = wg.to(torch.bfloat16)
+    wg = gen_wg(c, device)
     return (x.double() @ wg.double().t()).to(torch.float32)
+
+
+def gen_wg(c: MoEConfig, device="cpu") -> torch.Tensor:
+    """Router (gate projection) weight W_g: BF16 [E, H], N(0, 1/H)."""
+    return normal_f32(c.seed, STREAM_WG, 0, c.E * c.H, 1.0 / math.sqrt(c.H), device).view(c.E, c.H).to(torch.bfloat16)
 
 
 def gen_w1_expert(c: MoEConfig, e: int, device="cpu") -> torch.Tensor:

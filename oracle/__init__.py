@@ -231,6 +231,18 @@ def dequant_rows(codes: np.ndarray, sf: np.ndarray) -> np.ndarray:
 # router and grouping
 # ---------------------------------------------------------------------------
 
+def router_logits(x_bf16: np.ndarray, wg_bf16: np.ndarray) -> np.ndarray:
+    """Router logits of the optional first stage, logits = x . W_g^T
+    [FlashInfer PR #4366, "Motivation": the MoE wrapper is handed routing
+    computed upstream from the gate projection; here that projection is the
+    layer's own first step].  Reading: BF16 x [T, H] and W_g [E, H] taken
+    exactly, products summed in FP64 (a library matmul), the sum rounded once
+    to FP32 (round to nearest even) -- the FP32 logits the router consumes."""
+    x = bf16_bits_to_f64(np.ascontiguousarray(x_bf16, dtype=np.uint16))
+    w = bf16_bits_to_f64(np.ascontiguousarray(wg_bf16, dtype=np.uint16))
+    return (x @ w.T).astype(np.float32)
+
+
 def router(logits: np.ndarray, bias: Optional[np.ndarray], K: int, renorm: bool = True):
     logits = np.ascontiguousarray(logits, dtype=np.float32)
     T, E = logits.shape

@@ -78,7 +78,17 @@ def test_invalid_arguments_rejected_before_cuda(L):
     W = ctypes.c_void_p(1 << 36)
     f = L.moe_nvfp4_forward
     # unknown flag bits, bad mode, bad activation
-    assert f(s, 1 << 13, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert f(s, 1 << 15, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    # the router-GEMM flag belongs to moe_nvfp4_forward_gate only
+    assert f(s, api.MOE_ROUTER_GEMM, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert api.moe_nvfp4_workspace_bytes(s, api.MOE_ROUTER_GEMM) >= wb + 16 * 8 * 4   # room for the logits
+    # the bounded-wait test hook: launch sequence, W4A4, standard orientation only
+    dbg, sn = api.MOE_DEBUG_FC1_SKIP_STAGE, api.MOE_GEMM_SWAP_NEVER
+    assert f(s, dbg, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert f(s, dbg | sn | api.MOE_FUSED_LAYER, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert f(s, dbg | sn | api.MOE_GEMM_PAIRS_ALWAYS, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert f(s, dbg | sn | api.MOE_W4A16, A, B, None, None, None, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
+    assert api.moe_nvfp4_workspace_bytes(s, dbg | sn) == wb
     # GEMM orientation hints: not both, and the swapped one only for W4A4 on the launch sequence
     sw, sn = api.MOE_GEMM_SWAP_ALWAYS, api.MOE_GEMM_SWAP_NEVER
     assert f(s, sw | sn, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG

@@ -1,7 +1,10 @@
 """Parity at the workloads' full sizes, through the same entry point and
 launch configuration the benchmark times: routing, permutation and the x
 quantization checked bit for bit on every token, the expert MLPs (FC2-input
-codes and y) on a seeded sample of tokens the oracle computes one by one."""
+codes, scales, per-token G2 and y) on a seeded sample of tokens the oracle
+computes one by one: 256 tokens ({0, 1, T-1} and 253 more) at the DSV3 shape
+with 4096 tokens and at prefill scale, fewer where a case only adds a
+variant of a path those two already cover."""
 import pytest
 
 from nvfp4_mixture_experts_router_gb300 import api, build, synth
@@ -20,7 +23,7 @@ def _lib():
 def test_dsv3_shape_T4096_deterministic():
     """DeepSeek-V3-like expert shape: T=4096, H=7168, I=2048, E=256, top-8,
     per-tensor scales, deterministic finalize."""
-    r = fullsize_parity(synth.config(2, 4096), n_tokens=24)
+    r = fullsize_parity(synth.config(2, 4096), n_tokens=256)
     assert r["code_match"] >= 0.999
 
 
@@ -52,7 +55,7 @@ def test_prefill_T16384_zipf():
     ids, _ = oracle.router(synth.gen_logits(c).numpy(), synth.gen_bias(c).numpy(), c.K)
     count = np.bincount(ids.reshape(-1), minlength=c.E)
     assert count.max() >= 10 * count.mean() and (count == 0).any()
-    r = fullsize_parity(c, n_tokens=16)
+    r = fullsize_parity(c, n_tokens=256)
     assert r["code_match"] >= 0.999
 
 
@@ -77,10 +80,13 @@ def test_prefill_T16384_single_kernel():
     assert r["code_match"] >= 0.999
 
 
-def test_fc2_output_slabs():
-    """Fused finalize with an accumulator beyond half the L2 (T x H x 4 B =
-    73 MB): FC2 walks its output width in slabs (51 and 5 N tiles here, a
-    narrower last slab) so a token's reductions stay in L2; same results."""
-    c = synth.MoEConfig("slab", 2560, 7168, 256, 8, 2, mode=synth.MODE_PER_TOKEN, seed=12, logits="normal")
+@pytest.mark.parametrize("T", [2560, 2000])
+def test_fc2_output_slabs(T):
+    """Fused finalize with an FP32 accumulator beyond 48 MB (T x H x 4 B =
+    73 MB at T = 2560, 57 MB at T = 2000): FC2 walks its output width in
+    slabs of at most 48 MiB of accumulator (38 + 18 and 49 + 7 of the 56
+    128-wide N tiles, the last slab narrower) so that a token's reductions
+    stay in L2; same results."""
+    c = synth.MoEConfig("slab", T, 7168, 256, 8, 2, mode=synth.MODE_PER_TOKEN, seed=12, logits="normal")
     r = fullsize_parity(c, n_tokens=24)
     assert r["code_match"] >= 0.999

@@ -395,6 +395,58 @@ def test_4over6_global_scale_bound():
 # router and grouping
 # ---------------------------------------------------------------------------
 
+def _f32_nearest(q) -> np.float32:
+    """The float32 nearest to the rational q, ties to the even significand
+    (exact comparisons of rationals; no intermediate rounding)."""
+    from fractions import Fraction
+    c = np.float32(float(q))
+    cands = [c, np.nextafter(c, np.float32(np.inf)), np.nextafter(c, np.float32(-np.inf))]
+    dist = [abs(Fraction(float(v)) - q) for v in cands]
+    best = min(dist)
+    tied = [v for v, d in zip(cands, dist) if d == best]
+    if len(tied) > 1:
+        tied = [v for v in tied if (np.array(v, np.float32).view(np.uint32) & 1) == 0]
+    return tied[0]
+
+
+def test_router_logits_exact_rational_bruteforce():
+    """x . W_g^T against sums of exact rationals rounded once to float32, on
+    random BF16 data (the products and sums carry no rounding at all)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(5)
+    T, E, H = 5, 7, 48
+    x = oracle.f64_to_bf16_bits(rng.standard_normal((T, H)))
+    wg = oracle.f64_to_bf16_bits(rng.standard_normal((E, H)) / np.sqrt(H))
+    got = oracle.router_logits(x, wg)
+    assert got.shape == (T, E) and got.dtype == np.float32
+    xf = oracle.bf16_bits_to_f64(x)
+    wf = oracle.bf16_bits_to_f64(wg)
+    for t in range(T):
+        for e in range(E):
+            q = sum(Fraction(float(xf[t, h])) * Fraction(float(wf[e, h])) for h in range(H))
+            assert got[t, e] == _f32_nearest(q), (t, e)
+
+
+def test_router_logits_closed_forms():
+    """Ones times a power of two is H * 2^-k exactly; a row that cancels
+    leaves exactly its last product; rows and columns follow x and W_g."""
+    H = 64
+    one = oracle.f64_to_bf16_bits(np.ones((2, H)))
+    wg = oracle.f64_to_bf16_bits(np.stack([np.full(H, 2.0 ** -k) for k in range(3)]))
+    got = oracle.router_logits(one, wg)
+    np.testing.assert_array_equal(got, np.tile(np.float32([H, H / 2, H / 4]), (2, 1)))
+    v = np.zeros(H)
+    v[0], v[1], v[2] = 3.0, -3.0, 0.375
+    got = oracle.router_logits(oracle.f64_to_bf16_bits(v[None, :]), oracle.f64_to_bf16_bits(np.ones((1, H))))
+    assert got[0, 0] == np.float32(0.375)
+    rng = np.random.default_rng(6)
+    x = oracle.f64_to_bf16_bits(rng.standard_normal((4, H)))
+    w = oracle.f64_to_bf16_bits(rng.standard_normal((5, H)))
+    base = oracle.router_logits(x, w)
+    np.testing.assert_array_equal(oracle.router_logits(x[::-1].copy(), w), base[::-1])
+    np.testing.assert_array_equal(oracle.router_logits(x, w[[4, 0, 2, 1, 3]].copy()), base[:, [4, 0, 2, 1, 3]])
+
+
 @pytest.mark.parametrize("renorm", [True, False])
 def test_router_matches_stable_sort(renorm):
     rng = np.random.default_rng(1)

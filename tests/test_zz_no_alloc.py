@@ -61,9 +61,14 @@ def test_route_noalloc_matches_forward_on_consecutive_calls():
     build.build()
     cases = [synth.config(1),                                              # T=512, E=64, top-6, biased logits
              synth.MoEConfig("b", 300, 256, 128, 16, 4, mode=synth.MODE_PER_TOKEN, seed=21,
-                             logits="normal", renorm=False)]
+                             logits="normal", renorm=False),
+             # decode sizes: the forward routes T <= 32 with its one-block
+             # router + scan; here E = 40 is not a multiple of 32
+             synth.config(0).with_(mode=synth.MODE_PER_TOKEN),             # T=16, E=8, top-2
+             synth.MoEConfig("d", 24, 256, 128, 40, 3, mode=synth.MODE_PER_TOKEN, seed=22,
+                             logits="normal")]
     refs = [_forward_routing(c) for c in cases]
-    # two calls in a row on the shared scratch, then the first shape again
+    # calls in a row on the shared scratch, then the first shape again
     for c, (logits, bias, ref, rows) in list(zip(cases, refs)) + [(cases[0], refs[0])]:
         out = _noalloc(c, logits, bias)
         for name in ["topk_ids", "count", "offsets", "padded_offsets", "row_of_route"]:
