@@ -74,7 +74,8 @@ def parse():
     p.add_argument("--fused", action="store_true",
                    help="the whole forward as one persistent kernel (MOE_FUSED_LAYER; W4A4, E <= 256)")
     p.add_argument("--gemm", default="auto", choices=["auto", "standard", "swapped", "pairs"],
-                   help="W4A4 GEMM variant: operand orientation (default: by routes per expert) or CTA pairs")
+                   help="W4A4 GEMM variant (default: by routes per expert): single-CTA standard or swapped "
+                        "orientation, or CTA pairs")
     p.add_argument("--finalize", default="config", choices=["config", "fused", "deterministic"],
                    help="finalize mode: the workload's own (default), the FC2-epilogue scatter or the fixed-order kernel")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -104,8 +105,10 @@ def workload_config(name, tokens, precision="nvfp4", four_over_six=False, fused=
         c = c.with_(fused=True)
     if gemm == "pairs":
         c = c.with_(gemm_pairs="always", gemm_swap="never")
-    elif gemm != "auto":
-        c = c.with_(gemm_swap="always" if gemm == "swapped" else "never")
+    elif gemm == "standard":
+        c = c.with_(gemm_pairs="never", gemm_swap="never")
+    elif gemm == "swapped":
+        c = c.with_(gemm_pairs="never", gemm_swap="always")
     if finalize != "config":
         c = c.with_(deterministic=finalize == "deterministic")
     return c

@@ -85,12 +85,13 @@ typedef enum {
 /* bit 6: router weights are the full softmax over all E experts evaluated
  * at the selected ones, instead of the softmax over the K selected. */
 #define MOE_ROUTE_NO_RENORM (1u << 6)
-/* bits 7-8: GEMM tile scheduling (W4A4 only; results are the same either
- * way up to FP32 accumulation order).  MOE_GEMM_PAIRS_ALWAYS runs each GEMM
- * whose weight height is a multiple of 256 on CTA pairs (cta_group::2
- * MMAs, 256 x 256 tiles over two 128-row M tiles of one expert); the default
- * and MOE_GEMM_PAIRS_NEVER run them on single CTAs, which measured faster
- * on every configuration so far.  Setting both is invalid. */
+/* bits 7-8: GEMM tile scheduling (NVFP4 W4A4 only; results are the same
+ * either way up to FP32 accumulation order).  A GEMM whose weight height is
+ * a multiple of 256 runs on CTA pairs (cta_group::2 MMAs, 256 x 256 tiles
+ * over two 128-row M tiles of one expert) when the experts holding routes
+ * hold at least 256 on average (T*K >= 256 * min(E, T*K)), else on single
+ * CTAs; MOE_GEMM_PAIRS_ALWAYS / MOE_GEMM_PAIRS_NEVER force pairs / single
+ * CTAs.  Setting both is invalid. */
 #define MOE_GEMM_PAIRS_NEVER (1u << 7)
 #define MOE_GEMM_PAIRS_ALWAYS (1u << 8)
 /* bit 9: 4-over-6 activation quantization (per-token W4A4 only) [PR #4366
@@ -304,12 +305,10 @@ MOE_API moe_status moe_nvfp4_forward_staged(moe_shape s, uint32_t flags,
                                             void* y_bf16, void* stream, void* const* events);
 
 /* Number of kernel launches one moe_nvfp4_forward enqueues for this shape
- * and flags on the current device (-1 if invalid): 6, one fewer for T <= 32
- * (router and permutation scan in one launch), 1 for MOE_FUSED_LAYER.  With
- * per-token scales the FC2-input quantization runs inside FC1's epilogue;
- * it is a seventh launch only on CTA pairs or when FC1 has more N tiles per
- * M tile than the device has SMs.  moe_nvfp4_forward_routed always launches
- * the scan separately.  No work is enqueued (reads the device's SM count). */
+ * and flags (-1 if invalid): 6 (7 with per-token scales: the FC2-input
+ * quantization), one fewer for T <= 32 (router and permutation scan in one
+ * launch), 1 for MOE_FUSED_LAYER.  moe_nvfp4_forward_routed always launches
+ * the scan separately.  Pure host call. */
 MOE_API int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags);
 
 /* Byte offsets of the intermediates inside the workspace (for tests and
@@ -347,10 +346,6 @@ typedef struct {
     uint64_t h_bf16;         /* bf16  [rows_cap][I] FC2 input (W4A16)        */
     uint64_t o_bf16;         /* bf16  [rows_cap][H] per-route FC2 output     */
     uint64_t y_acc;          /* f32   [T][H] fused-finalize accumulator      */
-    uint64_t row_amax;       /* u32   [rows_cap] per-token: float bits of    */
-                             /*   each route row's FC2-input |max|           */
-    uint64_t tile_done;      /* u32   [2*rows_cap/128] per-token: FC1        */
-                             /*   epilogue arrivals per M tile / half        */
     uint64_t logits;         /* f32   [T][E] router logits (MOE_ROUTER_GEMM) */
     uint64_t total;          /* workspace bytes                              */
 } moe_workspace_layout;

@@ -55,7 +55,7 @@ class moe_shape(ctypes.Structure):
 _LAYOUT_FIELDS = ["rows_cap", "status", "topk_ids", "topk_w", "count", "offsets", "padded_offsets", "meta",
                   "unit_base", "unit_mask", "row_of_route", "route_of_row", "tile_expert", "tile_pair", "tile_half", "g1",
                   "xq_codes", "xq_sf", "h_f32", "g2", "hq_codes", "hq_sf", "x_bf16_perm", "h_bf16", "o_bf16",
-                  "y_acc", "row_amax", "tile_done", "logits", "total"]
+                  "y_acc", "logits", "total"]
 
 
 class moe_workspace_layout(ctypes.Structure):

@@ -548,38 +548,6 @@ __device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// ---------------------------------------------------------------------------
-// cross-CTA counters (global memory, GPU scope)
-// ---------------------------------------------------------------------------
-// Fire-and-forget unsigned max (a non-negative float's bits order like the
-// float itself).
-__device__ __forceinline__ void red_max_u32(unsigned int* addr, unsigned int v) {
-    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-// Bounded wait until *counter >= target (acquire loads).  Gives up (returns
-// false) when *abort is set by another role, or after kWaitLimitNs, in which
-// case it sets *abort and ORs err_bit into the status word.
-__device__ __forceinline__ bool wait_counter(const unsigned int* counter, unsigned int target, volatile int* abort,
-                                             unsigned int* status, uint32_t err_bit) {
-    if (ld_acquire_u32(counter) >= target) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-        __nanosleep(64);
-        if (ld_acquire_u32(counter) >= target) return true;
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            if (status) atomicOr(status, err_bit);
-            return false;
-        }
-    }
-}
-
 // Programmatic dependent launch: wait for the preceding grid's results /
 // allow the next grid to start its prologue.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

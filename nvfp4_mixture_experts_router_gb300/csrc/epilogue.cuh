@@ -7,112 +7,46 @@
 
 namespace moe {
 
-// FC2-input values of chunk ch (32 of them) of this thread's 128
-// accumulator columns: SwiGLU (columns 0..63 gate, 64..127 up, the
-// prepared-weight interleave; chunks 0, 1) or ReLU2 (chunks 0..3), times the
-// input-side route weight pw.  Returns the first output column of the chunk
-// within the 128-column slice's outputs (64 per slice for SwiGLU, 128 for
-// ReLU2) relative to the slice start.
-__device__ __forceinline__ int fc1_chunk(uint32_t taddr, int ch, bool swiglu, float alpha, float pw, float (&h)[32]) {
-    if (swiglu) {
-        float u[32];
-        tmem_ld32(taddr + ch * 32, h);
-        tmem_ld32(taddr + 64 + ch * 32, u);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            // silu(z) = z / (1 + e^-z), ex2-based exponential and approximate
-            // division, exactly as in epilogue_fc1
-            const float zg = h[i] * alpha, zu = u[i] * alpha;
-            h[i] = __fdividef(zg, 1.0f + __expf(-zg)) * zu * pw;
-        }
-    } else {
-        tmem_ld32(taddr + ch * 32, h);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float z = fmaxf(h[i] * alpha, 0.0f);
-            h[i] = z * z * pw;
-        }
-    }
-    return ch * 32;
-}
+// Per-row scalars of an epilogue: the route of the row (-1 in pad rows), its
+// token, the product of the activation and weight global scales, the router
+// weight applied to the FC1 output (input side), and the per-tensor FC2-input
+// scale.  They depend only on the tile map and the routing, not on the
+// accumulator: the epilogue loops load them before waiting for the
+// accumulator, so that their (dependent) global-memory round trips overlap
+// the main loop instead of delaying the accumulator's release.
+struct EpiRow {
+    int route;
+    int token;
+    float alpha;   // FC1: G_act(token) * Gw1[e]; FC2: G_act(row) * Gw2[e] (* route weight when scattering)
+    float pw;      // FC1: route weight on the input side, else 1
+    float g2;      // FC1 per-tensor requantization: the FC2-input scale
+};
 
-// FC1 epilogue with the per-token FC2-input quantization fused in.  The
-// row's global scale G2 = amax/2688 (amax/1536 for 4-over-6) needs the
-// amax over all I outputs of the route row, spread over the N tiles of its
-// M tile, which run on other CTAs at about the same time (tiles are walked
-// n-fastest).  Pass 1: the activation of this thread's columns, their |h|
-// max into row_amax[row] (red.max on the float bits), one arrival per warp
-// on the M tile's counter.  Then a bounded wait until every epilogue warp
-// of every N tile of the M tile has arrived (`target`).  Pass 2: the
-// activation again from the accumulator, still held, quantized with the
-// row's G2; the slice with vtile 0 also stores G2 for FC2.  The values, G2,
-// codes and scales are those of an FP32 store followed by a per-row
-// quantization pass, bit for bit.  Warps whose slice lies beyond the tile
-// (`active` false) only arrive.  Returns false when the wait gave up.
-template <bool FOUR_SIX>
-__device__ __forceinline__ bool epilogue_fc1_tok(const GemmParams& p, uint32_t taddr, int row, int route, int e,
-                                                 int vtile, bool active, unsigned int* done, unsigned int target,
-                                                 volatile int* abort) {
-    const int token = route >= 0 ? route / p.topk : 0;
-    const float alpha = __fmul_rn(p.g_act[token], p.gw[e]);
-    const float pw = (p.weight_on_input && route >= 0) ? p.topk_w[route] : 1.0f;
-    const bool swiglu = p.act == MOE_ACT_SWIGLU;
-    const int chunks = swiglu ? 2 : 4;
-    const int cols = swiglu ? 64 : 128;          // outputs of this 128-column slice
-    if (active) {
-        float amax = 0.0f;
-        for (int ch = 0; ch < chunks; ++ch) {
-            float h[32];
-            fc1_chunk(taddr, ch, swiglu, alpha, pw, h);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
-        }
-        if (route >= 0) red_max_u32(p.row_amax + row, __float_as_uint(amax));
-    }
-    __threadfence();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) atomicAdd(done, 1u);
-    if (!active) return true;
-    if (!__all_sync(0xffffffffu, wait_counter(done, target, abort, p.status, kStatusTimeoutEpilogue))) return false;
-    const float amax_row = route >= 0 ? __uint_as_float(ld_acquire_u32(p.row_amax + row)) : 0.0f;
-    const float g2 = FOUR_SIX ? global_scale_from_amax_4over6(amax_row) : global_scale_from_amax(amax_row);
-    if (vtile == 0 && route >= 0) p.g2_out[row] = g2;
-    for (int ch = 0; ch < chunks; ++ch) {
-        float h[32];
-        const int col0 = vtile * cols + fc1_chunk(taddr, ch, swiglu, alpha, pw, h);
-        if (route < 0) continue;
-        uint32_t q[4];
-        float blk[16];
-        uint32_t c2[2];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) blk[i] = h[i];
-        const uint32_t s0 = FOUR_SIX ? quant_block16_4over6(blk, g2, c2) : quant_block16(blk, g2, c2);
-        q[0] = c2[0]; q[1] = c2[1];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) blk[i] = h[16 + i];
-        const uint32_t s1 = FOUR_SIX ? quant_block16_4over6(blk, g2, c2) : quant_block16(blk, g2, c2);
-        q[2] = c2[0]; q[3] = c2[1];
-        *reinterpret_cast<uint4*>(p.out_codes + (size_t)row * (p.out_cols / 2) + col0 / 2) =
-            make_uint4(q[0], q[1], q[2], q[3]);
-        *reinterpret_cast<uint16_t*>(p.out_sf + sf_offset(row, col0 / 16, p.out_cols)) = (uint16_t)(s0 | (s1 << 8));
-    }
-    return true;
+template <int EPI>
+__device__ __forceinline__ EpiRow epi_row(const GemmParams& p, int row, int e) {
+    constexpr bool kFc1 = EPI == kEpiFc1Quant || EPI == kEpiFc1F32 || EPI == kEpiFc1Bf16 || EPI == kEpiFc1Mx;
+    EpiRow m;
+    m.route = row >= 0 ? p.route_of_row[row] : -1;
+    m.token = m.route >= 0 ? m.route / p.topk : 0;
+    float g_act;
+    if (kFc1) g_act = p.g_act == nullptr ? 1.0f : (p.g_act_per_token ? p.g_act[m.token] : p.g_act[0]);
+    else g_act = p.g_act_per_token == 2 ? p.g_act[row] : (p.g_act ? p.g_act[0] : 1.0f);
+    m.alpha = __fmul_rn(g_act, p.gw[e]);
+    m.pw = (kFc1 && p.weight_on_input && m.route >= 0) ? p.topk_w[m.route] : 1.0f;
+    if (EPI == kEpiFc2Scatter && m.route >= 0 && p.weight_on_output) m.alpha = m.alpha * p.topk_w[m.route];
+    m.g2 = EPI == kEpiFc1Quant ? p.g2[0] : 1.0f;
+    return m;
 }
 
 // SwiGLU tile: columns 0..63 gate, 64..127 up (prepared-weight interleave);
 // yields 64 FC2-input values.  ReLU2 tile: 128 values.
 template <int EPI>
-__device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr, int row, int route, int e,
+__device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr, int row, const EpiRow& m,
                                              int n_tile) {
-    const int token = route >= 0 ? route / p.topk : 0;
-    const float g_act = p.g_act == nullptr ? 1.0f : (p.g_act_per_token ? p.g_act[token] : p.g_act[0]);
-    const float alpha = __fmul_rn(g_act, p.gw[e]);
-    const float pw = (p.weight_on_input && route >= 0) ? p.topk_w[route] : 1.0f;
+    const int route = m.route;
+    const float alpha = m.alpha, pw = m.pw, g2 = m.g2;
     const bool swiglu = p.act == MOE_ACT_SWIGLU;
     const int chunks = swiglu ? 2 : 4;
-    const float g2 = (EPI == kEpiFc1Quant) ? p.g2[0] : 1.0f;
     uint32_t sf_pair[4];
     for (int ch = 0; ch < chunks; ++ch) {
         float h[32];
@@ -231,15 +165,11 @@ __device__ __forceinline__ void staged_rows(uint32_t* stg, const uint32_t (&w)[N
 // warp's staging block stg (32 rows x COLS words); COLS = 0 writes straight
 // from registers.
 template <int EPI, int COLS = 0>
-__device__ __forceinline__ void epilogue_fc2(const GemmParams& p, uint32_t taddr, int row, int route, int e,
+__device__ __forceinline__ void epilogue_fc2(const GemmParams& p, uint32_t taddr, int row, const EpiRow& m,
                                              int n_tile, uint32_t* stg = nullptr) {
-    const float g_act = p.g_act_per_token == 2 ? p.g_act[row] : (p.g_act ? p.g_act[0] : 1.0f);
-    float alpha = __fmul_rn(g_act, p.gw[e]);
-    int token = 0;
-    if (EPI == kEpiFc2Scatter && route >= 0) {
-        token = route / p.topk;
-        if (p.weight_on_output) alpha = alpha * p.topk_w[route];
-    }
+    const int route = m.route;
+    const float alpha = m.alpha;
+    const int token = m.token;
     for (int ch = 0; ch < 4; ++ch) {
         float o[32];
         tmem_ld32(taddr + ch * 32, o);

@@ -37,8 +37,6 @@ static cudaError_t set_smem_all() {
     cudaError_t e;
     if ((e = set_smem_one<kEpiFc1Quant, BN, 0>())) return e;
     if ((e = set_smem_one<kEpiFc1F32, BN, 0>())) return e;
-    if ((e = set_smem_one<kEpiFc1Tok, BN, 0>())) return e;
-    if ((e = set_smem_one<kEpiFc1Tok46, BN, 0>())) return e;
     if ((e = set_smem_one<kEpiFc2Store, BN, 0>())) return e;
     if ((e = set_smem_one<kEpiFc2Scatter, BN, 0>())) return e;
     if ((e = set_smem_one<kEpiFc1Mx, BN, 1>())) return e;
@@ -67,8 +65,6 @@ static cudaError_t launch_bn(const LaunchCtx& c, int epilogue, int kind, const C
         switch (epilogue) {
             case kEpiFc1Quant: return launch_one<kEpiFc1Quant, BN, 0>(c, tmA, tmB, p, num_sms);
             case kEpiFc1F32: return launch_one<kEpiFc1F32, BN, 0>(c, tmA, tmB, p, num_sms);
-            case kEpiFc1Tok: return launch_one<kEpiFc1Tok, BN, 0>(c, tmA, tmB, p, num_sms);
-            case kEpiFc1Tok46: return launch_one<kEpiFc1Tok46, BN, 0>(c, tmA, tmB, p, num_sms);
             case kEpiFc2Store: return launch_one<kEpiFc2Store, BN, 0>(c, tmA, tmB, p, num_sms);
             case kEpiFc2Scatter: return launch_one<kEpiFc2Scatter, BN, 0>(c, tmA, tmB, p, num_sms);
             default: return cudaErrorInvalidValue;

@@ -404,33 +404,23 @@ __device__ __forceinline__ bool gemm_tiles(const Smem& s, uint32_t tmem_base, co
             decode_tile(p, tile, n_tiles, num_m_tiles, m_tile, n_tile);
             const int e = p.tile_expert[m_tile];
             if (e < 0 || e >= p.num_experts) break;
+            // the row's epilogue scalars, loaded while the main loop runs
+            const int row = m_tile * kBM + q * 32 + lane;
+            const EpiRow meta = epi_row<EPI>(p, row, e);
             // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
             if (!__all_sync(0xffffffffu, mbar_wait(&s.acc_full[acc], acc_phase, s.abort, p.status,
                                                    kStatusTimeoutEpilogue)))
                 break;
             tc_fence_after();
             const int width = min(BN, p.n - n_tile * BN);
-            if constexpr (EPI == kEpiFc1Tok || EPI == kEpiFc1Tok46) {
-                // every epilogue warp of every N tile of the M tile arrives
-                // once on its counter, then waits for all of them
-                const int row = m_tile * kBM + q * 32 + lane;
-                const int route = p.route_of_row[row];
-                const uint32_t taddr =
-                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + half * 128);
-                if (!epilogue_fc1_tok<EPI == kEpiFc1Tok46>(p, taddr, row, route, e, n_tile * C::kRowBlocks + half,
-                                                            half * 128 < width, p.tile_done + m_tile,
-                                                            (unsigned int)(n_tiles * C::kEpiWarps), s.abort))
-                    break;
-            } else if (half * 128 < width) {
-                const int row = m_tile * kBM + q * 32 + lane;
-                const int route = p.route_of_row[row];
+            if (half * 128 < width) {
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + half * 128);
                 const int vtile = n_tile * C::kRowBlocks + half;   // index of this 128-column slice
                 if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32 || EPI == kEpiFc1Mx)
-                    epilogue_fc1<EPI>(p, taddr, row, route, e, vtile);
+                    epilogue_fc1<EPI>(p, taddr, row, meta, vtile);
                 else
-                    epilogue_fc2<EPI, C::kStgCols>(p, taddr, row, route, e, vtile,
+                    epilogue_fc2<EPI, C::kStgCols>(p, taddr, row, meta, vtile,
                                                    s.stg + (warp - C::kEpiWarp0) * 32 * C::kStgCols);
             }
             tc_fence_before();

@@ -2,39 +2,45 @@
 // epilogues as gemm_nvf4.cu, computed by tcgen05.mma.cta_group::2 with a
 // 256 x 256 tile per pair of SMs.
 //
-// Why pairs: with the M = 256 pair MMA each SM keeps only its own 128 A rows
-// and half of the 256 B rows in shared memory, so the operand bytes each SM
-// loads per FLOP fall by a third against a single-CTA 128 x 256 tile.  The
-// cost is a cross-CTA handshake per pipeline stage and a single 256-column
-// accumulator (no room for two next to the scale slots), whose epilogue is
-// not overlapped with the next tile; measured, that cost outweighs the saved
-// bytes, so the library uses this kernel only on request
-// (MOE_GEMM_PAIRS_ALWAYS).
+// Why pairs: the L2 -> SM copy rate of one SM's TMA ring is the limit of the
+// single-CTA kernel at compute-bound shapes (measured on GB300: about 148
+// GB/s per SM with all SMs loading, while a 128 x 256 tile needs about 218
+// GB/s to keep the block-scaled MMA busy).  With the M = 256 pair MMA each SM
+// holds its own 128 A rows and half of the 256 B rows, so it loads a third
+// fewer operand bytes per FLOP (about 153 GB/s at the full MMA rate).
 //
-// Pair tile: two consecutive 128-row M tiles of ONE expert (the scan kernel
-// lists them in tile_pair: (first << 1) | has_second) x 256 weight rows.  The
-// even CTA holds the first M tile, B rows 0..127 of the tile and the
-// accumulator rows 0..127; the odd CTA the second M tile (when the expert
-// has an odd number of M tiles it loads the first one again and discards its
-// rows), B rows 128..255 and accumulator rows 128..255.  Both CTAs hold the
-// B scales of all 256 rows in tensor memory, as the pair MMA requires.
+// Pair tile: two consecutive 128-row M tiles of ONE expert (the scan lists
+// them in tile_pair: (first << 1) | has_second) x 256 weight rows.  CTA rank 0
+// (even) holds the first M tile, B rows 0..127 of the tile and accumulator
+// rows 0..127; rank 1 the second M tile, B rows 128..255 and accumulator rows
+// 128..255 (an expert with an odd number of M tiles leaves rank 1 of its
+// last pair loading the first tile again and discarding its rows).  Both
+// CTAs hold the B scales of all 256 rows in tensor memory, as the pair MMA
+// requires.
 //
-// Roles per CTA (448 threads):
-//   warp 0      producer: scale atoms (own 128 A rows, all 256 B rows) on
-//               sf_full, then the A tile and this CTA's half of the B tile
-//               (cp.async.bulk.tensor, 128-byte swizzle) on full.
-//   warps 2-5   scale writers (one per tensor-memory lane quadrant), as in
-//               the single-CTA kernel.
-//   warp 1      allocates 512 tensor-memory columns in both CTAs together.
-//               Even CTA, lane 0: waits for its own stage (data + scales)
-//               and for the odd CTA's report, issues four 256x256x64 pair
-//               MMAs and commits the stage to the empty barriers of both
-//               CTAs (multicast).  Odd CTA, lane 0: waits for its own stage
-//               and reports it to the even CTA's peer_ready barrier.
-//   warps 6-13  epilogue over this CTA's 128 rows, 128 columns per warp
-//               group; the accumulator (256 columns, one buffer) is released
-//               to the even CTA's acc_empty barrier by every epilogue warp of
-//               both CTAs.
+// Hand-off between the two CTAs, without a relay thread:
+//   * operands: each CTA's producer copies its own A rows and B half with
+//     cp.async.bulk.tensor.cta_group::2 whose completion is counted on the
+//     stage barrier of rank 0 (rank 0 announces the bytes of both CTAs);
+//   * scales: each CTA's four scale writers store their own tensor memory
+//     (tcgen05.st) and arrive, one lane per warp, on rank 0's sf_ready
+//     barrier (eight arrivals per stage);
+//   * rank 0's MMA thread issues the pair MMAs and commits each stage to the
+//     empty barriers of both CTAs (multicast), the finished accumulator to
+//     both acc_full barriers;
+//   * every epilogue warp of both CTAs releases the accumulator on rank 0's
+//     acc_empty (sixteen arrivals).
+// Operand stages hold CH = 2 128-byte K chunks of every operand row (one
+// 32 KB copy per operand and CTA: the copy rate of an SM's TMA ring grows
+// with the bytes per stage, ~100 GB/s at 16-32 KB, ~148 GB/s at 64 KB), three
+// of them; the scale atoms of a stage go through a separate two-deep ring
+// (shared memory and tensor-memory slots), refilled as soon as the writers
+// have read a slot and the MMAs two stages back have finished.
+//
+// Roles per CTA (448 threads): warp 0 producer, warp 1 tensor-memory
+// allocation (both CTAs together) and, in rank 0, the MMA issuer; warps 2-5
+// scale writers; warps 6-13 epilogue over this CTA's 128 rows (two groups of
+// four warps, 128 accumulator columns each).
 // Every wait is bounded (1 s); a timeout sets a status bit, marks both CTAs
 // aborted, and all roles drain and reach the final pair barrier.
 #include "common.cuh"
@@ -45,61 +51,123 @@ namespace moe {
 
 namespace {
 
-constexpr int kPStages = 5;
 constexpr int kPRows = 128;                      // A rows per CTA (256 per pair)
 constexpr int kPN = 256;                         // weight rows per pair tile (128 per CTA)
-constexpr int kPKBytes = 128;                    // 256 E2M1 elements per stage row
-constexpr int kPTileA = kPRows * kPKBytes;       // 16 KB
-constexpr int kPTileB = (kPN / 2) * kPKBytes;    // 16 KB
-constexpr int kPSfA = 4 * 512;                   // own 128 rows, 4 k-blocks of 64
-constexpr int kPSfB = 2 * 4 * 512;               // all 256 B rows, 4 k-blocks
-constexpr int kPStageBytes = kPTileA + kPTileB + kPSfA + kPSfB;
 constexpr int kPSfWarps = 4;
 constexpr int kPEpiWarp0 = 2 + kPSfWarps;
 constexpr int kPEpiWarps = 8;
 constexpr int kPThreads = (kPEpiWarp0 + kPEpiWarps) * 32;
 constexpr uint32_t kPTmemCols = 512;
 constexpr uint32_t kPSfCol0 = kPN;               // accumulator: columns 0..255
-constexpr uint32_t kPSfColsStage = 16 + 32;      // A scales 4 x 4, B scales 4 x 8 columns
-constexpr int kPSmemBytes = kPStages * kPStageBytes + 1024 + 512;
-static_assert(kPSfCol0 + kPStages * kPSfColsStage <= kPTmemCols, "tensor memory budget");
+// Two rings: operand stages (CH = 2 128-byte K chunks of every operand row)
+// and scale stages (the same K range), the latter two deep in both shared and
+// tensor memory, which is what bounds them.  The FC2 epilogues stage their
+// row segments through shared memory (64-byte segments: 16 words per row and
+// warp); they get two operand stages, the FC1 epilogues (no staging) three.
+template <int EPI>
+struct PCfg {
+    static constexpr bool kFc2 = EPI == kEpiFc2Store || EPI == kEpiFc2Scatter;
+    static constexpr int kCh = 2;                            // 128-byte K chunks per operand stage
+    static constexpr int kKb = 4 * kCh;                      // 64-element MMA steps per stage
+    static constexpr int kTileA = kPRows * 128 * kCh;        // own 128 A rows
+    static constexpr int kTileB = (kPN / 2) * 128 * kCh;     // own half of the B rows
+    static constexpr int kSfA = kKb * 512;                   // own A rows' scale atoms
+    static constexpr int kSfB = 2 * kKb * 512;               // all 256 B rows' scale atoms
+    static constexpr int kSfStages = 2;
+    static constexpr int kStages = kFc2 ? 2 : 3;             // operand stages
+    static constexpr int kStgCols = kFc2 ? 16 : 0;           // FC2 epilogue staging, words per row
+    static constexpr int kStgBytes = kPEpiWarps * 32 * kStgCols * 4;
+    static constexpr uint32_t kSfColsA = 4 * kKb;
+    static constexpr uint32_t kSfColsB = 8 * kKb;
+    static constexpr uint32_t kSfColsStage = kSfColsA + kSfColsB;
+    static constexpr int kSmemBytes =
+        kStages * (kTileA + kTileB) + kSfStages * (kSfA + kSfB) + kStgBytes + 1024 + 512;
+    static_assert(kPSfCol0 + kSfStages * kSfColsStage <= kPTmemCols, "tensor memory budget");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
 
 struct PairSmem {
     uint8_t* a;
     uint8_t* b;
     uint8_t* sfa;
     uint8_t* sfb;
-    uint64_t* full;
-    uint64_t* sf_full;
-    uint64_t* empty;
-    uint64_t* sf_ready;
-    uint64_t* peer_ready;   // even CTA: the odd CTA's stage is ready
+    uint32_t* stg;
+    uint64_t* full;        // [kStages] rank 0: both CTAs' operand bytes of a stage
+    uint64_t* empty;       // [kStages] both CTAs: the stage's MMAs are done
+    uint64_t* sf_full;     // [kSfStages] this CTA's scale atoms of a stage landed
+    uint64_t* sf_free;     // [kSfStages] this CTA's scale writers have read them
+    uint64_t* sf_ready;    // [kSfStages] rank 0: both CTAs' scale writers are done
     uint64_t* acc_full;
-    uint64_t* acc_empty;    // even CTA: both CTAs' epilogues released the accumulator
+    uint64_t* acc_empty;   // rank 0: both CTAs' epilogues released the accumulator
     uint64_t* drain;
     uint32_t* tmem_holder;
     volatile int* abort;
 };
 
+template <int EPI>
 __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
+    using PC = PCfg<EPI>;
     PairSmem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.a = base;
-    s.b = s.a + kPStages * kPTileA;
-    s.sfa = s.b + kPStages * kPTileB;
-    s.sfb = s.sfa + kPStages * kPSfA;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.sfb + kPStages * kPSfB);
+    s.b = s.a + PC::kStages * PC::kTileA;
+    s.sfa = s.b + PC::kStages * PC::kTileB;
+    s.sfb = s.sfa + PC::kSfStages * PC::kSfA;
+    s.stg = reinterpret_cast<uint32_t*>(s.sfb + PC::kSfStages * PC::kSfB);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.stg) + PC::kStgBytes);
     s.full = bars;
-    s.sf_full = bars + kPStages;
-    s.empty = bars + 2 * kPStages;
-    s.sf_ready = bars + 3 * kPStages;
-    s.peer_ready = bars + 4 * kPStages;
-    s.acc_full = bars + 5 * kPStages;
+    s.empty = bars + PC::kStages;
+    s.sf_full = bars + 2 * PC::kStages;
+    s.sf_free = s.sf_full + PC::kSfStages;
+    s.sf_ready = s.sf_free + PC::kSfStages;
+    s.acc_full = s.sf_ready + PC::kSfStages;
     s.acc_empty = s.acc_full + 1;
     s.drain = s.acc_empty + 1;
     s.tmem_holder = reinterpret_cast<uint32_t*>(s.drain + 1);
     s.abort = reinterpret_cast<volatile int*>(s.tmem_holder + 1);
     return s;
+}
+
+// Tile copies whose completion is counted on an mbarrier of either CTA of the
+// pair (`bar` a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
+// Pair tile -> (M tile of this CTA, the pair's first M tile, N tile), N
+// tiles fastest; with slabs of p.n_slab N tiles the output width is walked
+// slab by slab, every pair within a slab before the next (the fused-finalize
+// scatter then keeps adding into one slab of the accumulator, which stays in
+// L2).  m_tile is -1 for rank 1 of a pair without a second M tile.
+__device__ __forceinline__ void decode_pair(const GemmParams& p, int tile, int n_tiles, int num_pairs, uint32_t rank,
+                                            int& m_tile, int& m0, int& n_tile) {
+    int pr;
+    if (p.n_slab <= 0) {
+        pr = tile / n_tiles;
+        n_tile = tile % n_tiles;
+    } else {
+        const int per_slab = num_pairs * p.n_slab;
+        const int slab = tile / per_slab, rem = tile % per_slab;
+        const int width = min(p.n_slab, n_tiles - slab * p.n_slab);   // the last slab may be narrower
+        pr = rem / width;
+        n_tile = slab * p.n_slab + rem % width;
+    }
+    const int v = p.tile_pair[pr];
+    m0 = v >> 1;
+    m_tile = rank == 0 ? m0 : ((v & 1) ? m0 + 1 : -1);
 }
 
 }  // namespace
@@ -108,20 +176,23 @@ template <int EPI>
 __global__ void __launch_bounds__(kPThreads, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const GemmParams p) {
+    using PC = PCfg<EPI>;
     extern __shared__ uint8_t smem_raw[];
-    const PairSmem s = carve_pair(smem_raw);
+    const PairSmem s = carve_pair<EPI>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_cta_rank();          // 0: issues the pair MMAs
     const int pair_slot = blockIdx.x >> 1, pair_slots = gridDim.x >> 1;
     volatile int no_abort = 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kPStages; ++i) {
+        for (int i = 0; i < PC::kStages; ++i) {
             mbar_init(&s.full[i], 1);
-            mbar_init(&s.sf_full[i], 1);
             mbar_init(&s.empty[i], 1);
-            mbar_init(&s.sf_ready[i], kPSfWarps * 32);
-            mbar_init(&s.peer_ready[i], 1);
+        }
+        for (int i = 0; i < PC::kSfStages; ++i) {
+            mbar_init(&s.sf_full[i], 1);
+            mbar_init(&s.sf_free[i], kPSfWarps);
+            mbar_init(&s.sf_ready[i], 2 * kPSfWarps);
         }
         mbar_init(s.acc_full, 1);
         mbar_init(s.acc_empty, 2 * kPEpiWarps);
@@ -136,7 +207,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_relinquish_pair();
     }
     // both CTAs' barriers initialized and tensor memory allocated before any
-    // cross-CTA arrival or pair MMA
+    // cross-CTA copy, arrival or pair MMA
     tc_fence_before();
     cluster_sync_all();
     tc_fence_after();
@@ -148,154 +219,194 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int num_m_tiles = p.meta[1];
     const int n_tiles = p.n / kPN;
     const int total = num_pairs * n_tiles;
-    const int kblocks = p.kdim / 64;
-    const int kstages = (kblocks + 3) / 4;
+    const int kblocks = p.kdim / 64;                           // 64-element MMA steps = scale atoms per 128 rows
+    const int kstages = (kblocks + PC::kKb - 1) / PC::kKb;
+    const int row_chunks = (p.kdim / 2 + 127) / 128;           // 128-byte chunks per row
     const int rb_per_expert = p.n / 128;
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_normal();
-            int stage = 0;
-            uint32_t phase = 0;
+            // slabs: the activation rows are re-read once per slab; evict them
+            // first so that the slab of the accumulator stays in L2
+            const uint64_t pol_a = p.n_slab > 0 ? policy_evict_first() : pol;
+            const uint32_t full0 = cluster_map(s.full, 0);      // rank 0's stage barriers
+            int stage = 0, sfs = 0;
+            uint32_t phase = 0, sfp = 0;
             for (int tile = pair_slot; tile < total; tile += pair_slots) {
-                const int pr = tile / n_tiles, n_tile = tile % n_tiles;
-                const int v = p.tile_pair[pr];
-                const int m0 = v >> 1;
-                const int m_tile = (rank == 1 && (v & 1)) ? m0 + 1 : m0;
+                int m_tile, m0, n_tile;
+                decode_pair(p, tile, n_tiles, num_pairs, rank, m_tile, m0, n_tile);
+                const int ld_m = m_tile >= 0 ? m_tile : m0;     // rank 1 without a second tile reloads the first
                 const int e = (m0 >= 0 && m0 < num_m_tiles) ? p.tile_expert[m0] : -1;
-                if (e < 0 || e >= p.num_experts || m_tile >= num_m_tiles) {
+                if (e < 0 || e >= p.num_experts || ld_m >= num_m_tiles) {
                     atomicOr(p.status, kStatusBadExpert);
                     *s.abort = 1;
                     break;
                 }
-                const int a_row = m_tile * kPRows;
+                const int a_row = ld_m * kPRows;
                 const int b_row = e * p.n + n_tile * kPN + (int)rank * (kPN / 2);
-                const uint8_t* sfa_src = p.sfa + (size_t)m_tile * kblocks * 512;
+                const uint8_t* sfa_src = p.sfa + (size_t)ld_m * kblocks * 512;
                 const uint8_t* sfb_src = p.sfb + ((size_t)e * rb_per_expert + (size_t)n_tile * 2) * kblocks * 512;
                 for (int ks = 0; ks < kstages; ++ks) {
-                    if (!mbar_wait(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
-                    const int nkb = min(4, kblocks - 4 * ks);
+                    const int nkb = min(PC::kKb, kblocks - PC::kKb * ks);
                     const uint32_t sf_bytes = (uint32_t)nkb * 512u;
-                    mbar_arrive_expect_tx(&s.sf_full[stage], 3u * sf_bytes);
-                    bulk_load(s.sfa + stage * kPSfA, sfa_src + (size_t)ks * 4 * 512, sf_bytes, &s.sf_full[stage], pol);
+                    // this CTA's scale atoms (its own A rows, all 256 B rows)
+                    // into the scale ring once the writers have read that slot
+                    if (!mbar_wait(&s.sf_free[sfs], sfp ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
+                    mbar_arrive_expect_tx(&s.sf_full[sfs], 3u * sf_bytes);
+                    bulk_load(s.sfa + sfs * PC::kSfA, sfa_src + (size_t)ks * PC::kKb * 512, sf_bytes,
+                              &s.sf_full[sfs], pol);
                     for (int rb = 0; rb < 2; ++rb)
-                        bulk_load(s.sfb + stage * kPSfB + rb * kPSfA,
-                                  sfb_src + ((size_t)rb * kblocks + (size_t)ks * 4) * 512, sf_bytes,
-                                  &s.sf_full[stage], pol);
-                    mbar_arrive_expect_tx(&s.full[stage], kPTileA + kPTileB);
-                    tma_load_2d(s.a + stage * kPTileA, &tmA, &s.full[stage], ks * kPKBytes, a_row, pol);
-                    tma_load_2d(s.b + stage * kPTileB, &tmB, &s.full[stage], ks * kPKBytes, b_row, pol);
-                    if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+                        bulk_load(s.sfb + sfs * PC::kSfB + rb * PC::kSfA,
+                                  sfb_src + ((size_t)rb * kblocks + (size_t)ks * PC::kKb) * 512, sf_bytes,
+                                  &s.sf_full[sfs], pol);
+                    if (++sfs == PC::kSfStages) { sfs = 0; sfp ^= 1u; }
+                    // completed by rank 0's commit: acquire at cluster scope
+                    if (!mbar_wait<true>(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer))
+                        goto done;
+                    // operands: counted on rank 0's barrier, which rank 0
+                    // announces for both CTAs
+                    uint8_t* a_dst = s.a + stage * PC::kTileA;
+                    uint8_t* b_dst = s.b + stage * PC::kTileB;
+                    const int c0 = PC::kCh * ks;
+                    const uint32_t bar = full0 + (uint32_t)stage * 8u;
+                    if (p.chunk_maps) {
+                        if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2u * (PC::kTileA + PC::kTileB));
+                        tma_load_3d_pair(a_dst, &tmA, bar, 0, a_row, c0, pol_a);
+                        tma_load_3d_pair(b_dst, &tmB, bar, 0, b_row, c0, pol);
+                    } else {
+                        const int nch = min(PC::kCh, row_chunks - c0);
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(&s.full[stage], 2u * (uint32_t)nch * (kPRows * 128 + (kPN / 2) * 128));
+                        for (int c = 0; c < nch; ++c) {
+                            tma_load_2d_pair(a_dst + c * kPRows * 128, &tmA, bar, (c0 + c) * 128, a_row, pol_a);
+                            tma_load_2d_pair(b_dst + c * (kPN / 2) * 128, &tmB, bar, (c0 + c) * 128, b_row, pol);
+                        }
+                    }
+                    if (++stage == PC::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             const uint32_t idesc = idesc_nvf4(2 * kPRows, kPN);
-            int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int stage = 0, sfs = 0;
+            uint32_t phase = 0, sfp = 0, acc_phase = 0;
             for (int tile = pair_slot; tile < total; tile += pair_slots) {
-                if (!mbar_wait(s.acc_empty, acc_phase ^ 1u, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                if (!mbar_wait<true>(s.acc_empty, acc_phase ^ 1u, s.abort, p.status, kStatusTimeoutMma)) goto done;
                 tc_fence_after();
                 for (int ks = 0; ks < kstages; ++ks) {
-                    if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
-                    if (!mbar_wait(&s.sf_ready[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
-                    if (!mbar_wait(&s.peer_ready[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                    if (!mbar_wait<true>(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                    if (!mbar_wait<true>(&s.sf_ready[sfs], sfp, s.abort, p.status, kStatusTimeoutMma)) goto done;
                     tc_fence_after();
-                    const int nkb = min(4, kblocks - 4 * ks);
-                    const uint32_t sfa_t = tmem_base + kPSfCol0 + (uint32_t)stage * kPSfColsStage;
-                    const uint32_t sfb_t = sfa_t + 16;
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(s.a + stage * kPTileA));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(s.b + stage * kPTileB));
-                    for (int j = 0; j < nkb; ++j)
-                        tc_mma_nvf4_pair(tmem_base, adesc + 2u * j, bdesc + 2u * j, idesc, sfa_t + 4 * j,
+                    const int nkb = min(PC::kKb, kblocks - PC::kKb * ks);
+                    const uint32_t sfa_t = tmem_base + kPSfCol0 + (uint32_t)sfs * PC::kSfColsStage;
+                    const uint32_t sfb_t = sfa_t + PC::kSfColsA;
+                    const uint32_t a_s = smem_u32(s.a + stage * PC::kTileA);
+                    const uint32_t b_s = smem_u32(s.b + stage * PC::kTileB);
+                    for (int j = 0; j < nkb; ++j) {
+                        const int c = j >> 2, jj = j & 3;
+                        tc_mma_nvf4_pair(tmem_base, sdesc_kmajor_sw128(a_s + c * kPRows * 128) + 2u * jj,
+                                         sdesc_kmajor_sw128(b_s + c * (kPN / 2) * 128) + 2u * jj, idesc, sfa_t + 4 * j,
                                          sfb_t + 8 * j, (ks | j) != 0);
+                    }
                     tc_commit_pair_mc(&s.empty[stage], 0x3);
-                    if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+                    if (++stage == PC::kStages) { stage = 0; phase ^= 1u; }
+                    if (++sfs == PC::kSfStages) { sfs = 0; sfp ^= 1u; }
                 }
                 tc_commit_pair_mc(s.acc_full, 0x3);
                 acc_phase ^= 1u;
             }
-        } else if (lane == 0) {
-            // odd CTA: report each landed and scale-written stage to the even CTA
-            const uint32_t ready0 = cluster_map(s.peer_ready, 0);
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int tile = pair_slot; tile < total; tile += pair_slots) {
-                for (int ks = 0; ks < kstages; ++ks) {
-                    if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
-                    if (!mbar_wait(&s.sf_ready[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
-                    mbar_arrive_cluster(ready0 + (uint32_t)stage * 8u);
-                    if (++stage == kPStages) { stage = 0; phase ^= 1u; }
-                }
-            }
         }
     } else if (warp < kPEpiWarp0) {
-        // scale writer for lane quadrant warp % 4 (same layout as the
-        // single-CTA kernel with 256-wide tiles)
+        // scale writer for lane quadrant warp % 4: the stage's A atoms into
+        // columns 4j..4j+3 of its slot, the B atoms of MMA step j (row block
+        // rb) into columns 8j + 4rb .. +3 of the B part
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        int stage = 0;
-        uint32_t phase = 0;
+        const uint32_t ready0 = cluster_map(s.sf_ready, 0);
+        int sfs = 0, es = 0;                  // scale slot; operand stage of the MMAs two stages back
+        uint32_t sfp = 0, ep = 0;
+        long long n = 0;                      // stages written so far
         for (int tile = pair_slot; tile < total; tile += pair_slots) {
-            for (int ks = 0; ks < kstages; ++ks) {
-                // warp-uniform outcome: tcgen05.st below is a warp-collective instruction
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&s.sf_full[stage], phase, s.abort, p.status, kStatusTimeoutMma)))
-                    goto done;
-                const uint32_t sfa_t = tmem_base + kPSfCol0 + (uint32_t)stage * kPSfColsStage;
-                const uint32_t sfb_t = sfa_t + 16;
-                uint32_t ra[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(s.sfa + stage * kPSfA + j * 512 + lane * 16);
-                    ra[4 * j] = v.x; ra[4 * j + 1] = v.y; ra[4 * j + 2] = v.z; ra[4 * j + 3] = v.w;
+            for (int ks = 0; ks < kstages; ++ks, ++n) {
+                // the tensor-memory scale slot is free once the MMAs of the
+                // stage that used it (two stages back) are done: their
+                // operand stage's empty barrier (completed by rank 0's
+                // commit, hence cluster scope; it cannot run two phases ahead
+                // of this writer, whose next stage those MMAs would need)
+                bool ok = mbar_wait(&s.sf_full[sfs], sfp, s.abort, p.status, kStatusTimeoutMma);
+                if (ok && n >= PC::kSfStages) {
+                    ok = mbar_wait<true>(&s.empty[es], ep, s.abort, p.status, kStatusTimeoutMma);
+                    if (++es == PC::kStages) { es = 0; ep ^= 1u; }
                 }
-                tmem_st16(sfa_t + lane_off, ra);
-                uint32_t rb_[32];
+                // warp-uniform outcome: tcgen05.st below is a warp-collective instruction
+                if (!__all_sync(0xffffffffu, ok)) goto done;
+                const uint32_t sfa_t = tmem_base + kPSfCol0 + (uint32_t)sfs * PC::kSfColsStage;
+                const uint32_t sfb_t = sfa_t + PC::kSfColsA;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int g = 0; g < PC::kKb / 4; ++g) {
+                    uint32_t ra[16];
 #pragma unroll
-                    for (int rb = 0; rb < 2; ++rb) {
+                    for (int j = 0; j < 4; ++j) {
                         const uint4 v =
-                            *reinterpret_cast<const uint4*>(s.sfb + stage * kPSfB + rb * kPSfA + j * 512 + lane * 16);
-                        rb_[8 * j + 4 * rb] = v.x; rb_[8 * j + 4 * rb + 1] = v.y;
-                        rb_[8 * j + 4 * rb + 2] = v.z; rb_[8 * j + 4 * rb + 3] = v.w;
+                            *reinterpret_cast<const uint4*>(s.sfa + sfs * PC::kSfA + (4 * g + j) * 512 + lane * 16);
+                        ra[4 * j] = v.x; ra[4 * j + 1] = v.y; ra[4 * j + 2] = v.z; ra[4 * j + 3] = v.w;
                     }
-                tmem_st32(sfb_t + lane_off, rb_);
+                    tmem_st16(sfa_t + 16 * g + lane_off, ra);
+                    uint32_t rb_[32];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int rb = 0; rb < 2; ++rb) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(s.sfb + sfs * PC::kSfB + rb * PC::kSfA +
+                                                                            (4 * g + j) * 512 + lane * 16);
+                            rb_[8 * j + 4 * rb] = v.x; rb_[8 * j + 4 * rb + 1] = v.y;
+                            rb_[8 * j + 4 * rb + 2] = v.z; rb_[8 * j + 4 * rb + 3] = v.w;
+                        }
+                    tmem_st32(sfb_t + 32 * g + lane_off, rb_);
+                }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&s.sf_ready[stage]);
-                if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&s.sf_free[sfs]);
+                    if (rank == 0) mbar_arrive(&s.sf_ready[sfs]);
+                    else mbar_arrive_cluster(ready0 + (uint32_t)sfs * 8u);
+                }
+                if (++sfs == PC::kSfStages) { sfs = 0; sfp ^= 1u; }
             }
         }
     } else {
         const int q = warp & 3;                            // tensor-memory lane quadrant of this warp
         const int half = (warp - kPEpiWarp0) >> 2;         // accumulator columns 0..127 or 128..255
         const uint32_t release = cluster_map(s.acc_empty, 0);
+        uint32_t* stg = s.stg + (warp - kPEpiWarp0) * 32 * PC::kStgCols;
         uint32_t acc_phase = 0;
         for (int tile = pair_slot; tile < total; tile += pair_slots) {
-            const int pr = tile / n_tiles, n_tile = tile % n_tiles;
-            const int v = p.tile_pair[pr];
-            const int m0 = v >> 1;
-            const int m_tile = rank == 0 ? m0 : ((v & 1) ? m0 + 1 : -1);
+            int m_tile, m0, n_tile;
+            decode_pair(p, tile, n_tiles, num_pairs, rank, m_tile, m0, n_tile);
             const int e = (m0 >= 0 && m0 < num_m_tiles) ? p.tile_expert[m0] : -1;
             if (e < 0 || e >= p.num_experts || m_tile >= num_m_tiles) break;
+            // the row's epilogue scalars, loaded while the main loop runs
+            const int row = m_tile >= 0 ? m_tile * kPRows + q * 32 + lane : -1;
+            const EpiRow meta = epi_row<EPI>(p, row, e);
             // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
             if (!__all_sync(0xffffffffu,
-                            mbar_wait(s.acc_full, acc_phase, s.abort, p.status, kStatusTimeoutEpilogue)))
+                            mbar_wait<true>(s.acc_full, acc_phase, s.abort, p.status, kStatusTimeoutEpilogue)))
                 break;
             tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
+            const int vtile = n_tile * 2 + half;           // index of this 128-column slice
             if (m_tile >= 0) {
-                const int row = m_tile * kPRows + q * 32 + lane;
-                const int route = p.route_of_row[row];
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
-                const int vtile = n_tile * 2 + half;        // index of this 128-column slice
-                if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32) epilogue_fc1<EPI>(p, taddr, row, route, e, vtile);
-                else epilogue_fc2<EPI>(p, taddr, row, route, e, vtile);
+                if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32) epilogue_fc1<EPI>(p, taddr, row, meta, vtile);
+                else epilogue_fc2<EPI, PC::kStgCols>(p, taddr, row, meta, vtile, stg);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(release);
+            if (lane == 0) {
+                if (rank == 0) mbar_arrive(s.acc_empty);
+                else mbar_arrive_cluster(release);
+            }
             acc_phase ^= 1u;
         }
     }
@@ -315,7 +426,8 @@ done:
     tc_fence_before();
     __syncthreads();
     // neither CTA frees tensor memory or leaves (its shared memory is an
-    // operand of the other CTA's MMAs) before both are done
+    // operand of the other CTA's MMAs and copies complete on its barriers)
+    // before both are done
     cluster_sync_all();
     pdl_launch_dependents();
     if (warp == 1) {
@@ -326,25 +438,27 @@ done:
 
 namespace {
 int g_pair_grid[64] = {};
+
+template <int EPI>
+cudaError_t set_pair_smem() {
+    return cudaFuncSetAttribute(gemm_nvf4_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                PCfg<EPI>::kSmemBytes);
 }
+}  // namespace
+
+int gemm_pair_chunks() { return PCfg<kEpiFc1Quant>::kCh; }
 
 cudaError_t setup_gemm_pair_kernels(int device, int num_sms) {
     cudaError_t e;
-    const int b = kPSmemBytes;
-    if ((e = cudaFuncSetAttribute(gemm_nvf4_pair_kernel<kEpiFc1Quant>, cudaFuncAttributeMaxDynamicSharedMemorySize, b)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gemm_nvf4_pair_kernel<kEpiFc1F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, b)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gemm_nvf4_pair_kernel<kEpiFc2Store>, cudaFuncAttributeMaxDynamicSharedMemorySize, b)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gemm_nvf4_pair_kernel<kEpiFc2Scatter>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  b)))
-        return e;
+    if ((e = set_pair_smem<kEpiFc1Quant>())) return e;
+    if ((e = set_pair_smem<kEpiFc1F32>())) return e;
+    if ((e = set_pair_smem<kEpiFc2Store>())) return e;
+    if ((e = set_pair_smem<kEpiFc2Scatter>())) return e;
     // persistent grid: as many CTA pairs as can be resident at once
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(num_sms / 2 * 2));
     cfg.blockDim = dim3(kPThreads);
-    cfg.dynamicSmemBytes = kPSmemBytes;
+    cfg.dynamicSmemBytes = PCfg<kEpiFc1Quant>::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -359,20 +473,24 @@ cudaError_t setup_gemm_pair_kernels(int device, int num_sms) {
     return cudaSuccess;
 }
 
+int gemm_pair_grid(int device) { return (device >= 0 && device < 64) ? g_pair_grid[device] : 0; }
+
 cudaError_t launch_gemm_nvf4_pair(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   const GemmParams& p, int device) {
     if (device < 0 || device >= 64 || g_pair_grid[device] < 2) return cudaErrorInvalidValue;
     LaunchCtx cc = c;
     cc.cluster = 2;
     const dim3 grid((unsigned)g_pair_grid[device]), block(kPThreads);
-    const size_t smem = kPSmemBytes;
+#define MOE_PAIR_LAUNCH(E) \
+    cc.launch(gemm_nvf4_pair_kernel<E>, grid, block, (size_t)PCfg<E>::kSmemBytes, tmA, tmB, p)
     switch (epilogue) {
-        case kEpiFc1Quant: return cc.launch(gemm_nvf4_pair_kernel<kEpiFc1Quant>, grid, block, smem, tmA, tmB, p);
-        case kEpiFc1F32: return cc.launch(gemm_nvf4_pair_kernel<kEpiFc1F32>, grid, block, smem, tmA, tmB, p);
-        case kEpiFc2Store: return cc.launch(gemm_nvf4_pair_kernel<kEpiFc2Store>, grid, block, smem, tmA, tmB, p);
-        case kEpiFc2Scatter: return cc.launch(gemm_nvf4_pair_kernel<kEpiFc2Scatter>, grid, block, smem, tmA, tmB, p);
+        case kEpiFc1Quant: return MOE_PAIR_LAUNCH(kEpiFc1Quant);
+        case kEpiFc1F32: return MOE_PAIR_LAUNCH(kEpiFc1F32);
+        case kEpiFc2Store: return MOE_PAIR_LAUNCH(kEpiFc2Store);
+        case kEpiFc2Scatter: return MOE_PAIR_LAUNCH(kEpiFc2Scatter);
         default: return cudaErrorInvalidValue;
     }
+#undef MOE_PAIR_LAUNCH
 }
 
 }  // namespace moe

@@ -137,47 +137,17 @@ __device__ __forceinline__ void compose_sf(const uint4& b0, const uint4& b1, con
     w[2][3] = 0u;
 }
 
-// Squared dequantization error of one 4-over-6 candidate (block scale sv)
-// over the 16-lane block of value h, summed in element order (lane order
-// within the block) exactly as quant_candidate16 sums it: each lane's
-// (d*d) is gathered to the block's first lane in order.  Every lane of the
-// warp must call it; the result is valid on all 16 lanes of the block.
-__device__ __forceinline__ float block_sq_err16(float h, float g2, float sv) {
-    const int lane = threadIdx.x & 31;
-    const float inv = (sv == 0.0f) ? 0.0f : __fdiv_rn(1.0f, __fmul_rn(sv, g2));
-    const uint32_t c = f32x2_to_e2m1x2(__fmul_rn(h, inv), 0.0f) & 0xFu;
-    const float d = __fsub_rn(h, __fmul_rn(__fmul_rn(e2m1_to_f32(c), sv), g2));
-    const float dd = __fmul_rn(d, d);
-    const int base = lane & 16;
-    float err = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) err = __fadd_rn(err, __shfl_sync(0xffffffffu, dd, base + k));
-    return err;
-}
-
 // Per-lane NVFP4 requantization of an FC2-input value h for route row `row`
 // and column i, the 16 lanes i & ~15 .. +15 of the warp forming one block:
 // the arithmetic of quant_block16, with the block max taken by shuffles.
-// FOUR_SIX: the 4-over-6 choice of quant_block16_4over6, its two squared
-// errors summed in element order over the block's lanes by shuffles.
 // Every lane of the warp must call it (the same row for the whole warp).
-template <bool FOUR_SIX = false>
 __device__ __forceinline__ void requant_lane(const GemmParams& p, float h, float g2, int row, int i, bool store) {
     const int lane = threadIdx.x & 31;
     float amax = fabsf(h);
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    uint32_t s;
-    float sv;
-    if (FOUR_SIX) {
-        const float t = __fdiv_rn(amax, g2);
-        const uint32_t s6 = f32_to_e4m3(__fdiv_rn(t, 6.0f)), s4 = f32_to_e4m3(__fdiv_rn(t, 4.0f));
-        const float e6 = block_sq_err16(h, g2, e4m3_to_f32(s6)), e4 = block_sq_err16(h, g2, e4m3_to_f32(s4));
-        s = e4 < e6 ? s4 : s6;
-    } else {
-        s = f32_to_e4m3(__fdiv_rn(__fdiv_rn(amax, g2), 6.0f));
-    }
-    sv = e4m3_to_f32(s);
+    const uint32_t s = f32_to_e4m3(__fdiv_rn(__fdiv_rn(amax, g2), 6.0f));
+    const float sv = e4m3_to_f32(s);
     const float inv = (sv == 0.0f) ? 0.0f : __fdiv_rn(1.0f, __fmul_rn(sv, g2));
     uint32_t v = f32x2_to_e2m1x2(__fmul_rn(h, inv), 0.0f) & 0xFu;
     v |= __shfl_down_sync(0xffffffffu, v, 1) << 4;     // byte: elements l, l+1 (even lanes)
@@ -367,13 +337,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int rb = m * kTileM + kNR * h + 32 * half;   // first route row of this warp's columns
             const int my_route = p.route_of_row[rb + lane];
             const int my_token = my_route >= 0 ? my_route / p.topk : 0;
-            constexpr bool kFc1 = EPI == kEpiFc1Quant || EPI == kEpiFc1F32 || EPI == kEpiFc1Tok || EPI == kEpiFc1Tok46;
-            constexpr bool kTok = EPI == kEpiFc1Tok || EPI == kEpiFc1Tok46;
             float g_act;
-            if (kFc1) g_act = p.g_act_per_token ? p.g_act[my_token] : p.g_act[0];
+            if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32) g_act = p.g_act_per_token ? p.g_act[my_token] : p.g_act[0];
             else g_act = p.g_act_per_token == 2 ? p.g_act[rb + lane] : p.g_act[0];
             float my_pw = 1.0f;
-            if (my_route >= 0 && ((kFc1 && p.weight_on_input) || (EPI == kEpiFc2Scatter && p.weight_on_output)))
+            if (my_route >= 0 && (((EPI == kEpiFc1Quant || EPI == kEpiFc1F32) && p.weight_on_input) ||
+                                  (EPI == kEpiFc2Scatter && p.weight_on_output)))
                 my_pw = p.topk_w[my_route];
             float my_alpha = __fmul_rn(g_act, gw);
             if (EPI == kEpiFc2Scatter && p.weight_on_output) my_alpha = my_alpha * my_pw;
@@ -395,52 +364,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // that the broadcasts of consecutive columns overlap.
             const uint32_t live_mask = __ballot_sync(0xffffffffu, my_route >= 0);
             const int ngroups = (32 - __clz(live_mask) + 7) / 8;
-            float my_g2 = 1.0f;
-            if constexpr (kTok) {
-                // per-token FC2-input scale inside FC1 (see epilogue_fc1_tok):
-                // pass 1 takes each route column's |h| max over this warp's 32
-                // weight rows into row_amax, every epilogue warp of the half's
-                // weight tiles arrives on its counter, then all of them are
-                // awaited and each lane derives the G2 of its own route column
-#pragma unroll 1
-                for (int g = 0; g < ngroups; ++g) {
-                    float a0[8], a1[8];
-                    tmem_ld8(tbase + 8 * g, a0);
-                    tmem_ld8(tbase + kNR + 8 * g, a1);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int src = 8 * g + j;
-                        const float alpha = __shfl_sync(0xffffffffu, my_alpha, src);
-                        const float pw = __shfl_sync(0xffffffffu, my_pw, src);
-                        float m;
-                        if (GATED) {
-                            const float zg = a0[j] * alpha, zu = a1[j] * alpha;
-                            m = fabsf(__fdividef(zg, 1.0f + __expf(-zg)) * zu * pw);
-                        } else {
-                            m = 0.0f;
-#pragma unroll
-                            for (int o = 0; o < kOps; ++o) {
-                                if (col0 + 64 * o >= p.n) continue;
-                                const float z = fmaxf((o ? a1[j] : a0[j]) * alpha, 0.0f);
-                                m = fmaxf(m, z * z * pw);
-                            }
-                        }
-                        m = warp_max(m);
-                        if (lane == src && my_route >= 0) red_max_u32(p.row_amax + rb + src, __float_as_uint(m));
-                    }
-                }
-                unsigned int* done = p.tile_done + tile / tm.n_wt;
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) atomicAdd(done, 1u);
-                if (!__all_sync(0xffffffffu, wait_counter(done, (unsigned int)(tm.n_wt * kEpiWarps), s.abort, p.status,
-                                                          kStatusTimeoutEpilogue)))
-                    break;
-                const float amax = my_route >= 0 ? __uint_as_float(ld_acquire_u32(p.row_amax + rb + lane)) : 0.0f;
-                my_g2 = EPI == kEpiFc1Tok46 ? global_scale_from_amax_4over6(amax) : global_scale_from_amax(amax);
-                if (wt == 0 && q == 0 && my_route >= 0) p.g2_out[rb + lane] = my_g2;
-            }
 #pragma unroll 1
             for (int g = 0; g < ngroups; ++g) {
                 float a0[8], a1[8];
@@ -453,9 +376,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const bool live = __shfl_sync(0xffffffffu, my_route, src) >= 0;   // pad rows: no store
                     const int row = rb + src;
                     const float alpha = __shfl_sync(0xffffffffu, my_alpha, src);
-                    if (kFc1) {
+                    if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32) {
                         const float pw = __shfl_sync(0xffffffffu, my_pw, src);
-                        const float g2 = kTok ? __shfl_sync(0xffffffffu, my_g2, src) : 1.0f;
                         if (GATED) {
                             // silu(z) as in the standard epilogue (ex2-based exponential,
                             // approximate division)
@@ -464,7 +386,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             if (EPI == kEpiFc1F32) {
                                 if (live) p.out_f32[(size_t)row * p.out_cols + col0] = hv;
                             } else {
-                                requant_lane<EPI == kEpiFc1Tok46>(p, hv, kTok ? g2 : p.g2[0], row, col0, live);
+                                requant_lane(p, hv, p.g2[0], row, col0, live);
                             }
                         } else {
 #pragma unroll
@@ -476,7 +398,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 if (EPI == kEpiFc1F32) {
                                     if (live) p.out_f32[(size_t)row * p.out_cols + col] = hv;
                                 } else {
-                                    requant_lane<EPI == kEpiFc1Tok46>(p, hv, kTok ? g2 : p.g2[0], row, col, live);
+                                    requant_lane(p, hv, p.g2[0], row, col, live);
                                 }
                             }
                         }
@@ -534,12 +456,8 @@ cudaError_t setup_gemm_swap_kernels() {
     cudaError_t e;
     if ((e = set_smem_one<kEpiFc1Quant, true>())) return e;
     if ((e = set_smem_one<kEpiFc1F32, true>())) return e;
-    if ((e = set_smem_one<kEpiFc1Tok, true>())) return e;
-    if ((e = set_smem_one<kEpiFc1Tok46, true>())) return e;
     if ((e = set_smem_one<kEpiFc1Quant, false>())) return e;
     if ((e = set_smem_one<kEpiFc1F32, false>())) return e;
-    if ((e = set_smem_one<kEpiFc1Tok, false>())) return e;
-    if ((e = set_smem_one<kEpiFc1Tok46, false>())) return e;
     if ((e = set_smem_one<kEpiFc2Store, false>())) return e;
     return set_smem_one<kEpiFc2Scatter, false>();
 }
@@ -553,16 +471,12 @@ cudaError_t launch_gemm_swap(const LaunchCtx& c, int epilogue, bool gated, const
         switch (epilogue) {
             case kEpiFc1Quant: return c.launch(gemm_swap_kernel<kEpiFc1Quant, true>, grid, block, smem, tmW, tmX, p);
             case kEpiFc1F32: return c.launch(gemm_swap_kernel<kEpiFc1F32, true>, grid, block, smem, tmW, tmX, p);
-            case kEpiFc1Tok: return c.launch(gemm_swap_kernel<kEpiFc1Tok, true>, grid, block, smem, tmW, tmX, p);
-            case kEpiFc1Tok46: return c.launch(gemm_swap_kernel<kEpiFc1Tok46, true>, grid, block, smem, tmW, tmX, p);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (epilogue) {
         case kEpiFc1Quant: return c.launch(gemm_swap_kernel<kEpiFc1Quant, false>, grid, block, smem, tmW, tmX, p);
         case kEpiFc1F32: return c.launch(gemm_swap_kernel<kEpiFc1F32, false>, grid, block, smem, tmW, tmX, p);
-        case kEpiFc1Tok: return c.launch(gemm_swap_kernel<kEpiFc1Tok, false>, grid, block, smem, tmW, tmX, p);
-        case kEpiFc1Tok46: return c.launch(gemm_swap_kernel<kEpiFc1Tok46, false>, grid, block, smem, tmW, tmX, p);
         case kEpiFc2Store: return c.launch(gemm_swap_kernel<kEpiFc2Store, false>, grid, block, smem, tmW, tmX, p);
         case kEpiFc2Scatter: return c.launch(gemm_swap_kernel<kEpiFc2Scatter, false>, grid, block, smem, tmW, tmX, p);
         default: return cudaErrorInvalidValue;

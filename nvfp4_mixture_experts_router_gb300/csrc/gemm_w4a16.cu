@@ -236,16 +236,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int m_tile = tile / n_tiles, n_tile = tile % n_tiles;
             const int e = p.tile_expert[m_tile];
             if (e < 0 || e >= p.num_experts) break;
+            // the row's epilogue scalars, loaded while the main loop runs
+            const int row = m_tile * kBM + q * 32 + lane;
+            const EpiRow meta = epi_row<EPI>(p, row, e);
             // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
             if (!__all_sync(0xffffffffu, mbar_wait(&s.acc_full[acc], acc_phase, s.abort, p.status,
                                                    kStatusTimeoutEpilogue)))
                 break;
             tc_fence_after();
-            const int row = m_tile * kBM + q * 32 + lane;
-            const int route = p.route_of_row[row];
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kAccCols;
-            if (EPI == kEpiFc1Bf16) epilogue_fc1<EPI>(p, taddr, row, route, e, n_tile);
-            else epilogue_fc2<EPI, kStgCols>(p, taddr, row, route, e, n_tile, s.stg + q * 32 * kStgCols);
+            if (EPI == kEpiFc1Bf16) epilogue_fc1<EPI>(p, taddr, row, meta, n_tile);
+            else epilogue_fc2<EPI, kStgCols>(p, taddr, row, meta, n_tile, s.stg + q * 32 * kStgCols);
             tc_fence_before();
             mbar_arrive(&s.acc_empty[acc]);
             acc ^= 1;

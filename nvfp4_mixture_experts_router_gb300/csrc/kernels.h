@@ -57,14 +57,11 @@ cudaError_t launch_route_given(const LaunchCtx& c, int T, int E, int K, const in
 cudaError_t launch_route_scan_small(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
                                     int renorm, int* ids, float* w, int* unit_base, uint32_t* unit_mask, int* count,
                                     int* offsets, int* padded_offsets, int* meta, int* tile_expert, int* tile_pair,
-                                    int* tile_half, int* route_of_row, unsigned int* status_reset,
-                                    unsigned int* tile_done = nullptr);
-// tile_pair / tile_half may be null (then only meta[2] / meta[3] count them);
-// tile_done (may be null): the FC1 epilogue's arrival counters, zeroed for
-// every M tile and every entry of the half list
+                                    int* tile_half, int* route_of_row, unsigned int* status_reset);
+// tile_pair / tile_half may be null (then only meta[2] / meta[3] count them)
 cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
                                 int* padded_offsets, int* meta, int* tile_expert, int* tile_pair, int* tile_half,
-                                int* route_of_row, unsigned int* tile_done = nullptr);
+                                int* route_of_row);
 cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* ids, int* unit_base,
                            uint32_t* unit_mask, int* count, int* offsets, int* padded_offsets, int* meta,
                            int* tile_expert, int* row_of_route, int* route_of_row, unsigned int* status);
@@ -78,7 +75,6 @@ struct RouteScatter {
     int E;
     int* row_of_route;          // [T*K] out
     int* route_of_row;          // [rows_cap] out (valid rows)
-    unsigned int* row_amax;     // [rows_cap] zeroed for every route row (null: not used)
 };
 
 // rowops.cu
@@ -113,10 +109,7 @@ enum GemmEpilogue : int {
     kEpiFc2Store = 2,   // FC2: BF16 per-route rows (deterministic finalize)
     kEpiFc2Scatter = 3, // FC2: weighted FP32 atomic add into the token row (fused finalize)
     kEpiFc1Bf16 = 4,    // FC1 (W4A16): activation, route weight, BF16 store
-    kEpiFc1Mx = 5,      // FC1 (MXFP8): activation, route weight, MXFP8 requant (block 32)
-    kEpiFc1Tok = 6,     // FC1: activation, route weight, NVFP4 requant with the per-row G2 (row amax
-                        // gathered across the M tile's N tiles through row_amax / tile_done)
-    kEpiFc1Tok46 = 7    // the same with 4-over-6 blocks
+    kEpiFc1Mx = 5       // FC1 (MXFP8): activation, route weight, MXFP8 requant (block 32)
 };
 
 struct GemmParams {
@@ -151,11 +144,6 @@ struct GemmParams {
                                  // (g_act == nullptr: no activation global scale, W4A16)
     __nv_bfloat16* out_bf16;     // FC2 store: [rows_cap][H]; FC1 BF16: [rows_cap][I]
     int debug_skip_first_stage;  // test hook: CTA 0's producer skips its first stage (standard GEMM)
-    // kEpiFc1Tok*: per-row FC2-input scale computed inside FC1
-    unsigned int* row_amax;      // [rows_cap] float bits of the row's |h| max, zero before FC1
-    unsigned int* tile_done;     // [2 rows_cap/128] epilogue-warp arrivals per M tile (standard) or per
-                                 // occupied half (swapped), zero before FC1
-    float* g2_out;               // [rows_cap] G2 of each route row
 };
 
 cudaError_t setup_gemm_kernels();
@@ -168,9 +156,13 @@ int gemm_nvf4_tile_n(int kdim, int n);
 cudaError_t launch_gemm_nvf4(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              const GemmParams& p, int num_sms, int tile_n, int kind);
 // gemm_nvf4_pair.cu — the same GEMMs on CTA pairs (256 x 256 pair tiles over
-// pairs of M tiles of one expert); needs n % 256 == 0 and a tmB box of 128
-// rows.  setup sizes the persistent grid for `device`.
+// pairs of M tiles of one expert); needs n % 256 == 0 and tmA / tmB boxes of
+// 128 rows (2-D one-chunk maps, or 3-D chunk maps when p.chunk_maps).
+// Epilogues kEpiFc1Quant / F32, kEpiFc2Store / Scatter.
+// setup sizes the persistent grid for `device`.
 cudaError_t setup_gemm_pair_kernels(int device, int num_sms);
+int gemm_pair_chunks();           // 128-byte K chunks per pipeline stage (1: 2-D maps; 2: 3-D chunk maps)
+int gemm_pair_grid(int device);   // CTAs of the persistent pair grid (0 before setup)
 cudaError_t launch_gemm_nvf4_pair(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   const GemmParams& p, int device);
 

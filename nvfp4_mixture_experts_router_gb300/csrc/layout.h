@@ -133,8 +133,6 @@ inline moe_workspace_layout workspace_layout(moe_shape s, uint32_t flags) {
         if (mode == kModePerToken) {
             L.h_f32 = take(4 * cap * I);
             L.g2 = take(4 * cap);
-            L.row_amax = take(4 * cap);
-            L.tile_done = take(4 * 2 * (cap / kTileM));
         }
     } else {
         L.x_bf16_perm = take(2 * cap * H);

@@ -177,13 +177,20 @@ bool use_swap_gemm(moe_shape s, uint32_t flags) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Run a W4A4 GEMM with `n` weight rows per expert on CTA pairs?  Only on
-// request: measured on every workload, the pair kernel's cross-CTA stage
-// handshake and its single (256-column) accumulator cost more than the
-// operand bytes it saves per SM.
+// Run a W4A4 GEMM with `n` weight rows per expert on CTA pairs?  Pair tiles
+// cover 256 routes of one expert; by default they are used when the experts
+// that hold routes hold at least 256 on average (measured on GB300, standard
+// vs pairs: prefill T = 16384 step 4.12 vs 3.68 ms, DSV3 shape T = 8192 FC1
+// 1094 vs 1025 us, 16 experts x 2048 routes FC1 442 vs 374 us; below that a
+// pair's second M tile is mostly padding).  MOE_GEMM_PAIRS_ALWAYS / _NEVER
+// force either.
+constexpr int64_t kPairMinRoutesPerExpert = 256;
 bool use_pair_gemm(moe_shape s, uint32_t flags, int n) {
-    (void)s;
-    return n % 256 == 0 && (flags & MOE_GEMM_PAIRS_ALWAYS) != 0;
+    if (n % 256 != 0 || (flags & MOE_GEMM_PAIRS_NEVER)) return false;
+    if (flags & MOE_GEMM_PAIRS_ALWAYS) return true;
+    const int64_t routes = (int64_t)s.T * s.K;
+    const int64_t busy = routes < s.E ? routes : s.E;
+    return routes >= kPairMinRoutesPerExpert * busy;
 }
 
 }  // namespace
@@ -436,16 +443,6 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     const bool pair1 = mode != kModeW4A16 && !mx && !swap && use_pair_gemm(s, flags, N1),
                pair2 = mode != kModeW4A16 && !mx && !swap && use_pair_gemm(s, flags, s.H);
     const int tn1 = pair1 ? 128 : gemm_nvf4_tile_n(s.H, N1), tn2 = pair2 ? 128 : gemm_nvf4_tile_n(s.I, s.H);
-    // Per-token FC2-input quantization inside the FC1 epilogue: the epilogue
-    // warps of an M tile's (a route half's) N tiles wait for one another, so
-    // all of them must be able to hold an accumulator at once -- at most one
-    // tile per CTA of the persistent grid.  Otherwise (and on CTA pairs) FC1
-    // stores FP32 and a separate kernel quantizes.
-    const int fc1_tiles_per_m = swap ? (N1 / 128 + 1) / 2 : (N1 + tn1 - 1) / tn1;
-    const bool tok_fused = false && per_token && !pair1 && fc1_tiles_per_m <= sms;
-    unsigned int* row_amax = tok_fused ? reinterpret_cast<unsigned int*>(wsp(W.row_amax)) : nullptr;
-    unsigned int* tile_done = tok_fused ? reinterpret_cast<unsigned int*>(wsp(W.tile_done)) : nullptr;
-
     LaunchCtx c;
     c.stream = static_cast<cudaStream_t>(stream);
     c.pdl = events == nullptr;   // stage events between kernels would serialize them anyway
@@ -473,7 +470,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
                                     reinterpret_cast<int*>(wsp(W.offsets)), reinterpret_cast<int*>(wsp(W.padded_offsets)),
                                     meta, tile_expert, reinterpret_cast<int*>(wsp(W.tile_pair)),
                                     reinterpret_cast<int*>(wsp(W.tile_half)), route_of_row,
-                                    rin.status_cleared ? nullptr : status, tile_done);
+                                    rin.status_cleared ? nullptr : status);
     } else {
         e = launch_route_count(c, s.T, s.E, s.K, rin.logits, rin.bias, (flags & MOE_ROUTE_NO_RENORM) ? 0 : 1, ids,
                                topk_w, reinterpret_cast<int*>(wsp(W.unit_base)),
@@ -485,7 +482,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
                                 reinterpret_cast<int*>(wsp(W.count)), reinterpret_cast<int*>(wsp(W.offsets)),
                                 reinterpret_cast<int*>(wsp(W.padded_offsets)), meta, tile_expert,
                                 reinterpret_cast<int*>(wsp(W.tile_pair)), reinterpret_cast<int*>(wsp(W.tile_half)),
-                                route_of_row, tile_done);
+                                route_of_row);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     if (!mark(2)) return MOE_ERR_CUDA;
@@ -497,7 +494,6 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     rs.E = s.E;
     rs.row_of_route = row_of_route;
     rs.route_of_row = route_of_row;
-    rs.row_amax = row_amax;
 
     if (mode == kModeW4A16) {
         // ---- W4A16: BF16 activations, weights widened on chip ----
@@ -582,8 +578,9 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
     // single-CTA GEMMs with 128-wide tiles over rows of a multiple of 128
     // bytes copy two chunks per TMA instruction (3-D maps); the others use
     // 2-D maps
-    const bool ch1 = !pair1 && tn1 == 128 && rbx % 128 == 0;
-    const bool ch2 = !pair2 && tn2 == 128 && rbh % 128 == 0;
+    const bool pch = gemm_pair_chunks() > 1;   // pair kernel with multi-chunk stages (3-D maps)
+    const bool ch1 = pair1 ? (pch && rbx % 128 == 0) : (tn1 == 128 && rbx % 128 == 0);
+    const bool ch2 = pair2 ? (pch && rbh % 128 == 0) : (tn2 == 128 && rbh % 128 == 0);
     CUtensorMap tmA1, tmB1, tmA2, tmB2;
     const bool ok1 = swap ? (encode_operand_map(&tmA1, xq_codes, W.rows_cap, rbx, 128, 64) &&
                              encode_swap_weight_map(&tmB1, pw + P.w1_codes, (uint64_t)s.E * N1, rbx))
@@ -627,15 +624,6 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         g1p.out_codes = hq_codes;
         g1p.out_sf = hq_sf;
         epi1 = kEpiFc1Mx;
-    } else if (per_token && tok_fused) {
-        g1p.g_act = g1;
-        g1p.g_act_per_token = 1;
-        g1p.out_codes = hq_codes;
-        g1p.out_sf = hq_sf;
-        g1p.row_amax = row_amax;
-        g1p.tile_done = tile_done;
-        g1p.g2_out = reinterpret_cast<float*>(wsp(W.g2));
-        epi1 = four_six ? kEpiFc1Tok46 : kEpiFc1Tok;
     } else if (per_token) {
         g1p.g_act = g1;
         g1p.g_act_per_token = 1;
@@ -653,7 +641,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         : pair1 ? launch_gemm_nvf4_pair(c, epi1, tmA1, tmB1, g1p, device)
                 : launch_gemm_nvf4(c, epi1, tmA1, tmB1, g1p, sms, tn1, mx ? 1 : 0);
     if (e != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
-    if (per_token && !tok_fused) {
+    if (per_token) {
         e = launch_quantize_h(c, W.rows_cap, s.I, meta, route_of_row, reinterpret_cast<const float*>(wsp(W.h_f32)),
                               reinterpret_cast<float*>(wsp(W.g2)), hq_codes, hq_sf, four_six ? 1 : 0);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -699,8 +687,8 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         // an accumulator beyond 48 MB: walk FC2's output width in slabs whose
         // accumulator slice stays in L2 (T x slab x 4 B <= 48 MB), so that a
         // token's K reductions do not each go through HBM
-        const uint64_t slab_bytes_per_tile = (uint64_t)s.T * (uint64_t)tn2 * 4u;
-        if (!swap && !pair2 && (uint64_t)s.T * s.H * 4u > kSlabAccBytes) {
+        const uint64_t slab_bytes_per_tile = (uint64_t)s.T * (uint64_t)(pair2 ? 256 : tn2) * 4u;
+        if (!swap && (uint64_t)s.T * s.H * 4u > kSlabAccBytes) {
             const uint64_t ns = kSlabAccBytes / slab_bytes_per_tile;
             g2p.n_slab = (int)(ns < 1 ? 1 : ns);
         }
@@ -823,18 +811,7 @@ moe_status moe_nvfp4_forward_gate(moe_shape s, uint32_t flags, const void* x_bf1
 int moe_nvfp4_forward_launches(moe_shape s, uint32_t flags) {
     if (validate_shape(s, flags) != MOE_OK) return -1;
     if (flags & MOE_FUSED_LAYER) return 1;
-    // the per-token FC2-input quantization is a separate kernel only on CTA
-    // pairs, or when FC1 has more N tiles per M tile (route half) than the
-    // GPU has SMs (the shapes of this check run on any sm_103 part)
-    int extra = 0;
-    if (mode_of(flags) == kModePerToken) {
-        const int N1 = n1_of(s.I, flags);
-        const bool swap = use_swap_gemm(s, flags), pair1 = !swap && use_pair_gemm(s, flags, N1);
-        const int per_m = swap ? (N1 / 128 + 1) / 2 : (N1 + gemm_nvf4_tile_n(s.H, N1) - 1) / gemm_nvf4_tile_n(s.H, N1);
-        int sms = 0;
-        const bool known = device_state(&sms) == MOE_OK;
-        extra = (true || pair1 || !known || per_m > sms) ? 1 : 0;
-    }
+    const int extra = mode_of(flags) == kModePerToken ? 1 : 0;   // the FC2-input quantization
     // T <= 32: router and scan in one launch
     if (s.T <= kUnitTokens) return 5 + extra;
     // router + unit counts, scan, quantize or gather (+ row scatter), FC1, [FC2-input quant], FC2, finalize

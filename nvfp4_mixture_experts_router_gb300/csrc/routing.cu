@@ -159,7 +159,6 @@ struct ScanOut {
     int* tile_pair;
     int* tile_half;
     int* route_of_row;
-    unsigned int* tile_done;   // may be null: per-M-tile / per-half counters of the FC1 epilogue, zeroed
 };
 
 // By a block of 1024 threads, given the per-expert route counts s_cnt[E]:
@@ -249,14 +248,6 @@ __device__ __forceinline__ void expert_outputs_block(int E, const int* s_cnt, co
             // the 64-row halves of this expert's M tiles that hold routes, in order
             const int nh = (cnt + kTileM / 2 - 1) / (kTileM / 2);
             for (int j = lane; j < nh; j += 32) o.tile_half[s_half[e] + j] = ((r0 / kTileM + (j >> 1)) << 1) | (j & 1);
-        }
-        if (o.tile_done != nullptr) {
-            // the FC1 epilogue counts arrivals per M tile (standard
-            // orientation) or per entry of the half list (swapped): zero both
-            // index ranges of this expert
-            for (int tl = r0 / kTileM + lane; tl < (r0 + pcnt) / kTileM; tl += 32) o.tile_done[tl] = 0u;
-            const int nh = (cnt + kTileM / 2 - 1) / (kTileM / 2);
-            for (int j = lane; j < nh; j += 32) o.tile_done[s_half[e] + j] = 0u;
         }
     }
 }
@@ -416,18 +407,17 @@ cudaError_t launch_route_count(const LaunchCtx& c, int T, int E, int K, const fl
 
 cudaError_t launch_permute_scan(const LaunchCtx& c, int T, int E, int* unit_base, int* count, int* offsets,
                                 int* padded_offsets, int* meta, int* tile_expert, int* tile_pair, int* tile_half,
-                                int* route_of_row, unsigned int* tile_done) {
-    const ScanOut o{count, offsets, padded_offsets, meta, tile_expert, tile_pair, tile_half, route_of_row, tile_done};
+                                int* route_of_row) {
+    const ScanOut o{count, offsets, padded_offsets, meta, tile_expert, tile_pair, tile_half, route_of_row};
     return c.launch(permute_scan_kernel, dim3(1), dim3(1024), 0, T, E, unit_base, o);
 }
 
 cudaError_t launch_route_scan_small(const LaunchCtx& c, int T, int E, int K, const float* logits, const float* bias,
                                     int renorm, int* ids, float* w, int* unit_base, uint32_t* unit_mask, int* count,
                                     int* offsets, int* padded_offsets, int* meta, int* tile_expert, int* tile_pair,
-                                    int* tile_half, int* route_of_row, unsigned int* status_reset,
-                                    unsigned int* tile_done) {
+                                    int* tile_half, int* route_of_row, unsigned int* status_reset) {
     if (T > kUnitTokens) return cudaErrorInvalidValue;
-    const ScanOut o{count, offsets, padded_offsets, meta, tile_expert, tile_pair, tile_half, route_of_row, tile_done};
+    const ScanOut o{count, offsets, padded_offsets, meta, tile_expert, tile_pair, tile_half, route_of_row};
     MOE_EPL_DISPATCH(E, route_scan_small_kernel, dim3(1), dim3(1024), 0, T, E, K, logits, bias, renorm, ids, w,
                      unit_base, unit_mask, o, status_reset);
 }
@@ -442,7 +432,7 @@ cudaError_t launch_permute(const LaunchCtx& c, int T, int E, int K, const int* i
                    status);
     if (err != cudaSuccess) return err;
     err = launch_permute_scan(c, T, E, unit_base, count, offsets, padded_offsets, meta, tile_expert, nullptr, nullptr,
-                              route_of_row, nullptr);
+                              route_of_row);
     if (err != cudaSuccess) return err;
     const int64_t routes = (int64_t)T * K;
     return c.launch(permute_scatter_kernel, dim3((unsigned)((routes + 255) / 256)), dim3(256), 0, T, E, K, ids,

@@ -54,7 +54,6 @@ __device__ __forceinline__ int scatter_token_routes(int t, int T, int K, int lan
     const int row = route_row(t, e, U, rs.unit_base, rs.unit_mask);
     rs.row_of_route[r] = row;
     rs.route_of_row[row] = r;
-    if (rs.row_amax) rs.row_amax[row] = 0u;
     return row;
 }
 
