@@ -85,13 +85,14 @@ typedef enum {
 /* bit 6: router weights are the full softmax over all E experts evaluated
  * at the selected ones, instead of the softmax over the K selected. */
 #define MOE_ROUTE_NO_RENORM (1u << 6)
-/* bits 7-8: GEMM tile scheduling (NVFP4 W4A4 only; results are the same
- * either way up to FP32 accumulation order).  A GEMM whose weight height is
- * a multiple of 256 runs on CTA pairs (cta_group::2 MMAs, 256 x 256 tiles
- * over two 128-row M tiles of one expert) when the experts holding routes
- * hold at least 256 on average (T*K >= 256 * min(E, T*K)), else on single
- * CTAs; MOE_GEMM_PAIRS_ALWAYS / MOE_GEMM_PAIRS_NEVER force pairs / single
- * CTAs.  Setting both is invalid. */
+/* bits 7-8: GEMM tile scheduling (W4A4 NVFP4 and W4A16; ignored by MXFP8;
+ * results are the same either way up to FP32 accumulation order).  A GEMM
+ * whose weight height is a multiple of 256 runs on CTA pairs (cta_group::2
+ * MMAs, 256 x 256 tiles over two 128-row M tiles of one expert) when the
+ * experts holding routes hold at least 256 on average (T*K >= 256 *
+ * min(E, T*K)), else on single CTAs; MOE_GEMM_PAIRS_ALWAYS /
+ * MOE_GEMM_PAIRS_NEVER force pairs / single CTAs.  W4A16 GEMMs run on
+ * pairs only with MOE_GEMM_PAIRS_ALWAYS.  Setting both is invalid. */
 #define MOE_GEMM_PAIRS_NEVER (1u << 7)
 #define MOE_GEMM_PAIRS_ALWAYS (1u << 8)
 /* bit 9: 4-over-6 activation quantization (per-token W4A4 only) [PR #4366

@@ -434,6 +434,15 @@ __device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Arrive on the other CTA's mbarrier after writes to this CTA's own shared
+// memory that the pair MMA (issued by the other CTA) reads: release at CTA
+// scope orders the writes (and, after __syncwarp, the warp's) before the
+// arrival without the cluster-wide fence of a cluster-scope release, which
+// waits for the SM's outstanding memory traffic (microseconds under load).
+// The writer issues fence.proxy.async first, for the tensor core's reads.
+__device__ __forceinline__ void mbar_arrive_remote_cta_release(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
@@ -462,6 +471,35 @@ __device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc
         " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+// Tile copies whose completion is counted on an mbarrier of either CTA of the
+// pair (`bar` a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
+// M = 256 BF16 MMA over the CTA pair (kind::f16, FP32 accumulate), issued by
+// the even CTA; operand halves split as in tc_mma_nvf4_pair, no scales.
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrive on the mbarrier at `bar`'s offset in every CTA of `cta_mask` once all
@@ -547,6 +585,21 @@ __device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]
     else tmem_st32(taddr, r);
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute the
+// same instruction).  An increase waits until the block's pool, fixed at
+// launch (threads x registers per thread), has the registers free, so the
+// kernels that use these check the launch register count on the host.
+template <uint32_t N>
+__device__ __forceinline__ void regs_release() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_claim() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // Programmatic dependent launch: wait for the preceding grid's results /
 // allow the next grid to start its prologue.

@@ -38,86 +38,120 @@ __device__ __forceinline__ EpiRow epi_row(const GemmParams& p, int row, int e) {
     return m;
 }
 
+// FC1 activation of 32 columns in place.  SwiGLU: h holds 32 gate and u the
+// matching 32 up accumulators; h <- silu(alpha g) (alpha u) pw.  ReLU2
+// (u unused): h <- max(alpha h, 0)^2 pw.
+__device__ __forceinline__ void fc1_act32(float (&h)[32], const float (&u)[32], bool swiglu, float alpha, float pw) {
+    if (swiglu) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            // silu(z) = z / (1 + e^-z) with the ex2-based exponential and
+            // the approximate division (relative error ~1e-6; for z below
+            // about -88 the denominator is +inf and the result 0).  The
+            // IEEE division + full-range expf, or a correctly rounded
+            // reciprocal, cost 3-6x this epilogue and made FC1
+            // epilogue-bound.
+            const float zg = h[i] * alpha, zu = u[i] * alpha;
+            h[i] = __fdividef(zg, 1.0f + __expf(-zg)) * zu * pw;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float z = fmaxf(h[i] * alpha, 0.0f);
+            h[i] = z * z * pw;
+        }
+    }
+}
+
+// Store 32 activated FC1 outputs of route row `row` at columns col0..col0+31
+// in the FC2-input format of EPI.
+template <int EPI>
+__device__ __forceinline__ void fc1_emit32(const GemmParams& p, const float (&h)[32], int row, int col0, float g2) {
+    if (EPI == kEpiFc1Mx) {
+        // one MXFP8 block per 32 columns: 32 E4M3 bytes and an E8M0 byte
+        uint32_t q[8];
+        const uint32_t sc = quant_block32_mx(h, q);
+        uint4* dst = reinterpret_cast<uint4*>(p.out_codes + (size_t)row * p.out_cols + col0);
+        dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+        p.out_sf[sf_offset_mx(row, col0 / 32, p.out_cols)] = (uint8_t)sc;
+    } else if (EPI == kEpiFc1Quant) {
+        uint32_t q[4];
+        float blk[16];
+        uint32_t c2[2];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) blk[i] = h[i];
+        const uint32_t s0 = quant_block16(blk, g2, c2);
+        q[0] = c2[0]; q[1] = c2[1];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) blk[i] = h[16 + i];
+        const uint32_t s1 = quant_block16(blk, g2, c2);
+        q[2] = c2[0]; q[3] = c2[1];
+        *reinterpret_cast<uint4*>(p.out_codes + (size_t)row * (p.out_cols / 2) + col0 / 2) =
+            make_uint4(q[0], q[1], q[2], q[3]);
+        // two scales per 32 columns: a 16-bit store at an even scale index
+        *reinterpret_cast<uint16_t*>(p.out_sf + sf_offset(row, col0 / 16, p.out_cols)) = (uint16_t)(s0 | (s1 << 8));
+    } else if (EPI == kEpiFc1Bf16) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(h[2 * i], h[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + (size_t)row * p.out_cols + col0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else {
+        float4* dst = reinterpret_cast<float4*>(p.out_f32 + (size_t)row * p.out_cols + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+    }
+}
+
 // SwiGLU tile: columns 0..63 gate, 64..127 up (prepared-weight interleave);
-// yields 64 FC2-input values.  ReLU2 tile: 128 values.
+// yields 64 FC2-input values.  ReLU2 tile: 128 values.  Reads the
+// accumulator chunk by chunk from tensor memory.
 template <int EPI>
 __device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr, int row, const EpiRow& m,
                                              int n_tile) {
-    const int route = m.route;
-    const float alpha = m.alpha, pw = m.pw, g2 = m.g2;
     const bool swiglu = p.act == MOE_ACT_SWIGLU;
     const int chunks = swiglu ? 2 : 4;
-    uint32_t sf_pair[4];
     for (int ch = 0; ch < chunks; ++ch) {
-        float h[32];
-        int col0;
-        if (swiglu) {
-            float u[32];
-            tmem_ld32(taddr + ch * 32, h);
-            tmem_ld32(taddr + 64 + ch * 32, u);
-            tmem_ld_wait();
+        float h[32], u[32];
+        tmem_ld32(taddr + ch * 32, h);
+        if (swiglu) tmem_ld32(taddr + 64 + ch * 32, u);
+        tmem_ld_wait();
+        fc1_act32(h, u, swiglu, m.alpha, m.pw);
+        if (m.route >= 0) fc1_emit32<EPI>(p, h, row, (swiglu ? n_tile * 64 : n_tile * 128) + ch * 32, m.g2);
+    }
+}
+
+// The same epilogue on a slice the caller has already copied out of tensor
+// memory (acc[c] = accumulator column c of the thread's row), so that the
+// accumulator can be handed back to the MMA before this work starts.
+template <int EPI>
+__device__ __forceinline__ void epilogue_fc1_held(const GemmParams& p, const float (&acc)[128], int row,
+                                                  const EpiRow& m, int n_tile) {
+    if (p.act == MOE_ACT_SWIGLU) {
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+            float h[32], u[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                // silu(z) = z / (1 + e^-z) with the ex2-based exponential and
-                // the approximate division (relative error ~1e-6; for z below
-                // about -88 the denominator is +inf and the result 0).  The
-                // IEEE division + full-range expf, or a correctly rounded
-                // reciprocal, cost 3-6x this epilogue and made FC1
-                // epilogue-bound.
-                const float zg = h[i] * alpha, zu = u[i] * alpha;
-                h[i] = __fdividef(zg, 1.0f + __expf(-zg)) * zu * pw;
+                h[i] = acc[ch * 32 + i];
+                u[i] = acc[64 + ch * 32 + i];
             }
-            col0 = n_tile * 64 + ch * 32;
-        } else {
-            tmem_ld32(taddr + ch * 32, h);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float z = fmaxf(h[i] * alpha, 0.0f);
-                h[i] = z * z * pw;
-            }
-            col0 = n_tile * 128 + ch * 32;
+            fc1_act32(h, u, true, m.alpha, m.pw);
+            if (m.route >= 0) fc1_emit32<EPI>(p, h, row, n_tile * 64 + ch * 32, m.g2);
         }
-        if (route < 0) continue;
-        if (EPI == kEpiFc1Mx) {
-            // one MXFP8 block per 32 columns: 32 E4M3 bytes and an E8M0 byte
-            uint32_t q[8];
-            const uint32_t sc = quant_block32_mx(h, q);
-            uint4* dst = reinterpret_cast<uint4*>(p.out_codes + (size_t)row * p.out_cols + col0);
-            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-            p.out_sf[sf_offset_mx(row, col0 / 32, p.out_cols)] = (uint8_t)sc;
-        } else if (EPI == kEpiFc1Quant) {
-            uint32_t q[4];
-            float blk[16];
-            uint32_t c2[2];
+    } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) blk[i] = h[i];
-            const uint32_t s0 = quant_block16(blk, g2, c2);
-            q[0] = c2[0]; q[1] = c2[1];
+        for (int ch = 0; ch < 4; ++ch) {
+            float h[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) blk[i] = h[16 + i];
-            const uint32_t s1 = quant_block16(blk, g2, c2);
-            q[2] = c2[0]; q[3] = c2[1];
-            *reinterpret_cast<uint4*>(p.out_codes + (size_t)row * (p.out_cols / 2) + col0 / 2) =
-                make_uint4(q[0], q[1], q[2], q[3]);
-            sf_pair[ch] = s0 | (s1 << 8);
-            // two scales per 32 columns: a 16-bit store at an even scale index
-            *reinterpret_cast<uint16_t*>(p.out_sf + sf_offset(row, col0 / 16, p.out_cols)) = (uint16_t)sf_pair[ch];
-        } else if (EPI == kEpiFc1Bf16) {
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const __nv_bfloat162 b = __floats2bfloat162_rn(h[2 * i], h[2 * i + 1]);
-                w[i] = *reinterpret_cast<const uint32_t*>(&b);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + (size_t)row * p.out_cols + col0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        } else {
-            float4* dst = reinterpret_cast<float4*>(p.out_f32 + (size_t)row * p.out_cols + col0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+            for (int i = 0; i < 32; ++i) h[i] = acc[ch * 32 + i];
+            fc1_act32(h, h, false, m.alpha, m.pw);
+            if (m.route >= 0) fc1_emit32<EPI>(p, h, row, n_tile * 128 + ch * 32, m.g2);
         }
     }
 }
@@ -161,67 +195,88 @@ __device__ __forceinline__ void staged_rows(uint32_t* stg, const uint32_t (&w)[N
     __syncwarp();
 }
 
-// COLS > 0: the scatter and the BF16 store go through staged_rows with the
-// warp's staging block stg (32 rows x COLS words); COLS = 0 writes straight
-// from registers.
-template <int EPI, int COLS = 0>
-__device__ __forceinline__ void epilogue_fc2(const GemmParams& p, uint32_t taddr, int row, const EpiRow& m,
-                                             int n_tile, uint32_t* stg = nullptr) {
+// FC2 output of 32 columns (accumulators o, columns col0..col0+31 of the
+// output row): BF16 per-route row (store) or alpha-scaled FP32 reduction
+// into the token's row (scatter).  COLS > 0: through staged_rows with the
+// warp's staging block stg (32 rows x COLS words), every lane taking part;
+// COLS = 0 writes straight from registers.
+template <int EPI, int COLS>
+__device__ __forceinline__ void fc2_emit32(const GemmParams& p, const float (&o)[32], int row, const EpiRow& m,
+                                           int col0, uint32_t* stg) {
     const int route = m.route;
     const float alpha = m.alpha;
-    const int token = m.token;
-    for (int ch = 0; ch < 4; ++ch) {
-        float o[32];
-        tmem_ld32(taddr + ch * 32, o);
-        tmem_ld_wait();
-        const int col0 = n_tile * 128 + ch * 32;
-        if constexpr (COLS > 0) {
-            // every lane takes part (shuffles); rows without a route write nothing
-            if constexpr (EPI == kEpiFc2Store) {
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * i] * alpha, o[2 * i + 1] * alpha);
-                    w[i] = *reinterpret_cast<const uint32_t*>(&b);
-                }
-                const int row0 = row - (threadIdx.x & 31);
-                staged_rows<COLS>(stg, w, [&](int r, int w0, uint4 v) {
-                    if (__shfl_sync(0xffffffffu, route, r) >= 0)
-                        *reinterpret_cast<uint4*>(p.out_bf16 + (size_t)(row0 + r) * p.out_cols + col0 + 2 * w0) = v;
-                });
-            } else {
-                uint32_t w[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * alpha);
-                const int tk_lane = route >= 0 ? token : -1;
-                staged_rows<COLS>(stg, w, [&](int r, int w0, uint4 v) {
-                    const int tk = __shfl_sync(0xffffffffu, tk_lane, r);
-                    if (tk >= 0)
-                        red_add_f32x4(reinterpret_cast<float4*>(p.out_f32 + (size_t)tk * p.out_cols + col0 + w0),
-                                      __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                                      __uint_as_float(v.w));
-                });
-            }
-            continue;
-        }
-        if (route < 0) continue;
-        if (EPI == kEpiFc2Store) {
+    if constexpr (COLS > 0) {
+        // rows without a route write nothing
+        if constexpr (EPI == kEpiFc2Store) {
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * i] * alpha, o[2 * i + 1] * alpha);
                 w[i] = *reinterpret_cast<const uint32_t*>(&b);
             }
-            uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + (size_t)row * p.out_cols + col0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            const int row0 = row - (threadIdx.x & 31);
+            staged_rows<COLS>(stg, w, [&](int r, int w0, uint4 v) {
+                if (__shfl_sync(0xffffffffu, route, r) >= 0)
+                    *reinterpret_cast<uint4*>(p.out_bf16 + (size_t)(row0 + r) * p.out_cols + col0 + 2 * w0) = v;
+            });
         } else {
-            float4* dst = reinterpret_cast<float4*>(p.out_f32 + (size_t)token * p.out_cols + col0);
+            uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                red_add_f32x4(dst + i, o[4 * i] * alpha, o[4 * i + 1] * alpha, o[4 * i + 2] * alpha,
-                              o[4 * i + 3] * alpha);
+            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * alpha);
+            const int tk_lane = route >= 0 ? m.token : -1;
+            staged_rows<COLS>(stg, w, [&](int r, int w0, uint4 v) {
+                const int tk = __shfl_sync(0xffffffffu, tk_lane, r);
+                if (tk >= 0)
+                    red_add_f32x4(reinterpret_cast<float4*>(p.out_f32 + (size_t)tk * p.out_cols + col0 + w0),
+                                  __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                                  __uint_as_float(v.w));
+            });
         }
+        return;
+    }
+    if (route < 0) return;
+    if (EPI == kEpiFc2Store) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * i] * alpha, o[2 * i + 1] * alpha);
+            w[i] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + (size_t)row * p.out_cols + col0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else {
+        float4* dst = reinterpret_cast<float4*>(p.out_f32 + (size_t)m.token * p.out_cols + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            red_add_f32x4(dst + i, o[4 * i] * alpha, o[4 * i + 1] * alpha, o[4 * i + 2] * alpha,
+                          o[4 * i + 3] * alpha);
+    }
+}
+
+// FC2 epilogue of a 128-column slice, read chunk by chunk from tensor memory.
+template <int EPI, int COLS = 0>
+__device__ __forceinline__ void epilogue_fc2(const GemmParams& p, uint32_t taddr, int row, const EpiRow& m,
+                                             int n_tile, uint32_t* stg = nullptr) {
+    for (int ch = 0; ch < 4; ++ch) {
+        float o[32];
+        tmem_ld32(taddr + ch * 32, o);
+        tmem_ld_wait();
+        fc2_emit32<EPI, COLS>(p, o, row, m, n_tile * 128 + ch * 32, stg);
+    }
+}
+
+// The same on a slice already copied out of tensor memory (see
+// epilogue_fc1_held).
+template <int EPI, int COLS = 0>
+__device__ __forceinline__ void epilogue_fc2_held(const GemmParams& p, const float (&acc)[128], int row,
+                                                  const EpiRow& m, int n_tile, uint32_t* stg = nullptr) {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+        float o[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = acc[ch * 32 + i];
+        fc2_emit32<EPI, COLS>(p, o, row, m, n_tile * 128 + ch * 32, stg);
     }
 }
 

@@ -29,7 +29,13 @@
 //     empty barriers of both CTAs (multicast), the finished accumulator to
 //     both acc_full barriers;
 //   * every epilogue warp of both CTAs releases the accumulator on rank 0's
-//     acc_empty (sixteen arrivals).
+//     acc_empty (sixteen arrivals) as soon as it has copied its 32 rows x 128
+//     columns into registers; the activation, quantization and stores of
+//     that tile then run while the MMAs of the next tile fill the
+//     accumulator again.  (A second 256-column accumulator does not fit
+//     beside the scale slots in the 512 tensor-memory columns; with a
+//     single one that is drained in place, the MMA thread spent 26 % of the
+//     K = 7168 FC1 and half of the scatter FC2 waiting for the epilogue.)
 // Operand stages hold CH = 2 128-byte K chunks of every operand row (one
 // 32 KB copy per operand and CTA: the copy rate of an SM's TMA ring grows
 // with the bytes per stage, ~100 GB/s at 16-32 KB, ~148 GB/s at 64 KB), three
@@ -37,15 +43,21 @@
 // (shared memory and tensor-memory slots), refilled as soon as the writers
 // have read a slot and the MMAs two stages back have finished.
 //
-// Roles per CTA (448 threads): warp 0 producer, warp 1 tensor-memory
-// allocation (both CTAs together) and, in rank 0, the MMA issuer; warps 2-5
-// scale writers; warps 6-13 epilogue over this CTA's 128 rows (two groups of
-// four warps, 128 accumulator columns each).
+// Roles per CTA (512 threads, four warpgroups): warpgroup 0 = warp 0
+// producer, warp 1 tensor-memory allocation (both CTAs together) and, in
+// rank 0, the MMA issuer, warps 2-3 idle; warpgroup 1 = the four scale
+// writers; warpgroups 2-3 = the epilogue over this CTA's 128 rows (two groups
+// of four warps, 128 accumulator columns each).  The launch gives every
+// thread 128 registers; warpgroups 0 and 1 hand theirs down to 48 and 80 so
+// that the epilogue warps can hold a 128-column slice (192 each; the split
+// is the same on each of the four SM sub-partitions, which hold one warp of
+// every warpgroup).
 // Every wait is bounded (1 s); a timeout sets a status bit, marks both CTAs
 // aborted, and all roles drain and reach the final pair barrier.
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "pair_tiles.cuh"
 
 namespace moe {
 
@@ -54,9 +66,19 @@ namespace {
 constexpr int kPRows = 128;                      // A rows per CTA (256 per pair)
 constexpr int kPN = 256;                         // weight rows per pair tile (128 per CTA)
 constexpr int kPSfWarps = 4;
-constexpr int kPEpiWarp0 = 2 + kPSfWarps;
-constexpr int kPEpiWarps = 8;
+constexpr int kPSfWarp0 = 4;                     // warpgroup 1
+constexpr int kPEpiWarp0 = kPSfWarp0 + kPSfWarps;
+constexpr int kPEpiWarps = 8;                    // warpgroups 2 and 3
 constexpr int kPThreads = (kPEpiWarp0 + kPEpiWarps) * 32;
+// Register split (setmaxnreg, per warpgroup) within the launch's pool of
+// kPThreads x kPRegsLaunch; the host refuses to launch if the compiled
+// kernel's count differs from kPRegsLaunch.
+constexpr uint32_t kPRegsLaunch = 65536 / kPThreads;
+constexpr uint32_t kPRegsCtl = 48;
+constexpr uint32_t kPRegsSf = 80;
+constexpr uint32_t kPRegsEpi = 192;
+static_assert(kPThreads == 512, "four warpgroups");
+static_assert(128 * (kPRegsCtl + kPRegsSf) + 256 * kPRegsEpi <= kPThreads * kPRegsLaunch, "register split");
 constexpr uint32_t kPTmemCols = 512;
 constexpr uint32_t kPSfCol0 = kPN;               // accumulator: columns 0..255
 // Two rings: operand stages (CH = 2 128-byte K chunks of every operand row)
@@ -128,48 +150,6 @@ __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
     return s;
 }
 
-// Tile copies whose completion is counted on an mbarrier of either CTA of the
-// pair (`bar` a shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                                 uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                                 int z, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
-        : "memory");
-}
-
-// Pair tile -> (M tile of this CTA, the pair's first M tile, N tile), N
-// tiles fastest; with slabs of p.n_slab N tiles the output width is walked
-// slab by slab, every pair within a slab before the next (the fused-finalize
-// scatter then keeps adding into one slab of the accumulator, which stays in
-// L2).  m_tile is -1 for rank 1 of a pair without a second M tile.
-__device__ __forceinline__ void decode_pair(const GemmParams& p, int tile, int n_tiles, int num_pairs, uint32_t rank,
-                                            int& m_tile, int& m0, int& n_tile) {
-    int pr;
-    if (p.n_slab <= 0) {
-        pr = tile / n_tiles;
-        n_tile = tile % n_tiles;
-    } else {
-        const int per_slab = num_pairs * p.n_slab;
-        const int slab = tile / per_slab, rem = tile % per_slab;
-        const int width = min(p.n_slab, n_tiles - slab * p.n_slab);   // the last slab may be narrower
-        pr = rem / width;
-        n_tile = slab * p.n_slab + rem % width;
-    }
-    const int v = p.tile_pair[pr];
-    m0 = v >> 1;
-    m_tile = rank == 0 ? m0 : ((v & 1) ? m0 + 1 : -1);
-}
-
 }  // namespace
 
 template <int EPI>
@@ -224,101 +204,105 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int row_chunks = (p.kdim / 2 + 127) / 128;           // 128-byte chunks per row
     const int rb_per_expert = p.n / 128;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_normal();
-            // slabs: the activation rows are re-read once per slab; evict them
-            // first so that the slab of the accumulator stays in L2
-            const uint64_t pol_a = p.n_slab > 0 ? policy_evict_first() : pol;
-            const uint32_t full0 = cluster_map(s.full, 0);      // rank 0's stage barriers
-            int stage = 0, sfs = 0;
-            uint32_t phase = 0, sfp = 0;
-            for (int tile = pair_slot; tile < total; tile += pair_slots) {
-                int m_tile, m0, n_tile;
-                decode_pair(p, tile, n_tiles, num_pairs, rank, m_tile, m0, n_tile);
-                const int ld_m = m_tile >= 0 ? m_tile : m0;     // rank 1 without a second tile reloads the first
-                const int e = (m0 >= 0 && m0 < num_m_tiles) ? p.tile_expert[m0] : -1;
-                if (e < 0 || e >= p.num_experts || ld_m >= num_m_tiles) {
-                    atomicOr(p.status, kStatusBadExpert);
-                    *s.abort = 1;
-                    break;
-                }
-                const int a_row = ld_m * kPRows;
-                const int b_row = e * p.n + n_tile * kPN + (int)rank * (kPN / 2);
-                const uint8_t* sfa_src = p.sfa + (size_t)ld_m * kblocks * 512;
-                const uint8_t* sfb_src = p.sfb + ((size_t)e * rb_per_expert + (size_t)n_tile * 2) * kblocks * 512;
-                for (int ks = 0; ks < kstages; ++ks) {
-                    const int nkb = min(PC::kKb, kblocks - PC::kKb * ks);
-                    const uint32_t sf_bytes = (uint32_t)nkb * 512u;
-                    // this CTA's scale atoms (its own A rows, all 256 B rows)
-                    // into the scale ring once the writers have read that slot
-                    if (!mbar_wait(&s.sf_free[sfs], sfp ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
-                    mbar_arrive_expect_tx(&s.sf_full[sfs], 3u * sf_bytes);
-                    bulk_load(s.sfa + sfs * PC::kSfA, sfa_src + (size_t)ks * PC::kKb * 512, sf_bytes,
-                              &s.sf_full[sfs], pol);
-                    for (int rb = 0; rb < 2; ++rb)
-                        bulk_load(s.sfb + sfs * PC::kSfB + rb * PC::kSfA,
-                                  sfb_src + ((size_t)rb * kblocks + (size_t)ks * PC::kKb) * 512, sf_bytes,
+    if (warp < kPSfWarp0) {
+        regs_release<kPRegsCtl>();
+        if (warp == 0) {
+            if (lane == 0) {
+                const uint64_t pol = policy_evict_normal();
+                // slabs: the activation rows are re-read once per slab; evict them
+                // first so that the slab of the accumulator stays in L2
+                const uint64_t pol_a = p.n_slab > 0 ? policy_evict_first() : pol;
+                const uint32_t full0 = cluster_map(s.full, 0);      // rank 0's stage barriers
+                int stage = 0, sfs = 0;
+                uint32_t phase = 0, sfp = 0;
+                for (int tile = pair_slot; tile < total; tile += pair_slots) {
+                    int m_tile, m0, n_tile;
+                    decode_pair(p, tile, n_tiles, num_pairs, rank, m_tile, m0, n_tile);
+                    const int ld_m = m_tile >= 0 ? m_tile : m0;     // rank 1 without a second tile reloads the first
+                    const int e = (m0 >= 0 && m0 < num_m_tiles) ? p.tile_expert[m0] : -1;
+                    if (e < 0 || e >= p.num_experts || ld_m >= num_m_tiles) {
+                        atomicOr(p.status, kStatusBadExpert);
+                        *s.abort = 1;
+                        break;
+                    }
+                    const int a_row = ld_m * kPRows;
+                    const int b_row = e * p.n + n_tile * kPN + (int)rank * (kPN / 2);
+                    const uint8_t* sfa_src = p.sfa + (size_t)ld_m * kblocks * 512;
+                    const uint8_t* sfb_src = p.sfb + ((size_t)e * rb_per_expert + (size_t)n_tile * 2) * kblocks * 512;
+                    for (int ks = 0; ks < kstages; ++ks) {
+                        const int nkb = min(PC::kKb, kblocks - PC::kKb * ks);
+                        const uint32_t sf_bytes = (uint32_t)nkb * 512u;
+                        // this CTA's scale atoms (its own A rows, all 256 B rows)
+                        // into the scale ring once the writers have read that slot
+                        if (!mbar_wait(&s.sf_free[sfs], sfp ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
+                        mbar_arrive_expect_tx(&s.sf_full[sfs], 3u * sf_bytes);
+                        bulk_load(s.sfa + sfs * PC::kSfA, sfa_src + (size_t)ks * PC::kKb * 512, sf_bytes,
                                   &s.sf_full[sfs], pol);
-                    if (++sfs == PC::kSfStages) { sfs = 0; sfp ^= 1u; }
-                    // completed by rank 0's commit: acquire at cluster scope
-                    if (!mbar_wait<true>(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer))
-                        goto done;
-                    // operands: counted on rank 0's barrier, which rank 0
-                    // announces for both CTAs
-                    uint8_t* a_dst = s.a + stage * PC::kTileA;
-                    uint8_t* b_dst = s.b + stage * PC::kTileB;
-                    const int c0 = PC::kCh * ks;
-                    const uint32_t bar = full0 + (uint32_t)stage * 8u;
-                    if (p.chunk_maps) {
-                        if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2u * (PC::kTileA + PC::kTileB));
-                        tma_load_3d_pair(a_dst, &tmA, bar, 0, a_row, c0, pol_a);
-                        tma_load_3d_pair(b_dst, &tmB, bar, 0, b_row, c0, pol);
-                    } else {
-                        const int nch = min(PC::kCh, row_chunks - c0);
-                        if (rank == 0)
-                            mbar_arrive_expect_tx(&s.full[stage], 2u * (uint32_t)nch * (kPRows * 128 + (kPN / 2) * 128));
-                        for (int c = 0; c < nch; ++c) {
-                            tma_load_2d_pair(a_dst + c * kPRows * 128, &tmA, bar, (c0 + c) * 128, a_row, pol_a);
-                            tma_load_2d_pair(b_dst + c * (kPN / 2) * 128, &tmB, bar, (c0 + c) * 128, b_row, pol);
+                        for (int rb = 0; rb < 2; ++rb)
+                            bulk_load(s.sfb + sfs * PC::kSfB + rb * PC::kSfA,
+                                      sfb_src + ((size_t)rb * kblocks + (size_t)ks * PC::kKb) * 512, sf_bytes,
+                                      &s.sf_full[sfs], pol);
+                        if (++sfs == PC::kSfStages) { sfs = 0; sfp ^= 1u; }
+                        // completed by rank 0's commit: acquire at cluster scope
+                        if (!mbar_wait<true>(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer))
+                            goto done;
+                        // operands: counted on rank 0's barrier, which rank 0
+                        // announces for both CTAs
+                        uint8_t* a_dst = s.a + stage * PC::kTileA;
+                        uint8_t* b_dst = s.b + stage * PC::kTileB;
+                        const int c0 = PC::kCh * ks;
+                        const uint32_t bar = full0 + (uint32_t)stage * 8u;
+                        if (p.chunk_maps) {
+                            if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2u * (PC::kTileA + PC::kTileB));
+                            tma_load_3d_pair(a_dst, &tmA, bar, 0, a_row, c0, pol_a);
+                            tma_load_3d_pair(b_dst, &tmB, bar, 0, b_row, c0, pol);
+                        } else {
+                            const int nch = min(PC::kCh, row_chunks - c0);
+                            if (rank == 0)
+                                mbar_arrive_expect_tx(&s.full[stage], 2u * (uint32_t)nch * (kPRows * 128 + (kPN / 2) * 128));
+                            for (int c = 0; c < nch; ++c) {
+                                tma_load_2d_pair(a_dst + c * kPRows * 128, &tmA, bar, (c0 + c) * 128, a_row, pol_a);
+                                tma_load_2d_pair(b_dst + c * (kPN / 2) * 128, &tmB, bar, (c0 + c) * 128, b_row, pol);
+                            }
                         }
+                        if (++stage == PC::kStages) { stage = 0; phase ^= 1u; }
                     }
-                    if (++stage == PC::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            const uint32_t idesc = idesc_nvf4(2 * kPRows, kPN);
-            int stage = 0, sfs = 0;
-            uint32_t phase = 0, sfp = 0, acc_phase = 0;
-            for (int tile = pair_slot; tile < total; tile += pair_slots) {
-                if (!mbar_wait<true>(s.acc_empty, acc_phase ^ 1u, s.abort, p.status, kStatusTimeoutMma)) goto done;
-                tc_fence_after();
-                for (int ks = 0; ks < kstages; ++ks) {
-                    if (!mbar_wait<true>(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
-                    if (!mbar_wait<true>(&s.sf_ready[sfs], sfp, s.abort, p.status, kStatusTimeoutMma)) goto done;
+        } else if (warp == 1) {
+            if (lane == 0 && rank == 0) {
+                const uint32_t idesc = idesc_nvf4(2 * kPRows, kPN);
+                int stage = 0, sfs = 0;
+                uint32_t phase = 0, sfp = 0, acc_phase = 0;
+                for (int tile = pair_slot; tile < total; tile += pair_slots) {
+                    if (!mbar_wait<true>(s.acc_empty, acc_phase ^ 1u, s.abort, p.status, kStatusTimeoutMma)) goto done;
                     tc_fence_after();
-                    const int nkb = min(PC::kKb, kblocks - PC::kKb * ks);
-                    const uint32_t sfa_t = tmem_base + kPSfCol0 + (uint32_t)sfs * PC::kSfColsStage;
-                    const uint32_t sfb_t = sfa_t + PC::kSfColsA;
-                    const uint32_t a_s = smem_u32(s.a + stage * PC::kTileA);
-                    const uint32_t b_s = smem_u32(s.b + stage * PC::kTileB);
-                    for (int j = 0; j < nkb; ++j) {
-                        const int c = j >> 2, jj = j & 3;
-                        tc_mma_nvf4_pair(tmem_base, sdesc_kmajor_sw128(a_s + c * kPRows * 128) + 2u * jj,
-                                         sdesc_kmajor_sw128(b_s + c * (kPN / 2) * 128) + 2u * jj, idesc, sfa_t + 4 * j,
-                                         sfb_t + 8 * j, (ks | j) != 0);
+                    for (int ks = 0; ks < kstages; ++ks) {
+                        if (!mbar_wait<true>(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                        if (!mbar_wait<true>(&s.sf_ready[sfs], sfp, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                        tc_fence_after();
+                        const int nkb = min(PC::kKb, kblocks - PC::kKb * ks);
+                        const uint32_t sfa_t = tmem_base + kPSfCol0 + (uint32_t)sfs * PC::kSfColsStage;
+                        const uint32_t sfb_t = sfa_t + PC::kSfColsA;
+                        const uint32_t a_s = smem_u32(s.a + stage * PC::kTileA);
+                        const uint32_t b_s = smem_u32(s.b + stage * PC::kTileB);
+                        for (int j = 0; j < nkb; ++j) {
+                            const int c = j >> 2, jj = j & 3;
+                            tc_mma_nvf4_pair(tmem_base, sdesc_kmajor_sw128(a_s + c * kPRows * 128) + 2u * jj,
+                                             sdesc_kmajor_sw128(b_s + c * (kPN / 2) * 128) + 2u * jj, idesc, sfa_t + 4 * j,
+                                             sfb_t + 8 * j, (ks | j) != 0);
+                        }
+                        tc_commit_pair_mc(&s.empty[stage], 0x3);
+                        if (++stage == PC::kStages) { stage = 0; phase ^= 1u; }
+                        if (++sfs == PC::kSfStages) { sfs = 0; sfp ^= 1u; }
                     }
-                    tc_commit_pair_mc(&s.empty[stage], 0x3);
-                    if (++stage == PC::kStages) { stage = 0; phase ^= 1u; }
-                    if (++sfs == PC::kSfStages) { sfs = 0; sfp ^= 1u; }
+                    tc_commit_pair_mc(s.acc_full, 0x3);
+                    acc_phase ^= 1u;
                 }
-                tc_commit_pair_mc(s.acc_full, 0x3);
-                acc_phase ^= 1u;
             }
-        }
+        }  // warps 2-3: no role
     } else if (warp < kPEpiWarp0) {
+        regs_release<kPRegsSf>();
         // scale writer for lane quadrant warp % 4: the stage's A atoms into
         // columns 4j..4j+3 of its slot, the B atoms of MMA step j (row block
         // rb) into columns 8j + 4rb .. +3 of the B part
@@ -377,6 +361,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
         }
     } else {
+        regs_claim<kPRegsEpi>();
         const int q = warp & 3;                            // tensor-memory lane quadrant of this warp
         const int half = (warp - kPEpiWarp0) >> 2;         // accumulator columns 0..127 or 128..255
         const uint32_t release = cluster_map(s.acc_empty, 0);
@@ -397,9 +382,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
             const int vtile = n_tile * 2 + half;           // index of this 128-column slice
+            // copy the slice out and hand the accumulator back at once
+            float acc[128];
             if (m_tile >= 0) {
-                if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32) epilogue_fc1<EPI>(p, taddr, row, meta, vtile);
-                else epilogue_fc2<EPI, PC::kStgCols>(p, taddr, row, meta, vtile, stg);
+                float a0[32], a1[32], a2[32], a3[32];
+                tmem_ld32(taddr, a0);
+                tmem_ld32(taddr + 32, a1);
+                tmem_ld32(taddr + 64, a2);
+                tmem_ld32(taddr + 96, a3);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    acc[i] = a0[i];
+                    acc[32 + i] = a1[i];
+                    acc[64 + i] = a2[i];
+                    acc[96 + i] = a3[i];
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -408,6 +406,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 else mbar_arrive_cluster(release);
             }
             acc_phase ^= 1u;
+            if (m_tile >= 0) {
+                if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32) epilogue_fc1_held<EPI>(p, acc, row, meta, vtile);
+                else epilogue_fc2_held<EPI, PC::kStgCols>(p, acc, row, meta, vtile, stg);
+            }
         }
     }
 done:
@@ -420,7 +422,7 @@ done:
             tc_commit_pair(s.drain);
             mbar_wait(s.drain, 0, &no_abort, p.status, kStatusTimeoutMma);
         }
-        if (warp >= 2 && warp < kPEpiWarp0) tmem_st_wait();
+        if (warp >= kPSfWarp0 && warp < kPEpiWarp0) tmem_st_wait();
         for (int i = 0; i < 100; ++i) __nanosleep(10000);
     }
     tc_fence_before();
@@ -441,6 +443,12 @@ int g_pair_grid[64] = {};
 
 template <int EPI>
 cudaError_t set_pair_smem() {
+    // the register split assumes the launch's pool of 128 registers a
+    // thread; with fewer, the epilogue's increase would never be granted
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, gemm_nvf4_pair_kernel<EPI>);
+    if (e != cudaSuccess) return e;
+    if ((uint32_t)((fa.numRegs + 7) / 8 * 8) != kPRegsLaunch) return cudaErrorInvalidKernelImage;
     return cudaFuncSetAttribute(gemm_nvf4_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 PCfg<EPI>::kSmemBytes);
 }

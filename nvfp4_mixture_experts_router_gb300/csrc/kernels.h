@@ -150,6 +150,12 @@ cudaError_t setup_gemm_kernels();
 cudaError_t setup_gemm_w4a16_kernels();
 cudaError_t launch_gemm_w4a16(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmBq,
                               const GemmParams& p, int num_sms);
+// The same on CTA pairs (256 x 256 pair tiles over pairs of M tiles of one
+// expert, p.tile_pair / meta[2]); needs n % 256 == 0, the same 128-row maps.
+// setup sizes the persistent grid for `device`.
+cudaError_t setup_gemm_w4a16_pair_kernels(int device, int num_sms);
+cudaError_t launch_gemm_w4a16_pair(const LaunchCtx& c, int epilogue, const CUtensorMap& tmA,
+                                   const CUtensorMap& tmBq, const GemmParams& p, int device);
 // tile_n = gemm_nvf4_tile_n(kdim, n) (128 or 256); tmB's box must be tile_n rows high.
 // kind 0: NVFP4 operands (kind::mxf4nvf4); 1: MXFP8 operands (kind::mxf8f6f4).
 int gemm_nvf4_tile_n(int kdim, int n);

@@ -43,6 +43,7 @@ moe_status device_state(int* sms, int* device = nullptr) {
             d.status = MOE_ERR_UNSUPPORTED;  // the binary carries sm_103a code only
         } else if (setup_routing_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess ||
                    setup_gemm_w4a16_kernels() != cudaSuccess || setup_gemm_pair_kernels(dev, d.sms) != cudaSuccess ||
+                   setup_gemm_w4a16_pair_kernels(dev, d.sms) != cudaSuccess ||
                    setup_fused_layer_kernel() != cudaSuccess || setup_gemm_swap_kernels() != cudaSuccess ||
                    setup_router_gemm_kernel() != cudaSuccess) {
             d.status = MOE_ERR_CUDA;
@@ -191,6 +192,12 @@ bool use_pair_gemm(moe_shape s, uint32_t flags, int n) {
     const int64_t routes = (int64_t)s.T * s.K;
     const int64_t busy = routes < s.E ? routes : s.E;
     return routes >= kPairMinRoutesPerExpert * busy;
+}
+
+// W4A16 GEMMs on CTA pairs: only when forced (MOE_GEMM_PAIRS_ALWAYS) until
+// the pair kernel is measured faster than the single-CTA one.
+bool use_w4a16_pairs(moe_shape s, uint32_t flags, int n) {
+    return (flags & MOE_GEMM_PAIRS_ALWAYS) && use_pair_gemm(s, flags, n);
 }
 
 }  // namespace
@@ -523,7 +530,9 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         a.weight_on_input = on_input ? 1 : 0;
         a.out_cols = s.I;
         a.out_bf16 = h_bf16;
-        e = launch_gemm_w4a16(c, kEpiFc1Bf16, tA1, tB1, a, sms);
+        a.tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
+        e = use_w4a16_pairs(s, flags, N1) ? launch_gemm_w4a16_pair(c, kEpiFc1Bf16, tA1, tB1, a, device)
+                                        : launch_gemm_w4a16(c, kEpiFc1Bf16, tA1, tB1, a, sms);
         if (e != cudaSuccess || !mark(4) || !mark(5)) return MOE_ERR_CUDA;
         GemmParams b{};
         b.sfb = pw + P.w2_sf;
@@ -548,7 +557,9 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
             b.out_f32 = y_acc;
             epi2 = kEpiFc2Scatter;
         }
-        e = launch_gemm_w4a16(c, epi2, tA2, tB2, b, sms);
+        b.tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
+        e = use_w4a16_pairs(s, flags, s.H) ? launch_gemm_w4a16_pair(c, epi2, tA2, tB2, b, device)
+                                         : launch_gemm_w4a16(c, epi2, tA2, tB2, b, sms);
         if (e != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
         if (det)
             e = launch_finalize_deterministic(c, s.T, s.H, s.K, row_of_route, topk_w, on_input ? 0 : 1,

@@ -137,7 +137,7 @@ def test_wide_tile_parity(H, I, mode, act, on_input, det):
 PAIRS = []
 for T, H, I, E, K in [(1, 256, 128, 8, 2), (200, 256, 128, 8, 2), (300, 512, 256, 4, 2), (40, 256, 256, 16, 1),
                       (333, 4096, 512, 4, 3)]:
-    for mode in (synth.MODE_PER_TENSOR, synth.MODE_PER_TOKEN):
+    for mode in (synth.MODE_PER_TENSOR, synth.MODE_PER_TOKEN, synth.MODE_W4A16):
         for act in (0, 1):
             for det in (False, True):
                 PAIRS.append((T, H, I, E, K, mode, act, det))
@@ -146,7 +146,8 @@ for T, H, I, E, K in [(1, 256, 128, 8, 2), (200, 256, 128, 8, 2), (300, 512, 256
 @pytest.mark.parametrize("T,H,I,E,K,mode,act,det", PAIRS)
 def test_pair_gemm_parity(T, H, I, E, K, mode, act, det):
     """GEMMs forced onto CTA pairs (256 x 256 tiles over two M tiles of one
-    expert): experts with an odd number of M tiles (half-filled pairs),
+    expert; NVFP4 and W4A16 kernels): experts with an odd number of M tiles
+    (half-filled pairs),
     empty experts, one token, a reduction length of 4096, and ReLU2 shapes
     whose FC1 (I = 128 rows) stays on single CTAs while FC2 runs on pairs."""
     seed = (T * 17 + H + I * 3 + E * 5 + K + mode * 13 + act * 7 + det) % 1000
