@@ -91,8 +91,8 @@ typedef enum {
  * MMAs, 256 x 256 tiles over two 128-row M tiles of one expert) when the
  * experts holding routes hold at least 256 on average (T*K >= 256 *
  * min(E, T*K)), else on single CTAs; MOE_GEMM_PAIRS_ALWAYS /
- * MOE_GEMM_PAIRS_NEVER force pairs / single CTAs.  W4A16 GEMMs run on
- * pairs only with MOE_GEMM_PAIRS_ALWAYS.  Setting both is invalid. */
+ * MOE_GEMM_PAIRS_NEVER force pairs / single CTAs.  Setting both is
+ * invalid. */
 #define MOE_GEMM_PAIRS_NEVER (1u << 7)
 #define MOE_GEMM_PAIRS_ALWAYS (1u << 8)
 /* bit 9: 4-over-6 activation quantization (per-token W4A4 only) [PR #4366

@@ -184,7 +184,10 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 // vs pairs: prefill T = 16384 step 4.12 vs 3.68 ms, DSV3 shape T = 8192 FC1
 // 1094 vs 1025 us, 16 experts x 2048 routes FC1 442 vs 374 us; below that a
 // pair's second M tile is mostly padding).  MOE_GEMM_PAIRS_ALWAYS / _NEVER
-// force either.
+// force either.  The W4A16 GEMMs follow the same rule (measured on GB300 at
+// H = 4096, I = 1536, E = 128, top-8: T = 4096 (256 routes per expert) FC1
+// 650 -> 455 us and FC2 663 -> 486 us on pairs; T = 512 (32 per expert)
+// 275 -> 329 and 262 -> 330 us when forced, i.e. slower).
 constexpr int64_t kPairMinRoutesPerExpert = 256;
 bool use_pair_gemm(moe_shape s, uint32_t flags, int n) {
     if (n % 256 != 0 || (flags & MOE_GEMM_PAIRS_NEVER)) return false;
@@ -192,12 +195,6 @@ bool use_pair_gemm(moe_shape s, uint32_t flags, int n) {
     const int64_t routes = (int64_t)s.T * s.K;
     const int64_t busy = routes < s.E ? routes : s.E;
     return routes >= kPairMinRoutesPerExpert * busy;
-}
-
-// W4A16 GEMMs on CTA pairs: only when forced (MOE_GEMM_PAIRS_ALWAYS) until
-// the pair kernel is measured faster than the single-CTA one.
-bool use_w4a16_pairs(moe_shape s, uint32_t flags, int n) {
-    return (flags & MOE_GEMM_PAIRS_ALWAYS) && use_pair_gemm(s, flags, n);
 }
 
 }  // namespace
@@ -531,7 +528,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         a.out_cols = s.I;
         a.out_bf16 = h_bf16;
         a.tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
-        e = use_w4a16_pairs(s, flags, N1) ? launch_gemm_w4a16_pair(c, kEpiFc1Bf16, tA1, tB1, a, device)
+        e = use_pair_gemm(s, flags, N1) ? launch_gemm_w4a16_pair(c, kEpiFc1Bf16, tA1, tB1, a, device)
                                         : launch_gemm_w4a16(c, kEpiFc1Bf16, tA1, tB1, a, sms);
         if (e != cudaSuccess || !mark(4) || !mark(5)) return MOE_ERR_CUDA;
         GemmParams b{};
@@ -558,7 +555,7 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
             epi2 = kEpiFc2Scatter;
         }
         b.tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
-        e = use_w4a16_pairs(s, flags, s.H) ? launch_gemm_w4a16_pair(c, epi2, tA2, tB2, b, device)
+        e = use_pair_gemm(s, flags, s.H) ? launch_gemm_w4a16_pair(c, epi2, tA2, tB2, b, device)
                                          : launch_gemm_w4a16(c, epi2, tA2, tB2, b, sms);
         if (e != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
         if (det)
