@@ -323,20 +323,29 @@ __device__ __forceinline__ bool gemm_tiles(const Smem& s, uint32_t tmem_base, co
                     // the scale writers' stores for this stage are done
                     if (!mbar_wait(&s.sf_ready[stage], phase, s.abort, p.status, kStatusTimeoutMma)) return false;
                     tc_fence_after();
-                    const uint32_t a_s = smem_u32(s.a + stage * C::kTileBytesA);
-                    const uint32_t b_s = smem_u32(s.b + stage * C::kTileBytesB);
-                    for (int j = 0; j < nkb; ++j) {
-                        // chunk j / 4, then 32 bytes (64 E2M1 / 32 E4M3) along K
-                        // inside its swizzled 128-byte rows
+                    // chunk j / 4, then 32 bytes (64 E2M1 / 32 E4M3) along K inside
+                    // its swizzled 128-byte rows; descriptor start addresses
+                    // count 16-byte units
+                    const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(s.a + stage * C::kTileBytesA));
+                    const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(s.b + stage * C::kTileBytesB));
+                    auto issue = [&](int j) {
                         const int c = j >> 2, jj = j & 3;
-                        const uint64_t adesc = sdesc_kmajor_sw128(a_s + c * kChunkBytesA) + 2u * jj;
-                        const uint64_t bdesc = sdesc_kmajor_sw128(b_s + c * C::kChunkBytesB) + 2u * jj;
+                        const uint64_t adesc = adesc0 + (uint64_t)c * (kChunkBytesA / 16) + 2u * jj;
+                        const uint64_t bdesc = bdesc0 + (uint64_t)c * (C::kChunkBytesB / 16) + 2u * jj;
                         if (KIND == 0)
                             tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + C::kSfColsB * j,
                                         (ks | j) != 0);
                         else
                             tc_mma_mxf8(d_tmem, adesc, bdesc, idesc_mxf8(kBM, width, jj), sfa_t + 4 * c,
                                         sfb_t + C::kSfColsB * c, (ks | j) != 0);
+                    };
+                    if (nkb == kKbPerStage) {
+                        // a full stage, unrolled: constant offsets of the stage's
+                        // descriptors, a few instructions per MMA
+#pragma unroll
+                        for (int j = 0; j < kKbPerStage; ++j) issue(j);
+                    } else {
+                        for (int j = 0; j < nkb; ++j) issue(j);
                     }
                     tc_commit(&s.empty[stage]);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }

@@ -284,13 +284,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         const int nkb = min(PC::kKb, kblocks - PC::kKb * ks);
                         const uint32_t sfa_t = tmem_base + kPSfCol0 + (uint32_t)sfs * PC::kSfColsStage;
                         const uint32_t sfb_t = sfa_t + PC::kSfColsA;
-                        const uint32_t a_s = smem_u32(s.a + stage * PC::kTileA);
-                        const uint32_t b_s = smem_u32(s.b + stage * PC::kTileB);
-                        for (int j = 0; j < nkb; ++j) {
-                            const int c = j >> 2, jj = j & 3;
-                            tc_mma_nvf4_pair(tmem_base, sdesc_kmajor_sw128(a_s + c * kPRows * 128) + 2u * jj,
-                                             sdesc_kmajor_sw128(b_s + c * (kPN / 2) * 128) + 2u * jj, idesc, sfa_t + 4 * j,
-                                             sfb_t + 8 * j, (ks | j) != 0);
+                        const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(s.a + stage * PC::kTileA));
+                        const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(s.b + stage * PC::kTileB));
+                        // descriptor start addresses count 16-byte units: a chunk of
+                        // 128 rows x 128 bytes is 1024 of them, a 32-byte K step 2
+                        constexpr uint64_t kChunkA = kPRows * 128 / 16, kChunkB = (kPN / 2) * 128 / 16;
+                        if (nkb == PC::kKb) {
+                            // a full stage, unrolled: every operand of the eight MMAs
+                            // is a constant offset of the stage's descriptors, so the
+                            // issuing thread spends a few instructions per MMA
+    #pragma unroll
+                            for (int j = 0; j < PC::kKb; ++j)
+                                tc_mma_nvf4_pair(tmem_base, adesc + (uint64_t)(j >> 2) * kChunkA + 2u * (j & 3),
+                                                 bdesc + (uint64_t)(j >> 2) * kChunkB + 2u * (j & 3), idesc,
+                                                 sfa_t + 4 * j, sfb_t + 8 * j, (ks | j) != 0);
+                        } else {
+                            for (int j = 0; j < nkb; ++j)
+                                tc_mma_nvf4_pair(tmem_base, adesc + (uint64_t)(j >> 2) * kChunkA + 2u * (j & 3),
+                                                 bdesc + (uint64_t)(j >> 2) * kChunkB + 2u * (j & 3), idesc,
+                                                 sfa_t + 4 * j, sfb_t + 8 * j, (ks | j) != 0);
                         }
                         tc_commit_pair_mc(&s.empty[stage], 0x3);
                         if (++stage == PC::kStages) { stage = 0; phase ^= 1u; }

@@ -257,16 +257,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     tc_fence_after();
                     const int nkb = min(4, kblocks - 4 * ks);
                     const uint32_t sf_t = tmem_base + kSfColBase + (uint32_t)stage * kSfColsPerStage;
-                    const uint32_t w_s = smem_u32(s.w + stage * kSlotW);
-                    const uint32_t x_s = smem_u32(s.x + stage * kXBytes);
-                    for (int j = 0; j < nkb; ++j) {
-                        const uint64_t bdesc = sdesc_kmajor_sw128(x_s) + 2u * j;
+                    // descriptor start addresses count 16-byte units
+                    const uint64_t wdesc0 = sdesc_kmajor_sw128(smem_u32(s.w + stage * kSlotW));
+                    const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(s.x + stage * kXBytes));
+                    auto issue = [&](int j) {
 #pragma unroll
-                        for (int o = 0; o < kOps; ++o) {
-                            const uint64_t adesc = sdesc_kmajor_sw128(w_s + o * kWBytes) + 2u * j;
-                            tc_mma_nvf4(d_tmem + o * kNR, adesc, bdesc, idesc, sf_t + 16 * o + 4 * j, sf_t + 32 + 4 * j,
-                                        (ks | j) != 0);
-                        }
+                        for (int o = 0; o < kOps; ++o)
+                            tc_mma_nvf4(d_tmem + o * kNR, wdesc0 + (uint64_t)o * (kWBytes / 16) + 2u * j, bdesc0 + 2u * j,
+                                        idesc, sf_t + 16 * o + 4 * j, sf_t + 32 + 4 * j, (ks | j) != 0);
+                    };
+                    if (nkb == 4) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) issue(j);   // a full stage: constant descriptor offsets
+                    } else {
+                        for (int j = 0; j < nkb; ++j) issue(j);
                     }
                     tc_commit(&s.empty[stage]);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
