@@ -92,8 +92,12 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     return s;
 }
 
-// 8 E2M1 codes (4 bytes, low nibble first) times scale s -> 8 BF16.
-__device__ __forceinline__ uint4 dequant8(uint32_t codes, float s) {
+// 8 E2M1 codes (4 bytes, low nibble first) times scale s -> 8 BF16, given
+// s2 = s in both halves of an f16x2 (exact: E4M3 values are normal f16).
+// Each code pair is widened to f16x2 and multiplied by s2 in f16 -- exact,
+// the product has at most 6 significant bits and lies in [2^-10, 2688] --
+// then widened to FP32 and packed to BF16 (exact again).
+__device__ __forceinline__ uint4 dequant8(uint32_t codes, __half2 s2) {
     uint32_t h2[4];
     asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
         " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
@@ -103,9 +107,9 @@ __device__ __forceinline__ uint4 dequant8(uint32_t codes, float s) {
     uint32_t out[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const __half2 hv = *reinterpret_cast<const __half2*>(&h2[i]);
-        const float2 f = __half22float2(hv);
-        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);   // exact
+        const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&h2[i]), s2);   // exact
+        const float2 f = __half22float2(p);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);                    // exact
         out[i] = *reinterpret_cast<const uint32_t*>(&b);
     }
     return make_uint4(out[0], out[1], out[2], out[3]);
@@ -230,7 +234,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 uint8_t* brow = s.b + stage * kTileBytesB + r * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {          // 16-byte chunk c = elements 8c .. 8c+7
-                    const float sc = e4m3_to_f32((sfw >> (8 * (c >> 1))) & 0xFFu);
+                    const __half2 sc = __float2half2_rn(e4m3_to_f32((sfw >> (8 * (c >> 1))) & 0xFFu));
                     *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = dequant8(words[c], sc);
                 }
                 fence_proxy_async_smem();
@@ -500,7 +504,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {          // 16-byte chunk c = elements 8c .. 8c+7
                     const int c = 4 * hk + j;
-                    const float sc = e4m3_to_f32((sfw >> (8 * (c >> 1))) & 0xFFu);
+                    const __half2 sc = __float2half2_rn(e4m3_to_f32((sfw >> (8 * (c >> 1))) & 0xFFu));
                     *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = dequant8(words[j], sc);
                 }
                 fence_proxy_async_smem();

@@ -186,7 +186,8 @@ def config(idx: int, T: Optional[int] = None) -> MoEConfig:
                       act=ACT_RELU2, mode=MODE_W4A16, seed=3, logits="normal")
     elif idx == 4:
         c = MoEConfig("prefill_w4a4_T16384_H7168_I2048_E256_K8", 16384, 7168, 2048,
-                      256, 8, mode=MODE_PER_TOKEN, seed=4, logits="normal", bias="zipf")
+                      256, 8, mode=MODE_PER_TOKEN, deterministic=True, seed=4, logits="normal",
+                      bias="zipf")
     else:
         raise ValueError(idx)
     if T is not None:

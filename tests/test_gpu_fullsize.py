@@ -45,13 +45,14 @@ def test_w4a16_T4096():
     fullsize_parity(synth.config(3, 4096), n_tokens=24)
 
 
-def test_prefill_T16384_zipf():
+@pytest.mark.parametrize("finalize", ["deterministic", "fused"])
+def test_prefill_T16384_zipf(finalize):
     """Prefill scale: T=16384, H=7168, I=2048, E=256, top-8, per-token
     scales, Zipf-skewed expert popularity (one expert takes most tokens,
-    others none)."""
+    others none); both finalize modes (the workload's is deterministic)."""
     import numpy as np
     import oracle
-    c = synth.config(4)
+    c = synth.config(4).with_(deterministic=finalize == "deterministic")
     ids, _ = oracle.router(synth.gen_logits(c).numpy(), synth.gen_bias(c).numpy(), c.K)
     count = np.bincount(ids.reshape(-1), minlength=c.E)
     assert count.max() >= 10 * count.mean() and (count == 0).any()
@@ -74,8 +75,9 @@ def test_dsv3_shape_single_kernel(T):
 
 
 def test_prefill_T16384_single_kernel():
-    """The prefill workload (per-token scales, Zipf skew, fused finalize)
-    through the single persistent kernel: the same kernel at 16384 tokens."""
+    """The prefill workload (per-token scales, Zipf skew, deterministic
+    finalize) through the single persistent kernel: the same kernel at
+    16384 tokens."""
     r = fullsize_parity(synth.config(4).with_(fused=True), n_tokens=16)
     assert r["code_match"] >= 0.999
 
