@@ -126,12 +126,33 @@ __device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr
     }
 }
 
+template <int COLS, int NW, class Op>
+__device__ __forceinline__ void staged_rows(uint32_t* stg, const uint32_t (&w)[NW], Op op);
+
 // The same epilogue on a slice the caller has already copied out of tensor
 // memory (acc[c] = accumulator column c of the thread's row), so that the
-// accumulator can be handed back to the MMA before this work starts.
-template <int EPI>
+// accumulator can be handed back to the MMA before this work starts.  COLS >
+// 0 (FP32 output only): the rows go out through the warp's staging block stg
+// (see staged_rows), every lane taking part; rows without a route write
+// nothing.
+template <int EPI, int COLS = 0>
 __device__ __forceinline__ void epilogue_fc1_held(const GemmParams& p, const float (&acc)[128], int row,
-                                                  const EpiRow& m, int n_tile) {
+                                                  const EpiRow& m, int n_tile, uint32_t* stg = nullptr) {
+    auto emit = [&](const float (&h)[32], int col0) {
+        if constexpr (COLS > 0 && EPI == kEpiFc1F32) {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(h[i]);
+            const int row0 = row - (threadIdx.x & 31);
+            const int route = m.route;
+            staged_rows<COLS>(stg, w, [&](int r, int w0, uint4 v) {
+                if (__shfl_sync(0xffffffffu, route, r) >= 0)
+                    *reinterpret_cast<uint4*>(p.out_f32 + (size_t)(row0 + r) * p.out_cols + col0 + w0) = v;
+            });
+        } else {
+            if (m.route >= 0) fc1_emit32<EPI>(p, h, row, col0, m.g2);
+        }
+    };
     if (p.act == MOE_ACT_SWIGLU) {
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
@@ -142,7 +163,7 @@ __device__ __forceinline__ void epilogue_fc1_held(const GemmParams& p, const flo
                 u[i] = acc[64 + ch * 32 + i];
             }
             fc1_act32(h, u, true, m.alpha, m.pw);
-            if (m.route >= 0) fc1_emit32<EPI>(p, h, row, n_tile * 64 + ch * 32, m.g2);
+            emit(h, n_tile * 64 + ch * 32);
         }
     } else {
 #pragma unroll
@@ -151,7 +172,7 @@ __device__ __forceinline__ void epilogue_fc1_held(const GemmParams& p, const flo
 #pragma unroll
             for (int i = 0; i < 32; ++i) h[i] = acc[ch * 32 + i];
             fc1_act32(h, h, false, m.alpha, m.pw);
-            if (m.route >= 0) fc1_emit32<EPI>(p, h, row, n_tile * 128 + ch * 32, m.g2);
+            emit(h, n_tile * 128 + ch * 32);
         }
     }
 }

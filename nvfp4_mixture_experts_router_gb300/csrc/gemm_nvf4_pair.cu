@@ -97,7 +97,9 @@ struct PCfg {
     static constexpr int kSfB = 2 * kKb * 512;               // all 256 B rows' scale atoms
     static constexpr int kSfStages = 2;
     static constexpr int kStages = kFc2 ? 2 : 3;             // operand stages
-    static constexpr int kStgCols = kFc2 ? 16 : 0;           // FC2 epilogue staging, words per row
+    // epilogue staging, words per row: FC2 16; the FC1 FP32 store 8 (what
+    // fits beside its three stages); the FC1 requantization none
+    static constexpr int kStgCols = kFc2 ? 16 : (EPI == kEpiFc1F32 ? 8 : 0);
     static constexpr int kStgBytes = kPEpiWarps * 32 * kStgCols * 4;
     static constexpr uint32_t kSfColsA = 4 * kKb;
     static constexpr uint32_t kSfColsB = 8 * kKb;
@@ -419,7 +421,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             acc_phase ^= 1u;
             if (m_tile >= 0) {
-                if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32) epilogue_fc1_held<EPI>(p, acc, row, meta, vtile);
+                if (EPI == kEpiFc1Quant || EPI == kEpiFc1F32)
+                    epilogue_fc1_held<EPI, PC::kStgCols>(p, acc, row, meta, vtile, stg);
                 else epilogue_fc2_held<EPI, PC::kStgCols>(p, acc, row, meta, vtile, stg);
             }
         }
