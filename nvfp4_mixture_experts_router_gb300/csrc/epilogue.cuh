@@ -111,9 +111,15 @@ __device__ __forceinline__ void fc1_emit32(const GemmParams& p, const float (&h)
 // SwiGLU tile: columns 0..63 gate, 64..127 up (prepared-weight interleave);
 // yields 64 FC2-input values.  ReLU2 tile: 128 values.  Reads the
 // accumulator chunk by chunk from tensor memory.
-template <int EPI>
+// COLS > 0 (BF16 output only): the BF16 rows go out through the warp's
+// staging block stg in whole sectors (see staged_rows), every lane taking
+// part; rows without a route write nothing.
+template <int COLS, int NW, class Op>
+__device__ __forceinline__ void staged_rows(uint32_t* stg, const uint32_t (&w)[NW], Op op);
+
+template <int EPI, int COLS = 0>
 __device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr, int row, const EpiRow& m,
-                                             int n_tile) {
+                                             int n_tile, uint32_t* stg = nullptr) {
     const bool swiglu = p.act == MOE_ACT_SWIGLU;
     const int chunks = swiglu ? 2 : 4;
     for (int ch = 0; ch < chunks; ++ch) {
@@ -122,12 +128,25 @@ __device__ __forceinline__ void epilogue_fc1(const GemmParams& p, uint32_t taddr
         if (swiglu) tmem_ld32(taddr + 64 + ch * 32, u);
         tmem_ld_wait();
         fc1_act32(h, u, swiglu, m.alpha, m.pw);
-        if (m.route >= 0) fc1_emit32<EPI>(p, h, row, (swiglu ? n_tile * 64 : n_tile * 128) + ch * 32, m.g2);
+        const int col0 = (swiglu ? n_tile * 64 : n_tile * 128) + ch * 32;
+        if constexpr (COLS > 0 && EPI == kEpiFc1Bf16) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 b = __floats2bfloat162_rn(h[2 * i], h[2 * i + 1]);
+                w[i] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            const int row0 = row - (threadIdx.x & 31);
+            const int route = m.route;
+            staged_rows<COLS>(stg, w, [&](int r, int w0, uint4 v) {
+                if (__shfl_sync(0xffffffffu, route, r) >= 0)
+                    *reinterpret_cast<uint4*>(p.out_bf16 + (size_t)(row0 + r) * p.out_cols + col0 + 2 * w0) = v;
+            });
+        } else {
+            if (m.route >= 0) fc1_emit32<EPI>(p, h, row, col0, m.g2);
+        }
     }
 }
-
-template <int COLS, int NW, class Op>
-__device__ __forceinline__ void staged_rows(uint32_t* stg, const uint32_t (&w)[NW], Op op);
 
 // The same epilogue on a slice the caller has already copied out of tensor
 // memory (acc[c] = accumulator column c of the thread's row), so that the

@@ -98,7 +98,8 @@ struct PCfg {
     static constexpr int kSfStages = 2;
     static constexpr int kStages = kFc2 ? 2 : 3;             // operand stages
     // epilogue staging, words per row: FC2 16; the FC1 FP32 store 8 (what
-    // fits beside its three stages); the FC1 requantization none
+    // fits beside its three stages); the FC1 requantization none (staging
+    // its 16-byte code rows was measured slower)
     static constexpr int kStgCols = kFc2 ? 16 : (EPI == kEpiFc1F32 ? 8 : 0);
     static constexpr int kStgBytes = kPEpiWarps * 32 * kStgCols * 4;
     static constexpr uint32_t kSfColsA = 4 * kKb;

@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kAccCols;
-            if (EPI == kEpiFc1Bf16) epilogue_fc1<EPI>(p, taddr, row, meta, n_tile);
+            if (EPI == kEpiFc1Bf16)
+                epilogue_fc1<EPI, kStgCols>(p, taddr, row, meta, n_tile, s.stg + q * 32 * kStgCols);
             else epilogue_fc2<EPI, kStgCols>(p, taddr, row, meta, n_tile, s.stg + q * 32 * kStgCols);
             tc_fence_before();
             mbar_arrive(&s.acc_empty[acc]);
@@ -539,7 +540,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kQN + (uint32_t)(half * 128);
             const int vtile = n_tile * 2 + half;              // index of this 128-column slice
             if (m_tile >= 0) {
-                if (EPI == kEpiFc1Bf16) epilogue_fc1<EPI>(p, taddr, row, meta, vtile);
+                if (EPI == kEpiFc1Bf16) epilogue_fc1<EPI, kStgCols>(p, taddr, row, meta, vtile, stg);
                 else epilogue_fc2<EPI, kStgCols>(p, taddr, row, meta, vtile, stg);
             }
             tc_fence_before();
