@@ -44,8 +44,9 @@
 // have read a slot and the MMAs two stages back have finished.
 //
 // Roles per CTA (512 threads, four warpgroups): warpgroup 0 = warp 0
-// producer, warp 1 tensor-memory allocation (both CTAs together) and, in
-// rank 0, the MMA issuer, warps 2-3 idle; warpgroup 1 = the four scale
+// producer of the operand copies, warp 1 tensor-memory allocation (both
+// CTAs together) and, in rank 0, the MMA issuer, warp 2 producer of the
+// scale-atom copies, warp 3 idle; warpgroup 1 = the four scale
 // writers; warpgroups 2-3 = the epilogue over this CTA's 128 rows (two groups
 // of four warps, 128 accumulator columns each).  The launch gives every
 // thread 128 registers; warpgroups 0 and 1 hand theirs down to 48 and 80 so
@@ -209,8 +210,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     if (warp < kPSfWarp0) {
         regs_release<kPRegsCtl>();
-        if (warp == 0) {
+        if (warp == 0 || warp == 2) {
+            // warp 0: operand copies; warp 2: scale-atom copies, on their own
+            // ring, so that neither waits behind the other's free slots
             if (lane == 0) {
+                const bool sf_role = warp == 2;
                 const uint64_t pol = policy_evict_normal();
                 // slabs: the activation rows are re-read once per slab; evict them
                 // first so that the slab of the accumulator stays in L2
@@ -233,19 +237,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const uint8_t* sfa_src = p.sfa + (size_t)ld_m * kblocks * 512;
                     const uint8_t* sfb_src = p.sfb + ((size_t)e * rb_per_expert + (size_t)n_tile * 2) * kblocks * 512;
                     for (int ks = 0; ks < kstages; ++ks) {
-                        const int nkb = min(PC::kKb, kblocks - PC::kKb * ks);
-                        const uint32_t sf_bytes = (uint32_t)nkb * 512u;
-                        // this CTA's scale atoms (its own A rows, all 256 B rows)
-                        // into the scale ring once the writers have read that slot
-                        if (!mbar_wait(&s.sf_free[sfs], sfp ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
-                        mbar_arrive_expect_tx(&s.sf_full[sfs], 3u * sf_bytes);
-                        bulk_load(s.sfa + sfs * PC::kSfA, sfa_src + (size_t)ks * PC::kKb * 512, sf_bytes,
-                                  &s.sf_full[sfs], pol);
-                        for (int rb = 0; rb < 2; ++rb)
-                            bulk_load(s.sfb + sfs * PC::kSfB + rb * PC::kSfA,
-                                      sfb_src + ((size_t)rb * kblocks + (size_t)ks * PC::kKb) * 512, sf_bytes,
+                        if (sf_role) {
+                            const int nkb = min(PC::kKb, kblocks - PC::kKb * ks);
+                            const uint32_t sf_bytes = (uint32_t)nkb * 512u;
+                            // this CTA's scale atoms (its own A rows, all 256 B
+                            // rows) into the scale ring once the writers have
+                            // read that slot
+                            if (!mbar_wait(&s.sf_free[sfs], sfp ^ 1u, s.abort, p.status, kStatusTimeoutProducer))
+                                goto done;
+                            mbar_arrive_expect_tx(&s.sf_full[sfs], 3u * sf_bytes);
+                            bulk_load(s.sfa + sfs * PC::kSfA, sfa_src + (size_t)ks * PC::kKb * 512, sf_bytes,
                                       &s.sf_full[sfs], pol);
-                        if (++sfs == PC::kSfStages) { sfs = 0; sfp ^= 1u; }
+                            for (int rb = 0; rb < 2; ++rb)
+                                bulk_load(s.sfb + sfs * PC::kSfB + rb * PC::kSfA,
+                                          sfb_src + ((size_t)rb * kblocks + (size_t)ks * PC::kKb) * 512, sf_bytes,
+                                          &s.sf_full[sfs], pol);
+                            if (++sfs == PC::kSfStages) { sfs = 0; sfp ^= 1u; }
+                            continue;
+                        }
                         // completed by rank 0's commit: acquire at cluster scope
                         if (!mbar_wait<true>(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer))
                             goto done;
@@ -315,7 +324,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     acc_phase ^= 1u;
                 }
             }
-        }  // warps 2-3: no role
+        }  // warp 3: no role
     } else if (warp < kPEpiWarp0) {
         regs_release<kPRegsSf>();
         // scale writer for lane quadrant warp % 4: the stage's A atoms into
