@@ -88,17 +88,15 @@ __device__ __forceinline__ int route_token_scan(int t, int E, int K, const float
     return lane < K ? my_e : -1;
 }
 
-// Route one token (the calling warp): writes ids / weights (lanes < K) and
-// returns this lane's selected expert (slot = lane) or -1 for lane >= K.
-// Expert e lives in lane e % 32, register e / 32.  K rounds: the warp's
-// largest key (one 64-bit max reduction) is the next expert; the lane that
-// held it drops it and recomputes its own largest.  The weights' softmax
-// denominator adds the selected experts' terms in selection order.
+// Selection by keys (up to 256 experts): expert e lives in lane e % 32,
+// register e / 32.  K rounds: the warp's largest key (one 64-bit max
+// reduction) is the next expert; the lane that held it drops it and
+// recomputes its own largest.  The weights' softmax denominator adds the
+// selected experts' terms in selection order.
 template <int EPL>
-__device__ __forceinline__ int route_token(int t, int E, int K, const float* __restrict__ logits,
-                                           const float* __restrict__ bias, int renorm, int* __restrict__ topk_ids,
-                                           float* __restrict__ topk_w) {
-    if constexpr (EPL > 8) return route_token_scan<EPL>(t, E, K, logits, bias, renorm, topk_ids, topk_w);
+__device__ __forceinline__ int route_token_keys(int t, int E, int K, const float* __restrict__ logits,
+                                                const float* __restrict__ bias, int renorm,
+                                                int* __restrict__ topk_ids, float* __restrict__ topk_w) {
     const int lane = threadIdx.x & 31;
     float l[EPL];
     uint64_t key[EPL];
@@ -162,5 +160,17 @@ __device__ __forceinline__ int route_token(int t, int E, int K, const float* __r
     return lane < K ? my_e : -1;
 }
 
+
+// Route one token (the calling warp): writes ids / weights (lanes < K) and
+// returns this lane's selected expert (slot = lane) or -1 for lane >= K.
+template <int EPL>
+__device__ __forceinline__ int route_token(int t, int E, int K, const float* __restrict__ logits,
+                                           const float* __restrict__ bias, int renorm, int* __restrict__ topk_ids,
+                                           float* __restrict__ topk_w) {
+    if constexpr (EPL > 8)
+        return route_token_scan<EPL>(t, E, K, logits, bias, renorm, topk_ids, topk_w);
+    else
+        return route_token_keys<EPL>(t, E, K, logits, bias, renorm, topk_ids, topk_w);
+}
 
 }  // namespace moe
