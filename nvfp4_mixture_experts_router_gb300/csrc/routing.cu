@@ -271,6 +271,10 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
     // would chain E/32 dependent round trips per warp, twice.
     constexpr int kSmallU = 16;
     const bool small = U <= kSmallU;
+    // rows of a whole number of int4 (every row 16-byte aligned: the region
+    // is): each lane takes four consecutive units per access, a quarter of
+    // the instructions of a unit a lane
+    const bool vec = (U & 3) == 0;
     int ucnt[kSmallU];
     if (small) {
         if (tid < E) {
@@ -285,7 +289,16 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
     } else {
         for (int e = warp; e < E; e += 32) {
             int s = 0;
-            for (int u = lane; u < U; u += 32) s += unit_base[(size_t)e * U + u];
+            if (vec) {
+                const int4* row4 = reinterpret_cast<const int4*>(unit_base + (size_t)e * U);
+#pragma unroll 4
+                for (int i = lane; i < U / 4; i += 32) {
+                    const int4 v = row4[i];
+                    s += v.x + v.y + v.z + v.w;
+                }
+            } else {
+                for (int u = lane; u < U; u += 32) s += unit_base[(size_t)e * U + u];
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
             if (lane == 0) s_cnt[e] = s;
@@ -302,7 +315,27 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int* _
             run += ucnt[u];
         }
     }
-    for (int e = warp; !small && e < E; e += 32) {
+    for (int e = warp; !small && vec && e < E; e += 32) {
+        int carry = s_pad[e];
+        int4* row4 = reinterpret_cast<int4*>(unit_base + (size_t)e * U);
+        const int n4 = U / 4;
+#pragma unroll 2
+        for (int i0 = 0; i0 < n4; i0 += 32) {
+            const int i = i0 + lane;
+            const int4 v = i < n4 ? row4[i] : make_int4(0, 0, 0, 0);
+            const int sum = v.x + v.y + v.z + v.w;
+            int incl = sum;
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                const int a = __shfl_up_sync(0xffffffffu, incl, o2);
+                if (lane >= o2) incl += a;
+            }
+            const int b = carry + incl - sum;
+            if (i < n4) row4[i] = make_int4(b, b + v.x, b + v.x + v.y, b + v.x + v.y + v.z);
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    for (int e = warp; !small && !vec && e < E; e += 32) {
         int carry = s_pad[e];
         for (int u0 = 0; u0 < U; u0 += 32) {
             const int u = u0 + lane;

@@ -402,3 +402,14 @@ def test_small_T_router_and_scan(T, E, K, bias, renorm):
     full_parity(c)
     s = api.shape(T, 256, 128, E, K)
     assert api.moe_nvfp4_forward_launches(s, c.flags()) == (6 if T <= 32 else 7)
+
+
+@pytest.mark.parametrize("T,E,K", [(545, 16, 4), (640, 40, 3), (1000, 9, 2)])
+def test_scan_unit_layouts(T, E, K):
+    """More than 16 units of 32 tokens, so the scan reads the unit counts
+    from memory: four units a lane access where an expert's row is a whole
+    number of int4 (T = 640: 20 units; T = 1000: 32 units, the last one
+    partial), one unit a lane otherwise (T = 545: 18 units)."""
+    c = synth.MoEConfig("units", T, 256, 128, E, K, mode=synth.MODE_PER_TOKEN, seed=T + E, logits="normal",
+                        bias="normal")
+    full_parity(c)
