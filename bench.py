@@ -11,11 +11,12 @@ quantization, FC1 + activation + requantization, FC2, finalize) over one
 batch of T synthetic tokens.  Default workload: the prefill-scale
 configuration, the largest that runs on one GPU (T=16384, H=7168, I=2048,
 E=256, top-8, SwiGLU, W4A4 per-token scales, Zipf-skewed expert
-popularity, fused finalize).  With --sweep dsv3 (the default at N=1) the
+popularity, deterministic finalize).  With --sweep dsv3 (the default at N=1) the
 line also carries the DeepSeek-V3-like expert shape (H=7168, I=2048, E=256,
 top-8, per-tensor, deterministic finalize) at T in {1, 8, 64, 256, 1024,
 4096, 8192}: device-timed tokens/s, TFLOP/s and % of the dense FP4 peak
-per token count.
+per token count (cold-L2 median with p10 / p90, the warm-L2 median, and up
+to 256 tokens a CUDA-graph replay).
 
 Prints one JSON line (rank 0).  `value` is whole-job tokens/s with inputs
 resident in HBM; L2 is defeated by rotating several copies of the prepared
@@ -23,8 +24,11 @@ weights (together larger than the 129 MB L2) across steps.  `e2e` is the same
 metric through the C ABI with each step's x and logits copied from pinned
 host memory and y copied back inside the timed region.  `roofline` is the
 dominant kernel's algorithmic bytes (or FLOPs) per launch over its mean
-CUDA-event duration.  Multi-GPU: independent replicas (one per rank, no
-collective on the data path), weak scaling.
+CUDA-event duration.  `per_forward` times single forwards of the workload
+(median, p10, p90) with L2 evicted before each and with L2 warm, and up to
+256 tokens as one CUDA-graph replay.  `cpu_baseline` carries the oracle on
+all host threads and on one.  Multi-GPU: independent replicas (one per
+rank, no collective on the data path), weak scaling.
 
 --impl reference times the CPU oracle (oracle/, plain C++ FP64) on the host
 cores on a bounded token sample of the same workload per step.
@@ -381,9 +385,21 @@ def cpu_baseline(c, device, budget_s=15.0):
     t0 = time.perf_counter()
     r.run(toks)
     dt = time.perf_counter() - t0
-    return {"value": round(len(toks) / dt, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{len(toks)} of the workload's {c.T} tokens (seeded subset), all their routes; "
-                      f"expert weights prepared by the oracle beforehand (untimed)"}
+    out = {"value": round(len(toks) / dt, 3), "unit": "tokens/s", "cores": r.oracle.max_threads(), "kind": "oracle",
+           "sample": f"{len(toks)} of the workload's {c.T} tokens (seeded subset), all their routes; "
+                     f"expert weights prepared by the oracle beforehand (untimed)"}
+    # the same oracle on one host thread, over a third of the time budget
+    n1 = max(1, min(len(toks), int(budget_s / 3 / max(dt * r.oracle.max_threads() / len(toks), 1e-6))))
+    try:
+        r.oracle.set_threads(1)
+        t0 = time.perf_counter()
+        r.run(toks[:n1])
+        dt1 = time.perf_counter() - t0
+    finally:
+        r.oracle.set_threads(0)
+    out["single_thread"] = {"value": round(n1 / dt1, 3), "unit": "tokens/s", "cores": 1,
+                            "sample": f"the first {n1} tokens of the same sample"}
+    return out
 
 
 def run_reference(args, c, world, rank):
@@ -416,7 +432,8 @@ def run_reference(args, c, world, rank):
            "ms_per_step": round(1000 * dt / args.steps, 4), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64 (oracle, NVFP4 emulated)", "data": "synthetic",
            "config": {"workload": describe(c), "tokens_per_step": n},
-           "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+           "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": r.oracle.max_threads(),
+                            "kind": "oracle",
                             "sample": f"{n} token(s) of the workload per step, weights prepared untimed"},
            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -445,10 +462,42 @@ def per_tensor_scales(api, c, flags, prepared, x, logits, bias, dev):
     return g1, g2
 
 
+def forward_times(fn, n, flush=None, graph=False):
+    """CUDA-event times of n forwards, each timed alone: median, p10, p90 (ms).
+    flush: a buffer larger than L2, written before every forward outside its
+    events (cold L2).  graph: the forward is captured once into a CUDA graph
+    and each timed call is one replay (launch overhead of one graph)."""
+    import torch
+    call = fn
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+            fn()
+        torch.cuda.synchronize()
+        call = g.replay
+        for _ in range(3):
+            call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        if flush is not None:
+            flush.fill_(1)
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    t = sorted(a.elapsed_time(b) for a, b in evs)
+    q = lambda f: round(t[min(n - 1, int(round(f * (n - 1))))], 5)
+    return {"median_ms": q(0.5), "p10_ms": q(0.1), "p90_ms": q(0.9), "n": n}
+
+
 def dsv3_sweep(dev, steps, warmup, fp4_peak):
     """The DSV3-like expert shape over its token counts, one prepared weight
     set (6.3 GB) for all of them.  Every timed forward follows a 256 MB write
-    that evicts L2 and is timed alone with CUDA events; the median is kept."""
+    that evicts L2 and is timed alone with CUDA events; the median is kept
+    (p10 / p90 beside it), with the warm-L2 median (the same forward back to
+    back) and, up to 256 tokens, the median of a CUDA-graph replay."""
     import torch
     from nvfp4_mixture_experts_router_gb300 import api, synth
     c0 = synth.config(2)
@@ -476,21 +525,24 @@ def dsv3_sweep(dev, steps, warmup, fp4_peak):
         if api.moe_nvfp4_last_device_status(ws) != api.MOE_OK:
             raise RuntimeError(f"device status not OK in the DSV3 sweep at T={T}")
         n = max(5, min(steps, 50))
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-        for a, b in evs:
-            flush.fill_(1)
-            a.record()
-            api.moe_nvfp4_forward(s, flags, x, logits, None, g1, g2, prep, ws, y)
-            b.record()
-        torch.cuda.synchronize()
-        ms = sorted(a.elapsed_time(b) for a, b in evs)[n // 2]
+        fwd = lambda: api.moe_nvfp4_forward(s, flags, x, logits, None, g1, g2, prep, ws, y)
+        cold = forward_times(fwd, n, flush)
+        warm = forward_times(fwd, n)
+        ms = cold["median_ms"]
         tflops = flops_per_step(c) / (ms / 1000.0) / 1e12
-        points.append({"T": T, "ms": round(ms, 5), "tokens_per_s": round(T / (ms / 1000.0), 1),
-                       "tflops": round(tflops, 2), "pct_fp4_peak": round(100 * tflops / fp4_peak, 3),
-                       "timed_steps": n})
+        pt = {"T": T, "ms": ms, "tokens_per_s": round(T / (ms / 1000.0), 1),
+              "tflops": round(tflops, 2), "pct_fp4_peak": round(100 * tflops / fp4_peak, 3),
+              "timed_steps": n, "p10_ms": cold["p10_ms"], "p90_ms": cold["p90_ms"], "warm_ms": warm["median_ms"]}
+        if T <= 256:
+            try:
+                pt["graph_ms"] = forward_times(fwd, n, flush, graph=True)["median_ms"]
+            except Exception as exc:
+                pt["graph_ms"] = f"capture failed: {type(exc).__name__}"
+        points.append(pt)
         del ws, y, x, logits
     return {"workload": describe(c0).split(":", 1)[1].replace(" T=4096,", "").strip(),
-            "l2": "256 MB write before every timed forward (evicts L2); median of per-forward CUDA-event times",
+            "l2": "256 MB write before every timed forward (evicts L2); median (p10, p90) of per-forward "
+                  "CUDA-event times; warm_ms: the same forward back to back; graph_ms: one CUDA-graph replay",
             "points": points}
 
 
@@ -622,6 +674,24 @@ def run_ours(args, c, world, rank, local):
         nv = 0.5625
         sbytes = {"fused_layer": sbytes["router"] + c.T * c.H * 2 + active * (c.N1 * c.H + c.H * c.I) * nv +
                   c.T * c.H * 2}
+
+    # each forward timed alone: cold L2 (a write larger than L2 before
+    # every forward), warm L2 (the same inputs and weights back to back),
+    # and up to 256 tokens the forward as one CUDA-graph replay
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    nd = max(5, min(args.steps, 50))
+    per_forward = {"cold": forward_times(lambda: step(0), nd, flush), "warm": forward_times(lambda: step(0), nd),
+                   "l2": "cold: a 256 MB write before every forward, outside its events; warm: the same "
+                         "inputs and prepared weights back to back"}
+    if c.T <= 256:
+        try:
+            per_forward["graph_cold"] = forward_times(lambda: step(0), nd, flush, graph=True)
+        except Exception as exc:
+            per_forward["graph_cold"] = f"capture failed: {type(exc).__name__}"
+    del flush
+    torch.cuda.synchronize()
+    if api.moe_nvfp4_last_device_status(ws) != api.MOE_OK:
+        raise RuntimeError("device status not OK after the per-forward timings")
 
     # end to end through the C ABI: every step copies its inputs (x and the
     # logits, or the given ids and weights) from pinned host memory, runs the
@@ -817,6 +887,7 @@ def run_ours(args, c, world, rank, local):
         "gpu_launches": (api.moe_nvfp4_forward_launches(s, flags & ~api.MOE_ROUTER_GEMM) + (1 if gate else 0))
                         * args.steps,
         "roofline": roof,
+        "per_forward": per_forward,
         "stages_us": {k: round(v * 1000, 2) for k, v in stage_ms.items()},
         "stage_gbs": {k: round(sbytes[k] / (stage_ms[k] / 1000) / 1e9, 1) for k in stage_ms if stage_ms[k] > 0},
         "active_experts": active,

@@ -83,6 +83,8 @@ def lib():
                 "orc_fc1": (None, [P, P, i64, i64, P, i64, i32, P, P]),
                 "orc_fc2": (None, [P, P, i64, i64, P, i64, P]),
                 "orc_finalize": (None, [i64, i32, i64, P, P, P, P]),
+                "orc_set_threads": (None, [i32]),
+                "orc_max_threads": (i32, []),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -90,6 +92,16 @@ def lib():
                 fn.argtypes = args
             _lib = L
     return _lib
+
+
+def set_threads(n: int) -> None:
+    """Host threads of the C steps' parallel loops (n < 1: the default).
+    For timing only: the results do not depend on it."""
+    lib().orc_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(lib().orc_max_threads())
 
 
 def _p(a: Optional[np.ndarray]):

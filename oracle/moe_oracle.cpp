@@ -6,6 +6,8 @@
  */
 #include "moe_oracle.h"
 
+#include <omp.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -465,3 +467,12 @@ void orc_finalize(int64_t n_tok, int K, int64_t H, const int64_t* o_index,
             y[t * H + n] = acc;
         }
 }
+
+static int g_default_threads = 0;
+
+void orc_set_threads(int n) {
+    if (g_default_threads == 0) g_default_threads = omp_get_max_threads();
+    omp_set_num_threads(n >= 1 ? n : g_default_threads);
+}
+
+int orc_max_threads(void) { return omp_get_max_threads(); }

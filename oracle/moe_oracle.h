@@ -115,6 +115,11 @@ void orc_fc2(const double* a, const double* alpha, int64_t rows, int64_t I,
 void orc_finalize(int64_t n_tok, int K, int64_t H, const int64_t* o_index,
                   const double* wk, const double* o, double* y);
 
+/* Host threads of the parallel loops above (timing only: every result is
+ * the same for any thread count).  n < 1 restores the default. */
+void orc_set_threads(int n);
+int  orc_max_threads(void);
+
 #ifdef __cplusplus
 }
 #endif

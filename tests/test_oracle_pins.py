@@ -747,3 +747,19 @@ def test_subset_forward_equals_full_forward():
     sub = oracle.forward(layer, x, logits, None, wf, tokens=[0, 5, 11])
     assert np.array_equal(sub.y_bf16, full.y_bf16[[0, 5, 11]])
     assert np.array_equal(sub.y64, full.y64[[0, 5, 11]])
+
+
+def test_thread_count_does_not_change_results():
+    """The single-thread timing of the oracle computes what the all-core
+    one does: every parallel loop writes disjoint outputs in a fixed order."""
+    c, layer, x, logits, w1, w2 = _tiny(T=40, E=6, K=3, exact=False, mode=1)
+    wf = lambda e: (w1[e], w2[e])
+    full = oracle.forward(layer, x, logits, None, wf)
+    try:
+        oracle.set_threads(1)
+        assert oracle.max_threads() == 1
+        one = oracle.forward(layer, x, logits, None, wf)
+    finally:
+        oracle.set_threads(0)
+    assert np.array_equal(one.y_bf16, full.y_bf16)
+    assert np.array_equal(one.y64, full.y64)
