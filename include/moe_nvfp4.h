@@ -117,15 +117,16 @@ typedef enum {
  * resident CTA (otherwise the launch fails: MOE_ERR_CUDA).  The staged entry
  * point records all eight events around the one kernel. */
 #define MOE_FUSED_LAYER (1u << 10)
-/* bits 11-12: GEMM operand orientation (W4A4 launch sequence; results are
- * the same either way up to FP32 accumulation order).  The swapped
- * orientation puts the expert's weights on the MMA's M side and 64 of its
- * routes on the N side, so that experts with few routes do not stream
- * 128-row activation tiles that are mostly padding.  Default: swapped when
- * the mean number of routes per expert holding any (T*K / min(E, T*K)) is
- * at most 64 and T*K >= 64.  MOE_GEMM_SWAP_NEVER / _ALWAYS force a choice; setting both,
- * or _ALWAYS with MOE_GEMM_PAIRS_ALWAYS, MOE_FUSED_LAYER or a non-W4A4 mode,
- * is invalid. */
+/* bits 11-12: GEMM operand orientation (W4A4 and W4A16 launch sequence;
+ * results are the same either way up to FP32 accumulation order).  The
+ * swapped orientation puts the expert's weights on the MMA's M side (W4A16:
+ * widened to BF16 on chip) and 64 of its routes on the N side, so that
+ * experts with few routes do not stream 128-row activation tiles that are
+ * mostly padding.  Default: swapped when the mean number of routes per
+ * expert holding any (T*K / min(E, T*K)) is at most 64 and T*K >= 64.
+ * MOE_GEMM_SWAP_NEVER / _ALWAYS force a choice; setting both, or _ALWAYS
+ * with MOE_GEMM_PAIRS_ALWAYS, MOE_FUSED_LAYER or MOE_W8A8_MXFP8, is
+ * invalid. */
 #define MOE_GEMM_SWAP_NEVER (1u << 11)
 #define MOE_GEMM_SWAP_ALWAYS (1u << 12)
 /* bit 13: test hook for the bounded waits.  The producer warp of the first

@@ -1,0 +1,404 @@
+// Grouped W4A16 GEMMs with the operands swapped: the expert's weights,
+// widened to BF16 on chip, are the MMA's M side (two 128-row operands per
+// tile) and the expert's routes its N side (one 64-route half of an M tile),
+// for experts that hold few routes [newruntime post on FlashInfer PR #5319,
+// "Retrieval answer": W4A16 with BF16 activations on the prepared NVFP4
+// weights].
+//
+//   D^T[w, r] = sum_k W_e[w, k] * X[r, k]         (r: routes of expert e)
+//
+// Why: in the standard orientation (gemm_w4a16.cu) a tile is 128 activation
+// rows, padded per expert, so at a few dozen routes per expert most of
+// every MMA, and of every activation tile read from memory, is padding,
+// while each weight element is still widened once per M tile.  Here the MMA
+// work and the activation bytes follow the routes (64-route halves, only
+// those holding routes are tiled), and the widening cost -- the same once
+// per weight element and route half -- is what the tile is sized for.
+//
+// Tile = two weight operands of 128 rows x one 64-route half.  The E2M1
+// codes come from one 3-D tensor map over the prepared weights viewed as
+// [128-row blocks][128 rows][K bytes], box 32 B x 64 rows x 2 blocks:
+// operand 0 = rows 0-63 of blocks 2t and 2t+1, operand 1 = rows 64-127.
+// With the SwiGLU interleave of the prepared FC1 weights (64 gate rows then
+// 64 up rows per block) operand 0 is 128 gate rows and operand 1 the 128 up
+// rows of the same outputs, so gate and up land in the same tensor-memory
+// lane of two accumulators; without a gate the operands are 256 consecutive
+// output columns (lane r of operand o = column 128 (r / 64) + 64 o + r % 64
+// of the tile).
+//
+// Two rings: a six-deep copy ring (per stage the 64 x 64 BF16 route tile,
+// 128-byte swizzle, the two 4 KB code tiles and the two 512-byte scale
+// atoms of 64 K elements) and a three-slot ring of widened weights (2 x 16
+// KB, the K-major 128-byte-swizzled layout): the copies run further ahead of
+// the MMAs than a ring holding the widened weights in every stage could.
+//
+// Roles (576 threads, one persistent CTA per SM): warp 0 TMA producer, warp
+// 1 tensor-memory allocation and MMA issuer (per 16-element K step one
+// 128 x 64 x 16 kind::f16 MMA per operand), warps 2-9 converters (thread =
+// one weight row of one operand: 64 codes x their 4 scales per stage),
+// warps 10-17 epilogue (thread = weight row, one column per route: two
+// warps per lane quadrant, 32 route columns each).  Accumulators
+// double-buffered: 2 x 2 operands x 64 columns.  The epilogue arithmetic is
+// that of epilogue.cuh (W4A16: no activation global scale), element for
+// element.  Every wait is bounded (1 s); a timeout sets a status bit and all
+// roles drain and exit.
+#include "common.cuh"
+#include "kernels.h"
+#include "w4a16_convert.cuh"
+#include "w4a16_swap.h"
+
+namespace moe {
+namespace swap16 {
+
+constexpr int kNW = 128;                         // weight rows per operand (MMA M)
+constexpr int kNR = 64;                          // route rows per tile (MMA N)
+constexpr int kOps = 2;
+constexpr int kLoadStages = 6;
+constexpr int kConvSlots = 3;
+constexpr int kXBytes = kNR * 128;               // 64 routes x 64 BF16
+constexpr int kQBytes = kNW * 32;                // one operand's codes: 128 rows x 64 E2M1
+constexpr int kSfBytes = 512;                    // one scale atom: 128 rows x 4 scales
+constexpr int kBBytes = kNW * 128;               // one operand's widened weights: 128 rows x 64 BF16
+constexpr int kConvWarps = 8;
+constexpr int kEpiWarp0 = 2 + kConvWarps;
+constexpr int kEpiWarps = 8;
+constexpr int kNumThreads = (kEpiWarp0 + kEpiWarps) * 32;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kAccCols = kOps * kNR;        // one accumulator buffer
+constexpr int kSmemBytes =
+    kLoadStages * (kXBytes + kOps * kQBytes + 2 * kSfBytes) + kConvSlots * kOps * kBBytes + 1024 + 256;
+static_assert(kConvWarps * 32 == kOps * kNW, "one converter thread per weight row of each operand");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Smem {
+    uint8_t* x;          // [kLoadStages][64][128 B], 128-byte swizzle
+    uint8_t* b;          // [kConvSlots][2][128][128 B], 128-byte swizzle
+    uint8_t* q;          // [kLoadStages][2][128][32 B]
+    uint8_t* sf;         // [kLoadStages][2][512 B]
+    uint64_t* full;      // copies of a stage landed
+    uint64_t* empty;     // MMAs of a stage done (its route tile and codes free)
+    uint64_t* conv_full; // a slot's widened weights written
+    uint64_t* conv_empty;
+    uint64_t* acc_full;
+    uint64_t* acc_empty;
+    uint64_t* drain;
+    uint32_t* tmem_holder;
+    volatile int* abort;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw) {
+    Smem s;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    s.x = base;
+    s.b = s.x + kLoadStages * kXBytes;
+    s.q = s.b + kConvSlots * kOps * kBBytes;
+    s.sf = s.q + kLoadStages * kOps * kQBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.sf + kLoadStages * 2 * kSfBytes);
+    s.full = bars;
+    s.empty = bars + kLoadStages;
+    s.conv_full = bars + 2 * kLoadStages;
+    s.conv_empty = s.conv_full + kConvSlots;
+    s.acc_full = s.conv_empty + kConvSlots;
+    s.acc_empty = s.acc_full + 2;
+    s.drain = s.acc_empty + 2;
+    s.tmem_holder = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.abort = reinterpret_cast<volatile int*>(s.tmem_holder + 1);
+    return s;
+}
+
+// tile -> (occupied 64-route half of an M tile, from the scan's list, and
+// weight tile of 256 rows), weight tiles fastest: CTAs running at the same
+// time share the route rows and walk one expert's weights
+struct TileMap {
+    int n_wt;
+    __device__ __forceinline__ void decode(const GemmParams& p, int tile, int& m, int& h, int& wt) const {
+        const int entry = p.tile_half[tile / n_wt];
+        m = entry >> 1;
+        h = entry & 1;
+        wt = tile % n_wt;
+    }
+};
+
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+template <int EPI, bool GATED>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    gemm_w4a16_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                           const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem s = carve(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmW);
+        prefetch_tensormap(&tmX);
+        for (int i = 0; i < kLoadStages; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], 1);
+        }
+        for (int i = 0; i < kConvSlots; ++i) {
+            mbar_init(&s.conv_full[i], kConvWarps);
+            mbar_init(&s.conv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.acc_full[i], 1);
+            mbar_init(&s.acc_empty[i], kEpiWarps * 32);
+        }
+        mbar_init(s.drain, 1);
+        *s.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(s.tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s.tmem_holder;
+    pdl_wait();   // routes, tile lists and the gathered activations come from earlier kernels
+
+    const int kblocks = p.kdim / 64;                 // one 64-element K block per stage
+    const int rb_per_expert = p.n / 128;
+    TileMap tm;
+    tm.n_wt = (rb_per_expert + 1) / 2;
+    const int total = p.meta[3] * tm.n_wt;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_normal();
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+                int m, h, wt;
+                tm.decode(p, tile, m, h, wt);
+                const int e = p.tile_expert[m];
+                if (e < 0 || e >= p.num_experts) {
+                    atomicOr(p.status, kStatusBadExpert);
+                    *s.abort = 1;
+                    break;
+                }
+                const int blk0 = e * rb_per_expert + 2 * wt;
+                const int nblk = min(2, rb_per_expert - 2 * wt);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
+                    mbar_arrive_expect_tx(&s.full[stage],
+                                          (uint32_t)(kXBytes + kOps * kQBytes + nblk * kSfBytes));
+                    tma_load_2d(s.x + stage * kXBytes, &tmX, &s.full[stage], kb * 128, m * kTileM + kNR * h, pol);
+                    for (int o = 0; o < kOps; ++o)
+                        tma_load_3d(s.q + (stage * kOps + o) * kQBytes, &tmW, &s.full[stage], kb * 32, 64 * o, blk0,
+                                    pol);
+                    for (int b = 0; b < nblk; ++b)
+                        bulk_load(s.sf + (stage * 2 + b) * kSfBytes, p.sfb + ((size_t)(blk0 + b) * kblocks + kb) * kSfBytes,
+                                  kSfBytes, &s.full[stage], pol);
+                    if (++stage == kLoadStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, slot = 0, acc = 0;
+            uint32_t phase = 0, cphase = 0, acc_phase = 0;
+            const uint32_t idesc = idesc_bf16(kNW, kNR);
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+                if (!mbar_wait(&s.acc_empty[acc], acc_phase ^ 1u, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kAccCols);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                    if (!mbar_wait(&s.conv_full[slot], cphase, s.abort, p.status, kStatusTimeoutMma)) goto done;
+                    tc_fence_after();
+                    // descriptor start addresses count 16-byte units: 32 bytes = one K step
+                    const uint64_t wdesc0 = sdesc_kmajor_sw128(smem_u32(s.b + slot * kOps * kBBytes));
+                    const uint64_t xdesc0 = sdesc_kmajor_sw128(smem_u32(s.x + stage * kXBytes));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int o = 0; o < kOps; ++o)
+                            tc_mma_bf16(d_tmem + o * kNR, wdesc0 + (uint64_t)o * (kBBytes / 16) + 2u * j,
+                                        xdesc0 + 2u * j, idesc, (kb | j) != 0);
+                    tc_commit(&s.empty[stage]);
+                    tc_commit(&s.conv_empty[slot]);
+                    if (++stage == kLoadStages) { stage = 0; phase ^= 1u; }
+                    if (++slot == kConvSlots) { slot = 0; cphase ^= 1u; }
+                }
+                tc_commit(&s.acc_full[acc]);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+        }
+    } else if (warp < kEpiWarp0) {
+        // converter: thread (o, r) widens row r of operand o, i.e. row
+        // 64 o + r % 64 of weight block 2t + r / 64
+        const int t = (warp - 2) * 32 + lane;
+        const int o = t >> 7, r = t & 127;
+        const int rr = 64 * o + (r & 63);
+        const uint32_t sf_off = (uint32_t)(r >> 6) * kSfBytes + (uint32_t)(rr & 31) * 16u + (uint32_t)(rr >> 5) * 4u;
+        int stage = 0, slot = 0;
+        uint32_t phase = 0, cphase = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutProducer)))
+                    goto done;
+                if (!__all_sync(0xffffffffu, mbar_wait(&s.conv_empty[slot], cphase ^ 1u, s.abort, p.status,
+                                                       kStatusTimeoutProducer)))
+                    goto done;
+                const uint8_t* qrow = s.q + (stage * kOps + o) * kQBytes + r * 32;
+                const uint4 c0 = *reinterpret_cast<const uint4*>(qrow);
+                const uint4 c1 = *reinterpret_cast<const uint4*>(qrow + 16);
+                const uint32_t sfw = *reinterpret_cast<const uint32_t*>(s.sf + stage * 2 * kSfBytes + sf_off);
+                const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                uint8_t* brow = s.b + (slot * kOps + o) * kBBytes + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {          // 16-byte chunk c = elements 8c .. 8c+7
+                    const __half2 sc = __float2half2_rn(e4m3_to_f32((sfw >> (8 * (c >> 1))) & 0xFFu));
+                    *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = dequant8(words[c], sc);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.conv_full[slot]);
+                if (++stage == kLoadStages) { stage = 0; phase ^= 1u; }
+                if (++slot == kConvSlots) { slot = 0; cphase ^= 1u; }
+            }
+        }
+    } else {
+        // epilogue: lane quadrant q, thread = weight row r = 32 q + lane of
+        // each operand; warp half `half` takes route columns 32 half .. +31,
+        // broadcast lane by lane
+        const int q = warp & 3;
+        const int half = (warp - kEpiWarp0) >> 2;
+        const int r = 32 * q + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            int m, h, wt;
+            tm.decode(p, tile, m, h, wt);
+            const int e = p.tile_expert[m];
+            if (e < 0 || e >= p.num_experts) break;
+            // this lane's route column (32 half + lane): route, token and the
+            // epilogue scalars of epi_row (no activation global scale),
+            // loaded before the accumulator is ready
+            const int rb = m * kTileM + kNR * h + 32 * half;   // first route row of this warp's columns
+            const int my_route = p.route_of_row[rb + lane];
+            const int my_token = my_route >= 0 ? my_route / p.topk : 0;
+            float my_alpha = __fmul_rn(1.0f, p.gw[e]);
+            float my_pw = 1.0f;
+            if (EPI == kEpiFc1Bf16 && p.weight_on_input && my_route >= 0) my_pw = p.topk_w[my_route];
+            if (EPI == kEpiFc2Scatter && p.weight_on_output && my_route >= 0) my_alpha = my_alpha * p.topk_w[my_route];
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.acc_full[acc], acc_phase, s.abort, p.status,
+                                                   kStatusTimeoutEpilogue)))
+                break;
+            tc_fence_after();
+            const int col0 = GATED ? 128 * wt + r : 256 * wt + 128 * (r >> 6) + (r & 63);
+            const uint32_t tbase =
+                tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kAccCols) + (uint32_t)(32 * half);
+            // an expert's routes fill its rows from the start: this warp's
+            // live columns are a prefix, only the groups of 8 holding one
+            // are visited
+            const uint32_t live_mask = __ballot_sync(0xffffffffu, my_route >= 0);
+            const int ngroups = (32 - __clz(live_mask) + 7) / 8;
+#pragma unroll 1
+            for (int g = 0; g < ngroups; ++g) {
+                float a0[8], a1[8];
+                tmem_ld8(tbase + 8 * g, a0);
+                tmem_ld8(tbase + kNR + 8 * g, a1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int src = 8 * g + j;
+                    const bool live = __shfl_sync(0xffffffffu, my_route, src) >= 0;   // pad rows: no store
+                    const int row = rb + src;
+                    const float alpha = __shfl_sync(0xffffffffu, my_alpha, src);
+                    if (EPI == kEpiFc1Bf16) {
+                        const float pw = __shfl_sync(0xffffffffu, my_pw, src);
+                        if (GATED) {
+                            // silu as in fc1_act32 (ex2-based exponential, approximate division)
+                            const float zg = a0[j] * alpha, zu = a1[j] * alpha;
+                            const float hv = __fdividef(zg, 1.0f + __expf(-zg)) * zu * pw;
+                            if (live) p.out_bf16[(size_t)row * p.out_cols + col0] = __float2bfloat16_rn(hv);
+                        } else {
+#pragma unroll
+                            for (int oo = 0; oo < kOps; ++oo) {
+                                const int col = col0 + 64 * oo;
+                                if (col - lane >= p.n || !live) continue;   // past the segment: uniform
+                                const float z = fmaxf((oo ? a1[j] : a0[j]) * alpha, 0.0f);
+                                p.out_bf16[(size_t)row * p.out_cols + col] = __float2bfloat16_rn(z * z * pw);
+                            }
+                        }
+                    } else {
+                        const int token = __shfl_sync(0xffffffffu, my_token, src);
+#pragma unroll
+                        for (int oo = 0; oo < kOps; ++oo) {
+                            const int col = col0 + 64 * oo;
+                            if (col - lane >= p.n || !live) continue;
+                            const float v = (oo ? a1[j] : a0[j]) * alpha;
+                            if (EPI == kEpiFc2Store) p.out_bf16[(size_t)row * p.out_cols + col] = __float2bfloat16_rn(v);
+                            else red_add_f32(p.out_f32 + (size_t)token * p.out_cols + col, v);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&s.acc_empty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+done:
+    {
+        // after an abort let in-flight copies land and retire issued MMAs
+        // before the tensor memory is freed
+        volatile int no_abort = 0;
+        if (*s.abort) {
+            if (warp == 1 && lane == 0) {
+                tc_commit(s.drain);
+                mbar_wait(s.drain, 0, &no_abort, p.status, kStatusTimeoutMma);
+            }
+            for (int i = 0; i < 100; ++i) __nanosleep(10000);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    pdl_launch_dependents();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <int EPI, bool GATED>
+cudaError_t set_smem_one() {
+    return cudaFuncSetAttribute(gemm_w4a16_swap_kernel<EPI, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBytes);
+}
+
+}  // namespace swap16
+
+cudaError_t setup_gemm_w4a16_swap_kernels() {
+    using namespace swap16;
+    cudaError_t e;
+    if ((e = set_smem_one<kEpiFc1Bf16, true>())) return e;
+    if ((e = set_smem_one<kEpiFc1Bf16, false>())) return e;
+    if ((e = set_smem_one<kEpiFc2Store, false>())) return e;
+    return set_smem_one<kEpiFc2Scatter, false>();
+}
+
+cudaError_t launch_gemm_w4a16_swap(const LaunchCtx& c, int epilogue, bool gated, const CUtensorMap& tmW,
+                                   const CUtensorMap& tmX, const GemmParams& p, int num_sms) {
+    using namespace swap16;
+    const dim3 grid(num_sms), block(kNumThreads);
+    const size_t smem = kSmemBytes;
+    if (gated)
+        return epilogue == kEpiFc1Bf16
+                   ? c.launch(gemm_w4a16_swap_kernel<kEpiFc1Bf16, true>, grid, block, smem, tmW, tmX, p)
+                   : cudaErrorInvalidValue;
+    switch (epilogue) {
+        case kEpiFc1Bf16: return c.launch(gemm_w4a16_swap_kernel<kEpiFc1Bf16, false>, grid, block, smem, tmW, tmX, p);
+        case kEpiFc2Store: return c.launch(gemm_w4a16_swap_kernel<kEpiFc2Store, false>, grid, block, smem, tmW, tmX, p);
+        case kEpiFc2Scatter:
+            return c.launch(gemm_w4a16_swap_kernel<kEpiFc2Scatter, false>, grid, block, smem, tmW, tmX, p);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace moe

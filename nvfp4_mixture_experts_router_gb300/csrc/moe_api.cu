@@ -10,6 +10,7 @@
 #include "../../include/moe_nvfp4.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "w4a16_swap.h"
 #include "layout.h"
 
 using namespace moe;
@@ -45,6 +46,7 @@ moe_status device_state(int* sms, int* device = nullptr) {
                    setup_gemm_w4a16_kernels() != cudaSuccess || setup_gemm_pair_kernels(dev, d.sms) != cudaSuccess ||
                    setup_gemm_w4a16_pair_kernels(dev, d.sms) != cudaSuccess ||
                    setup_fused_layer_kernel() != cudaSuccess || setup_gemm_swap_kernels() != cudaSuccess ||
+                   setup_gemm_w4a16_swap_kernels() != cudaSuccess ||
                    setup_router_gemm_kernel() != cudaSuccess) {
             d.status = MOE_ERR_CUDA;
         } else {
@@ -80,8 +82,7 @@ moe_status validate_shape(moe_shape s, uint32_t flags) {
     if ((flags & MOE_QUANT_4OVER6) && mode_of(flags) != kModePerToken) return MOE_ERR_INVALID_ARG;
     if ((flags & MOE_GEMM_SWAP_NEVER) && (flags & MOE_GEMM_SWAP_ALWAYS)) return MOE_ERR_INVALID_ARG;
     if ((flags & MOE_GEMM_SWAP_ALWAYS) &&
-        ((mode_of(flags) != kModePerTensor && mode_of(flags) != kModePerToken) ||
-         (flags & (MOE_GEMM_PAIRS_ALWAYS | MOE_FUSED_LAYER))))
+        (mode_of(flags) == kModeMxfp8 || (flags & (MOE_GEMM_PAIRS_ALWAYS | MOE_FUSED_LAYER))))
         return MOE_ERR_INVALID_ARG;
     if (flags & MOE_FUSED_LAYER) {
         // one persistent kernel: the NVFP4 activation modes, the router's
@@ -143,20 +144,24 @@ bool encode_chunk_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_
 }
 
 // 3-D uint8 tensor map over prepared weight codes [rows][row_bytes] viewed
-// as [rows/128 blocks][128 rows][row_bytes], box 128 B x 64 rows x 2 blocks
-// (the swapped-orientation GEMM's weight operands).
-bool encode_swap_weight_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes) {
+// as [rows/128 blocks][128 rows][row_bytes], box box_bytes x 64 rows x 2
+// blocks (the swapped-orientation GEMMs' weight operands): 128-byte boxes
+// with the 128-byte swizzle (NVFP4 operands), narrower ones unswizzled
+// (W4A16 codes, widened by the converter warps).
+bool encode_swap_weight_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes,
+                            uint32_t box_bytes = 128) {
     const cuuint64_t dims[3] = {row_bytes, 128, rows / 128};
     const cuuint64_t strides[2] = {row_bytes, 128 * row_bytes};
-    const cuuint32_t box[3] = {128, 64, 2};
+    const cuuint32_t box[3] = {box_bytes, 64, 2};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
-                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-// Run the W4A4 GEMMs in the swapped orientation?  When asked to, or by
+// Run the W4A4 (and W4A16) GEMMs in the swapped orientation?  When asked to, or by
 // default when the experts that hold routes hold at most 64 on average
 // (their 128-row activation tiles would be half padding or more) and there
 // are at least 64 routes in all.  With fewer (a decode step of one token,
@@ -164,7 +169,8 @@ bool encode_swap_weight_map(CUtensorMap* map, const void* base, uint64_t rows, u
 // kernel's 256-wide tile has the shorter fixed latency (measured on GB300:
 // T = 1 at the DSV3 shape 68.6 us standard vs 72.3 us swapped; T = 16
 // 452.7 vs 440.8; the mid workload 77.8 vs 74.9; T = 4096: 128 routes per
-// expert, standard).
+// expert, standard).  W4A16 (H = 4096, I = 1536, E = 128, top-8): T = 16
+// step 385 -> 351 us, T = 512 532 -> 503 us swapped.
 constexpr uint64_t kSlabAccBytes = 48ull << 20;   // FC2 accumulator slice kept in L2 (of 129 MB)
 constexpr int64_t kSwapMaxRoutesPerExpert = 64;
 constexpr int64_t kSwapMinRoutes = 64;
@@ -505,12 +511,20 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         __nv_bfloat16* h_bf16 = reinterpret_cast<__nv_bfloat16*>(wsp(W.h_bf16));
         e = launch_gather_x_bf16(c, s.T, s.H, s.K, x_bf16, rs, x_perm, y_acc);
         if (e != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
+        // few routes per expert: weights on the MMA's M side, 64-route halves on N
+        const bool swap16 = use_swap_gemm(s, flags);
         CUtensorMap tA1, tB1, tA2, tB2;
-        if (!encode_operand_map(&tA1, x_perm, W.rows_cap, (uint64_t)s.H * 2) ||
-            !encode_operand_map(&tB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 32) ||
-            !encode_operand_map(&tA2, h_bf16, W.rows_cap, (uint64_t)s.I * 2) ||
-            !encode_operand_map(&tB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 32))
-            return MOE_ERR_CUDA;
+        const bool maps_ok =
+            swap16 ? (encode_operand_map(&tA1, x_perm, W.rows_cap, (uint64_t)s.H * 2, 128, 64) &&
+                      encode_swap_weight_map(&tB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 32) &&
+                      encode_operand_map(&tA2, h_bf16, W.rows_cap, (uint64_t)s.I * 2, 128, 64) &&
+                      encode_swap_weight_map(&tB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 32))
+                   : (encode_operand_map(&tA1, x_perm, W.rows_cap, (uint64_t)s.H * 2) &&
+                      encode_operand_map(&tB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 32) &&
+                      encode_operand_map(&tA2, h_bf16, W.rows_cap, (uint64_t)s.I * 2) &&
+                      encode_operand_map(&tB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 32));
+        if (!maps_ok) return MOE_ERR_CUDA;
+        int* tile_half16 = reinterpret_cast<int*>(wsp(W.tile_half));
         GemmParams a{};
         a.sfb = pw + P.w1_sf;
         a.kdim = s.H;
@@ -528,8 +542,10 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         a.out_cols = s.I;
         a.out_bf16 = h_bf16;
         a.tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
-        e = use_pair_gemm(s, flags, N1) ? launch_gemm_w4a16_pair(c, kEpiFc1Bf16, tA1, tB1, a, device)
-                                        : launch_gemm_w4a16(c, kEpiFc1Bf16, tA1, tB1, a, sms);
+        a.tile_half = tile_half16;
+        e = swap16 ? launch_gemm_w4a16_swap(c, kEpiFc1Bf16, act == MOE_ACT_SWIGLU, tB1, tA1, a, sms)
+            : use_pair_gemm(s, flags, N1) ? launch_gemm_w4a16_pair(c, kEpiFc1Bf16, tA1, tB1, a, device)
+                                          : launch_gemm_w4a16(c, kEpiFc1Bf16, tA1, tB1, a, sms);
         if (e != cudaSuccess || !mark(4) || !mark(5)) return MOE_ERR_CUDA;
         GemmParams b{};
         b.sfb = pw + P.w2_sf;
@@ -555,8 +571,10 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
             epi2 = kEpiFc2Scatter;
         }
         b.tile_pair = reinterpret_cast<int*>(wsp(W.tile_pair));
-        e = use_pair_gemm(s, flags, s.H) ? launch_gemm_w4a16_pair(c, epi2, tA2, tB2, b, device)
-                                         : launch_gemm_w4a16(c, epi2, tA2, tB2, b, sms);
+        b.tile_half = tile_half16;
+        e = swap16 ? launch_gemm_w4a16_swap(c, epi2, false, tB2, tA2, b, sms)
+            : use_pair_gemm(s, flags, s.H) ? launch_gemm_w4a16_pair(c, epi2, tA2, tB2, b, device)
+                                           : launch_gemm_w4a16(c, epi2, tA2, tB2, b, sms);
         if (e != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
         if (det)
             e = launch_finalize_deterministic(c, s.T, s.H, s.K, row_of_route, topk_w, on_input ? 0 : 1,

@@ -133,7 +133,7 @@ class MoEConfig:
     gemm_pairs: str = "auto"      # GEMM tile scheduling: "auto" | "never" | "always"
     four_over_six: bool = False   # per-token W4A4: 4-over-6 activation quantization
     fused: bool = False           # W4A4: the whole forward as one persistent kernel
-    gemm_swap: str = "auto"       # W4A4 GEMM orientation: "auto" | "never" | "always"
+    gemm_swap: str = "auto"       # W4A4 / W4A16 GEMM orientation: "auto" | "never" | "always"
     extra: dict = field(default_factory=dict)
 
     @property

@@ -89,12 +89,11 @@ def test_invalid_arguments_rejected_before_cuda(L):
     assert f(s, dbg | sn | api.MOE_GEMM_PAIRS_ALWAYS, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, dbg | sn | api.MOE_W4A16, A, B, None, None, None, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert api.moe_nvfp4_workspace_bytes(s, dbg | sn) == wb
-    # GEMM orientation hints: not both, and the swapped one only for W4A4 on the launch sequence
+    # GEMM orientation hints: not both, and the swapped one only for W4A4 / W4A16 on the launch sequence
     sw, sn = api.MOE_GEMM_SWAP_ALWAYS, api.MOE_GEMM_SWAP_NEVER
     assert f(s, sw | sn, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, sw | api.MOE_GEMM_PAIRS_ALWAYS, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, sw | api.MOE_FUSED_LAYER, A, B, None, A, A, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
-    assert f(s, sw | api.MOE_W4A16, A, B, None, None, None, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert f(s, sw | api.MOE_W8A8_MXFP8, A, B, None, None, None, A, W, wb, Y, None) == api.MOE_ERR_INVALID_ARG
     assert api.moe_nvfp4_workspace_bytes(s, sw) == wb and api.moe_nvfp4_workspace_bytes(s, sn | api.MOE_W4A16) > 0
     # the single-kernel layer: NVFP4 activation modes, E <= 256, single-CTA tiles
