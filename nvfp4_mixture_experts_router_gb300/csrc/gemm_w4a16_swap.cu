@@ -26,19 +26,27 @@
 // output columns (lane r of operand o = column 128 (r / 64) + 64 o + r % 64
 // of the tile).
 //
-// Two rings: a six-deep copy ring (per stage the 64 x 64 BF16 route tile,
-// 128-byte swizzle, the two 4 KB code tiles and the two 512-byte scale
-// atoms of 64 K elements) and a three-slot ring of widened weights (2 x 16
-// KB, the K-major 128-byte-swizzled layout): the copies run further ahead of
-// the MMAs than a ring holding the widened weights in every stage could.
+// The widened weights never touch shared memory: each converter thread
+// owns one weight row, i.e. one tensor-memory lane, and stores its 64 BF16
+// of a stage as 32 columns with tcgen05.st; the MMA reads its A operand from
+// tensor memory.  (Through shared memory a stage moved ~100 KB -- codes,
+// route tile, the widened weights written and read back, the route tile read
+// once per operand -- and that traffic, not the converters' issue rate,
+// bounded the kernel.)  Two rings: an eight-deep copy ring in shared memory
+// (per stage the 64 x 64 BF16 route tile, 128-byte swizzle, the two 4 KB
+// code tiles and the two 512-byte scale atoms of 64 K elements) and four
+// slots of widened weights in tensor memory (2 operands x 32 columns each).
+//
+// Tensor memory (512 columns): accumulators at 0-255 (two buffers of 2
+// operands x 64 route columns), widened-weight slots at 256-511.
 //
 // Roles (576 threads, one persistent CTA per SM): warp 0 TMA producer, warp
 // 1 tensor-memory allocation and MMA issuer (per 16-element K step one
-// 128 x 64 x 16 kind::f16 MMA per operand), warps 2-9 converters (thread =
-// one weight row of one operand: 64 codes x their 4 scales per stage),
-// warps 10-17 epilogue (thread = weight row, one column per route: two
-// warps per lane quadrant, 32 route columns each).  Accumulators
-// double-buffered: 2 x 2 operands x 64 columns.  The epilogue arithmetic is
+// 128 x 64 x 16 kind::f16 MMA per operand, A from tensor memory), warps 2-9
+// converters (thread = one weight row of one operand, on its own lane: 64
+// codes x their 4 scales per stage), warps 10-17 epilogue (thread = weight
+// row, one column per route: two warps per lane quadrant, 32 route columns
+// each).  The epilogue arithmetic is
 // that of epilogue.cuh (W4A16: no activation global scale), element for
 // element.  Every wait is bounded (1 s); a timeout sets a status bit and all
 // roles drain and exit.
@@ -53,26 +61,27 @@ namespace swap16 {
 constexpr int kNW = 128;                         // weight rows per operand (MMA M)
 constexpr int kNR = 64;                          // route rows per tile (MMA N)
 constexpr int kOps = 2;
-constexpr int kLoadStages = 6;
-constexpr int kConvSlots = 3;
+constexpr int kLoadStages = 8;
+constexpr int kConvSlots = 4;
 constexpr int kXBytes = kNR * 128;               // 64 routes x 64 BF16
 constexpr int kQBytes = kNW * 32;                // one operand's codes: 128 rows x 64 E2M1
 constexpr int kSfBytes = 512;                    // one scale atom: 128 rows x 4 scales
-constexpr int kBBytes = kNW * 128;               // one operand's widened weights: 128 rows x 64 BF16
 constexpr int kConvWarps = 8;
 constexpr int kEpiWarp0 = 2 + kConvWarps;
 constexpr int kEpiWarps = 8;
 constexpr int kNumThreads = (kEpiWarp0 + kEpiWarps) * 32;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kOps * kNR;        // one accumulator buffer
-constexpr int kSmemBytes =
-    kLoadStages * (kXBytes + kOps * kQBytes + 2 * kSfBytes) + kConvSlots * kOps * kBBytes + 1024 + 256;
+constexpr uint32_t kACol0 = 2 * kAccCols;        // first widened-weight column
+constexpr uint32_t kAOpCols = 32;                // 64 BF16 of one row per stage, two per column
+constexpr uint32_t kASlotCols = kOps * kAOpCols;
+static_assert(kACol0 + kConvSlots * kASlotCols <= kTmemCols, "tensor memory budget");
+constexpr int kSmemBytes = kLoadStages * (kXBytes + kOps * kQBytes + 2 * kSfBytes) + 1024 + 256;
 static_assert(kConvWarps * 32 == kOps * kNW, "one converter thread per weight row of each operand");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Smem {
     uint8_t* x;          // [kLoadStages][64][128 B], 128-byte swizzle
-    uint8_t* b;          // [kConvSlots][2][128][128 B], 128-byte swizzle
     uint8_t* q;          // [kLoadStages][2][128][32 B]
     uint8_t* sf;         // [kLoadStages][2][512 B]
     uint64_t* full;      // copies of a stage landed
@@ -90,8 +99,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     Smem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.x = base;
-    s.b = s.x + kLoadStages * kXBytes;
-    s.q = s.b + kConvSlots * kOps * kBBytes;
+    s.q = s.x + kLoadStages * kXBytes;
     s.sf = s.q + kLoadStages * kOps * kQBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s.sf + kLoadStages * 2 * kSfBytes);
     s.full = bars;
@@ -118,6 +126,16 @@ struct TileMap {
         wt = tile % n_wt;
     }
 };
+
+// kind::f16 MMA with the A operand (M x 16 BF16) in tensor memory
+__device__ __forceinline__ void tc_mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
     asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
@@ -209,15 +227,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
                     if (!mbar_wait(&s.conv_full[slot], cphase, s.abort, p.status, kStatusTimeoutMma)) goto done;
                     tc_fence_after();
-                    // descriptor start addresses count 16-byte units: 32 bytes = one K step
-                    const uint64_t wdesc0 = sdesc_kmajor_sw128(smem_u32(s.b + slot * kOps * kBBytes));
+                    // descriptor start addresses count 16-byte units: 32 bytes = one K
+                    // step; in tensor memory one K step of A is 8 columns
+                    const uint32_t a0 = tmem_base + kACol0 + (uint32_t)slot * kASlotCols;
                     const uint64_t xdesc0 = sdesc_kmajor_sw128(smem_u32(s.x + stage * kXBytes));
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
 #pragma unroll
                         for (int o = 0; o < kOps; ++o)
-                            tc_mma_bf16(d_tmem + o * kNR, wdesc0 + (uint64_t)o * (kBBytes / 16) + 2u * j,
-                                        xdesc0 + 2u * j, idesc, (kb | j) != 0);
+                            tc_mma_bf16_tmem_a(d_tmem + o * kNR, a0 + (uint32_t)(o * kAOpCols + 8 * j), xdesc0 + 2u * j,
+                                               idesc, (kb | j) != 0);
                     tc_commit(&s.empty[stage]);
                     tc_commit(&s.conv_empty[slot]);
                     if (++stage == kLoadStages) { stage = 0; phase ^= 1u; }
@@ -229,9 +248,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
     } else if (warp < kEpiWarp0) {
         // converter: thread (o, r) widens row r of operand o, i.e. row
-        // 64 o + r % 64 of weight block 2t + r / 64
-        const int t = (warp - 2) * 32 + lane;
-        const int o = t >> 7, r = t & 127;
+        // 64 o + r % 64 of weight block 2t + r / 64, into tensor-memory lane
+        // r (a warp reaches the lanes of quadrant warp % 4 only)
+        const int q = warp & 3;
+        const int o = (warp - 2) >> 2, r = 32 * q + lane;
         const int rr = 64 * o + (r & 63);
         const uint32_t sf_off = (uint32_t)(r >> 6) * kSfBytes + (uint32_t)(rr & 31) * 16u + (uint32_t)(rr >> 5) * 4u;
         int stage = 0, slot = 0;
@@ -244,18 +264,27 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (!__all_sync(0xffffffffu, mbar_wait(&s.conv_empty[slot], cphase ^ 1u, s.abort, p.status,
                                                        kStatusTimeoutProducer)))
                     goto done;
+                tc_fence_after();                      // the slot's last MMAs are complete
                 const uint8_t* qrow = s.q + (stage * kOps + o) * kQBytes + r * 32;
                 const uint4 c0 = *reinterpret_cast<const uint4*>(qrow);
                 const uint4 c1 = *reinterpret_cast<const uint4*>(qrow + 16);
                 const uint32_t sfw = *reinterpret_cast<const uint32_t*>(s.sf + stage * 2 * kSfBytes + sf_off);
                 const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                uint8_t* brow = s.b + (slot * kOps + o) * kBBytes + r * 128;
+                uint32_t wv[32];                       // column i = elements 2i (low half), 2i + 1
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {          // 16-byte chunk c = elements 8c .. 8c+7
+                for (int c = 0; c < 8; ++c) {          // elements 8c .. 8c+7
                     const __half2 sc = __float2half2_rn(e4m3_to_f32((sfw >> (8 * (c >> 1))) & 0xFFu));
-                    *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = dequant8(words[c], sc);
+                    const uint4 v = dequant8(words[c], sc);
+                    wv[4 * c] = v.x;
+                    wv[4 * c + 1] = v.y;
+                    wv[4 * c + 2] = v.z;
+                    wv[4 * c + 3] = v.w;
                 }
-                fence_proxy_async_smem();
+                tmem_st32(tmem_base + ((uint32_t)(32 * q) << 16) + kACol0 + (uint32_t)slot * kASlotCols +
+                              (uint32_t)(o * kAOpCols),
+                          wv);
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s.conv_full[slot]);
                 if (++stage == kLoadStages) { stage = 0; phase ^= 1u; }
@@ -346,14 +375,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
 done:
     {
-        // after an abort let in-flight copies land and retire issued MMAs
-        // before the tensor memory is freed
+        // after an abort let in-flight copies land and retire issued MMAs and
+        // tensor-memory stores before the tensor memory is freed
         volatile int no_abort = 0;
         if (*s.abort) {
             if (warp == 1 && lane == 0) {
                 tc_commit(s.drain);
                 mbar_wait(s.drain, 0, &no_abort, p.status, kStatusTimeoutMma);
             }
+            if (warp >= 2 && warp < kEpiWarp0) tmem_st_wait();
             for (int i = 0; i < 100; ++i) __nanosleep(10000);
         }
     }

@@ -170,7 +170,7 @@ bool encode_swap_weight_map(CUtensorMap* map, const void* base, uint64_t rows, u
 // T = 1 at the DSV3 shape 68.6 us standard vs 72.3 us swapped; T = 16
 // 452.7 vs 440.8; the mid workload 77.8 vs 74.9; T = 4096: 128 routes per
 // expert, standard).  W4A16 (H = 4096, I = 1536, E = 128, top-8): T = 16
-// step 385 -> 351 us, T = 512 532 -> 503 us swapped.
+// step 385 -> 325 us, T = 512 532 -> 466 us swapped.
 constexpr uint64_t kSlabAccBytes = 48ull << 20;   // FC2 accumulator slice kept in L2 (of 129 MB)
 constexpr int64_t kSwapMaxRoutesPerExpert = 64;
 constexpr int64_t kSwapMinRoutes = 64;
