@@ -78,8 +78,8 @@ def parse():
     p.add_argument("--fused", action="store_true",
                    help="the whole forward as one persistent kernel (MOE_FUSED_LAYER; W4A4, E <= 256)")
     p.add_argument("--gemm", default="auto", choices=["auto", "standard", "swapped", "pairs"],
-                   help="W4A4 GEMM variant (default: by routes per expert): single-CTA standard or swapped "
-                        "orientation, or CTA pairs")
+                   help="W4A4 / W4A16 GEMM variant (default: by routes per expert): single-CTA standard or "
+                        "swapped orientation, or CTA pairs")
     p.add_argument("--finalize", default="config", choices=["config", "fused", "deterministic"],
                    help="finalize mode: the workload's own (default), the FC2-epilogue scatter or the fixed-order kernel")
     p.add_argument("--no-cpu-baseline", action="store_true")
