@@ -17,7 +17,7 @@
 //
 // Tile = two weight operands of 128 rows x one 64-route half.  The E2M1
 // codes come from one 3-D tensor map over the prepared weights viewed as
-// [128-row blocks][128 rows][K bytes], box 32 B x 64 rows x 2 blocks:
+// [128-row blocks][128 rows][K bytes], box 64 B x 64 rows x 2 blocks:
 // operand 0 = rows 0-63 of blocks 2t and 2t+1, operand 1 = rows 64-127.
 // With the SwiGLU interleave of the prepared FC1 weights (64 gate rows then
 // 64 up rows per block) operand 0 is 128 gate rows and operand 1 the 128 up
@@ -27,16 +27,19 @@
 // of the tile).
 //
 // The widened weights never touch shared memory: each converter thread
-// owns one weight row, i.e. one tensor-memory lane, and stores its 64 BF16
-// of a stage as 32 columns with tcgen05.st; the MMA reads its A operand from
+// owns one weight row, i.e. one tensor-memory lane, and stores its 128
+// BF16 of a stage as 64 columns with tcgen05.st; the MMA reads its A operand from
 // tensor memory.  (Through shared memory a stage moved ~100 KB -- codes,
 // route tile, the widened weights written and read back, the route tile read
 // once per operand; keeping the widened weights in tensor memory cut the
 // shared-memory wavefronts threefold and the GEMM time by ~8 %.)  Two
-// rings: an eight-deep copy ring in shared memory (per stage the 64 x 64
-// BF16 route tile, 128-byte swizzle, the two 4 KB code tiles and the two
-// 512-byte scale atoms of 64 K elements) and four slots of widened weights
-// in tensor memory (2 operands x 32 columns each).
+// rings: a six-deep copy ring in shared memory (per stage of 128 K
+// elements: the route tile as two 64 x 64 BF16 sub-tiles, 128-byte swizzle,
+// the two 8 KB code tiles and each weight block's two scale atoms) and two
+// slots of widened weights in tensor memory (2 operands x 64 columns each).
+// Stages of 128 elements make the code copies 64-byte row segments: with
+// 64-element stages (32-byte segments) the copies bounded the kernel, and
+// doubling the segment cut the GEMM time by a further ~17 %.
 //
 // Tensor memory (512 columns): accumulators at 0-255 (two buffers of 2
 // operands x 64 route columns), widened-weight slots at 256-511.
@@ -44,8 +47,8 @@
 // Roles (576 threads, one persistent CTA per SM): warp 0 TMA producer, warp
 // 1 tensor-memory allocation and MMA issuer (per 16-element K step one
 // 128 x 64 x 16 kind::f16 MMA per operand, A from tensor memory), warps 2-9
-// converters (thread = one weight row of one operand, on its own lane: 64
-// codes x their 4 scales per stage), warps 10-17 epilogue (thread = weight
+// converters (thread = one weight row of one operand, on its own lane: 128
+// codes x their 8 scales per stage), warps 10-17 epilogue (thread = weight
 // row, one column per route: two warps per lane quadrant, 32 route columns
 // each).  The epilogue arithmetic is
 // that of epilogue.cuh (W4A16: no activation global scale), element for
@@ -62,11 +65,14 @@ namespace swap16 {
 constexpr int kNW = 128;                         // weight rows per operand (MMA M)
 constexpr int kNR = 64;                          // route rows per tile (MMA N)
 constexpr int kOps = 2;
-constexpr int kLoadStages = 8;
-constexpr int kConvSlots = 4;
-constexpr int kXBytes = kNR * 128;               // 64 routes x 64 BF16
-constexpr int kQBytes = kNW * 32;                // one operand's codes: 128 rows x 64 E2M1
-constexpr int kSfBytes = 512;                    // one scale atom: 128 rows x 4 scales
+constexpr int kKStage = 128;                     // K elements per stage
+constexpr int kLoadStages = 6;
+constexpr int kConvSlots = 2;
+constexpr int kXHalf = kNR * 128;                // 64 routes x 64 BF16: one 128-byte-swizzled sub-tile
+constexpr int kXBytes = 2 * kXHalf;              // 64 routes x 128 BF16
+constexpr int kQBytes = kNW * kKStage / 2;       // one operand's codes: 128 rows x 128 E2M1
+constexpr int kAtom = 512;                       // one scale atom: 128 rows x 4 scales (64 K elements)
+constexpr int kSfBytes = 2 * kAtom;              // one weight block's scales of a stage
 constexpr int kConvWarps = 8;
 constexpr int kEpiWarp0 = 2 + kConvWarps;
 constexpr int kEpiWarps = 8;
@@ -74,7 +80,7 @@ constexpr int kNumThreads = (kEpiWarp0 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kOps * kNR;        // one accumulator buffer
 constexpr uint32_t kACol0 = 2 * kAccCols;        // first widened-weight column
-constexpr uint32_t kAOpCols = 32;                // 64 BF16 of one row per stage, two per column
+constexpr uint32_t kAOpCols = kKStage / 2;       // 128 BF16 of one row per stage, two per column
 constexpr uint32_t kASlotCols = kOps * kAOpCols;
 static_assert(kACol0 + kConvSlots * kASlotCols <= kTmemCols, "tensor memory budget");
 constexpr int kSmemBytes = kLoadStages * (kXBytes + kOps * kQBytes + 2 * kSfBytes) + 1024 + 256;
@@ -82,9 +88,9 @@ static_assert(kConvWarps * 32 == kOps * kNW, "one converter thread per weight ro
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Smem {
-    uint8_t* x;          // [kLoadStages][64][128 B], 128-byte swizzle
-    uint8_t* q;          // [kLoadStages][2][128][32 B]
-    uint8_t* sf;         // [kLoadStages][2][512 B]
+    uint8_t* x;          // [kLoadStages][2 sub-tiles][64][128 B], 128-byte swizzle
+    uint8_t* q;          // [kLoadStages][2 operands][128][64 B]
+    uint8_t* sf;         // [kLoadStages][2 blocks][2 atoms][512 B]
     uint64_t* full;      // copies of a stage landed
     uint64_t* empty;     // MMAs of a stage done (its route tile and codes free)
     uint64_t* conv_full; // a slot's widened weights written
@@ -178,7 +184,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t tmem_base = *s.tmem_holder;
     pdl_wait();   // routes, tile lists and the gathered activations come from earlier kernels
 
-    const int kblocks = p.kdim / 64;                 // one 64-element K block per stage
+    const int kblocks = p.kdim / 64;                 // 64-element K blocks (scale atoms per weight block)
+    const int ksteps = p.kdim / kKStage;             // stages per tile
     const int rb_per_expert = p.n / 128;
     TileMap tm;
     tm.n_wt = (rb_per_expert + 1) / 2;
@@ -200,17 +207,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 const int blk0 = e * rb_per_expert + 2 * wt;
                 const int nblk = min(2, rb_per_expert - 2 * wt);
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int ks = 0; ks < ksteps; ++ks) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1u, s.abort, p.status, kStatusTimeoutProducer)) goto done;
                     mbar_arrive_expect_tx(&s.full[stage],
                                           (uint32_t)(kXBytes + kOps * kQBytes + nblk * kSfBytes));
-                    tma_load_2d(s.x + stage * kXBytes, &tmX, &s.full[stage], kb * 128, m * kTileM + kNR * h, pol);
+                    for (int xh = 0; xh < 2; ++xh)
+                        tma_load_2d(s.x + stage * kXBytes + xh * kXHalf, &tmX, &s.full[stage], ks * 256 + xh * 128,
+                                    m * kTileM + kNR * h, pol);
                     for (int o = 0; o < kOps; ++o)
-                        tma_load_3d(s.q + (stage * kOps + o) * kQBytes, &tmW, &s.full[stage], kb * 32, 64 * o, blk0,
-                                    pol);
+                        tma_load_3d(s.q + (stage * kOps + o) * kQBytes, &tmW, &s.full[stage], ks * (kKStage / 2), 64 * o,
+                                    blk0, pol);
+                    // the two atoms of K blocks 2 ks, 2 ks + 1 are adjacent
                     for (int b = 0; b < nblk; ++b)
-                        bulk_load(s.sf + (stage * 2 + b) * kSfBytes, p.sfb + ((size_t)(blk0 + b) * kblocks + kb) * kSfBytes,
-                                  kSfBytes, &s.full[stage], pol);
+                        bulk_load(s.sf + (stage * 2 + b) * kSfBytes,
+                                  p.sfb + ((size_t)(blk0 + b) * kblocks + 2 * ks) * kAtom, kSfBytes, &s.full[stage], pol);
                     if (++stage == kLoadStages) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -224,7 +234,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (!mbar_wait(&s.acc_empty[acc], acc_phase ^ 1u, s.abort, p.status, kStatusTimeoutMma)) goto done;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kAccCols);
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int ks = 0; ks < ksteps; ++ks) {
                     if (!mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutMma)) goto done;
                     if (!mbar_wait(&s.conv_full[slot], cphase, s.abort, p.status, kStatusTimeoutMma)) goto done;
                     tc_fence_after();
@@ -233,11 +243,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t a0 = tmem_base + kACol0 + (uint32_t)slot * kASlotCols;
                     const uint64_t xdesc0 = sdesc_kmajor_sw128(smem_u32(s.x + stage * kXBytes));
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
+                    for (int j = 0; j < kKStage / 16; ++j)
 #pragma unroll
                         for (int o = 0; o < kOps; ++o)
-                            tc_mma_bf16_tmem_a(d_tmem + o * kNR, a0 + (uint32_t)(o * kAOpCols + 8 * j), xdesc0 + 2u * j,
-                                               idesc, (kb | j) != 0);
+                            tc_mma_bf16_tmem_a(d_tmem + o * kNR, a0 + (uint32_t)(o * kAOpCols + 8 * j),
+                                               xdesc0 + (uint64_t)((j >> 2) * (kXHalf / 16) + 2 * (j & 3)), idesc,
+                                               (ks | j) != 0);
                     tc_commit(&s.empty[stage]);
                     tc_commit(&s.conv_empty[slot]);
                     if (++stage == kLoadStages) { stage = 0; phase ^= 1u; }
@@ -255,10 +266,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const int o = (warp - 2) >> 2, r = 32 * q + lane;
         const int rr = 64 * o + (r & 63);
         const uint32_t sf_off = (uint32_t)(r >> 6) * kSfBytes + (uint32_t)(rr & 31) * 16u + (uint32_t)(rr >> 5) * 4u;
+        const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + kACol0 + (uint32_t)(o * kAOpCols);
         int stage = 0, slot = 0;
         uint32_t phase = 0, cphase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            for (int kb = 0; kb < kblocks; ++kb) {
+            for (int ks = 0; ks < ksteps; ++ks) {
                 if (!__all_sync(0xffffffffu,
                                 mbar_wait(&s.full[stage], phase, s.abort, p.status, kStatusTimeoutProducer)))
                     goto done;
@@ -266,24 +278,27 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                        kStatusTimeoutProducer)))
                     goto done;
                 tc_fence_after();                      // the slot's last MMAs are complete
-                const uint8_t* qrow = s.q + (stage * kOps + o) * kQBytes + r * 32;
-                const uint4 c0 = *reinterpret_cast<const uint4*>(qrow);
-                const uint4 c1 = *reinterpret_cast<const uint4*>(qrow + 16);
-                const uint32_t sfw = *reinterpret_cast<const uint32_t*>(s.sf + stage * 2 * kSfBytes + sf_off);
-                const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                uint32_t wv[32];                       // column i = elements 2i (low half), 2i + 1
+                const uint8_t* qrow = s.q + (stage * kOps + o) * kQBytes + r * (kKStage / 2);
+                // two 64-element halves: codes from 32 bytes, scales from one atom each
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {          // elements 8c .. 8c+7
-                    const __half2 sc = __float2half2_rn(e4m3_to_f32((sfw >> (8 * (c >> 1))) & 0xFFu));
-                    const uint4 v = dequant8(words[c], sc);
-                    wv[4 * c] = v.x;
-                    wv[4 * c + 1] = v.y;
-                    wv[4 * c + 2] = v.z;
-                    wv[4 * c + 3] = v.w;
+                for (int a = 0; a < 2; ++a) {
+                    const uint4 c0 = *reinterpret_cast<const uint4*>(qrow + 32 * a);
+                    const uint4 c1 = *reinterpret_cast<const uint4*>(qrow + 32 * a + 16);
+                    const uint32_t sfw =
+                        *reinterpret_cast<const uint32_t*>(s.sf + stage * 2 * kSfBytes + a * kAtom + sf_off);
+                    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    uint32_t wv[32];                   // column i = elements 2i (low half), 2i + 1
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {      // elements 8c .. 8c+7 of the half
+                        const __half2 sc = __float2half2_rn(e4m3_to_f32((sfw >> (8 * (c >> 1))) & 0xFFu));
+                        const uint4 v = dequant8(words[c], sc);
+                        wv[4 * c] = v.x;
+                        wv[4 * c + 1] = v.y;
+                        wv[4 * c + 2] = v.z;
+                        wv[4 * c + 3] = v.w;
+                    }
+                    tmem_st32(t_row + (uint32_t)slot * kASlotCols + (uint32_t)(32 * a), wv);
                 }
-                tmem_st32(tmem_base + ((uint32_t)(32 * q) << 16) + kACol0 + (uint32_t)slot * kASlotCols +
-                              (uint32_t)(o * kAOpCols),
-                          wv);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();

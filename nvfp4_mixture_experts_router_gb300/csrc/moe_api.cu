@@ -170,7 +170,7 @@ bool encode_swap_weight_map(CUtensorMap* map, const void* base, uint64_t rows, u
 // T = 1 at the DSV3 shape 68.6 us standard vs 72.3 us swapped; T = 16
 // 452.7 vs 440.8; the mid workload 77.8 vs 74.9; T = 4096: 128 routes per
 // expert, standard).  W4A16 (H = 4096, I = 1536, E = 128, top-8): T = 16
-// step 385 -> 325 us, T = 512 532 -> 466 us swapped.
+// step 385 -> 273 us, T = 512 532 -> 389 us swapped.
 constexpr uint64_t kSlabAccBytes = 48ull << 20;   // FC2 accumulator slice kept in L2 (of 129 MB)
 constexpr int64_t kSwapMaxRoutesPerExpert = 64;
 constexpr int64_t kSwapMinRoutes = 64;
@@ -516,9 +516,9 @@ static moe_status forward_impl(moe_shape s, uint32_t flags, const void* x_bf16, 
         CUtensorMap tA1, tB1, tA2, tB2;
         const bool maps_ok =
             swap16 ? (encode_operand_map(&tA1, x_perm, W.rows_cap, (uint64_t)s.H * 2, 128, 64) &&
-                      encode_swap_weight_map(&tB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 32) &&
+                      encode_swap_weight_map(&tB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 64) &&
                       encode_operand_map(&tA2, h_bf16, W.rows_cap, (uint64_t)s.I * 2, 128, 64) &&
-                      encode_swap_weight_map(&tB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 32))
+                      encode_swap_weight_map(&tB2, pw + P.w2_codes, (uint64_t)s.E * s.H, (uint64_t)s.I / 2, 64))
                    : (encode_operand_map(&tA1, x_perm, W.rows_cap, (uint64_t)s.H * 2) &&
                       encode_operand_map(&tB1, pw + P.w1_codes, (uint64_t)s.E * N1, (uint64_t)s.H / 2, 32) &&
                       encode_operand_map(&tA2, h_bf16, W.rows_cap, (uint64_t)s.I * 2) &&
